@@ -1,0 +1,38 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+    config.addinivalue_line("markers", "slow: long-running (full-size workloads)")
+
+
+def load_golden(name):
+    """Parse a tests/golden/*.txt fixture: 'key v v v' lines, a 'logits' block, 'expect <mode>' sections."""
+    path = os.path.join(ROOT, "tests", "golden", name)
+    out = {"expect": {}}
+    cur = out
+    lines = [l.strip() for l in open(path) if l.strip() and not l.startswith("#")]
+    i = 0
+    while i < len(lines):
+        parts = lines[i].split()
+        if parts[0] == "logits":
+            T, E = out["T"], out["E"]
+            out["logits"] = [[float(v) for v in lines[i + 1 + t].split()] for t in range(T)]
+            i += 1 + T
+            continue
+        if parts[0] == "expect":
+            cur = {}
+            out["expect"][parts[1]] = cur
+        elif len(parts) == 2 and parts[0] in ("T", "E", "K", "m_tile"):
+            out[parts[0]] = int(parts[1])
+        else:
+            cur[parts[0]] = [float(v) for v in parts[1:]]
+        i += 1
+    return out

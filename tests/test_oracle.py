@@ -1,0 +1,345 @@
+"""Pins of the CPU oracle to facts it does not compute itself: library routines on special cases, brute
+force on tiny inputs, hand-worked fixtures, finite differences, an independent autograd derivation,
+closed forms and the token-rounding invariants.  Some tests plant a mistake in the oracle (on the CPU)
+to show that a pin catches it."""
+import itertools
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+from conftest import load_golden
+from fine_grained_mixture_gb300 import synth
+from oracle import moe_oracle as orc
+
+# ----------------------------------------------------------------------------------------------- routing
+
+
+@pytest.mark.parametrize("name", ["tiny", "fine7b", "sparse", "skew", "coarse"])
+def test_topk_equals_stable_argsort_on_workload_logits(name):
+    w = synth.WORKLOADS[name]
+    z = synth.make_logits_only(w, seed=0).numpy()
+    got = orc.topk_token_choice(z, w.K)
+    ref = np.argsort(-z.astype(np.float64), axis=1, kind="stable")[:, : w.K]
+    assert np.array_equal(got, ref)
+
+
+def test_topk_bruteforce_with_ties():
+    rng = np.random.default_rng(1)
+    for _ in range(200):
+        T, E, K = 3, 5, int(rng.integers(1, 5))
+        z = rng.choice([-1.0, 0.0, 0.5, 1.0], size=(T, E)).astype(np.float32)
+        got = orc.topk_token_choice(z, K)
+        for t in range(T):
+            # brute force: the K-subset whose (logit desc, expert asc) key list is smallest, listed in key order
+            best = None
+            for S in itertools.combinations(range(E), K):
+                key = sorted((-float(z[t, e]), e) for e in S)
+                if best is None or key < best:
+                    best = key
+            assert [e for _, e in best] == list(got[t])
+
+
+def test_scores_are_softmax_of_selected():
+    rng = np.random.default_rng(2)
+    z = rng.standard_normal((64, 16)).astype(np.float32)
+    idx = orc.topk_token_choice(z, 4)
+    s = orc.gate_scores(z, idx)
+    sel = np.take_along_axis(z.astype(np.float64), idx, axis=1)
+    assert np.allclose(s, scipy.special.softmax(sel, axis=1), rtol=1e-14, atol=0)
+    assert np.allclose(s.sum(1), 1.0, rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("f,M,T,r", [
+    (0, 128, 10**6, 0), (1, 128, 10**6, 0), (63, 128, 10**6, 0), (64, 128, 10**6, 0),   # tie -> floor
+    (65, 128, 10**6, 128), (127, 128, 10**6, 128), (128, 128, 10**6, 128), (129, 128, 10**6, 128),
+    (192, 128, 10**6, 128), (193, 128, 10**6, 256), (100, 128, 120, 0),                  # ceil > T -> floor
+    (3, 4, 100, 4), (5, 4, 100, 4), (2, 4, 100, 0), (6, 4, 100, 4), (7, 4, 100, 8),
+])
+def test_round_and_sparsify_table(f, M, T, r):
+    assert int(orc.round_and_sparsify(np.array([f]), M, T)[0]) == r
+
+
+def _check_tr_invariants(z, K, M):
+    tc = orc.route_tc(z, K, M)
+    tr = orc.route_tr(z, K, M)
+    T, E = z.shape
+    z64 = z.astype(np.float64)
+    f, r = tc["counts"], tr["counts"]
+    assert np.array_equal(tr["tc_counts"], f)
+    assert np.all(r % M == 0)
+    hi = -((-f) // M) * M
+    near = hi <= T                                            # padding possible: nearest multiple
+    assert np.all(np.abs(r - f)[near] <= M // 2)              # never more than half a tile away
+    assert np.all(np.abs(r - f) < M)                          # deviation within one tile
+    for e in range(E):
+        tc_set = tc["row_token"][tc["offsets"][e]:tc["offsets"][e + 1]]
+        kept = tr["row_token"][tr["offsets"][e]:tr["offsets"][e + 1]]
+        assert np.all(np.diff(kept) > 0)                      # ascending token ids
+        tcs, ks = set(tc_set.tolist()), set(kept.tolist())
+        if r[e] >= f[e]:
+            assert tcs <= ks                                  # every TC token kept before any EC token
+            added = np.array(sorted(ks - tcs), dtype=np.int64)
+            rest = np.array(sorted(set(range(T)) - ks), dtype=np.int64)
+            if len(added) and len(rest):
+                assert z64[added, e].min() >= z64[rest, e].max()
+        else:
+            assert ks <= tcs                                  # drops only among TC tokens ...
+            dropped = np.array(sorted(tcs - ks), dtype=np.int64)
+            if len(dropped) and len(kept):
+                assert z64[kept, e].min() >= z64[dropped, e].max()   # ... the weakest ones
+        sl = slice(tr["offsets"][e], tr["offsets"][e + 1])
+        for t, k, s in zip(tr["row_token"][sl], tr["row_slot"][sl], tr["row_score"][sl]):
+            if k >= 0:
+                assert tc["topk_idx"][t, k] == e and s == tc["topk_score"][t, k]
+            else:
+                assert e not in tc["topk_idx"][t]
+    return tc, tr
+
+
+@pytest.mark.parametrize("name", ["tiny", "sparse", "skew", "fine7b"])
+def test_tr_invariants_on_workloads(name):
+    w = synth.WORKLOADS[name]
+    _check_tr_invariants(synth.make_logits_only(w, 0).numpy(), w.K, synth.M_TILE)
+
+
+def test_tr_invariants_random_seeds():
+    rng = np.random.default_rng(3)
+    for seed in range(40):
+        T = int(rng.integers(1, 700))
+        E = int(rng.integers(2, 20))
+        K = int(rng.integers(1, min(E, 6) + 1))
+        M = int(rng.choice([4, 16, 128]))
+        z = rng.standard_normal((T, E)).astype(np.float32)
+        if seed % 4 == 0:
+            z = np.round(z * 2) / 2                          # heavy ties
+        _check_tr_invariants(z, K, M)
+
+
+def test_tr_bruteforce_tiny():
+    rng = np.random.default_rng(4)
+    for _ in range(60):
+        T, E, K, M = int(rng.integers(2, 11)), 3, int(rng.integers(1, 3)), 4
+        z = rng.choice([-1.0, -0.5, 0.0, 0.25, 0.5, 1.0], size=(T, E)).astype(np.float32)
+        tc = orc.route_tc(z, K, M)
+        tr = orc.route_tr(z, K, M)
+        member = np.zeros((T, E), bool)
+        for t in range(T):
+            member[t, tc["topk_idx"][t]] = True
+        for e in range(E):
+            r = int(tr["counts"][e])
+            # brute force: the r-subset whose descending key list is lexicographically largest
+            best = None
+            for S in itertools.combinations(range(T), r):
+                key = sorted(((int(member[t, e]), float(z[t, e]), -t) for t in S), reverse=True)
+                if best is None or key > best:
+                    best, bestS = key, S
+            kept = tr["row_token"][tr["offsets"][e]:tr["offsets"][e + 1]]
+            assert list(kept) == sorted(bestS)
+
+
+def test_tr_expected_total_unchanged():
+    rng = np.random.default_rng(5)
+    T, E, K, M = 4096, 64, 4, 128
+    diffs = []
+    for _ in range(100):
+        z = rng.standard_normal((T, E)).astype(np.float32)
+        tc = orc.route_tc(z, K, M)
+        r = orc.round_and_sparsify(tc["counts"], M, T)
+        diffs.append(int(r.sum()) - T * K)
+    diffs = np.array(diffs, dtype=np.float64)
+    # rounding to the nearest tile moves each expert by at most M/2 either way; the mean change of the
+    # total stays within a few standard errors of zero (plus the half-token tie bias per expert)
+    se = diffs.std(ddof=1) / np.sqrt(len(diffs))
+    assert abs(diffs.mean()) <= 4 * se + E * 0.5
+    assert abs(diffs.mean()) / (T * K) < 0.01
+
+
+@pytest.mark.parametrize("fixture", ["tr_pad_and_drop.txt", "tr_tie_rounds_down.txt"])
+def test_routing_golden(fixture):
+    g = load_golden(fixture)
+    z = np.array(g["logits"], dtype=np.float32)
+    for mode, exp in g["expect"].items():
+        rt = orc.route(z, g["K"], mode, g["m_tile"])
+        for key, val in exp.items():
+            got = rt[key]
+            if key in ("row_score", "topk_score"):
+                assert np.allclose(np.ravel(got), val, rtol=1e-15, atol=0), key
+            else:
+                assert list(np.ravel(got).astype(np.int64)) == [int(v) for v in val], (mode, key)
+
+
+# ------------------------------------------------------------------------------------- layer arithmetic
+
+
+def _tiny_problem(seed=0, T=8, d=8, n=4, E=4, K=2):
+    rng = np.random.default_rng(seed)
+    z = rng.standard_normal((T, E)).astype(np.float32)
+    rt = orc.route_tc(z, K, 4)
+    X = rng.standard_normal((T, d))
+    W1 = rng.standard_normal((E, d, 2 * n)) / np.sqrt(d)
+    W2 = rng.standard_normal((E, n, d)) / np.sqrt(n)
+    dO = rng.standard_normal((T, d))
+    return rt, X, W1, W2, dO
+
+
+def _loss(X, W1, W2, dO, rt, s=None):
+    s = rt["row_score"] if s is None else s
+    f = orc.forward(X, W1, W2, rt["row_token"], rt["row_expert"], s)
+    return float((dO * f["O"]).sum())
+
+
+def test_golden_single_row():
+    g = load_golden("swiglu_single_row.txt")
+    X = np.array(g["x"]).reshape(1, 2)
+    W1 = np.array(g["W1"]).reshape(1, 2, 2)
+    W2 = np.array(g["W2"]).reshape(1, 1, 2)
+    dO = np.array(g["dO"]).reshape(1, 2)
+    tok, ex, sc = np.array([0]), np.array([0]), np.array([1.0])
+    f = orc.forward(X, W1, W2, tok, ex, sc)
+    b = orc.backward(dO, X, W1, W2, tok, ex, sc, f)
+    assert np.allclose(f["O"][0], g["O"], rtol=1e-15)
+    assert np.allclose(b["dS"], g["dS"], rtol=1e-15)
+    assert np.allclose(b["dH"][0], g["dgate"] + g["dup"], rtol=1e-14)
+    assert np.allclose(b["dW2"][0, 0], [g["dS"][0]] * 2, rtol=1e-15)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_finite_differences(seed):
+    rt, X, W1, W2, dO = _tiny_problem(seed)
+    f, b = orc.layer(X, W1, W2, dO, rt)
+    h = 1e-6
+
+    def fd(arr, setter):
+        g = np.zeros_like(arr)
+        for i in np.ndindex(arr.shape):
+            old = arr[i]
+            arr[i] = old + h
+            lp = setter()
+            arr[i] = old - h
+            lm = setter()
+            arr[i] = old
+            g[i] = (lp - lm) / (2 * h)
+        return g
+
+    L = lambda: _loss(X, W1, W2, dO, rt)
+    for name, arr in (("dX", X), ("dW1", W1), ("dW2", W2)):
+        g = fd(arr, L)
+        err = np.abs(g - b[name]).max() / np.abs(b[name]).max()
+        assert err <= 1e-6, (name, err)
+    s = rt["row_score"].copy()
+    g = fd(s, lambda: _loss(X, W1, W2, dO, rt, s))
+    assert np.abs(g - b["dS"]).max() / np.abs(b["dS"]).max() <= 1e-6
+
+
+def test_independent_autograd_derivation():
+    """A per-token dense formulation differentiated by torch autograd in fp64 (not the oracle's chain rule)."""
+    rt, X, W1, W2, dO = _tiny_problem(7, T=16, d=16, n=8, E=6, K=3)
+    f, b = orc.layer(X, W1, W2, dO, rt)
+    Xt = torch.tensor(X, requires_grad=True)
+    W1t = torch.tensor(W1, requires_grad=True)
+    W2t = torch.tensor(W2, requires_grad=True)
+    st = torch.tensor(rt["topk_score"], requires_grad=True)
+    n = W1.shape[2] // 2
+    outs = []
+    for t in range(X.shape[0]):
+        acc = torch.zeros(X.shape[1], dtype=torch.float64)
+        for k in range(rt["K"]):
+            e = int(rt["topk_idx"][t, k])
+            h = Xt[t] @ W1t[e]
+            acc = acc + st[t, k] * ((torch.nn.functional.silu(h[:n]) * h[n:]) @ W2t[e])
+        outs.append(acc)
+    O = torch.stack(outs)
+    (O * torch.tensor(dO)).sum().backward()
+    assert np.allclose(O.detach().numpy(), f["O"], rtol=1e-12, atol=1e-13)
+    assert np.allclose(Xt.grad.numpy(), b["dX"], rtol=1e-11, atol=1e-12)
+    assert np.allclose(W1t.grad.numpy(), b["dW1"], rtol=1e-11, atol=1e-12)
+    assert np.allclose(W2t.grad.numpy(), b["dW2"], rtol=1e-11, atol=1e-12)
+    ds_dense = st.grad.numpy()[rt["row_token"], rt["row_slot"]]
+    assert np.allclose(ds_dense, b["dS"], rtol=1e-11, atol=1e-12)
+
+
+def test_dense_swiglu_mlp_special_case():
+    """K = E = 1 with score 1: the layer is a dense SwiGLU MLP."""
+    rng = np.random.default_rng(9)
+    T, d, n = 12, 16, 8
+    X = rng.standard_normal((T, d))
+    W1 = rng.standard_normal((1, d, 2 * n))
+    W2 = rng.standard_normal((1, n, d))
+    rt = orc.route_tc(np.zeros((T, 1), np.float32), 1, 4)
+    assert np.all(rt["row_score"] == 1.0)
+    f = orc.forward(X, W1, W2, rt["row_token"], rt["row_expert"], rt["row_score"])
+    lin = torch.nn.functional.linear
+    xt = torch.tensor(X)
+    h_gate = lin(xt, torch.tensor(W1[0][:, :n].T))
+    h_up = lin(xt, torch.tensor(W1[0][:, n:].T))
+    ref = lin(torch.nn.functional.silu(h_gate) * h_up, torch.tensor(W2[0].T)).numpy()
+    assert np.allclose(f["O"], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_ds_via_h_equals_ds_via_y():
+    rt, X, W1, W2, dO = _tiny_problem(11, T=32, d=24, n=8, E=5, K=2)
+    f, b = orc.layer(X, W1, W2, dO, rt)
+    ds2 = orc.ds_via_h(dO, W2, rt["row_token"], rt["row_expert"], f["H"])
+    assert np.abs(ds2 - b["dS"]).max() <= 1e-12 * np.abs(b["dS"]).max()
+
+
+def test_flop_count_by_counting_macs(monkeypatch):
+    rt, X, W1, W2, dO = _tiny_problem(12, T=20, d=16, n=8, E=4, K=2)
+    macs = []
+    real = orc._matmul
+
+    def counting(a, b):
+        macs.append(a.shape[0] * a.shape[1] * b.shape[1])
+        return real(a, b)
+
+    monkeypatch.setattr(orc, "_matmul", counting)
+    f = orc.forward(X, W1, W2, rt["row_token"], rt["row_expert"], rt["row_score"])
+    fwd_macs = sum(macs)
+    macs.clear()
+    orc.backward(dO, X, W1, W2, rt["row_token"], rt["row_expert"], rt["row_score"], f)
+    bwd_macs = sum(macs)
+    P, n, d = rt["P"], 8, 16
+    ff, bf = orc.layer_flops(P, n, d)
+    assert 2 * fwd_macs == ff and 2 * bwd_macs == bf
+    assert P == 20 * 2 and ff + bf == 18 * 20 * n * 2 * d       # (6+12) T n K d under token choice
+
+
+def test_cached_bytes_are_x_and_h():
+    T, d, n, K = 64, 32, 16, 4
+    X = torch.empty((T, d), dtype=torch.bfloat16)
+    H = torch.empty((T * K, 2 * n), dtype=torch.bfloat16)
+    assert orc.cached_activation_bytes(T, d, n, T * K) == X.nbytes + H.nbytes
+
+
+# ------------------------------------------------------------------------- planted mistakes are caught
+
+
+def test_planted_sign_error_in_dgate_is_caught(monkeypatch):
+    rt, X, W1, W2, dO = _tiny_problem(0)
+    real_sigmoid = orc.sigmoid
+    monkeypatch.setattr(orc, "sigmoid", lambda x: 1.0 - real_sigmoid(x))   # a wrong sigmoid in the backward
+    f, b = orc.layer(X, W1, W2, dO, rt)
+    h = 1e-6
+    i = (0, 1, 0)
+    old = W1[i]
+    W1[i] = old + h
+    lp = _loss(X, W1, W2, dO, rt)
+    W1[i] = old - h
+    lm = _loss(X, W1, W2, dO, rt)
+    W1[i] = old
+    assert abs((lp - lm) / (2 * h) - b["dW1"][i]) > 1e-4
+
+
+def test_planted_transposed_tie_break_is_caught(monkeypatch):
+    g = load_golden("tr_tie_rounds_down.txt")
+    z = np.array(g["logits"], dtype=np.float32)
+    real = orc.topk_token_choice
+
+    def last_max(z, K):                              # ties to the higher expert index
+        return real(np.asarray(z)[:, ::-1], K)[:, :] * -1 + (np.asarray(z).shape[1] - 1)
+
+    monkeypatch.setattr(orc, "topk_token_choice", last_max)
+    rt = orc.route_tc(z, g["K"], g["m_tile"])
+    assert list(rt["topk_idx"].ravel()) != [int(v) for v in g["expect"]["tc"]["topk_idx"]]
