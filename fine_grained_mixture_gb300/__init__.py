@@ -1,0 +1,11 @@
+"""GB300-native (sm_103a) fine-grained MoE expert layer: routing, forward and backward behind a C ABI.
+
+The compute runs in libmoe.so (hand-written CUDA); ``moe`` is the thin ctypes binding over it.
+"""
+from .moe import (M_TILE, MOE_ROUTE_TC, MOE_ROUTE_TR, MoeError, Routing, kernel_launch_count, library,
+                  moe_backward, moe_backward_workspace_size, moe_forward, moe_forward_workspace_size, moe_route,
+                  moe_route_capacity, moe_route_workspace_size)
+
+__all__ = ["M_TILE", "MOE_ROUTE_TC", "MOE_ROUTE_TR", "MoeError", "Routing", "kernel_launch_count", "library",
+           "moe_backward", "moe_backward_workspace_size", "moe_forward", "moe_forward_workspace_size", "moe_route",
+           "moe_route_capacity", "moe_route_workspace_size"]

@@ -1,0 +1,320 @@
+// api.cu - the extern "C" entry points of libmoe: argument validation, workspace carving, tensor-map
+// encoding and the launch sequence of each call.  See include/moe.h for the contract of every function.
+#include <atomic>
+#include <cstring>
+
+#include "internal.h"
+
+namespace moe {
+
+static thread_local int g_last_cuda_error = 0;
+static std::atomic<uint64_t> g_launches{0};
+
+int record_cuda_error(cudaError_t err) {
+  g_last_cuda_error = static_cast<int>(err);
+  return MOE_ERR_CUDA;
+}
+
+int record_cu_error(CUresult res) {
+  g_last_cuda_error = static_cast<int>(res);
+  return MOE_ERR_CUDA;
+}
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+constexpr int kMaxDevices = 64;
+
+int num_sms() {
+  static int cache[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 1;
+  }
+  return cache[dev];
+}
+
+// 0 = not checked yet, 1 = supported, 2 = not supported
+static int check_device() {
+  static int cache[kMaxDevices] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return record_cuda_error(err);
+  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_DEVICE;
+  if (cache[dev] == 0) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cache[dev] = (major == 10 && minor == 3) ? 1 : 2;
+  }
+  return cache[dev] == 1 ? MOE_OK : MOE_ERR_DEVICE;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+int make_tmap_bf16(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return record_cuda_error(cudaErrorNotSupported);
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : record_cu_error(r);
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+static int check_route_shape(int T, int E, int K, int mode) {
+  if (T <= 0 || E <= 0 || K <= 0 || K > E) return MOE_ERR_INVALID_ARG;
+  if (mode != MOE_ROUTE_TC && mode != MOE_ROUTE_TR) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxExperts || K > kMaxTopK) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (mode == MOE_ROUTE_TR && T > kMaxTrTokens) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((int64_t)T * K > (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+static int check_layer_shape(int T, int d, int n, int E, int K, size_t p_cap) {
+  if (T <= 0 || d <= 0 || n <= 0 || E <= 0 || K <= 0 || K > E) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxExperts || K > kMaxTopK) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d % 256 != 0 || n % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (p_cap < (size_t)T * K || p_cap >= ((size_t)1 << 31)) return MOE_ERR_INVALID_ARG;
+  if ((uint64_t)E * d * 2 * n >= ((uint64_t)1 << 40)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+static bool routing_ok(const moe_routing *r) {
+  return r && r->topk_idx && r->topk_score && r->tc_counts && r->counts && r->offsets && r->tile_offsets &&
+         r->row_token && r->row_slot && r->row_score && r->status;
+}
+
+static size_t fwd_ws_bytes(int T, int d, int n, size_t p_cap) {
+  return align256(p_cap * n * 2) + align256((size_t)T * d * 4);
+}
+
+static size_t bwd_ws_bytes(int T, int d, int n, size_t p_cap) {
+  return align256(p_cap * 2 * n * 2) + align256(p_cap * n * 2) + align256((size_t)T * d * 4);
+}
+
+static GemmArgs base_args(const moe_routing *r, int T, int d, int n, int E, size_t p_cap) {
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.offsets = r->offsets;
+  a.tile_offsets = r->tile_offsets;
+  a.row_token = r->row_token;
+  a.row_score = r->row_score;
+  a.status = r->status;
+  a.T = T;
+  a.d = d;
+  a.n = n;
+  a.E = E;
+  a.p_cap = static_cast<int>(p_cap);
+  return a;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_route_capacity(int T, int E, int K, int mode, size_t *p_cap) {
+  if (!p_cap) return MOE_ERR_INVALID_ARG;
+  const int rc = check_route_shape(T, E, K, mode);
+  if (rc != MOE_OK) return rc;
+  *p_cap = (size_t)T * K + (mode == MOE_ROUTE_TR ? (size_t)E * (MOE_M_TILE / 2) : 0);
+  return MOE_OK;
+}
+
+int moe_route_workspace_size(int T, int E, int K, int mode, size_t *bytes) {
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  const int rc = check_route_shape(T, E, K, mode);
+  if (rc != MOE_OK) return rc;
+  *bytes = route_workspace_bytes(T, E, K, mode);
+  return MOE_OK;
+}
+
+int moe_route(const float *logits, int T, int E, int K, int mode, const moe_routing *r, void *ws, size_t ws_bytes,
+              int32_t *P_host, void *stream) {
+  int rc = check_route_shape(T, E, K, mode);
+  if (rc != MOE_OK) return rc;
+  if (!logits || !routing_ok(r)) return MOE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < route_workspace_bytes(T, E, K, mode)) return MOE_ERR_WORKSPACE;
+  rc = check_device();
+  if (rc != MOE_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = launch_route(logits, T, E, K, mode, r, ws, s);
+  if (rc != MOE_OK) return rc;
+  if (P_host) {
+    cudaError_t err = cudaMemcpyAsync(P_host, r->status + 1, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(s);
+    if (err != cudaSuccess) return record_cuda_error(err);
+  }
+  return MOE_OK;
+}
+
+int moe_forward_workspace_size(int T, int d, int n, int E, int K, size_t p_cap, size_t *bytes) {
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  const int rc = check_layer_shape(T, d, n, E, K, p_cap);
+  if (rc != MOE_OK) return rc;
+  *bytes = fwd_ws_bytes(T, d, n, p_cap);
+  return MOE_OK;
+}
+
+int moe_forward(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const moe_routing *r, int T, int d, int n,
+                int E, int K, size_t p_cap, moe_bf16 *O, moe_bf16 *H, void *ws, size_t ws_bytes, void *stream) {
+  int rc = check_layer_shape(T, d, n, E, K, p_cap);
+  if (rc != MOE_OK) return rc;
+  if (!X || !W1 || !W2 || !O || !H || !routing_ok(r)) return MOE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < fwd_ws_bytes(T, d, n, p_cap)) return MOE_ERR_WORKSPACE;
+  rc = check_device();
+  if (rc != MOE_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char *p = static_cast<char *>(ws);
+  moe_bf16 *A = reinterpret_cast<moe_bf16 *>(p);
+  p += align256(p_cap * n * 2);
+  float *O32 = reinterpret_cast<float *>(p);
+
+  cudaError_t err = cudaMemsetAsync(O32, 0, (size_t)T * d * 4, s);
+  if (err != cudaSuccess) return record_cuda_error(err);
+
+  GemmArgs a = base_args(r, T, d, n, E, p_cap);
+  TensorMaps tm;
+  // up-projection: H = X[tok] W1_e (N = 2n, K = d)
+  if ((rc = make_tmap_bf16(&tm.a, X, d, T, 1)) != MOE_OK) return rc;
+  if ((rc = make_tmap_bf16(&tm.b, W1, 2 * (uint64_t)n, (uint64_t)E * d, 64)) != MOE_OK) return rc;
+  a.Ndim = 2 * n;
+  a.Kdim = d;
+  a.out0 = H;
+  a.out1 = A;
+  if ((rc = launch_up(a, tm, s)) != MOE_OK) return rc;
+  // down-projection + aggregation: O32[tok] += s * A W2_e (N = d, K = n)
+  if ((rc = make_tmap_bf16(&tm.a, A, n, p_cap, 128)) != MOE_OK) return rc;
+  if ((rc = make_tmap_bf16(&tm.b, W2, d, (uint64_t)E * n, 64)) != MOE_OK) return rc;
+  a.Ndim = d;
+  a.Kdim = n;
+  a.out0 = nullptr;
+  a.out1 = nullptr;
+  a.out_f32 = O32;
+  if ((rc = launch_down(a, tm, s)) != MOE_OK) return rc;
+  return launch_f32_to_bf16(O32, O, (size_t)T * d, s);
+}
+
+int moe_backward_workspace_size(int T, int d, int n, int E, int K, size_t p_cap, size_t *bytes) {
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  const int rc = check_layer_shape(T, d, n, E, K, p_cap);
+  if (rc != MOE_OK) return rc;
+  *bytes = bwd_ws_bytes(T, d, n, p_cap);
+  return MOE_OK;
+}
+
+int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const moe_bf16 *H,
+                 const moe_routing *r, int T, int d, int n, int E, int K, size_t p_cap, moe_bf16 *dX, moe_bf16 *dW1,
+                 moe_bf16 *dW2, float *dS, void *ws, size_t ws_bytes, void *stream) {
+  int rc = check_layer_shape(T, d, n, E, K, p_cap);
+  if (rc != MOE_OK) return rc;
+  if (!dO || !X || !W1 || !W2 || !H || !dX || !dW1 || !dW2 || !dS || !routing_ok(r)) return MOE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < bwd_ws_bytes(T, d, n, p_cap)) return MOE_ERR_WORKSPACE;
+  rc = check_device();
+  if (rc != MOE_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char *p = static_cast<char *>(ws);
+  moe_bf16 *dH = reinterpret_cast<moe_bf16 *>(p);
+  p += align256(p_cap * 2 * n * 2);
+  moe_bf16 *sA = reinterpret_cast<moe_bf16 *>(p);
+  p += align256(p_cap * n * 2);
+  float *dX32 = reinterpret_cast<float *>(p);
+
+  cudaError_t err = cudaMemsetAsync(dX32, 0, (size_t)T * d * 4, s);
+  if (err == cudaSuccess) err = cudaMemsetAsync(dS, 0, p_cap * 4, s);
+  if (err != cudaSuccess) return record_cuda_error(err);
+
+  GemmArgs a = base_args(r, T, d, n, E, p_cap);
+  TensorMaps tm;
+  // dH: dA' = dO[tok] W2_e^T (N = n, K = d); epilogue dSwiGLU, dS, s*A
+  const int bn = (n % 256 == 0) ? 256 : 128;
+  if ((rc = make_tmap_bf16(&tm.a, dO, d, T, 1)) != MOE_OK) return rc;
+  if ((rc = make_tmap_bf16(&tm.b, W2, d, (uint64_t)E * n, bn)) != MOE_OK) return rc;
+  a.Ndim = n;
+  a.Kdim = d;
+  a.out0 = dH;
+  a.out1 = sA;
+  a.dS = dS;
+  a.Hin = H;
+  if ((rc = launch_dh(a, tm, s, bn)) != MOE_OK) return rc;
+  // dX~: dX32[tok] += dH W1_e^T (N = d, K = 2n)
+  if ((rc = make_tmap_bf16(&tm.a, dH, 2 * (uint64_t)n, p_cap, 128)) != MOE_OK) return rc;
+  if ((rc = make_tmap_bf16(&tm.b, W1, 2 * (uint64_t)n, (uint64_t)E * d, 256)) != MOE_OK) return rc;
+  GemmArgs ax = base_args(r, T, d, n, E, p_cap);
+  ax.Ndim = d;
+  ax.Kdim = 2 * n;
+  ax.out_f32 = dX32;
+  if ((rc = launch_dx(ax, tm, s)) != MOE_OK) return rc;
+  if ((rc = launch_f32_to_bf16(dX32, dX, (size_t)T * d, s)) != MOE_OK) return rc;
+  // dW1_e = X[tok]^T dH_e (M = d, N = 2n, K = rows of e)
+  if ((rc = make_tmap_bf16(&tm.a, X, d, T, 1)) != MOE_OK) return rc;
+  if ((rc = make_tmap_bf16(&tm.b, dH, 2 * (uint64_t)n, p_cap, 1)) != MOE_OK) return rc;
+  GemmArgs aw = base_args(r, T, d, n, E, p_cap);
+  aw.Mdim = d;
+  aw.Ndim = 2 * n;
+  aw.out0 = dW1;
+  if ((rc = launch_dw1(aw, tm, s)) != MOE_OK) return rc;
+  // dW2_e = (s*A)_e^T dO[tok] (M = n, N = d, K = rows of e)
+  if ((rc = make_tmap_bf16(&tm.a, sA, n, p_cap, 1)) != MOE_OK) return rc;
+  if ((rc = make_tmap_bf16(&tm.b, dO, d, T, 1)) != MOE_OK) return rc;
+  aw.Mdim = n;
+  aw.Ndim = d;
+  aw.out0 = dW2;
+  return launch_dw2(aw, tm, s);
+}
+
+int moe_get_status(const moe_routing *r, int32_t *code, int32_t *P, void *stream) {
+  if (!r || !r->status) return MOE_ERR_INVALID_ARG;
+  int32_t words[MOE_STATUS_WORDS];
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t err = cudaMemcpyAsync(words, r->status, sizeof(words), cudaMemcpyDeviceToHost, s);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(s);
+  if (err != cudaSuccess) return record_cuda_error(err);
+  if (code) *code = words[0];
+  if (P) *P = words[1];
+  return MOE_OK;
+}
+
+const char *moe_strerror(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_NONFINITE_LOGITS: return "non-finite router logit";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
+    case MOE_ERR_BAD_METADATA: return "routing metadata out of range";
+    case MOE_ERR_DEVICE: return "device is not compute capability 10.3";
+    default: return "unknown status";
+  }
+}
+
+int moe_last_cuda_error(void) { return g_last_cuda_error; }
+
+uint64_t moe_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

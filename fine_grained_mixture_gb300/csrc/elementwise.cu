@@ -1,0 +1,28 @@
+// elementwise.cu - the fp32 -> bf16 cast that finishes the fused aggregations (O and dX are accumulated
+// in fp32 by the down-projection and dX~ epilogues, then rounded once to bf16).
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+__global__ void __launch_bounds__(256) f32_to_bf16_kernel(const float4 *__restrict__ src, uint2 *__restrict__ dst,
+                                                          size_t n4) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+    const float4 v = __ldcs(src + i);
+    uint2 o;
+    o.x = pack_bf16x2(v.x, v.y);
+    o.y = pack_bf16x2(v.z, v.w);
+    __stcs(dst + i, o);
+  }
+}
+
+int launch_f32_to_bf16(const float *src, void *dst, size_t count, cudaStream_t s) {
+  const size_t n4 = count / 4;  // count is a multiple of 256 (d % 256 == 0)
+  const int blocks = num_sms() * 8;
+  f32_to_bf16_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4 *>(src), reinterpret_cast<uint2 *>(dst), n4);
+  count_launch();
+  const cudaError_t err = cudaGetLastError();
+  return err == cudaSuccess ? MOE_OK : record_cuda_error(err);
+}
+
+}  // namespace moe

@@ -1,0 +1,532 @@
+// gemm.cuh - the grouped-GEMM kernel family of the MoE layer on tcgen05 / TMEM / TMA (sm_103a).
+//
+// "SonicMoE: Accelerating MoE with IO and Tile-aware Optimizations" (ICLR 2026 reading note) splits the
+// layer into varlen-M grouped GEMMs (rows of one expert are a variable-length M range) and varlen-K
+// grouped GEMMs (the weight gradients reduce over an expert's rows), with the token gather fused into the
+// operand load and elementwise work fused into the epilogue ("Key design 2: IO-aware fused kernels"), and
+// on Blackwell a two-stage TMEM accumulator so one tile's epilogue overlaps the next tile's MMAs.
+//
+// One persistent kernel template serves all six GEMMs of the layer:
+//   kUp   H = X[tok] W1_e, epilogue SwiGLU -> H (bf16, cached) and A (bf16)        M=rows  N=2n  K=d
+//   kDown O32[tok] += s * (A W2_e)  (Y never stored)                              M=rows  N=d   K=n
+//   kDH   dA' = dO[tok] W2_e^T, epilogue: A'=SwiGLU(H), dS=<dA',A'>, dH, s*A'      M=rows  N=n   K=d
+//   kDX   dX32[tok] += dH W1_e^T                                                    M=rows  N=d   K=2n
+//   kDW1  dW1_e = X[tok]^T dH   (reduction over the expert's rows)                  M=d     N=2n  K=rows
+//   kDW2  dW2_e = (sA)^T dO[tok]                                                    M=n     N=d   K=rows
+//
+// CTA = 6 warps: warp 0 issues TMA (tiled loads for dense operands, tile::gather4 for token-indexed rows),
+// warp 1 owns TMEM and one elected lane issues tcgen05.mma, warps 2..5 drain TMEM in the epilogue.
+// Tiles: 128 x BN x 64, STAGES-deep shared-memory ring, two TMEM accumulators of BN fp32 columns.
+// Every wait is bounded; on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT, drains its own copies and
+// MMAs, frees TMEM and returns.
+#pragma once
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+enum GemmMode : int { kUp = 0, kDown = 1, kDH = 2, kDX = 3, kDW1 = 4, kDW2 = 5 };
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kGemmThreads = 192;
+constexpr int kABytes = kBM * kBK * 2;  // 16 KB per stage
+
+template <int MODE>
+struct Traits {
+  static constexpr bool varlen_k = (MODE == kDW1 || MODE == kDW2);
+  static constexpr bool a_gather = (MODE == kUp || MODE == kDH);  // A rows fetched by token id
+  static constexpr bool a_mn = varlen_k;                          // A operand MN-major in shared memory
+  static constexpr bool b_mn = (MODE == kUp || MODE == kDown || varlen_k);
+  static constexpr bool nt_outer = (MODE == kDown || MODE == kDX);  // keep one fp32 column slab hot in L2
+};
+
+template <int BN, int STAGES>
+struct Smem {
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kBarOff = STAGES * kStageBytes;
+  static constexpr int kBytes = kBarOff + 256 + 1024;  // + barriers/flags + alignment slack
+};
+
+struct Tile {
+  int e, m0, n0, row0, row_end, kblocks;
+};
+
+// Largest e in [0, E) with tile_offsets[e] <= mt.
+__device__ __forceinline__ int find_expert(const int32_t *__restrict__ tile_offsets, int E, int mt) {
+  int lo = 0, hi = E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(&tile_offsets[mid]) <= mt) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
+template <int MODE, int BN>
+__device__ __forceinline__ int total_tiles(const GemmArgs &a) {
+  if (Traits<MODE>::varlen_k) return a.E * (a.Mdim / kBM) * (a.Ndim / BN);
+  return __ldg(&a.tile_offsets[a.E]) * (a.Ndim / BN);
+}
+
+template <int MODE, int BN>
+__device__ __forceinline__ Tile decode_tile(const GemmArgs &a, int tile, int total_m) {
+  Tile t;
+  const int n_tiles = a.Ndim / BN;
+  if (Traits<MODE>::varlen_k) {
+    const int m_tiles = a.Mdim / kBM;
+    const int per_e = m_tiles * n_tiles;
+    t.e = tile / per_e;
+    const int rem = tile - t.e * per_e;
+    const int mt = rem / n_tiles;
+    t.m0 = mt * kBM;
+    t.n0 = (rem - mt * n_tiles) * BN;
+    t.row0 = __ldg(&a.offsets[t.e]);
+    t.row_end = __ldg(&a.offsets[t.e + 1]);
+    if (t.row0 < 0 || t.row_end < t.row0 || t.row_end > a.p_cap) {
+      set_status(a.status, MOE_ERR_BAD_METADATA);
+      t.row_end = t.row0 = 0;
+    }
+    t.kblocks = (t.row_end - t.row0 + kBK - 1) / kBK;
+  } else {
+    int mt, nt;
+    if (Traits<MODE>::nt_outer) {
+      nt = tile / total_m;
+      mt = tile - nt * total_m;
+    } else {
+      mt = tile / n_tiles;
+      nt = tile - mt * n_tiles;
+    }
+    t.e = find_expert(a.tile_offsets, a.E, mt);
+    t.m0 = 0;
+    t.n0 = nt * BN;
+    t.row0 = __ldg(&a.offsets[t.e]) + (mt - __ldg(&a.tile_offsets[t.e])) * kBM;
+    t.row_end = __ldg(&a.offsets[t.e + 1]);
+    t.kblocks = a.Kdim / kBK;
+    if (t.row0 < 0 || t.row_end > a.p_cap || t.row0 >= t.row_end) {
+      set_status(a.status, MOE_ERR_BAD_METADATA);
+      t.kblocks = 0;
+    }
+  }
+  return t;
+}
+
+// Token id of row r, or an out-of-range row (zero fill) when r is past the expert or the id is invalid.
+__device__ __forceinline__ int token_or_oob(const GemmArgs &a, int r, int row_end) {
+  if (r >= row_end) return a.T;
+  const int t = __ldg(&a.row_token[r]);
+  return (t >= 0 && t < a.T) ? t : a.T;
+}
+
+template <int MODE, int BN, int STAGES>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const GemmArgs a) {
+  using TR = Traits<MODE>;
+  using SM = Smem<BN, STAGES>;
+  constexpr uint32_t kTmemCols = 2 * BN;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *gbase = smem_raw + (base - raw);
+  const uint32_t sA = base;
+  const uint32_t sB = base + STAGES * kABytes;
+  const uint32_t bar = base + SM::kBarOff;
+  auto full_bar = [&](int s) { return bar + 8u * s; };
+  auto empty_bar = [&](int s) { return bar + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bar + 8u * (2 * STAGES + 4);
+  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + SM::kBarOff + 8 * (2 * STAGES + 5));
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + SM::kBarOff + 8 * (2 * STAGES + 5) + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int total = total_tiles<MODE, BN>(a);
+  const int total_m = TR::varlen_k ? 0 : __ldg(&a.tile_offsets[a.E]);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------------------ TMA producer
+    const uint64_t pol_w = policy_evict_last();
+    const uint64_t pol_x = policy_evict_normal();
+    int s = 0;
+    uint32_t ph = 0;
+    int issued = 0;
+    bool aborted = false;
+    for (int tile = blockIdx.x; tile < total && !aborted; tile += gridDim.x) {
+      const Tile t = decode_tile<MODE, BN>(a, tile, total_m);
+      int tok[4];
+      if (TR::a_gather) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tok[j] = token_or_oob(a, t.row0 + lane * 4 + j, t.row_end);
+      }
+      for (int kb = 0; kb < t.kblocks; ++kb) {
+        int ok = 1;
+        if (lane == 0) {
+          ok = mbar_wait(empty_bar(s), ph ^ 1u) ? 1 : 0;
+          if (ok && *abort_flag) ok = 0;
+          if (ok) mbar_arrive_expect_tx(full_bar(s), SM::kStageBytes);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          if (lane == 0) {
+            set_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
+          }
+          aborted = true;
+          break;
+        }
+        const uint32_t a_dst = sA + s * kABytes;
+        const uint32_t b_dst = sB + s * SM::kBBytes;
+        const uint32_t fb = full_bar(s);
+        if (MODE == kUp || MODE == kDH) {
+          // A: 128 gathered token rows, 64 K-elements each (K-major); four rows per gather4
+          tma_gather4(a_dst + lane * 512, &tmA, kb * kBK, tok[0], tok[1], tok[2], tok[3], fb, pol_x);
+          if (lane == 0) {
+            if (MODE == kUp) {
+              // B: W1_e rows [kb*64, +64), gate columns [n0/2, +128) and up columns [n + n0/2, +128)
+              const int hcol = t.n0 / 2;
+              const int wrow = t.e * a.d + kb * kBK;
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const int col = (c < 2 ? 0 : a.n) + hcol + (c & 1) * 64;
+                tma_load_2d(b_dst + c * 8192, &tmB, col, wrow, fb, pol_w);
+              }
+            } else {
+              // B (K-major): W2_e rows n0..n0+BN (the N index), K-elements [kb*64, +64)
+              tma_load_2d(b_dst, &tmB, kb * kBK, t.e * a.n + t.n0, fb, pol_w);
+            }
+          }
+        } else if (MODE == kDown || MODE == kDX) {
+          if (lane == 0) {
+            tma_load_2d(a_dst, &tmA, kb * kBK, t.row0, fb, pol_x);
+            if (MODE == kDown) {
+#pragma unroll
+              for (int c = 0; c < BN / 64; ++c)
+                tma_load_2d(b_dst + c * 8192, &tmB, t.n0 + c * 64, t.e * a.n + kb * kBK, fb, pol_w);
+            } else {
+              tma_load_2d(b_dst, &tmB, kb * kBK, t.e * a.d + t.n0, fb, pol_w);
+            }
+          }
+        } else {
+          // varlen-K: both operands MN-major; K index = row of the expert
+          const int rb = t.row0 + kb * kBK;
+          {
+            const int c = lane >> 4, g = lane & 15;
+            int idx[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int r = rb + 4 * g + j;
+              idx[j] = (MODE == kDW1) ? token_or_oob(a, r, t.row_end) : (r < t.row_end ? r : a.p_cap);
+            }
+            tma_gather4(a_dst + c * 8192 + g * 512, &tmA, t.m0 + c * 64, idx[0], idx[1], idx[2], idx[3], fb, pol_x);
+          }
+#pragma unroll
+          for (int i = lane; i < (BN / 64) * 16; i += 32) {
+            const int c = i >> 4, g = i & 15;
+            int idx[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int r = rb + 4 * g + j;
+              idx[j] = (MODE == kDW2) ? token_or_oob(a, r, t.row_end) : (r < t.row_end ? r : a.p_cap);
+            }
+            tma_gather4(b_dst + c * 8192 + g * 512, &tmB, t.n0 + c * 64, idx[0], idx[1], idx[2], idx[3], fb, pol_x);
+          }
+        }
+        ++issued;
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    if (aborted && lane == 0) {
+      // let every copy this CTA issued land before the CTA's shared memory is released
+      for (int st = 0; st < STAGES && st < issued; ++st) {
+        const int last = st + ((issued - 1 - st) / STAGES) * STAGES;
+        mbar_wait(full_bar(st), static_cast<uint32_t>((last / STAGES) & 1));
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, TR::a_mn, TR::b_mn);
+      int s = 0;
+      uint32_t ph = 0;
+      int buf = 0;
+      uint32_t bph = 0;
+      bool aborted = false;
+      for (int tile = blockIdx.x; tile < total && !aborted; tile += gridDim.x) {
+        const Tile t = decode_tile<MODE, BN>(a, tile, total_m);
+        if (t.kblocks == 0) continue;
+        if (!mbar_wait(tempty_bar(buf), bph ^ 1u) || *abort_flag) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+        for (int kb = 0; kb < t.kblocks; ++kb) {
+          if (!mbar_wait(full_bar(s), ph) || *abort_flag) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_st = sA + s * kABytes;
+          const uint32_t b_st = sB + s * SM::kBBytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t ad = TR::a_mn ? smem_desc_sw128(a_st + k * 2048, 8192, 1024)
+                                         : smem_desc_sw128(a_st + k * 32, 16, 1024);
+            const uint64_t bd = TR::b_mn ? smem_desc_sw128(b_st + k * 2048, 8192, 1024)
+                                         : smem_desc_sw128(b_st + k * 32, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(empty_bar(s));
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (aborted) break;
+        umma_commit(tfull_bar(buf));
+        if (++buf == 2) {
+          buf = 0;
+          bph ^= 1u;
+        }
+      }
+      if (aborted) {
+        set_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    int buf = 0;
+    uint32_t bph = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const Tile t = decode_tile<MODE, BN>(a, tile, total_m);
+      if (t.kblocks == 0) {
+        if (TR::varlen_k) {  // an expert without rows has an exactly zero weight gradient
+          uint8_t *dst = static_cast<uint8_t *>(a.out0) +
+                         (((size_t)t.e * a.Mdim + t.m0 + row) * a.Ndim + t.n0) * 2;
+          for (int c = 0; c < BN * 2; c += 16) st_v4(dst + c, 0u, 0u, 0u, 0u);
+        }
+        continue;
+      }
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(tfull_bar(buf), bph) && !*abort_flag;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) {
+          set_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
+
+      if (MODE == kUp) {
+        const int r = t.row0 + row;
+        const bool valid = r < t.row_end;
+        const int j0 = t.n0 / 2;
+        uint8_t *hrow = static_cast<uint8_t *>(a.out0) + (size_t)r * (2 * a.n) * 2;
+        uint8_t *arow = static_cast<uint8_t *>(a.out1) + (size_t)r * a.n * 2;
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+          uint32_t g[32], u[32];
+          tmem_ld32(tacc + c * 32, g);
+          tmem_ld32(tacc + BN / 2 + c * 32, u);
+          tmem_ld_wait();
+          if (valid) {
+            uint32_t hg[16], hu[16], av[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+              const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+              const float a0 = g0 / (1.f + __expf(-g0)) * u0;
+              const float a1 = g1 / (1.f + __expf(-g1)) * u1;
+              hg[i] = pack_bf16x2(g0, g1);
+              hu[i] = pack_bf16x2(u0, u1);
+              av[i] = pack_bf16x2(a0, a1);
+            }
+            const int j = j0 + c * 32;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              st_v4(hrow + (size_t)j * 2 + v * 16, hg[4 * v], hg[4 * v + 1], hg[4 * v + 2], hg[4 * v + 3]);
+              st_v4(hrow + (size_t)(a.n + j) * 2 + v * 16, hu[4 * v], hu[4 * v + 1], hu[4 * v + 2], hu[4 * v + 3]);
+              st_v4(arow + (size_t)j * 2 + v * 16, av[4 * v], av[4 * v + 1], av[4 * v + 2], av[4 * v + 3]);
+            }
+          }
+        }
+      } else if (MODE == kDown || MODE == kDX) {
+        const int r = t.row0 + row;
+        bool valid = r < t.row_end;
+        int tok = 0;
+        float sc = 1.f;
+        if (valid) {
+          tok = __ldg(&a.row_token[r]);
+          if (tok < 0 || tok >= a.T) {
+            set_status(a.status, MOE_ERR_BAD_METADATA);
+            valid = false;
+          }
+          if (MODE == kDown) sc = __ldg(&a.row_score[r]);
+        }
+        float *dst = a.out_f32 + (size_t)tok * a.d + t.n0;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tacc + c * 32, v);
+          tmem_ld_wait();
+          if (valid) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              red_add_v4(dst + c * 32 + 4 * i, sc * __uint_as_float(v[4 * i]), sc * __uint_as_float(v[4 * i + 1]),
+                         sc * __uint_as_float(v[4 * i + 2]), sc * __uint_as_float(v[4 * i + 3]));
+          }
+        }
+      } else if (MODE == kDH) {
+        const int r = t.row0 + row;
+        const bool valid = r < t.row_end;
+        const float sc = valid ? __ldg(&a.row_score[r]) : 0.f;
+        const uint8_t *hrow = static_cast<const uint8_t *>(a.Hin) + (size_t)r * (2 * a.n) * 2;
+        uint8_t *dhrow = static_cast<uint8_t *>(a.out0) + (size_t)r * (2 * a.n) * 2;
+        uint8_t *sarow = static_cast<uint8_t *>(a.out1) + (size_t)r * a.n * 2;
+        float ds = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tacc + c * 32, v);
+          tmem_ld_wait();
+          if (valid) {
+            const int j = t.n0 + c * 32;
+            uint4 hg4[4], hu4[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              hg4[w] = __ldg(reinterpret_cast<const uint4 *>(hrow + (size_t)j * 2) + w);
+              hu4[w] = __ldg(reinterpret_cast<const uint4 *>(hrow + (size_t)(a.n + j) * 2) + w);
+            }
+            const uint32_t *hg = reinterpret_cast<const uint32_t *>(hg4);
+            const uint32_t *hu = reinterpret_cast<const uint32_t *>(hu4);
+            uint32_t dg[16], du[16], sa[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float o_g[2], o_u[2], o_a[2];
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const float gg = h ? bf16_hi(hg[i]) : bf16_lo(hg[i]);
+                const float uu = h ? bf16_hi(hu[i]) : bf16_lo(hu[i]);
+                const float dap = __uint_as_float(v[2 * i + h]);
+                const float sig = 1.f / (1.f + __expf(-gg));
+                const float silu = gg * sig;
+                const float act = silu * uu;
+                ds += dap * act;
+                const float da = sc * dap;
+                o_g[h] = da * uu * sig * (1.f + gg * (1.f - sig));
+                o_u[h] = da * silu;
+                o_a[h] = sc * act;
+              }
+              dg[i] = pack_bf16x2(o_g[0], o_g[1]);
+              du[i] = pack_bf16x2(o_u[0], o_u[1]);
+              sa[i] = pack_bf16x2(o_a[0], o_a[1]);
+            }
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              st_v4(dhrow + (size_t)j * 2 + w * 16, dg[4 * w], dg[4 * w + 1], dg[4 * w + 2], dg[4 * w + 3]);
+              st_v4(dhrow + (size_t)(a.n + j) * 2 + w * 16, du[4 * w], du[4 * w + 1], du[4 * w + 2], du[4 * w + 3]);
+              st_v4(sarow + (size_t)j * 2 + w * 16, sa[4 * w], sa[4 * w + 1], sa[4 * w + 2], sa[4 * w + 3]);
+            }
+          }
+        }
+        if (valid) atomicAdd(&a.dS[r], ds);
+      } else {
+        // weight gradients: bf16 rows of dW_e
+        uint8_t *dst = static_cast<uint8_t *>(a.out0) + (((size_t)t.e * a.Mdim + t.m0 + row) * a.Ndim + t.n0) * 2;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tacc + c * 32, v);
+          tmem_ld_wait();
+          uint32_t p[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+#pragma unroll
+          for (int w = 0; w < 4; ++w) st_v4(dst + c * 64 + w * 16, p[4 * w], p[4 * w + 1], p[4 * w + 2], p[4 * w + 3]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(buf));
+      if (++buf == 2) {
+        buf = 0;
+        bph ^= 1u;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    if (*abort_flag && lane == 0) {
+      umma_commit(drain_bar);  // all MMAs this CTA issued are complete once this arrives
+      mbar_wait(drain_bar, 0);
+    }
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// Host launcher for one instantiation.
+template <int MODE, int BN, int STAGES>
+int launch_gemm(const GemmArgs &a, const TensorMaps &tm, cudaStream_t stream) {
+  using SM = Smem<BN, STAGES>;
+  static int attr_dev = -1;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return record_cuda_error(err);
+  if (attr_dev != dev) {
+    err = cudaFuncSetAttribute(moe_gemm_kernel<MODE, BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SM::kBytes);
+    if (err != cudaSuccess) return record_cuda_error(err);
+    attr_dev = dev;
+  }
+  moe_gemm_kernel<MODE, BN, STAGES><<<num_sms(), kGemmThreads, SM::kBytes, stream>>>(tm.a, tm.b, a);
+  count_launch();
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return record_cuda_error(err);
+  return MOE_OK;
+}
+
+}  // namespace moe

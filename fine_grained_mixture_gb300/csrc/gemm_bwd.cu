@@ -1,0 +1,22 @@
+// gemm_bwd.cu - backward instantiations of the grouped-GEMM kernel: dH (dSwiGLU and dS in the epilogue),
+// dX~ with the scatter-sum into dX, and the varlen-K weight gradients dW1 and dW2.
+#include "gemm.cuh"
+
+namespace moe {
+
+int launch_dh(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, int bn) {
+  if (bn == 256) return launch_gemm<kDH, 256, 4>(a, tm, s);
+  return launch_gemm<kDH, 128, 6>(a, tm, s);
+}
+
+int launch_dx(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) { return launch_gemm<kDX, 256, 4>(a, tm, s); }
+
+int launch_dw1(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) {
+  return launch_gemm<kDW1, 256, 4>(a, tm, s);
+}
+
+int launch_dw2(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) {
+  return launch_gemm<kDW2, 256, 4>(a, tm, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,13 @@
+// gemm_fwd.cu - forward instantiations of the grouped-GEMM kernel: up-projection with the token gather and
+// SwiGLU epilogue, down-projection with the score-weighted aggregation epilogue.
+#include "gemm.cuh"
+
+namespace moe {
+
+int launch_up(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) { return launch_gemm<kUp, 256, 4>(a, tm, s); }
+
+int launch_down(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) {
+  return launch_gemm<kDown, 256, 4>(a, tm, s);
+}
+
+}  // namespace moe

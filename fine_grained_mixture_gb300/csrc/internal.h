@@ -1,0 +1,65 @@
+// internal.h - declarations shared by the library's translation units (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kMaxTrTokens = 49152;  // token rounding keeps one expert's keys for all T tokens in shared memory
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+
+// Remembers `err` as this thread's last CUDA error and returns MOE_ERR_CUDA.
+int record_cuda_error(cudaError_t err);
+int record_cu_error(CUresult res);
+void count_launch();
+
+// routing (route.cu)
+size_t route_workspace_bytes(int T, int E, int K, int mode);
+int launch_route(const float *logits, int T, int E, int K, int mode, const moe_routing *r, void *ws,
+                 cudaStream_t stream);
+
+// grouped GEMMs (gemm_fwd.cu, gemm_bwd.cu)
+struct GemmArgs {
+  const int32_t *offsets;
+  const int32_t *tile_offsets;
+  const int32_t *row_token;
+  const float *row_score;
+  int32_t *status;
+  int T, d, n, E;
+  int p_cap;
+  int Mdim;  // varlen-K: output rows of one expert's weight gradient
+  int Ndim;  // output columns
+  int Kdim;  // varlen-M: reduction length
+  void *out0;        // up: H;  dH: dH;  dW1/dW2: the weight gradient
+  void *out1;        // up: A;  dH: s*A
+  float *out_f32;    // down: fp32 O;  dX~: fp32 dX
+  float *dS;         // dH: per-row dS
+  const void *Hin;   // dH: cached H
+};
+
+struct TensorMaps {
+  CUtensorMap a, b;
+};
+
+// Encodes a 2D bf16 tensor map over [rows, inner] (row-major) with a {64, box_rows} box, 128-byte swizzle.
+int make_tmap_bf16(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t rows, uint32_t box_rows);
+
+int num_sms();
+
+int launch_up(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s);
+int launch_down(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s);
+int launch_dh(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, int bn);
+int launch_dx(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s);
+int launch_dw1(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s);
+int launch_dw2(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s);
+
+// elementwise (elementwise.cu)
+int launch_f32_to_bf16(const float *src, void *dst, size_t count, cudaStream_t s);
+
+}  // namespace moe

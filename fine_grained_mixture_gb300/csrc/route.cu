@@ -1,0 +1,393 @@
+// route.cu - routing metadata kernels: token-choice top-K, per-expert counts and offsets, and token
+// rounding.  Integer/compare work plus one fp32 softmax per token; every output is deterministic.
+//
+// Method: "SonicMoE: Accelerating MoE with IO and Tile-aware Optimizations" (ICLR 2026 reading note),
+// "Key design 1: Token Rounding routing": token choice first; per expert, an expert-choice ordering of the
+// tokens with the token-choice tokens ahead of expert-choice candidates; round_and_sparsify pads an
+// expert with expert-choice tokens when the distance up to the next multiple of M_tile is strictly
+// smaller than the distance down, and drops its weakest token-choice tokens otherwise.
+//
+// Pipeline (one stream, no host synchronisation):
+//   route_topk_kernel   one warp per token: top-K by (logit desc, expert asc), softmax over the K,
+//                       per-chunk (256 tokens) expert histograms, membership bitmap (TR only)
+//   route_scan_kernel   one CTA: per-chunk bases, counts (TC f_e or TR r_e), offsets, tile offsets
+//   route_fill_tc       one CTA per 256-token chunk: rows in ascending token order via bitmap ranks
+//   route_fill_tr       one CTA per expert: radix selection of the kept set, rows in token order
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+constexpr int kChunk = 256;  // tokens per routing chunk
+
+// Total order on fp32 logits used everywhere: larger value first; -0.0 equals +0.0.
+__device__ __forceinline__ uint32_t order_key(float z) {
+  uint32_t b = __float_as_uint(z);
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+template <int NV>  // NV = logits held per lane = ceil(E / 32)
+__global__ void __launch_bounds__(256) route_topk_kernel(const float *__restrict__ logits, int T, int E, int K,
+                                                         int want_member, int32_t *__restrict__ topk_idx,
+                                                         float *__restrict__ topk_score, float *__restrict__ tok_max,
+                                                         float *__restrict__ tok_den, int32_t *__restrict__ chunk_cnt,
+                                                         uint32_t *__restrict__ member, int member_words,
+                                                         int32_t *__restrict__ status) {
+  extern __shared__ int32_t hist[];  // [E]
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int chunk = blockIdx.x;
+  for (int i = 0; i < 32; ++i) {
+    const int t = chunk * kChunk + warp * 32 + i;
+    if (t >= T) break;
+    float v[NV];
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int e = lane + 32 * j;
+      v[j] = (e < E) ? logits[(size_t)t * E + e] : -INFINITY;
+      if (e < E && !isfinite(v[j])) bad = true;
+    }
+    if (__any_sync(0xffffffffu, bad)) {
+      if (lane == 0) set_status(status, MOE_ERR_NONFINITE_LOGITS);
+#pragma unroll
+      for (int j = 0; j < NV; ++j)
+        if (!isfinite(v[j])) v[j] = -INFINITY;
+    }
+    uint32_t taken = 0;  // bit j: v[j] already selected
+    int my_e = -1;       // lane k keeps the k-th selection
+    float my_z = 0.f, z0 = 0.f;
+    for (int k = 0; k < K; ++k) {
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int j = 0; j < NV; ++j) {
+        const int e = lane + 32 * j;
+        if (e < E && !((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < be) || be == 0x7fffffff)) {
+          bv = v[j];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+        if (ov > bv || (ov == bv && oe < be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (k == 0) z0 = bv;
+      if (lane == k) {
+        my_e = be;
+        my_z = bv;
+      }
+    }
+    // softmax over the K selected logits, in selection order
+    const float w = (lane < K) ? expf(my_z - z0) : 0.f;
+    float den = 0.f;
+    for (int k = 0; k < K; ++k) den += __shfl_sync(0xffffffffu, w, k);
+    if (lane < K) {
+      topk_idx[(size_t)t * K + lane] = my_e;
+      topk_score[(size_t)t * K + lane] = w / den;
+      atomicAdd(&hist[my_e], 1);
+      if (want_member) atomicOr(&member[(size_t)my_e * member_words + (t >> 5)], 1u << (t & 31));
+    }
+    if (lane == 0) {
+      tok_max[t] = z0;
+      tok_den[t] = den;
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_cnt[(size_t)chunk * E + e] = hist[e];
+}
+
+// Exclusive scan of one value per thread across a block of 1024 threads; returns the exclusive prefix and
+// writes the block total to *total.
+__device__ __forceinline__ int block_exclusive_scan_1024(int v, int *scratch /*[32]*/, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int s = scratch[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, off);
+      if (lane >= off) s += y;
+    }
+    scratch[lane] = s;  // inclusive per-warp totals
+  }
+  __syncthreads();
+  const int before = (warp > 0 ? scratch[warp - 1] : 0);
+  *total = scratch[31];
+  __syncthreads();
+  return before + x - v;
+}
+
+__global__ void __launch_bounds__(1024) route_scan_kernel(int T, int E, int nchunks, int mode, int m_tile,
+                                                          const int32_t *__restrict__ chunk_cnt,
+                                                          int32_t *__restrict__ chunk_base, int32_t *__restrict__ tc_counts,
+                                                          int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                                                          int32_t *__restrict__ tile_offsets, int32_t *__restrict__ status) {
+  __shared__ int scratch[32];
+  const int e = threadIdx.x;
+  int f = 0;
+  if (e < E) {
+    for (int c = 0; c < nchunks; ++c) {
+      chunk_base[(size_t)c * E + e] = f;
+      f += chunk_cnt[(size_t)c * E + e];
+    }
+  }
+  int cnt = f;
+  if (mode == MOE_ROUTE_TR && e < E) {
+    const int lo = (f / m_tile) * m_tile;
+    const int hi = ((f + m_tile - 1) / m_tile) * m_tile;
+    cnt = ((hi - f) < (f - lo) && hi <= T) ? hi : lo;
+  }
+  if (e >= E) cnt = 0;
+  const int tiles = (cnt + m_tile - 1) / m_tile;
+  int P = 0, total_tiles = 0;
+  const int off = block_exclusive_scan_1024(cnt, scratch, &P);
+  const int toff = block_exclusive_scan_1024(tiles, scratch, &total_tiles);
+  if (e < E) {
+    tc_counts[e] = f;
+    counts[e] = cnt;
+    offsets[e] = off;
+    tile_offsets[e] = toff;
+  }
+  if (e == 0) {
+    offsets[E] = P;
+    tile_offsets[E] = total_tiles;
+    status[1] = P;
+    status[2] = total_tiles;
+  }
+}
+
+__global__ void __launch_bounds__(kChunk) route_fill_tc_kernel(int T, int E, int K, const int32_t *__restrict__ topk_idx,
+                                                               const float *__restrict__ topk_score,
+                                                               const int32_t *__restrict__ chunk_base,
+                                                               const int32_t *__restrict__ offsets,
+                                                               int32_t *__restrict__ row_token, int32_t *__restrict__ row_slot,
+                                                               float *__restrict__ row_score) {
+  extern __shared__ uint32_t bm[];  // [E][8]: bit i of word w = token chunk*256 + 32w + i chose the expert
+  const int chunk = blockIdx.x;
+  for (int i = threadIdx.x; i < E * 8; i += blockDim.x) bm[i] = 0u;
+  __syncthreads();
+  const int tl = threadIdx.x;
+  const int t = chunk * kChunk + tl;
+  const bool live = t < T;
+  if (live)
+    for (int k = 0; k < K; ++k) atomicOr(&bm[topk_idx[(size_t)t * K + k] * 8 + (tl >> 5)], 1u << (tl & 31));
+  __syncthreads();
+  if (!live) return;
+  for (int k = 0; k < K; ++k) {
+    const int e = topk_idx[(size_t)t * K + k];
+    const uint32_t *w = &bm[e * 8];
+    int rank = __popc(w[tl >> 5] & ((1u << (tl & 31)) - 1u));
+    for (int j = 0; j < (tl >> 5); ++j) rank += __popc(w[j]);
+    const int row = offsets[e] + chunk_base[(size_t)chunk * E + e] + rank;
+    row_token[row] = t;
+    row_slot[row] = k;
+    row_score[row] = topk_score[(size_t)t * K + k];
+  }
+}
+
+// One CTA (1024 threads) per expert.  Keys of all T tokens for this expert live in shared memory.
+__global__ void __launch_bounds__(1024) route_fill_tr_kernel(
+    const float *__restrict__ logits, int T, int E, int K, const int32_t *__restrict__ topk_idx,
+    const float *__restrict__ topk_score, const float *__restrict__ tok_max, const float *__restrict__ tok_den,
+    const uint32_t *__restrict__ member, int member_words, const int32_t *__restrict__ tc_counts,
+    const int32_t *__restrict__ counts, const int32_t *__restrict__ offsets, int32_t *__restrict__ row_token,
+    int32_t *__restrict__ row_slot, float *__restrict__ row_score) {
+  extern __shared__ uint32_t sm[];
+  uint32_t *key = sm;                        // [T]
+  uint32_t *mem = sm + T;                    // [member_words]
+  int *hist = reinterpret_cast<int *>(mem + member_words);  // [256]
+  __shared__ int scratch[32];
+  __shared__ int sel_state[3];
+  const int e = blockIdx.x;
+  const int f = tc_counts[e], r = counts[e], base = offsets[e];
+  if (r == 0) return;
+  for (int w = threadIdx.x; w < member_words; w += blockDim.x) mem[w] = member[(size_t)e * member_words + w];
+  for (int t = threadIdx.x; t < T; t += blockDim.x) key[t] = order_key(logits[(size_t)t * E + e]);
+  __syncthreads();
+  // candidates: token-choice tokens when dropping, the other tokens when padding
+  const bool drop = r < f;
+  const int R = drop ? r : r - f;  // how many candidates to keep
+  uint32_t prefix = 0u, mask = 0u;
+  int remaining = R;
+  if (r != f) {
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+      __syncthreads();
+      for (int t = threadIdx.x; t < T; t += blockDim.x) {
+        const bool tc = (mem[t >> 5] >> (t & 31)) & 1u;
+        if (tc == drop && (key[t] & mask) == prefix) atomicAdd(&hist[(key[t] >> shift) & 255u], 1);
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        int acc = 0, b = 255;
+        for (; b > 0; --b) {
+          if (acc + hist[b] >= remaining) break;
+          acc += hist[b];
+        }
+        sel_state[0] = b;
+        sel_state[1] = remaining - acc;
+      }
+      __syncthreads();
+      prefix |= static_cast<uint32_t>(sel_state[0]) << shift;
+      mask |= 255u << shift;
+      remaining = sel_state[1];
+      __syncthreads();
+    }
+  }
+  // prefix = key of the R-th best candidate; `remaining` candidates equal to it are kept, lowest token first
+  int eq_carry = 0, row_carry = 0;
+  for (int t0 = 0; t0 < T; t0 += blockDim.x) {
+    const int t = t0 + threadIdx.x;
+    bool tc = false, cand = false, eq = false, gt = false;
+    if (t < T) {
+      tc = (mem[t >> 5] >> (t & 31)) & 1u;
+      cand = (r != f) && (tc == drop);
+      gt = cand && key[t] > prefix;
+      eq = cand && key[t] == prefix;
+    }
+    int eq_total;
+    const int eq_rank = block_exclusive_scan_1024(eq ? 1 : 0, scratch, &eq_total) + eq_carry;
+    eq_carry += eq_total;
+    bool keep;
+    if (r == f) keep = tc;
+    else if (drop) keep = gt || (eq && eq_rank < remaining);
+    else keep = tc || gt || (eq && eq_rank < remaining);
+    int kept_total;
+    const int pos = block_exclusive_scan_1024(keep ? 1 : 0, scratch, &kept_total) + row_carry;
+    row_carry += kept_total;
+    if (keep) {
+      const int row = base + pos;
+      int slot = -1;
+      float s;
+      if (tc) {
+        for (int k = 0; k < K; ++k)
+          if (topk_idx[(size_t)t * K + k] == e) slot = k;
+      }
+      if (slot >= 0) {
+        s = topk_score[(size_t)t * K + slot];
+      } else {
+        s = expf(logits[(size_t)t * E + e] - tok_max[t]) / tok_den[t];
+      }
+      row_token[row] = t;
+      row_slot[row] = slot;
+      row_score[row] = s;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------- host
+
+struct RouteWs {
+  int32_t *chunk_cnt, *chunk_base;
+  uint32_t *member;
+  float *tok_max, *tok_den;
+  int nchunks, member_words;
+};
+
+static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+size_t route_workspace_bytes(int T, int E, int K, int mode) {
+  (void)K;
+  const size_t nchunks = (T + kChunk - 1) / kChunk;
+  const size_t words = (T + 31) / 32;
+  size_t b = 0;
+  b += align256(nchunks * E * 4) * 2;
+  b += (mode == MOE_ROUTE_TR) ? align256(words * E * 4) : 0;
+  b += align256((size_t)T * 4) * 2;
+  return b;
+}
+
+static RouteWs carve(void *ws, int T, int E, int mode) {
+  RouteWs w{};
+  w.nchunks = (T + kChunk - 1) / kChunk;
+  w.member_words = (T + 31) / 32;
+  char *p = static_cast<char *>(ws);
+  w.chunk_cnt = reinterpret_cast<int32_t *>(p);
+  p += align256((size_t)w.nchunks * E * 4);
+  w.chunk_base = reinterpret_cast<int32_t *>(p);
+  p += align256((size_t)w.nchunks * E * 4);
+  if (mode == MOE_ROUTE_TR) {
+    w.member = reinterpret_cast<uint32_t *>(p);
+    p += align256((size_t)w.member_words * E * 4);
+  }
+  w.tok_max = reinterpret_cast<float *>(p);
+  p += align256((size_t)T * 4);
+  w.tok_den = reinterpret_cast<float *>(p);
+  return w;
+}
+
+size_t route_tr_smem_bytes(int T) { return (size_t)T * 4 + (size_t)((T + 31) / 32) * 4 + 256 * 4; }
+
+int launch_route(const float *logits, int T, int E, int K, int mode, const moe_routing *r, void *ws,
+                 cudaStream_t stream) {
+  RouteWs w = carve(ws, T, E, mode);
+  cudaError_t err;
+  err = cudaMemsetAsync(r->status, 0, MOE_STATUS_WORDS * sizeof(int32_t), stream);
+  if (err != cudaSuccess) return record_cuda_error(err);
+  if (mode == MOE_ROUTE_TR) {
+    err = cudaMemsetAsync(w.member, 0, (size_t)w.member_words * E * 4, stream);
+    if (err != cudaSuccess) return record_cuda_error(err);
+  }
+  const int want_member = mode == MOE_ROUTE_TR;
+  const size_t hist_smem = (size_t)E * 4;
+  const int nv = (E + 31) / 32;
+#define MOE_TOPK_LAUNCH(NV)                                                                                       \
+  route_topk_kernel<NV><<<w.nchunks, 256, hist_smem, stream>>>(logits, T, E, K, want_member, r->topk_idx,          \
+                                                               r->topk_score, w.tok_max, w.tok_den, w.chunk_cnt, \
+                                                               w.member, w.member_words, r->status)
+  if (nv <= 1) MOE_TOPK_LAUNCH(1);
+  else if (nv <= 2) MOE_TOPK_LAUNCH(2);
+  else if (nv <= 4) MOE_TOPK_LAUNCH(4);
+  else if (nv <= 8) MOE_TOPK_LAUNCH(8);
+  else if (nv <= 16) MOE_TOPK_LAUNCH(16);
+  else MOE_TOPK_LAUNCH(32);
+#undef MOE_TOPK_LAUNCH
+  count_launch();
+  route_scan_kernel<<<1, 1024, 0, stream>>>(T, E, w.nchunks, mode, MOE_M_TILE, w.chunk_cnt, w.chunk_base,
+                                            r->tc_counts, r->counts, r->offsets, r->tile_offsets, r->status);
+  count_launch();
+  if (mode == MOE_ROUTE_TC) {
+    route_fill_tc_kernel<<<w.nchunks, kChunk, (size_t)E * 8 * 4, stream>>>(
+        T, E, K, r->topk_idx, r->topk_score, w.chunk_base, r->offsets, r->row_token, r->row_slot, r->row_score);
+  } else {
+    const size_t smem = route_tr_smem_bytes(T);
+    static int attr_set_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (attr_set_dev != dev) {
+      err = cudaFuncSetAttribute(route_fill_tr_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(route_tr_smem_bytes(kMaxTrTokens)));
+      if (err != cudaSuccess) return record_cuda_error(err);
+      attr_set_dev = dev;
+    }
+    route_fill_tr_kernel<<<E, 1024, smem, stream>>>(logits, T, E, K, r->topk_idx, r->topk_score, w.tok_max, w.tok_den,
+                                                    w.member, w.member_words, r->tc_counts, r->counts, r->offsets,
+                                                    r->row_token, r->row_slot, r->row_score);
+  }
+  count_launch();
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return record_cuda_error(err);
+  return MOE_OK;
+}
+
+}  // namespace moe

@@ -1,0 +1,219 @@
+"""Thin Python binding of libmoe (the C ABI in include/moe.h): argument marshalling only.
+
+Every step of the layer runs in the library's CUDA kernels; this module allocates the caller-owned
+device buffers with torch, passes raw pointers and the current CUDA stream, and turns status codes into
+exceptions.  There is no fallback: if libmoe.so is missing or the device is not a GB300 the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+MOE_ROUTE_TC = 0
+MOE_ROUTE_TR = 1
+M_TILE = 128
+STATUS_WORDS = 4
+MODES = {"tc": MOE_ROUTE_TC, "tr": MOE_ROUTE_TR}
+
+ERRORS = {
+    0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_WORKSPACE",
+    4: "MOE_ERR_CUDA", 5: "MOE_ERR_NONFINITE_LOGITS", 6: "MOE_ERR_DEVICE_TIMEOUT", 7: "MOE_ERR_BAD_METADATA",
+    8: "MOE_ERR_DEVICE",
+}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = f"{where}: {ERRORS.get(code, code)}"
+        if code == 4 and _LIB is not None:
+            msg += f" (cuda error {_LIB.moe_last_cuda_error()})"
+        super().__init__(msg)
+
+
+class moe_routing(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_void_p) for name in (
+        "topk_idx", "topk_score", "tc_counts", "counts", "offsets", "tile_offsets",
+        "row_token", "row_slot", "row_score", "status")]
+
+
+_LIB = None
+_c_int, _c_size, _vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+
+
+def library() -> ctypes.CDLL:
+    """Load libmoe.so from the package directory (built by __graft_entry__.build())."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(_build.LIB):
+        raise ImportError(f"libmoe.so is not built ({_build.LIB}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(_build.LIB)
+    sz = ctypes.POINTER(_c_size)
+    lib.moe_route_capacity.argtypes = [_c_int, _c_int, _c_int, _c_int, sz]
+    lib.moe_route_workspace_size.argtypes = [_c_int, _c_int, _c_int, _c_int, sz]
+    lib.moe_route.argtypes = [_vp, _c_int, _c_int, _c_int, _c_int, ctypes.POINTER(moe_routing), _vp, _c_size,
+                              ctypes.POINTER(ctypes.c_int32), _vp]
+    lib.moe_forward_workspace_size.argtypes = [_c_int] * 5 + [_c_size, sz]
+    lib.moe_forward.argtypes = [_vp, _vp, _vp, ctypes.POINTER(moe_routing)] + [_c_int] * 5 + [_c_size, _vp, _vp, _vp,
+                                                                                              _c_size, _vp]
+    lib.moe_backward_workspace_size.argtypes = [_c_int] * 5 + [_c_size, sz]
+    lib.moe_backward.argtypes = [_vp] * 5 + [ctypes.POINTER(moe_routing)] + [_c_int] * 5 + [_c_size] + [_vp] * 5 + [
+        _c_size, _vp]
+    lib.moe_get_status.argtypes = [ctypes.POINTER(moe_routing), ctypes.POINTER(ctypes.c_int32),
+                                   ctypes.POINTER(ctypes.c_int32), _vp]
+    lib.moe_strerror.argtypes = [_c_int]
+    lib.moe_strerror.restype = ctypes.c_char_p
+    lib.moe_last_cuda_error.argtypes = []
+    lib.moe_kernel_launch_count.argtypes = []
+    lib.moe_kernel_launch_count.restype = ctypes.c_uint64
+    for f in ("moe_route_capacity", "moe_route_workspace_size", "moe_route", "moe_forward_workspace_size",
+              "moe_forward", "moe_backward_workspace_size", "moe_backward", "moe_get_status", "moe_last_cuda_error"):
+        getattr(lib, f).restype = _c_int
+    _LIB = lib
+    return lib
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise MoeError(code, where)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, numel: int | None = None):
+    if not (t.is_cuda and t.is_contiguous() and t.dtype == dtype):
+        raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor, got {t.dtype} {tuple(t.shape)}")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name}: needs {numel} elements, has {t.numel()}")
+
+
+def _mode(mode) -> int:
+    return MODES[mode] if isinstance(mode, str) else int(mode)
+
+
+def moe_route_capacity(T: int, E: int, K: int, mode="tc") -> int:
+    out = _c_size(0)
+    _check(library().moe_route_capacity(T, E, K, _mode(mode), ctypes.byref(out)), "moe_route_capacity")
+    return out.value
+
+
+def moe_route_workspace_size(T: int, E: int, K: int, mode="tc") -> int:
+    out = _c_size(0)
+    _check(library().moe_route_workspace_size(T, E, K, _mode(mode), ctypes.byref(out)), "moe_route_workspace_size")
+    return out.value
+
+
+def moe_forward_workspace_size(T, d, n, E, K, p_cap) -> int:
+    out = _c_size(0)
+    _check(library().moe_forward_workspace_size(T, d, n, E, K, p_cap, ctypes.byref(out)), "moe_forward_workspace_size")
+    return out.value
+
+
+def moe_backward_workspace_size(T, d, n, E, K, p_cap) -> int:
+    out = _c_size(0)
+    _check(library().moe_backward_workspace_size(T, d, n, E, K, p_cap, ctypes.byref(out)),
+           "moe_backward_workspace_size")
+    return out.value
+
+
+class Routing:
+    """Caller-owned routing metadata buffers (torch tensors on one device) and the C struct over them."""
+
+    def __init__(self, T: int, E: int, K: int, mode="tc", device="cuda"):
+        self.T, self.E, self.K, self.mode = T, E, K, _mode(mode)
+        self.p_cap = moe_route_capacity(T, E, K, self.mode)
+        i32 = dict(dtype=torch.int32, device=device)
+        f32 = dict(dtype=torch.float32, device=device)
+        self.topk_idx = torch.empty(T * K, **i32)
+        self.topk_score = torch.empty(T * K, **f32)
+        self.tc_counts = torch.empty(E, **i32)
+        self.counts = torch.empty(E, **i32)
+        self.offsets = torch.empty(E + 1, **i32)
+        self.tile_offsets = torch.empty(E + 1, **i32)
+        self.row_token = torch.empty(self.p_cap, **i32)
+        self.row_slot = torch.empty(self.p_cap, **i32)
+        self.row_score = torch.empty(self.p_cap, **f32)
+        self.status = torch.zeros(STATUS_WORDS, **i32)
+        self.ws = torch.empty(moe_route_workspace_size(T, E, K, self.mode), dtype=torch.uint8, device=device)
+        self.struct = moe_routing(*[t.data_ptr() for t in (
+            self.topk_idx, self.topk_score, self.tc_counts, self.counts, self.offsets, self.tile_offsets,
+            self.row_token, self.row_slot, self.row_score, self.status)])
+
+    def device_status(self, stream=None):
+        """(device error code, P) after synchronising the stream."""
+        code, P = ctypes.c_int32(0), ctypes.c_int32(0)
+        _check(library().moe_get_status(ctypes.byref(self.struct), ctypes.byref(code), ctypes.byref(P),
+                                        _stream(stream)), "moe_get_status")
+        return code.value, P.value
+
+
+def moe_route(logits: torch.Tensor, K: int, mode="tc", routing: Routing | None = None, want_P=False, stream=None):
+    """Routing metadata for fp32 logits [T, E]; returns the Routing (and P when want_P)."""
+    T, E = logits.shape
+    _need(logits, "logits", torch.float32)
+    if routing is None:
+        routing = Routing(T, E, K, mode, logits.device)
+    P = ctypes.c_int32(0)
+    _check(library().moe_route(_ptr(logits), T, E, K, routing.mode, ctypes.byref(routing.struct),
+                               _ptr(routing.ws), routing.ws.numel(), ctypes.byref(P) if want_P else None,
+                               _stream(stream)), "moe_route")
+    return (routing, P.value) if want_P else routing
+
+
+def moe_forward(X, W1, W2, routing: Routing, O=None, H=None, ws=None, stream=None):
+    """O = sum_k s_k SwiGLU(X W1_e) W2_e; returns (O [T, d] bf16, H [P_cap, 2n] bf16)."""
+    T, d = X.shape
+    E, _, n2 = W1.shape
+    n = n2 // 2
+    K, p_cap = routing.K, routing.p_cap
+    bf = torch.bfloat16
+    _need(X, "X", bf, T * d)
+    _need(W1, "W1", bf, E * d * n2)
+    _need(W2, "W2", bf, E * n * d)
+    O = torch.empty((T, d), dtype=bf, device=X.device) if O is None else O
+    H = torch.empty((p_cap, n2), dtype=bf, device=X.device) if H is None else H
+    need = moe_forward_workspace_size(T, d, n, E, K, p_cap)
+    ws = torch.empty(need, dtype=torch.uint8, device=X.device) if ws is None else ws
+    _need(O, "O", bf, T * d)
+    _need(H, "H", bf, p_cap * n2)
+    _check(library().moe_forward(_ptr(X), _ptr(W1), _ptr(W2), ctypes.byref(routing.struct), T, d, n, E, K, p_cap,
+                                 _ptr(O), _ptr(H), _ptr(ws), ws.numel(), _stream(stream)), "moe_forward")
+    return O, H
+
+
+def moe_backward(dO, X, W1, W2, H, routing: Routing, dX=None, dW1=None, dW2=None, dS=None, ws=None, stream=None):
+    """Gradients for upstream dO; returns (dX [T, d], dW1 [E, d, 2n], dW2 [E, n, d], dS [P_cap] fp32)."""
+    T, d = X.shape
+    E, _, n2 = W1.shape
+    n = n2 // 2
+    K, p_cap = routing.K, routing.p_cap
+    bf = torch.bfloat16
+    for t, name in ((dO, "dO"), (X, "X"), (W1, "W1"), (W2, "W2"), (H, "H")):
+        _need(t, name, bf)
+    dev = X.device
+    dX = torch.empty((T, d), dtype=bf, device=dev) if dX is None else dX
+    dW1 = torch.empty((E, d, n2), dtype=bf, device=dev) if dW1 is None else dW1
+    dW2 = torch.empty((E, n, d), dtype=bf, device=dev) if dW2 is None else dW2
+    dS = torch.empty(p_cap, dtype=torch.float32, device=dev) if dS is None else dS
+    need = moe_backward_workspace_size(T, d, n, E, K, p_cap)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev) if ws is None else ws
+    _check(library().moe_backward(_ptr(dO), _ptr(X), _ptr(W1), _ptr(W2), _ptr(H), ctypes.byref(routing.struct),
+                                  T, d, n, E, K, p_cap, _ptr(dX), _ptr(dW1), _ptr(dW2), _ptr(dS), _ptr(ws),
+                                  ws.numel(), _stream(stream)), "moe_backward")
+    return dX, dW1, dW2, dS
+
+
+def kernel_launch_count() -> int:
+    return int(library().moe_kernel_launch_count())

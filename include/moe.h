@@ -1,0 +1,153 @@
+/*
+ * moe.h - C ABI of the GB300 (sm_103a) fine-grained MoE expert layer (SonicMoE hot path).
+ *
+ * The layer, per token t with routed rows r (one row per (token, expert) pair):
+ *     H_r = X_t W1_e            (gate | up, [2n])
+ *     A_r = SiLU(H_r[:n]) * H_r[n:]
+ *     O_t = sum_r s_r A_r W2_e
+ * as set out in "SonicMoE: Accelerating MoE with IO and Tile-aware Optimizations" (ICLR 2026 reading note),
+ * section "Method details / overall framework" (up-projection, down-projection, expert aggregation; dH,
+ * dX~, dX, dW1, dW2), with routing from "Key design 1: Token Rounding routing", the fused epilogues of
+ * "Key design 2: IO-aware fused kernels" and the X/H-only activation cache of "Key design 3:
+ * minimal-activation-cache backward".
+ *
+ * Conventions shared by every call
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library allocates no device memory.
+ *     Tensors are contiguous and row-major.  "bf16" arguments hold IEEE bfloat16 bit patterns (moe_bf16).
+ *   - Every compute call is asynchronous on `stream` (a cudaStream_t passed as void*; NULL = legacy default
+ *     stream) and returns a status code (MOE_OK = 0) for host-side validation and launch errors.  Errors
+ *     found on the device (bad routing metadata, a bounded wait that ran out) are written to the routing
+ *     status block and read with moe_get_status().
+ *   - Shapes: E <= 1024, 1 <= K <= min(E, 32), d % 256 == 0, n % 128 == 0, M_tile = 128.  Other shapes
+ *     return MOE_ERR_UNSUPPORTED_SHAPE.
+ *   - Only an sm_100-family device with compute capability 10.3 is accepted (MOE_ERR_DEVICE otherwise).
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16;
+
+enum moe_status_code {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,        /* null pointer, T/E/K <= 0, K > E, unknown mode                       */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2,  /* shape outside the limits above                                     */
+  MOE_ERR_WORKSPACE = 3,          /* workspace pointer null or smaller than the *_workspace_size query  */
+  MOE_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed (moe_last_cuda_error() has it)   */
+  MOE_ERR_NONFINITE_LOGITS = 5,   /* device: a router logit is NaN or +-inf                             */
+  MOE_ERR_DEVICE_TIMEOUT = 6,     /* device: a bounded pipeline wait ran out; the kernel returned early */
+  MOE_ERR_BAD_METADATA = 7,       /* device: a row's token id or an offset is out of range              */
+  MOE_ERR_DEVICE = 8              /* current device is not compute capability 10.3 (GB300)              */
+};
+
+enum moe_route_mode {
+  MOE_ROUTE_TC = 0,  /* token choice: each token's top-K experts                                   */
+  MOE_ROUTE_TR = 1   /* token rounding: token choice, then each expert's count rounded to M_tile   */
+};
+
+#define MOE_M_TILE 128
+#define MOE_STATUS_WORDS 4
+
+/*
+ * Routing metadata (all device pointers, caller-allocated).  P_cap comes from moe_route_capacity().
+ *   topk_idx   int32 [T*K]   token t's k-th expert, best first (logit descending, expert ascending on ties)
+ *   topk_score fp32  [T*K]   softmax over the token's K selected logits
+ *   tc_counts  int32 [E]     token-choice count f_e of each expert
+ *   counts     int32 [E]     rows per expert (TC: f_e; TR: r_e = round_and_sparsify(f_e))
+ *   offsets    int32 [E+1]   exclusive prefix sum of counts; offsets[E] = P (rows of expert e are
+ *                            [offsets[e], offsets[e+1]), ordered by ascending token id)
+ *   tile_offsets int32 [E+1] exclusive prefix sum of ceil(counts/M_tile) (the grouped-GEMM schedule)
+ *   row_token  int32 [P_cap] token of each row
+ *   row_slot   int32 [P_cap] k with topk_idx[token*K+k] == expert, or -1 for a pair added by rounding
+ *   row_score  fp32  [P_cap] the row's gate score s_r (a pair added by rounding uses its token's
+ *                            token-choice softmax normaliser)
+ *   status     int32 [MOE_STATUS_WORDS]  [0] device error code, [1] P, [2] total M-tiles, [3] reserved
+ * Rows at and beyond P are left untouched.
+ */
+typedef struct moe_routing {
+  int32_t *topk_idx;
+  float *topk_score;
+  int32_t *tc_counts;
+  int32_t *counts;
+  int32_t *offsets;
+  int32_t *tile_offsets;
+  int32_t *row_token;
+  int32_t *row_slot;
+  float *row_score;
+  int32_t *status;
+} moe_routing;
+
+/* Upper bound on P: T*K for TC; T*K + E*M_tile/2 for TR (rounding pads an expert by < M_tile/2 rows). */
+int moe_route_capacity(int T, int E, int K, int mode, size_t *p_cap);
+
+/* Bytes of scratch moe_route needs (per-chunk histograms, membership bitmap, per-token normalisers). */
+int moe_route_workspace_size(int T, int E, int K, int mode, size_t *bytes);
+
+/*
+ * moe_route - routing metadata from router logits ("Key design 1: Token Rounding routing").
+ *   logits  fp32 [T, E] device.  Must be finite (else MOE_ERR_NONFINITE_LOGITS in status[0]).
+ *   mode    MOE_ROUTE_TC or MOE_ROUTE_TR.  TR supports T <= 49152.
+ *   r       filled routing struct; every pointer non-null.  status is cleared by this call.
+ *   ws      device scratch of at least moe_route_workspace_size() bytes (contents need not be zero).
+ *   P_host  optional host pointer: if non-null, the call synchronises `stream` and stores P there.
+ * Bit-exact and deterministic: same logits give the same metadata on every run.
+ */
+int moe_route(const float *logits, int T, int E, int K, int mode, const moe_routing *r, void *ws,
+              size_t ws_bytes, int32_t *P_host, void *stream);
+
+/* Forward scratch: A [P_cap, n] bf16 and the fp32 accumulation buffer of O [T, d]. */
+int moe_forward_workspace_size(int T, int d, int n, int E, int K, size_t p_cap, size_t *bytes);
+
+/*
+ * moe_forward - O = sum_k s_k SwiGLU(X W1_e) W2_e  ("Method details / overall framework").
+ *   X   bf16 [T, d];  W1 bf16 [E, d, 2n] (columns [0,n) gate, [n,2n) up);  W2 bf16 [E, n, d]
+ *   r   routing from moe_route on the same T, E, K
+ *   O   bf16 [T, d] output (a token with no rows gets zeros)
+ *   H   bf16 [P_cap, 2n] output: the pre-activation up-projection, the one per-row tensor kept for the
+ *       backward ("Key design 3"); rows >= P untouched
+ *   ws  scratch of moe_forward_workspace_size() bytes
+ * Y [P, d] is never written: the down-projection adds s_r * A_r W2_e straight into O's fp32 buffer.
+ */
+int moe_forward(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const moe_routing *r, int T,
+                int d, int n, int E, int K, size_t p_cap, moe_bf16 *O, moe_bf16 *H, void *ws,
+                size_t ws_bytes, void *stream);
+
+/* Backward scratch: dH [P_cap, 2n] bf16, s*A [P_cap, n] bf16 and the fp32 accumulation buffer of dX. */
+int moe_backward_workspace_size(int T, int d, int n, int E, int K, size_t p_cap, size_t *bytes);
+
+/*
+ * moe_backward - gradients of the layer for upstream gradient dO, routing held fixed
+ * ("Key design 2" for the dH epilogue, "Key design 3" for the cache).
+ *   dO  bf16 [T, d];  X, W1, W2 as in moe_forward;  H the forward's H output
+ *   dX  bf16 [T, d];  dW1 bf16 [E, d, 2n];  dW2 bf16 [E, n, d]  (an expert with no rows gets zeros)
+ *   dS  fp32 [P_cap]: dL/ds_r per row, computed as <dO_t W2_e^T, SwiGLU(H_r)> without Y or dY
+ *   ws  scratch of moe_backward_workspace_size() bytes
+ */
+int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2,
+                 const moe_bf16 *H, const moe_routing *r, int T, int d, int n, int E, int K, size_t p_cap,
+                 moe_bf16 *dX, moe_bf16 *dW1, moe_bf16 *dW2, float *dS, void *ws, size_t ws_bytes,
+                 void *stream);
+
+/* Synchronise `stream` and read the routing status block: device error code and P (either may be NULL). */
+int moe_get_status(const moe_routing *r, int32_t *code, int32_t *P, void *stream);
+
+/* Human-readable text of a status code (static storage). */
+const char *moe_strerror(int code);
+
+/* The cudaError_t of the last MOE_ERR_CUDA on this thread (0 if none). */
+int moe_last_cuda_error(void);
+
+/* Number of kernels the library launched since load (a counter for benchmarks and tests). */
+uint64_t moe_kernel_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

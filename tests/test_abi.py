@@ -1,0 +1,74 @@
+"""The C ABI without a GPU: the library loads, exports every function include/moe.h declares, and its
+host-side validation returns the documented status codes (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fine_grained_mixture_gb300 as moe
+from fine_grained_mixture_gb300 import build as b
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(moe_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    b.build()
+    return moe.library()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for f in ("moe_route", "moe_forward", "moe_backward", "moe_route_capacity", "moe_get_status"):
+        assert f in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [f for f in declared_functions() if not hasattr(lib, f)]
+    assert not missing, missing
+
+
+def test_capacity_and_workspace_queries(lib):
+    assert moe.moe_route_capacity(24576, 128, 8, "tc") == 24576 * 8
+    assert moe.moe_route_capacity(24576, 128, 8, "tr") == 24576 * 8 + 128 * 64
+    p = moe.moe_route_capacity(512, 8, 2, "tc")
+    fw = moe.moe_forward_workspace_size(512, 256, 128, 8, 2, p)
+    assert fw >= p * 128 * 2 + 512 * 256 * 4
+    bw = moe.moe_backward_workspace_size(512, 256, 128, 8, 2, p)
+    assert bw >= p * 256 * 2 + p * 128 * 2 + 512 * 256 * 4
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, 8, 2, 0), 1), ((16, 8, 9, 0), 1), ((16, 8, 2, 7), 1), ((16, 2000, 2, 0), 2), ((16, 64, 40, 0), 2),
+    ((60000, 8, 2, 1), 2),
+])
+def test_route_validation(lib, args, code):
+    out = ctypes.c_size_t(0)
+    assert lib.moe_route_capacity(*args, ctypes.byref(out)) == code
+
+
+@pytest.mark.parametrize("shape,code", [
+    ((512, 200, 128, 8, 2, 1024), 2),     # d not a multiple of 256
+    ((512, 256, 100, 8, 2, 1024), 2),     # n not a multiple of 128
+    ((512, 256, 128, 8, 2, 1000), 1),     # capacity below T*K
+    ((512, 256, 128, 8, 9, 4096), 1),     # K > E
+])
+def test_layer_validation(lib, shape, code):
+    out = ctypes.c_size_t(0)
+    assert lib.moe_forward_workspace_size(*shape, ctypes.byref(out)) == code
+    assert lib.moe_backward_workspace_size(*shape, ctypes.byref(out)) == code
+
+
+def test_null_arguments_rejected_before_any_device_work(lib):
+    r = moe.moe.moe_routing()
+    assert lib.moe_route(None, 16, 8, 2, 0, ctypes.byref(r), None, 0, None, None) == 1
+    assert lib.moe_forward(None, None, None, ctypes.byref(r), 512, 256, 128, 8, 2, 1024, None, None, None, 0,
+                           None) == 1
+    assert lib.moe_strerror(6) == b"device pipeline wait timed out"

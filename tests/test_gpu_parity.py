@@ -1,0 +1,129 @@
+"""GPU parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Routing: bit-exact integer metadata, scores within 1e-6 relative.  Layer tensors (O, H, dX, dW1, dW2, dS):
+relative Frobenius error <= 1e-2 and max |err| <= 3e-2 * max |ref| per tensor.  Small shapes compare every
+element; the full-size workloads compare sampled tokens, experts and rows that the oracle computes exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+from fine_grained_mixture_gb300 import synth
+from gpu_util import (assert_close, check_routing, f64, oracle_on_rows, run_gpu, to_dev)
+from oracle import moe_oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+ROUTE_CASES = [(name, "tc") for name in synth.WORKLOADS] + [(name, "tr") for name in synth.WORKLOADS]
+
+
+@pytest.mark.parametrize("name,mode", ROUTE_CASES)
+def test_routing_workloads(name, mode):
+    w = synth.WORKLOADS[name]
+    z = synth.make_logits_only(w, 0)
+    import fine_grained_mixture_gb300 as moe
+    rt, P = moe.moe_route(z.cuda(), w.K, mode, want_P=True)
+    code, P2 = rt.device_status()
+    assert code == 0 and P2 == P
+    check_routing(rt, orc.route(z.numpy(), w.K, mode), P)
+
+
+@pytest.mark.parametrize("T,E,K,mode,ties", [
+    (2048, 1024, 32, "tc", False), (2048, 1024, 32, "tr", False), (1, 8, 2, "tc", False), (1, 8, 2, "tr", False),
+    (777, 33, 5, "tc", True), (777, 33, 5, "tr", True), (300, 1, 1, "tr", False), (4099, 64, 8, "tr", True),
+])
+def test_routing_edge_shapes(T, E, K, mode, ties):
+    import fine_grained_mixture_gb300 as moe
+    gen = torch.Generator().manual_seed(T * 7 + E)
+    z = torch.randn((T, E), generator=gen)
+    if ties:
+        z = torch.round(z * 2) / 2          # many equal logits: exercises every tie-break rule
+    rt, P = moe.moe_route(z.cuda(), K, mode, want_P=True)
+    check_routing(rt, orc.route(z.numpy(), K, mode), P)
+
+
+def test_routing_nonfinite_logits_flagged():
+    import fine_grained_mixture_gb300 as moe
+    z = torch.randn((64, 8))
+    z[5, 3] = float("nan")
+    rt = moe.moe_route(z.cuda(), 2, "tc")
+    code, _ = rt.device_status()
+    assert code == 5  # MOE_ERR_NONFINITE_LOGITS
+
+
+def _full_compare(inp, K, mode):
+    g = to_dev(inp)
+    out = run_gpu(g, K, mode)
+    assert out["code"] == 0
+    ref = orc.route(inp["logits"].numpy(), K, mode)
+    check_routing(out["rt"], ref, out["P"])
+    X, W1, W2, dO = (f64(inp[k]) for k in ("X", "W1", "W2", "dO"))
+    fwd, bwd = orc.layer(X, W1, W2, dO, ref)
+    P = out["P"]
+    assert_close("O", f64(out["O"]), fwd["O"])
+    assert_close("H", f64(out["H"][:P]), fwd["H"])
+    assert_close("dS", f64(out["dS"][:P]), bwd["dS"])
+    assert_close("dX", f64(out["dX"]), bwd["dX"])
+    assert_close("dW1", f64(out["dW1"]), bwd["dW1"])
+    assert_close("dW2", f64(out["dW2"]), bwd["dW2"])
+    empty = np.nonzero(ref["counts"] == 0)[0]
+    if len(empty):
+        assert float(out["dW1"][torch.from_numpy(empty).cuda()].abs().max()) == 0.0
+        assert float(out["dW2"][torch.from_numpy(empty).cuda()].abs().max()) == 0.0
+
+
+@pytest.mark.parametrize("mode", ["tc", "tr"])
+def test_layer_tiny_full(mode):
+    w = synth.WORKLOADS["tiny"]
+    _full_compare(synth.make_inputs(w, 0), w.K, mode)
+
+
+@pytest.mark.parametrize("T,d,n,E,K,skew,mode", [
+    (300, 256, 128, 5, 2, False, "tc"),      # ragged tail tiles, T not a multiple of 128
+    (300, 256, 128, 5, 2, False, "tr"),
+    (1000, 512, 256, 16, 4, True, "tc"),     # skewed: experts without tokens, one crowded expert
+    (1000, 512, 256, 16, 4, True, "tr"),
+    (1, 256, 128, 4, 2, False, "tc"),        # a single token
+    (260, 256, 384, 1, 1, False, "tc"),      # one expert holds every token; n = 3 x 128
+    (640, 768, 128, 3, 3, False, "tc"),      # K = E: every token visits every expert
+])
+def test_layer_small_shapes(T, d, n, E, K, skew, mode):
+    w = synth.custom(T, d, n, E, K, skew=skew)
+    _full_compare(synth.make_inputs(w, 1), K, mode)
+
+
+@pytest.mark.parametrize("name,mode", [("fine7b", "tc"), ("fine7b", "tr"), ("coarse", "tc"), ("sparse", "tc"),
+                                       ("sparse", "tr"), ("skew", "tc"), ("skew", "tr")])
+def test_layer_full_size_sampled(name, mode):
+    w = synth.WORKLOADS[name]
+    inp = synth.make_inputs(w, 0)
+    g = to_dev(inp)
+    out = run_gpu(g, w.K, mode)
+    assert out["code"] == 0
+    ref = orc.route(inp["logits"].numpy(), w.K, mode)
+    check_routing(out["rt"], ref, out["P"])
+    rng = np.random.default_rng(0)
+    # tokens: O and dX of sampled tokens need exactly the rows of those tokens
+    toks = rng.choice(w.T, size=48, replace=False)
+    rows = np.nonzero(np.isin(ref["row_token"], toks))[0]
+    _, fwd, bwd = oracle_on_rows(inp, ref, rows)
+    tsel = torch.from_numpy(toks)
+    O_ref = fwd["O"][toks]
+    dX_ref = bwd["dX"][toks]
+    assert_close("O[sampled tokens]", f64(out["O"].cpu()[tsel]), O_ref)
+    assert_close("dX[sampled tokens]", f64(out["dX"].cpu()[tsel]), dX_ref)
+    rsel = torch.from_numpy(rows)
+    assert_close("H[rows of sampled tokens]", f64(out["H"].cpu()[rsel]), fwd["H"])
+    assert_close("dS[rows of sampled tokens]", f64(out["dS"].cpu()[rsel]), bwd["dS"])
+    # experts: the largest and a median non-empty one; empty experts must give exact zeros
+    counts = ref["counts"]
+    live = np.nonzero(counts > 0)[0]
+    picks = [int(np.argmax(counts)), int(live[np.argsort(counts[live])[len(live) // 2]])]
+    for e in picks:
+        erows = np.arange(ref["offsets"][e], ref["offsets"][e + 1])
+        _, fe, be = oracle_on_rows(inp, ref, erows)
+        assert_close(f"dW1[{e}]", f64(out["dW1"][e]), be["dW1"][0])
+        assert_close(f"dW2[{e}]", f64(out["dW2"][e]), be["dW2"][0])
+    for e in np.nonzero(counts == 0)[0][:4]:
+        assert float(out["dW1"][int(e)].abs().max()) == 0.0
+        assert float(out["dW2"][int(e)].abs().max()) == 0.0
