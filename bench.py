@@ -1,0 +1,514 @@
+#!/usr/bin/env python
+"""Throughput benchmark of the fine-grained MoE expert layer (routing + forward + backward) on GB300.
+
+One step = routing (token choice by default) + forward + backward of one MoE layer over one batch of
+seeded synthetic inputs already resident in HBM.  The metric is the layer's nominal FLOPs
+18*T*n*K*d per second (forward 6TnKd, backward 12TnKd), reported in TFLOPS and as a fraction of the
+measured dense BF16 peak.  Default workload: the fine-grained 7B-class layer T=24576, d=1536, n=256,
+E=128, K=8.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload fine7b] [--mode tc|tr]
+  python bench.py --impl reference ...      # the CPU oracle on the host cores, bounded sample per step
+
+Multi-GPU: the layer is run as independent replicas, one per rank (weak scaling, no collective on the
+data path); launch with torchrun, rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from fine_grained_mixture_gb300 import synth  # noqa: E402
+
+METRIC = "MoE layer fwd+bwd TFLOPS (18·T·n·K·d/s) on 1 GB300; % of BF16 dense peak"
+UNIT = "TFLOPS"
+L2_BYTES = 126 * 2**20
+DATA = "synthetic: seeded torch CPU generator; logits ~N(0,1), X/dO ~N(0,1), W1 ~N(0,1/d), W2 ~N(0,1/n), bf16"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="fine7b", choices=list(synth.WORKLOADS))
+    p.add_argument("--mode", default="tc", choices=["tc", "tr"])
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle baseline sample")
+    p.add_argument("--no-extras", action="store_true", help="skip the TR-vs-TC and e2e side measurements")
+    return p.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return dict(hbm=m["hbm_gbs"], bf16=m["bf16_tflops"], bf16_sus=m.get("bf16_tflops_sustained", m["bf16_tflops"]),
+                    src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def layer_flops(w, P=None):
+    rows = w.T * w.K if P is None else P
+    return 6.0 * rows * w.n * w.d, 12.0 * rows * w.n * w.d
+
+
+# ------------------------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) around the timed region; reads clocks and throttle reasons only."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+            except Exception:
+                continue
+        os.unlink(self.path)
+        inside = [r for r in rows if t0 - 0.25 <= r[0] <= t1 + 0.25]
+        use = inside if inside else rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median([r[1] for r in use]) if use else None,
+                "sm_max_mhz": max([r[2] for r in use]) if use else None,
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+# --------------------------------------------------------------------------------------- CPU oracle
+
+
+def oracle_sample(w, inp, ref, experts):
+    """Oracle forward+backward on the rows of `experts` (exact for those experts' rows)."""
+    from oracle import moe_oracle as orc
+
+    rows = np.concatenate([np.arange(ref["offsets"][e], ref["offsets"][e + 1]) for e in experts])
+    ex_list = np.array(sorted(set(int(e) for e in experts)))
+    remap = {e: i for i, e in enumerate(ex_list)}
+    tok = ref["row_token"][rows]
+    ex = np.array([remap[int(e)] for e in ref["row_expert"][rows]], dtype=np.int64)
+    sc = ref["row_score"][rows]
+    W1 = inp["W1_64"][ex_list]
+    W2 = inp["W2_64"][ex_list]
+    fwd = orc.forward(inp["X_64"], W1, W2, tok, ex, sc)
+    orc.backward(inp["dO_64"], inp["X_64"], W1, W2, tok, ex, sc, fwd)
+    return len(rows)
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+def prepare_oracle_inputs(w, inp, mode):
+    from oracle import moe_oracle as orc
+
+    ref = orc.route(inp["logits"].numpy(), w.K, mode)
+    ref_inp = {"X_64": inp["X"].double().numpy(), "dO_64": inp["dO"].double().numpy(),
+               "W1_64": inp["W1"].double().numpy(), "W2_64": inp["W2"].double().numpy()}
+    return ref, ref_inp
+
+
+def cpu_baseline(w, inp, mode, budget_s):
+    ref, ref_inp = prepare_oracle_inputs(w, inp, mode)
+    oracle_sample(w, ref_inp, ref, [0])  # warm the BLAS threads
+    t0 = time.perf_counter()
+    rows = 0
+    used = []
+    for e in range(w.E):
+        rows += oracle_sample(w, ref_inp, ref, [e])
+        used.append(e)
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    flops = 18.0 * rows * w.n * w.d
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"fp64 NumPy oracle forward+backward on the rows of experts 0..{used[-1]} "
+                      f"({rows} of {ref['P']} routed rows, {dt:.1f} s) of the {w.name} layer; routing untimed"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w = synth.WORKLOADS[args.workload]
+    inp = synth.make_inputs(w, seed=0)
+    ref, ref_inp = prepare_oracle_inputs(w, inp, args.mode)
+    per_step = 4
+    nsteps = args.warmup + args.steps
+    rows_timed = 0
+    t_timed = 0.0
+    for i in range(nsteps):
+        experts = [(i * per_step + j) % w.E for j in range(per_step)]
+        t0 = time.perf_counter()
+        r = oracle_sample(w, ref_inp, ref, experts)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            rows_timed += r
+            t_timed += dt
+    flops = 18.0 * rows_timed * w.n * w.d
+    value = flops / t_timed / 1e12
+    sample = (f"fp64 NumPy oracle forward+backward on the rows of {per_step} experts per step "
+              f"(experts cycled) of the {w.name} layer; routing untimed")
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * t_timed / max(args.steps, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": DATA, "impl": "reference",
+            "config": {"workload": f"{w.name}: T={w.T}, d={w.d}, n={w.n}, E={w.E}, K={w.K}, routing={args.mode}",
+                       "sample_per_step": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------------------- GPU arm
+
+
+class Layer:
+    """Resident device buffers for one workload and the step = route + forward + backward."""
+
+    def __init__(self, w, inp, mode, dev):
+        import fine_grained_mixture_gb300 as moe
+
+        self.moe, self.w, self.mode = moe, w, mode
+        self.g = {k: v.to(dev) for k, v in inp.items()}
+        self.rt = moe.Routing(w.T, w.E, w.K, mode, dev)
+        p = self.rt.p_cap
+        bf = torch.bfloat16
+        self.O = torch.empty((w.T, w.d), dtype=bf, device=dev)
+        self.H = torch.empty((p, 2 * w.n), dtype=bf, device=dev)
+        self.dX = torch.empty((w.T, w.d), dtype=bf, device=dev)
+        self.dW1 = torch.empty((w.E, w.d, 2 * w.n), dtype=bf, device=dev)
+        self.dW2 = torch.empty((w.E, w.n, w.d), dtype=bf, device=dev)
+        self.dS = torch.empty(p, dtype=torch.float32, device=dev)
+        self.wsf = torch.empty(moe.moe_forward_workspace_size(w.T, w.d, w.n, w.E, w.K, p), dtype=torch.uint8, device=dev)
+        self.wsb = torch.empty(moe.moe_backward_workspace_size(w.T, w.d, w.n, w.E, w.K, p), dtype=torch.uint8,
+                               device=dev)
+
+    def route(self):
+        self.moe.moe_route(self.g["logits"], self.w.K, self.mode, routing=self.rt)
+
+    def forward(self):
+        self.moe.moe_forward(self.g["X"], self.g["W1"], self.g["W2"], self.rt, O=self.O, H=self.H, ws=self.wsf)
+
+    def backward(self):
+        self.moe.moe_backward(self.g["dO"], self.g["X"], self.g["W1"], self.g["W2"], self.H, self.rt, dX=self.dX,
+                              dW1=self.dW1, dW2=self.dW2, dS=self.dS, ws=self.wsb)
+
+    def step(self):
+        self.route()
+        self.forward()
+        self.backward()
+
+    def cached_bytes(self):
+        """Bytes that live from forward to backward: X, H (P rows) and the routing metadata."""
+        code, P = self.rt.device_status()
+        meta = sum(t.numel() * t.element_size() for t in (
+            self.rt.topk_idx, self.rt.topk_score, self.rt.tc_counts, self.rt.counts, self.rt.offsets,
+            self.rt.tile_offsets, self.rt.row_token, self.rt.row_slot, self.rt.row_score, self.rt.status))
+        return dict(X=self.g["X"].numel() * 2, H_rows=P * 2 * self.w.n * 2, H_alloc=self.H.numel() * 2, meta=meta, P=P)
+
+
+def time_steps(layer, steps, split=False):
+    """Times `steps` back-to-back steps with CUDA events on the current stream."""
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    marks = []
+    ev[0].record()
+    for _ in range(steps):
+        if split:
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            e[0].record()
+            layer.route()
+            e[1].record()
+            layer.forward()
+            e[2].record()
+            layer.backward()
+            e[3].record()
+            marks.append(e)
+        else:
+            layer.step()
+    ev[1].record()
+    torch.cuda.synchronize()
+    total = ev[0].elapsed_time(ev[1])
+    parts = None
+    if split:
+        parts = [sum(m[i].elapsed_time(m[i + 1]) for m in marks) for i in range(3)]
+    return total, parts
+
+
+def kernel_flops_bytes(name, w, P):
+    """Algorithmic FLOPs (GEMM kernels) or bytes (memory-bound kernels) of one launch."""
+    n, d, T, E, K = w.n, w.d, w.T, w.E, w.K
+    flops = {"gemm_up": 4.0 * P * n * d, "gemm_down": 2.0 * P * n * d, "gemm_dh": 2.0 * P * n * d,
+             "gemm_dx": 4.0 * P * n * d, "gemm_dw1": 4.0 * P * n * d, "gemm_dw2": 2.0 * P * n * d}
+    if name in flops:
+        return "tensor", flops[name]
+    nbytes = {"cast_f32_bf16": T * d * 6.0, "route_topk": T * E * 4.0 + T * K * 8.0 + T * 8.0,
+              "route_fill_tc": T * K * 8.0 + P * 12.0, "route_fill_tr": T * E * 4.0 + P * 12.0,
+              "route_scan": 0.0}
+    return "hbm", nbytes.get(name, 0.0)
+
+
+def load_traffic(kernel, workload):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if taken on the current source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            table = json.load(f)
+    except Exception:
+        return None
+    ent = table.get(kernel, {}).get(workload)
+    if not ent:
+        return None
+    if ent.get("source_sha") != source_sha():
+        return None
+    return ent.get("bytes_per_launch")
+
+
+def source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fine_grained_mixture_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from fine_grained_mixture_gb300 import build as _b
+    _b.build()
+    import fine_grained_mixture_gb300 as moe
+
+    w = synth.WORKLOADS[args.workload]
+    pk = peaks()
+    inp = synth.make_inputs(w, seed=rank)
+    layer = Layer(w, inp, args.mode, dev)
+    for _ in range(max(args.warmup, 3)):
+        layer.step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = moe.kernel_launch_count()
+    moe.profile_enable(True)
+    t0 = time.time()
+    total_ms, parts = time_steps(layer, args.steps, split=True)
+    t1 = time.time()
+    moe.profile_enable(False)
+    launches = moe.kernel_launch_count() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop(t0, t1)
+    prof = moe.profile_summary()
+
+    ms_local = total_ms / args.steps
+    ms = ms_local
+    if world > 1:
+        t = torch.tensor([ms_local], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ff, fb = layer_flops(w)
+    value = world * (ff + fb) / (ms * 1e-3) / 1e12
+    cache = layer.cached_bytes()
+    P = cache["P"]
+
+    # roofline of the dominant kernel (largest share of the timed region)
+    kern = {}
+    for name, (n_launch, tot) in prof.items():
+        bound, work = kernel_flops_bytes(name, w, P)
+        avg = tot / n_launch
+        kern[name] = {"launches_per_step": n_launch / args.steps, "ms_per_launch": avg,
+                      "share": tot / sum(v[1] for v in prof.values()),
+                      ("tflops" if bound == "tensor" else "gbs"): (work / (avg * 1e-3) / (1e12 if bound == "tensor" else 1e9))}
+    top = max(prof.items(), key=lambda kv: kv[1][1])[0]
+    bound, work = kernel_flops_bytes(top, w, P)
+    avg_ms = prof[top][1] / prof[top][0]
+    if bound == "tensor":
+        achieved = work / (avg_ms * 1e-3) / 1e12
+        peak = pk["bf16_sus"]
+        roof = {"bound": "tensor", "kernel": top, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": load_traffic(top, w.name),
+                "algorithmic_per_launch": work, "peak_kind": f"{pk['src']} sustained bf16 (kernel timed inside the step loop)"}
+    else:
+        achieved = work / (avg_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": top, "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                "frac": achieved / pk["hbm"], "traffic": load_traffic(top, w.name), "algorithmic_per_launch": work,
+                "peak_kind": f"{pk['src']} HBM copy bandwidth"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": DATA,
+        "config": {"workload": f"{w.name}: T={w.T}, d={w.d}, n={w.n}, E={w.E}, K={w.K}, routing={args.mode}, "
+                               f"M_tile=128", "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": f"inputs larger than L2: one step touches ~{(2*w.T*w.d*3 + 6*w.E*w.d*w.n*2 + 12*P*w.n)/2**30:.1f} GiB"
+                         f" vs {L2_BYTES/2**20:.0f} MiB L2; no flush"},
+        "frac_of_peak": {"burst": value / world / pk["bf16"], "sustained": value / world / pk["bf16_sus"],
+                         "peak_source": pk["src"]},
+        "fwd_tflops": ff / ((parts[0] + parts[1]) / args.steps * 1e-3) / 1e12,
+        "bwd_tflops": fb / (parts[2] / args.steps * 1e-3) / 1e12,
+        "split_ms_per_step": {"route": parts[0] / args.steps, "forward": parts[1] / args.steps,
+                              "backward": parts[2] / args.steps},
+        "activation_bytes": {"cached_X_H_meta": cache["X"] + cache["H_rows"] + cache["meta"],
+                             "bound_2Td_4TKn_plus_meta": 2 * w.T * w.d + 4 * w.T * w.K * w.n + cache["meta"],
+                             "metadata": cache["meta"]},
+        "roofline": roof,
+        "kernels": kern,
+        "clocks": clocks,
+        "gpu_launches": launches,
+    }
+
+    if not args.no_extras:
+        line["e2e"] = e2e_measure(layer, inp, args, world, dev)
+        if rank == 0 and world == 1:
+            line["tr_vs_tc"] = tr_vs_tc(args, dev)
+    if rank == 0 and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w, inp, args.mode, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def e2e_measure(layer, inp, args, world, dev):
+    """Same metric through the public API with host buffers: per step H2D of the step's activations
+    (logits, X, dO) from pinned memory, the layer, and D2H of its results (O, dX)."""
+    w = layer.w
+    host_in = {k: inp[k].pin_memory() for k in ("logits", "X", "dO")}
+    host_out = {k: torch.empty((w.T, w.d), dtype=torch.bfloat16).pin_memory() for k in ("O", "dX")}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def one():
+        for k, t in host_in.items():
+            layer.g[k].copy_(t, non_blocking=True)
+        layer.step()
+        host_out["O"].copy_(layer.O, non_blocking=True)
+        host_out["dX"].copy_(layer.dX, non_blocking=True)
+
+    for _ in range(max(args.warmup, 3)):
+        one()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ff, fb = layer_flops(w)
+    return {"value": world * (ff + fb) / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "note": "weights and weight gradients stay resident in HBM; activations cross PCIe/C2C each step"}
+
+
+def tr_vs_tc(args, dev):
+    """Token rounding vs token choice on the high-sparsity layer (T=16384, d=1536, n=256, E=256, K=4)."""
+    w = synth.WORKLOADS["sparse"]
+    inp = synth.make_inputs(w, seed=0)
+    out = {}
+    for mode in ("tc", "tr"):
+        layer = Layer(w, inp, mode, dev)
+        for _ in range(3):
+            layer.step()
+        torch.cuda.synchronize()
+        total, _ = time_steps(layer, max(args.steps, 20))
+        ms = total / max(args.steps, 20)
+        code, P = layer.rt.device_status()
+        ff, fb = layer_flops(w)
+        fa, fba = layer_flops(w, P)
+        tc_counts = layer.rt.tc_counts.cpu().numpy()
+        counts = layer.rt.counts.cpu().numpy()
+        tiles = int(np.sum(-(-counts // 128)))
+        out[mode] = {"ms_per_step": ms, "tflops_nominal_TK": (ff + fb) / (ms * 1e-3) / 1e12,
+                     "tflops_actual_P": (fa + fba) / (ms * 1e-3) / 1e12, "P": P, "m_tiles": tiles,
+                     "max_abs_count_deviation": int(np.abs(counts - tc_counts).max())}
+        del layer
+        torch.cuda.empty_cache()
+    out["speedup_tr_over_tc"] = out["tc"]["ms_per_step"] / out["tr"]["ms_per_step"]
+    out["workload"] = f"sparse: T={w.T}, d={w.d}, n={w.n}, E={w.E}, K={w.K}"
+    return out
+
+
+if __name__ == "__main__":
+    sys.exit(main())

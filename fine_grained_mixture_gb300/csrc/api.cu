@@ -2,6 +2,9 @@
 // encoding and the launch sequence of each call.  See include/moe.h for the contract of every function.
 #include <atomic>
 #include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
 
 #include "internal.h"
 
@@ -21,6 +24,55 @@ int record_cu_error(CUresult res) {
 }
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+namespace {
+struct ProfRec {
+  const char *name;
+  cudaEvent_t start, stop;
+};
+struct ProfState {
+  std::mutex mu;
+  bool enabled = false;
+  std::vector<ProfRec> recs;       // recorded this session, in launch order
+  std::vector<cudaEvent_t> pool;   // events reused across sessions
+  size_t pool_used = 0;
+  struct Agg {
+    std::string name;
+    int launches;
+    double total_ms;
+  };
+  std::vector<Agg> summary;
+};
+ProfState &prof() {
+  static ProfState p;
+  return p;
+}
+cudaEvent_t prof_event(ProfState &p) {
+  if (p.pool_used == p.pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    p.pool.push_back(e);
+  }
+  return p.pool[p.pool_used++];
+}
+}  // namespace
+
+void prof_begin(const char *name, cudaStream_t s) {
+  ProfState &p = prof();
+  if (!p.enabled) return;
+  std::lock_guard<std::mutex> lk(p.mu);
+  ProfRec r{name, prof_event(p), prof_event(p)};
+  if (!r.start || !r.stop) return;
+  cudaEventRecord(r.start, s);
+  p.recs.push_back(r);
+}
+
+void prof_end(cudaStream_t s) {
+  ProfState &p = prof();
+  if (!p.enabled) return;
+  std::lock_guard<std::mutex> lk(p.mu);
+  if (!p.recs.empty()) cudaEventRecord(p.recs.back().stop, s);
+}
 
 constexpr int kMaxDevices = 64;
 
@@ -316,5 +368,52 @@ const char *moe_strerror(int code) {
 int moe_last_cuda_error(void) { return g_last_cuda_error; }
 
 uint64_t moe_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int moe_profile_enable(int on) {
+  ProfState &p = prof();
+  std::lock_guard<std::mutex> lk(p.mu);
+  if (on) {
+    p.recs.clear();
+    p.summary.clear();
+    p.pool_used = 0;
+    p.enabled = true;
+    return MOE_OK;
+  }
+  p.enabled = false;
+  // aggregate the session: per kernel name, launches and summed event time
+  p.summary.clear();
+  for (const ProfRec &r : p.recs) {
+    cudaError_t err = cudaEventSynchronize(r.stop);
+    if (err != cudaSuccess) return record_cuda_error(err);
+    float ms = 0.f;
+    err = cudaEventElapsedTime(&ms, r.start, r.stop);
+    if (err != cudaSuccess) return record_cuda_error(err);
+    size_t i = 0;
+    while (i < p.summary.size() && p.summary[i].name != r.name) ++i;
+    if (i == p.summary.size()) p.summary.push_back({r.name, 0, 0.0});
+    p.summary[i].launches += 1;
+    p.summary[i].total_ms += ms;
+  }
+  p.recs.clear();
+  p.pool_used = 0;
+  return MOE_OK;
+}
+
+int moe_profile_count(void) {
+  ProfState &p = prof();
+  std::lock_guard<std::mutex> lk(p.mu);
+  return static_cast<int>(p.summary.size());
+}
+
+int moe_profile_entry(int i, char *name, size_t name_len, int *launches, double *total_ms) {
+  ProfState &p = prof();
+  std::lock_guard<std::mutex> lk(p.mu);
+  if (i < 0 || static_cast<size_t>(i) >= p.summary.size() || !name || name_len == 0) return MOE_ERR_INVALID_ARG;
+  std::strncpy(name, p.summary[i].name.c_str(), name_len - 1);
+  name[name_len - 1] = 0;
+  if (launches) *launches = p.summary[i].launches;
+  if (total_ms) *total_ms = p.summary[i].total_ms;
+  return MOE_OK;
+}
 
 }  // extern "C"

@@ -19,7 +19,9 @@ __global__ void __launch_bounds__(256) f32_to_bf16_kernel(const float4 *__restri
 int launch_f32_to_bf16(const float *src, void *dst, size_t count, cudaStream_t s) {
   const size_t n4 = count / 4;  // count is a multiple of 256 (d % 256 == 0)
   const int blocks = num_sms() * 8;
+  prof_begin("cast_f32_bf16", s);
   f32_to_bf16_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4 *>(src), reinterpret_cast<uint2 *>(dst), n4);
+  prof_end(s);
   count_launch();
   const cudaError_t err = cudaGetLastError();
   return err == cudaSuccess ? MOE_OK : record_cuda_error(err);

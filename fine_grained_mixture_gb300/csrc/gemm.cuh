@@ -522,7 +522,10 @@ int launch_gemm(const GemmArgs &a, const TensorMaps &tm, cudaStream_t stream) {
     if (err != cudaSuccess) return record_cuda_error(err);
     attr_dev = dev;
   }
+  static const char *const kNames[] = {"gemm_up", "gemm_down", "gemm_dh", "gemm_dx", "gemm_dw1", "gemm_dw2"};
+  prof_begin(kNames[MODE], stream);
   moe_gemm_kernel<MODE, BN, STAGES><<<num_sms(), kGemmThreads, SM::kBytes, stream>>>(tm.a, tm.b, a);
+  prof_end(stream);
   count_launch();
   err = cudaGetLastError();
   if (err != cudaSuccess) return record_cuda_error(err);

@@ -19,6 +19,10 @@ int record_cuda_error(cudaError_t err);
 int record_cu_error(CUresult res);
 void count_launch();
 
+// Optional per-kernel CUDA-event timing (off unless moe_profile_enable(1)): brackets one kernel launch.
+void prof_begin(const char *name, cudaStream_t s);
+void prof_end(cudaStream_t s);
+
 // routing (route.cu)
 size_t route_workspace_bytes(int T, int E, int K, int mode);
 int launch_route(const float *logits, int T, int E, int K, int mode, const moe_routing *r, void *ws,

@@ -355,6 +355,7 @@ int launch_route(const float *logits, int T, int E, int K, int mode, const moe_r
   route_topk_kernel<NV><<<w.nchunks, 256, hist_smem, stream>>>(logits, T, E, K, want_member, r->topk_idx,          \
                                                                r->topk_score, w.tok_max, w.tok_den, w.chunk_cnt, \
                                                                w.member, w.member_words, r->status)
+  prof_begin("route_topk", stream);
   if (nv <= 1) MOE_TOPK_LAUNCH(1);
   else if (nv <= 2) MOE_TOPK_LAUNCH(2);
   else if (nv <= 4) MOE_TOPK_LAUNCH(4);
@@ -362,11 +363,15 @@ int launch_route(const float *logits, int T, int E, int K, int mode, const moe_r
   else if (nv <= 16) MOE_TOPK_LAUNCH(16);
   else MOE_TOPK_LAUNCH(32);
 #undef MOE_TOPK_LAUNCH
+  prof_end(stream);
   count_launch();
+  prof_begin("route_scan", stream);
   route_scan_kernel<<<1, 1024, 0, stream>>>(T, E, w.nchunks, mode, MOE_M_TILE, w.chunk_cnt, w.chunk_base,
                                             r->tc_counts, r->counts, r->offsets, r->tile_offsets, r->status);
+  prof_end(stream);
   count_launch();
   if (mode == MOE_ROUTE_TC) {
+    prof_begin("route_fill_tc", stream);
     route_fill_tc_kernel<<<w.nchunks, kChunk, (size_t)E * 8 * 4, stream>>>(
         T, E, K, r->topk_idx, r->topk_score, w.chunk_base, r->offsets, r->row_token, r->row_slot, r->row_score);
   } else {
@@ -380,10 +385,12 @@ int launch_route(const float *logits, int T, int E, int K, int mode, const moe_r
       if (err != cudaSuccess) return record_cuda_error(err);
       attr_set_dev = dev;
     }
+    prof_begin("route_fill_tr", stream);
     route_fill_tr_kernel<<<E, 1024, smem, stream>>>(logits, T, E, K, r->topk_idx, r->topk_score, w.tok_max, w.tok_den,
                                                     w.member, w.member_words, r->tc_counts, r->counts, r->offsets,
                                                     r->row_token, r->row_slot, r->row_score);
   }
+  prof_end(stream);
   count_launch();
   err = cudaGetLastError();
   if (err != cudaSuccess) return record_cuda_error(err);

@@ -71,6 +71,12 @@ def library() -> ctypes.CDLL:
     lib.moe_last_cuda_error.argtypes = []
     lib.moe_kernel_launch_count.argtypes = []
     lib.moe_kernel_launch_count.restype = ctypes.c_uint64
+    lib.moe_profile_enable.argtypes = [_c_int]
+    lib.moe_profile_count.argtypes = []
+    lib.moe_profile_entry.argtypes = [_c_int, ctypes.c_char_p, _c_size, ctypes.POINTER(_c_int),
+                                      ctypes.POINTER(ctypes.c_double)]
+    for f in ("moe_profile_enable", "moe_profile_count", "moe_profile_entry"):
+        getattr(lib, f).restype = _c_int
     for f in ("moe_route_capacity", "moe_route_workspace_size", "moe_route", "moe_forward_workspace_size",
               "moe_forward", "moe_backward_workspace_size", "moe_backward", "moe_get_status", "moe_last_cuda_error"):
         getattr(lib, f).restype = _c_int
@@ -217,3 +223,20 @@ def moe_backward(dO, X, W1, W2, H, routing: Routing, dX=None, dW1=None, dW2=None
 
 def kernel_launch_count() -> int:
     return int(library().moe_kernel_launch_count())
+
+
+def profile_enable(on: bool):
+    """Start (clearing old results) or stop per-kernel CUDA-event timing inside the library."""
+    _check(library().moe_profile_enable(1 if on else 0), "moe_profile_enable")
+
+
+def profile_summary() -> dict:
+    """{kernel name: (launches, total ms)} of the last finished profiling session."""
+    lib = library()
+    out = {}
+    buf = ctypes.create_string_buffer(64)
+    for i in range(lib.moe_profile_count()):
+        n, ms = _c_int(0), ctypes.c_double(0.0)
+        _check(lib.moe_profile_entry(i, buf, 64, ctypes.byref(n), ctypes.byref(ms)), "moe_profile_entry")
+        out[buf.value.decode()] = (n.value, ms.value)
+    return out

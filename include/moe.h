@@ -146,6 +146,18 @@ int moe_last_cuda_error(void);
 /* Number of kernels the library launched since load (a counter for benchmarks and tests). */
 uint64_t moe_kernel_launch_count(void);
 
+/*
+ * Per-kernel timing for benchmarks.  moe_profile_enable(1) clears earlier results and, until
+ * moe_profile_enable(0), brackets every kernel the library launches with two CUDA events on the launch
+ * stream.  moe_profile_enable(0) waits for those events and aggregates them per kernel name; the summary is
+ * then read with moe_profile_count() and moe_profile_entry(i, ...) (name copied NUL-terminated into a
+ * caller buffer of name_len bytes, number of launches, summed milliseconds).  Off by default; the host
+ * cost is two event records per launch while on.
+ */
+int moe_profile_enable(int on);
+int moe_profile_count(void);
+int moe_profile_entry(int i, char *name, size_t name_len, int *launches, double *total_ms);
+
 #ifdef __cplusplus
 }
 #endif
