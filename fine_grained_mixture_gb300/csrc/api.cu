@@ -250,9 +250,11 @@ int moe_forward(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const
 
   GemmArgs a = base_args(r, T, d, n, E, p_cap);
   TensorMaps tm;
-  // up-projection: H = X[tok] W1_e (N = 2n, K = d)
-  if ((rc = make_tmap_bf16(&tm.a, X, d, T, 1)) != MOE_OK) return rc;
+  // up-projection: H = X[tok] W1_e (N = 2n, K = d); X rows are gathered with cp.async
   if ((rc = make_tmap_bf16(&tm.b, W1, 2 * (uint64_t)n, (uint64_t)E * d, 64)) != MOE_OK) return rc;
+  tm.a = tm.b;  // unused by this GEMM
+  a.gsrc = X;
+  a.gld = d;
   a.Ndim = 2 * n;
   a.Kdim = d;
   a.out0 = H;
@@ -265,6 +267,7 @@ int moe_forward(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const
   a.Kdim = n;
   a.out0 = nullptr;
   a.out1 = nullptr;
+  a.gsrc = nullptr;
   a.out_f32 = O32;
   if ((rc = launch_down(a, tm, s)) != MOE_OK) return rc;
   return launch_f32_to_bf16(O32, O, (size_t)T * d, s);
@@ -303,8 +306,10 @@ int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, cons
   TensorMaps tm;
   // dH: dA' = dO[tok] W2_e^T (N = n, K = d); epilogue dSwiGLU, dS, s*A
   const int bn = (n % 256 == 0) ? 256 : 128;
-  if ((rc = make_tmap_bf16(&tm.a, dO, d, T, 1)) != MOE_OK) return rc;
   if ((rc = make_tmap_bf16(&tm.b, W2, d, (uint64_t)E * n, bn)) != MOE_OK) return rc;
+  tm.a = tm.b;  // unused: dO rows are gathered with cp.async
+  a.gsrc = dO;
+  a.gld = d;
   a.Ndim = n;
   a.Kdim = d;
   a.out0 = dH;
@@ -321,20 +326,26 @@ int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, cons
   ax.out_f32 = dX32;
   if ((rc = launch_dx(ax, tm, s)) != MOE_OK) return rc;
   if ((rc = launch_f32_to_bf16(dX32, dX, (size_t)T * d, s)) != MOE_OK) return rc;
-  // dW1_e = X[tok]^T dH_e (M = d, N = 2n, K = rows of e)
-  if ((rc = make_tmap_bf16(&tm.a, X, d, T, 1)) != MOE_OK) return rc;
-  if ((rc = make_tmap_bf16(&tm.b, dH, 2 * (uint64_t)n, p_cap, 1)) != MOE_OK) return rc;
+  // rows [P, P_cap) of dH and s*A are read as the zero tail of the last expert's k-blocks
+  if ((rc = launch_zero_tail(dH, sA, r->offsets, E, p_cap, 2 * n, n, s)) != MOE_OK) return rc;
+  // dW1_e = X[tok]^T dH_e (M = d, N = 2n, K = rows of e); X rows gathered with cp.async
+  if ((rc = make_tmap_bf16(&tm.b, dH, 2 * (uint64_t)n, p_cap, 64)) != MOE_OK) return rc;
+  tm.a = tm.b;
   GemmArgs aw = base_args(r, T, d, n, E, p_cap);
   aw.Mdim = d;
   aw.Ndim = 2 * n;
   aw.out0 = dW1;
+  aw.gsrc = X;
+  aw.gld = d;
   if ((rc = launch_dw1(aw, tm, s)) != MOE_OK) return rc;
-  // dW2_e = (s*A)_e^T dO[tok] (M = n, N = d, K = rows of e)
-  if ((rc = make_tmap_bf16(&tm.a, sA, n, p_cap, 1)) != MOE_OK) return rc;
-  if ((rc = make_tmap_bf16(&tm.b, dO, d, T, 1)) != MOE_OK) return rc;
+  // dW2_e = (s*A)_e^T dO[tok] (M = n, N = d, K = rows of e); dO rows gathered with cp.async
+  if ((rc = make_tmap_bf16(&tm.a, sA, n, p_cap, 64)) != MOE_OK) return rc;
+  tm.b = tm.a;
   aw.Mdim = n;
   aw.Ndim = d;
   aw.out0 = dW2;
+  aw.gsrc = dO;
+  aw.gld = d;
   return launch_dw2(aw, tm, s);
 }
 

@@ -27,4 +27,29 @@ int launch_f32_to_bf16(const float *src, void *dst, size_t count, cudaStream_t s
   return err == cudaSuccess ? MOE_OK : record_cuda_error(err);
 }
 
+__global__ void __launch_bounds__(256) zero_tail_kernel(uint4 *__restrict__ a, uint4 *__restrict__ b,
+                                                        const int32_t *__restrict__ offsets, int E, size_t p_cap,
+                                                        int ld_a, int ld_b) {
+  const size_t P = static_cast<size_t>(offsets[E]);
+  if (P >= p_cap) return;
+  const size_t va = ld_a / 8, vb = ld_b / 8;  // uint4 per row
+  const size_t na = (p_cap - P) * va, nb = (p_cap - P) * vb;
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < na + nb; i += (size_t)gridDim.x * blockDim.x) {
+    if (i < na) a[P * va + i] = z;
+    else b[P * vb + (i - na)] = z;
+  }
+}
+
+int launch_zero_tail(void *a, void *b, const int32_t *offsets, int E, size_t p_cap, int ld_a, int ld_b,
+                     cudaStream_t s) {
+  prof_begin("zero_tail", s);
+  zero_tail_kernel<<<num_sms(), 256, 0, s>>>(static_cast<uint4 *>(a), static_cast<uint4 *>(b), offsets, E, p_cap,
+                                             ld_a, ld_b);
+  prof_end(s);
+  count_launch();
+  const cudaError_t err = cudaGetLastError();
+  return err == cudaSuccess ? MOE_OK : record_cuda_error(err);
+}
+
 }  // namespace moe

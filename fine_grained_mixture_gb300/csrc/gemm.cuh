@@ -14,8 +14,11 @@
 //   kDW1  dW1_e = X[tok]^T dH   (reduction over the expert's rows)                  M=d     N=2n  K=rows
 //   kDW2  dW2_e = (sA)^T dO[tok]                                                    M=n     N=d   K=rows
 //
-// CTA = 6 warps: warp 0 issues TMA (tiled loads for dense operands, tile::gather4 for token-indexed rows),
-// warp 1 owns TMEM and one elected lane issues tcgen05.mma, warps 2..5 drain TMEM in the epilogue.
+// CTA = 6 or 10 warps: warp 0 issues TMA tiled loads of the dense operands, warp 1 owns TMEM and one
+// elected lane issues tcgen05.mma, warps 2..5 drain TMEM in the epilogue, and in the four GEMMs that read
+// rows by token id warps 6..9 gather those rows with 16-byte cp.async into the 128-byte-swizzled layout
+// (a TMA gather costs one request per 128-byte row, which starves the tensor cores here; the LSU path
+// moves the same rows at a fraction of the issue cost).
 // Tiles: 128 x BN x 64, STAGES-deep shared-memory ring, two TMEM accumulators of BN fp32 columns.
 // Every wait is bounded; on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT, drains its own copies and
 // MMAs, frees TMEM and returns.
@@ -30,17 +33,23 @@ enum GemmMode : int { kUp = 0, kDown = 1, kDH = 2, kDX = 3, kDW1 = 4, kDW2 = 5 }
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kGemmThreads = 192;
 constexpr int kABytes = kBM * kBK * 2;  // 16 KB per stage
 
 template <int MODE>
 struct Traits {
   static constexpr bool varlen_k = (MODE == kDW1 || MODE == kDW2);
-  static constexpr bool a_gather = (MODE == kUp || MODE == kDH);  // A rows fetched by token id
-  static constexpr bool a_mn = varlen_k;                          // A operand MN-major in shared memory
+  static constexpr bool gather_a_k = (MODE == kUp || MODE == kDH);  // A: token rows, K-major
+  static constexpr bool gather_a_mn = (MODE == kDW1);                // A: token rows along K, MN-major
+  static constexpr bool gather_b_mn = (MODE == kDW2);                // B: token rows along K, MN-major
+  static constexpr bool gather = gather_a_k || gather_a_mn || gather_b_mn;
+  static constexpr int threads = gather ? 320 : 192;
+  static constexpr bool a_mn = varlen_k;  // A operand MN-major in shared memory
   static constexpr bool b_mn = (MODE == kUp || MODE == kDown || varlen_k);
   static constexpr bool nt_outer = (MODE == kDown || MODE == kDX);  // keep one fp32 column slab hot in L2
 };
+
+constexpr int kGatherThreads = 128;
+constexpr int kGatherLag = 2;  // stages a gather thread keeps in flight before it signals the oldest
 
 template <int BN, int STAGES>
 struct Smem {
@@ -121,7 +130,7 @@ __device__ __forceinline__ int token_or_oob(const GemmArgs &a, int r, int row_en
 }
 
 template <int MODE, int BN, int STAGES>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmArgs a) {
   using TR = Traits<MODE>;
@@ -147,7 +156,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), TR::gather ? 1 + kGatherThreads : 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -179,103 +188,150 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------------------------------------ TMA producer
     const uint64_t pol_w = policy_evict_last();
     const uint64_t pol_x = policy_evict_normal();
+    constexpr uint32_t kTmaBytes = MODE == kUp ? SM::kBBytes
+                                   : MODE == kDH ? SM::kBBytes
+                                   : MODE == kDW1 ? SM::kBBytes
+                                   : MODE == kDW2 ? kABytes
+                                                  : SM::kStageBytes;
     int s = 0;
     uint32_t ph = 0;
     int issued = 0;
     bool aborted = false;
-    for (int tile = blockIdx.x; tile < total && !aborted; tile += gridDim.x) {
-      const Tile t = decode_tile<MODE, BN>(a, tile, total_m);
-      int tok[4];
-      if (TR::a_gather) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) tok[j] = token_or_oob(a, t.row0 + lane * 4 + j, t.row_end);
-      }
-      for (int kb = 0; kb < t.kblocks; ++kb) {
-        int ok = 1;
-        if (lane == 0) {
-          ok = mbar_wait(empty_bar(s), ph ^ 1u) ? 1 : 0;
-          if (ok && *abort_flag) ok = 0;
-          if (ok) mbar_arrive_expect_tx(full_bar(s), SM::kStageBytes);
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) {
-          if (lane == 0) {
+    if (lane == 0) {
+      for (int tile = blockIdx.x; tile < total && !aborted; tile += gridDim.x) {
+        const Tile t = decode_tile<MODE, BN>(a, tile, total_m);
+        for (int kb = 0; kb < t.kblocks; ++kb) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1u) || *abort_flag) {
             set_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
             *abort_flag = 1;
+            aborted = true;
+            break;
           }
+          mbar_arrive_expect_tx(full_bar(s), kTmaBytes);
+          const uint32_t a_dst = sA + s * kABytes;
+          const uint32_t b_dst = sB + s * SM::kBBytes;
+          const uint32_t fb = full_bar(s);
+          if (MODE == kUp) {
+            // W1_e rows [kb*64, +64): gate columns [n0/2, +128) and up columns [n + n0/2, +128)
+            const int hcol = t.n0 / 2;
+            const int wrow = t.e * a.d + kb * kBK;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              tma_load_2d(b_dst + c * 8192, &tmB, (c < 2 ? 0 : a.n) + hcol + (c & 1) * 64, wrow, fb, pol_w);
+          } else if (MODE == kDH) {
+            // K-major W2_e: N index = rows n0..n0+BN of W2_e, K-elements [kb*64, +64)
+            tma_load_2d(b_dst, &tmB, kb * kBK, t.e * a.n + t.n0, fb, pol_w);
+          } else if (MODE == kDown) {
+            tma_load_2d(a_dst, &tmA, kb * kBK, t.row0, fb, pol_x);
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c)
+              tma_load_2d(b_dst + c * 8192, &tmB, t.n0 + c * 64, t.e * a.n + kb * kBK, fb, pol_w);
+          } else if (MODE == kDX) {
+            tma_load_2d(a_dst, &tmA, kb * kBK, t.row0, fb, pol_x);
+            tma_load_2d(b_dst, &tmB, kb * kBK, t.e * a.d + t.n0, fb, pol_w);
+          } else if (MODE == kDW1) {
+            // B = dH rows [rb, rb+64) (MN-major); rows past the expert meet zero A rows
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c)
+              tma_load_2d(b_dst + c * 8192, &tmB, t.n0 + c * 64, t.row0 + kb * kBK, fb, pol_x);
+          } else {
+            // kDW2: A = (s*A) rows [rb, rb+64) (MN-major); rows past the expert meet zero B rows
+#pragma unroll
+            for (int c = 0; c < kBM / 64; ++c)
+              tma_load_2d(a_dst + c * 8192, &tmA, t.m0 + c * 64, t.row0 + kb * kBK, fb, pol_x);
+          }
+          ++issued;
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (aborted) {
+        // let every copy this CTA issued land before the CTA's shared memory is released
+        for (int st = 0; st < STAGES && st < issued; ++st) {
+          const int last = st + ((issued - 1 - st) / STAGES) * STAGES;
+          mbar_wait(full_bar(st), static_cast<uint32_t>((last / STAGES) & 1));
+        }
+      }
+    }
+  } else if (TR::gather && warp >= 6) {
+    // --------------------------------------------------------------- cp.async token-row gatherers
+    const int gt = threadIdx.x - 192;  // 0..127
+    const int j = gt & 7;              // 16-byte piece of a 128-byte row segment
+    const int rsub = gt >> 3;          // 0..15
+    const uint32_t swz = static_cast<uint32_t>((j ^ (rsub & 7)) << 4);
+    const uint8_t *src_base = static_cast<const uint8_t *>(a.gsrc);
+    const size_t ld_bytes = static_cast<size_t>(a.gld) * 2;
+    int s = 0;
+    uint32_t ph = 0;
+    int pending = 0, sig = 0;
+    bool aborted = false;
+    for (int tile = blockIdx.x; tile < total && !aborted; tile += gridDim.x) {
+      const Tile t = decode_tile<MODE, BN>(a, tile, total_m);
+      if (t.kblocks == 0) continue;
+      const uint8_t *rowp[8];
+      uint32_t rown[8];
+      if (TR::gather_a_k) {
+        // this thread copies piece j of rows rsub + 16q (q = 0..7) of the 128-row tile at every k-block
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int tok = token_or_oob(a, t.row0 + rsub + 16 * q, t.row_end);
+          rown[q] = tok < a.T ? 16u : 0u;
+          rowp[q] = src_base + (tok < a.T ? tok : 0) * ld_bytes + j * 16;
+        }
+      }
+      for (int kb = 0; kb < t.kblocks; ++kb) {
+        if (!TR::gather_a_k) {
+          // varlen-K: rows rb + rsub + 16q (q = 0..3) of this k-block, by token id
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int tok = token_or_oob(a, t.row0 + kb * kBK + rsub + 16 * q, t.row_end);
+            rown[q] = tok < a.T ? 16u : 0u;
+            rowp[q] = src_base + (tok < a.T ? tok : 0) * ld_bytes + j * 16;
+          }
+        }
+        if (!mbar_wait(empty_bar(s), ph ^ 1u) || *abort_flag) {
+          set_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
+          *abort_flag = 1;
           aborted = true;
           break;
         }
-        const uint32_t a_dst = sA + s * kABytes;
-        const uint32_t b_dst = sB + s * SM::kBBytes;
-        const uint32_t fb = full_bar(s);
-        if (MODE == kUp || MODE == kDH) {
-          // A: 128 gathered token rows, 64 K-elements each (K-major); four rows per gather4
-          tma_gather4(a_dst + lane * 512, &tmA, kb * kBK, tok[0], tok[1], tok[2], tok[3], fb, pol_x);
-          if (lane == 0) {
-            if (MODE == kUp) {
-              // B: W1_e rows [kb*64, +64), gate columns [n0/2, +128) and up columns [n + n0/2, +128)
-              const int hcol = t.n0 / 2;
-              const int wrow = t.e * a.d + kb * kBK;
+        if (TR::gather_a_k) {
+          const uint32_t dst = sA + s * kABytes + rsub * 128 + swz;
+          const size_t koff = static_cast<size_t>(kb) * kBK * 2;
 #pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                const int col = (c < 2 ? 0 : a.n) + hcol + (c & 1) * 64;
-                tma_load_2d(b_dst + c * 8192, &tmB, col, wrow, fb, pol_w);
-              }
-            } else {
-              // B (K-major): W2_e rows n0..n0+BN (the N index), K-elements [kb*64, +64)
-              tma_load_2d(b_dst, &tmB, kb * kBK, t.e * a.n + t.n0, fb, pol_w);
-            }
-          }
-        } else if (MODE == kDown || MODE == kDX) {
-          if (lane == 0) {
-            tma_load_2d(a_dst, &tmA, kb * kBK, t.row0, fb, pol_x);
-            if (MODE == kDown) {
-#pragma unroll
-              for (int c = 0; c < BN / 64; ++c)
-                tma_load_2d(b_dst + c * 8192, &tmB, t.n0 + c * 64, t.e * a.n + kb * kBK, fb, pol_w);
-            } else {
-              tma_load_2d(b_dst, &tmB, kb * kBK, t.e * a.d + t.n0, fb, pol_w);
-            }
-          }
+          for (int q = 0; q < 8; ++q) cp_async_16(dst + q * 2048, rowp[q] + koff, rown[q]);
         } else {
-          // varlen-K: both operands MN-major; K index = row of the expert
-          const int rb = t.row0 + kb * kBK;
-          {
-            const int c = lane >> 4, g = lane & 15;
-            int idx[4];
+          // MN-major: K-row k = rsub + 16q at byte k*128 of each 64-column chunk c (8 KB apart)
+          constexpr int kChunks = TR::gather_a_mn ? kBM / 64 : BN / 64;
+          const uint32_t base_dst = (TR::gather_a_mn ? sA + s * kABytes : sB + s * SM::kBBytes) + rsub * 128 + swz;
+          const int mn0 = TR::gather_a_mn ? t.m0 : t.n0;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int r = rb + 4 * g + j;
-              idx[j] = (MODE == kDW1) ? token_or_oob(a, r, t.row_end) : (r < t.row_end ? r : a.p_cap);
-            }
-            tma_gather4(a_dst + c * 8192 + g * 512, &tmA, t.m0 + c * 64, idx[0], idx[1], idx[2], idx[3], fb, pol_x);
-          }
+          for (int q = 0; q < 4; ++q)
 #pragma unroll
-          for (int i = lane; i < (BN / 64) * 16; i += 32) {
-            const int c = i >> 4, g = i & 15;
-            int idx[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int r = rb + 4 * g + j;
-              idx[j] = (MODE == kDW2) ? token_or_oob(a, r, t.row_end) : (r < t.row_end ? r : a.p_cap);
-            }
-            tma_gather4(b_dst + c * 8192 + g * 512, &tmB, t.n0 + c * 64, idx[0], idx[1], idx[2], idx[3], fb, pol_x);
-          }
+            for (int c = 0; c < kChunks; ++c)
+              cp_async_16(base_dst + q * 2048 + c * 8192, rowp[q] + static_cast<size_t>(mn0 + c * 64) * 2, rown[q]);
         }
-        ++issued;
+        cp_async_commit();
+        if (++pending > kGatherLag) {
+          cp_async_wait<kGatherLag>();
+          fence_proxy_async_smem();
+          mbar_arrive(full_bar(sig));
+          if (++sig == STAGES) sig = 0;
+          --pending;
+        }
         if (++s == STAGES) {
           s = 0;
           ph ^= 1u;
         }
       }
     }
-    if (aborted && lane == 0) {
-      // let every copy this CTA issued land before the CTA's shared memory is released
-      for (int st = 0; st < STAGES && st < issued; ++st) {
-        const int last = st + ((issued - 1 - st) / STAGES) * STAGES;
-        mbar_wait(full_bar(st), static_cast<uint32_t>((last / STAGES) & 1));
-      }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    for (; pending > 0; --pending) {
+      mbar_arrive(full_bar(sig));
+      if (++sig == STAGES) sig = 0;
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------------------------- MMA issuer
@@ -329,7 +385,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         *abort_flag = 1;
       }
     }
-  } else {
+  } else if (warp >= 2 && warp < 6) {
     // ---------------------------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
@@ -524,7 +580,7 @@ int launch_gemm(const GemmArgs &a, const TensorMaps &tm, cudaStream_t stream) {
   }
   static const char *const kNames[] = {"gemm_up", "gemm_down", "gemm_dh", "gemm_dx", "gemm_dw1", "gemm_dw2"};
   prof_begin(kNames[MODE], stream);
-  moe_gemm_kernel<MODE, BN, STAGES><<<num_sms(), kGemmThreads, SM::kBytes, stream>>>(tm.a, tm.b, a);
+  moe_gemm_kernel<MODE, BN, STAGES><<<num_sms(), Traits<MODE>::threads, SM::kBytes, stream>>>(tm.a, tm.b, a);
   prof_end(stream);
   count_launch();
   err = cudaGetLastError();

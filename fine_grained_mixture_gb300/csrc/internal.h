@@ -45,6 +45,8 @@ struct GemmArgs {
   float *out_f32;    // down: fp32 O;  dX~: fp32 dX
   float *dS;         // dH: per-row dS
   const void *Hin;   // dH: cached H
+  const void *gsrc;  // the operand gathered by token id: X (up, dW1) or dO (dH, dW2), bf16 rows
+  int gld;           // its row length in elements
 };
 
 struct TensorMaps {
@@ -65,5 +67,8 @@ int launch_dw2(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s);
 
 // elementwise (elementwise.cu)
 int launch_f32_to_bf16(const float *src, void *dst, size_t count, cudaStream_t s);
+// Zeroes rows [offsets[E], p_cap) of two bf16 row-major buffers with row lengths ld_a and ld_b.
+int launch_zero_tail(void *a, void *b, const int32_t *offsets, int E, size_t p_cap, int ld_a, int ld_b,
+                     cudaStream_t s);
 
 }  // namespace moe
