@@ -51,11 +51,17 @@ struct Traits {
 constexpr int kGatherThreads = 128;
 constexpr int kGatherLag = 2;  // stages a gather thread keeps in flight before it signals the oldest
 
-template <int BN, int STAGES>
+// Scatter-add epilogues transpose each warp's 32 x 32 fp32 chunk through shared memory so that one
+// red.v4 instruction covers four whole 128-byte rows; rows are padded by 16 bytes against bank conflicts.
+constexpr int kStgRowFloats = 36;
+constexpr int kStgWarpBytes = 32 * kStgRowFloats * 4;
+
+template <int BN, int STAGES, bool SCATTER>
 struct Smem {
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kBarOff = STAGES * kStageBytes;
+  static constexpr int kStgOff = STAGES * kStageBytes;
+  static constexpr int kBarOff = kStgOff + (SCATTER ? 4 * kStgWarpBytes : 0);
   static constexpr int kBytes = kBarOff + 256 + 1024;  // + barriers/flags + alignment slack
 };
 
@@ -134,7 +140,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmArgs a) {
   using TR = Traits<MODE>;
-  using SM = Smem<BN, STAGES>;
+  using SM = Smem<BN, STAGES, TR::nt_outer>;
   constexpr uint32_t kTmemCols = 2 * BN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -186,8 +192,10 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------------------------ TMA producer
-    const uint64_t pol_w = policy_evict_last();
-    const uint64_t pol_x = policy_evict_normal();
+    // weights: reused by the m-tiles of one expert, which run close together -> normal priority;
+    // the dense activation operand of the scatter-add GEMMs streams through once per column slab -> first
+    const uint64_t pol_w = policy_evict_normal();
+    const uint64_t pol_x = TR::nt_outer ? policy_evict_first() : policy_evict_normal();
     constexpr uint32_t kTmaBytes = MODE == kUp ? SM::kBBytes
                                    : MODE == kDH ? SM::kBBytes
                                    : MODE == kDW1 ? SM::kBBytes
@@ -449,29 +457,39 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
         }
       } else if (MODE == kDown || MODE == kDX) {
         const int r = t.row0 + row;
-        bool valid = r < t.row_end;
-        int tok = 0;
+        int tok = -1;
         float sc = 1.f;
-        if (valid) {
+        if (r < t.row_end) {
           tok = __ldg(&a.row_token[r]);
           if (tok < 0 || tok >= a.T) {
             set_status(a.status, MOE_ERR_BAD_METADATA);
-            valid = false;
+            tok = -1;
           }
           if (MODE == kDown) sc = __ldg(&a.row_score[r]);
         }
-        float *dst = a.out_f32 + (size_t)tok * a.d + t.n0;
+        const uint32_t stg = base + SM::kStgOff + q * kStgWarpBytes;
+        const uint32_t my_row = stg + lane * (kStgRowFloats * 4);
+        // read-back role: 8 lanes per row, 4 rows per instruction
+        const int sub_row = lane >> 3;
+        const int sub_col = (lane & 7) * 4;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(tacc + c * 32, v);
           tmem_ld_wait();
-          if (valid) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              red_add_v4(dst + c * 32 + 4 * i, sc * __uint_as_float(v[4 * i]), sc * __uint_as_float(v[4 * i + 1]),
+          for (int i = 0; i < 8; ++i)
+            st_shared_v4(my_row + i * 16, sc * __uint_as_float(v[4 * i]), sc * __uint_as_float(v[4 * i + 1]),
                          sc * __uint_as_float(v[4 * i + 2]), sc * __uint_as_float(v[4 * i + 3]));
+          __syncwarp();
+#pragma unroll
+          for (int rd = 0; rd < 8; ++rd) {
+            const int rr = rd * 4 + sub_row;
+            const int trr = __shfl_sync(0xffffffffu, tok, rr);
+            const float4 x = ld_shared_v4(stg + rr * (kStgRowFloats * 4) + sub_col * 4);
+            if (trr >= 0) red_add_v4(a.out_f32 + (size_t)trr * a.d + t.n0 + c * 32 + sub_col, x.x, x.y, x.z, x.w);
           }
+          __syncwarp();
         }
       } else if (MODE == kDH) {
         const int r = t.row0 + row;
@@ -567,7 +585,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
 // Host launcher for one instantiation.
 template <int MODE, int BN, int STAGES>
 int launch_gemm(const GemmArgs &a, const TensorMaps &tm, cudaStream_t stream) {
-  using SM = Smem<BN, STAGES>;
+  using SM = Smem<BN, STAGES, Traits<MODE>::nt_outer>;
   static int attr_dev = -1;
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
