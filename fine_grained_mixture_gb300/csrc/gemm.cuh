@@ -495,23 +495,32 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
         const int r = t.row0 + row;
         const bool valid = r < t.row_end;
         const float sc = valid ? __ldg(&a.row_score[r]) : 0.f;
-        const uint8_t *hrow = static_cast<const uint8_t *>(a.Hin) + (size_t)r * (2 * a.n) * 2;
+        const uint8_t *hrow = static_cast<const uint8_t *>(a.Hin) + (size_t)(valid ? r : t.row0) * (2 * a.n) * 2;
         uint8_t *dhrow = static_cast<uint8_t *>(a.out0) + (size_t)r * (2 * a.n) * 2;
         uint8_t *sarow = static_cast<uint8_t *>(a.out1) + (size_t)r * a.n * 2;
         float ds = 0.f;
+        // the cached H of chunk c+1 is fetched while chunk c is computed
+        uint4 hg4[4], hu4[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          hg4[w] = __ldg(reinterpret_cast<const uint4 *>(hrow + (size_t)t.n0 * 2) + w);
+          hu4[w] = __ldg(reinterpret_cast<const uint4 *>(hrow + (size_t)(a.n + t.n0) * 2) + w);
+        }
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(tacc + c * 32, v);
-          tmem_ld_wait();
-          if (valid) {
-            const int j = t.n0 + c * 32;
-            uint4 hg4[4], hu4[4];
+          const int j = t.n0 + c * 32;
+          uint4 ng4[4], nu4[4];
+          if (c + 1 < BN / 32) {
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
-              hg4[w] = __ldg(reinterpret_cast<const uint4 *>(hrow + (size_t)j * 2) + w);
-              hu4[w] = __ldg(reinterpret_cast<const uint4 *>(hrow + (size_t)(a.n + j) * 2) + w);
+              ng4[w] = __ldg(reinterpret_cast<const uint4 *>(hrow + (size_t)(j + 32) * 2) + w);
+              nu4[w] = __ldg(reinterpret_cast<const uint4 *>(hrow + (size_t)(a.n + j + 32) * 2) + w);
             }
+          }
+          tmem_ld_wait();
+          if (valid) {
             const uint32_t *hg = reinterpret_cast<const uint32_t *>(hg4);
             const uint32_t *hu = reinterpret_cast<const uint32_t *>(hu4);
             uint32_t dg[16], du[16], sa[16];
@@ -541,6 +550,13 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
               st_v4(dhrow + (size_t)j * 2 + w * 16, dg[4 * w], dg[4 * w + 1], dg[4 * w + 2], dg[4 * w + 3]);
               st_v4(dhrow + (size_t)(a.n + j) * 2 + w * 16, du[4 * w], du[4 * w + 1], du[4 * w + 2], du[4 * w + 3]);
               st_v4(sarow + (size_t)j * 2 + w * 16, sa[4 * w], sa[4 * w + 1], sa[4 * w + 2], sa[4 * w + 3]);
+            }
+          }
+          if (c + 1 < BN / 32) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              hg4[w] = ng4[w];
+              hu4[w] = nu4[w];
             }
           }
         }

@@ -8,7 +8,7 @@
 // smaller than the distance down, and drops its weakest token-choice tokens otherwise.
 //
 // Pipeline (one stream, no host synchronisation):
-//   route_topk_kernel   one warp per token: top-K by (logit desc, expert asc), softmax over the K,
+//   route_topk_kernel   one warp per token (32 warps per chunk): top-K by (logit desc, expert asc), softmax over the K,
 //                       per-chunk (256 tokens) expert histograms, membership bitmap (TR only)
 //   route_scan_kernel   one CTA: per-chunk bases, counts (TC f_e or TR r_e), offsets, tile offsets
 //   route_fill_tc       one CTA per 256-token chunk: rows in ascending token order via bitmap ranks
@@ -30,8 +30,11 @@ __device__ __forceinline__ uint32_t order_key(float z) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+constexpr int kTopkThreads = 1024;                   // 32 warps per 256-token chunk
+constexpr int kTokensPerWarp = kChunk / (kTopkThreads / 32);
+
 template <int NV>  // NV = logits held per lane = ceil(E / 32)
-__global__ void __launch_bounds__(256) route_topk_kernel(const float *__restrict__ logits, int T, int E, int K,
+__global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float *__restrict__ logits, int T, int E, int K,
                                                          int want_member, int32_t *__restrict__ topk_idx,
                                                          float *__restrict__ topk_score, float *__restrict__ tok_max,
                                                          float *__restrict__ tok_den, int32_t *__restrict__ chunk_cnt,
@@ -43,8 +46,8 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float *__restrict
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int chunk = blockIdx.x;
-  for (int i = 0; i < 32; ++i) {
-    const int t = chunk * kChunk + warp * 32 + i;
+  for (int i = 0; i < kTokensPerWarp; ++i) {
+    const int t = chunk * kChunk + warp * kTokensPerWarp + i;
     if (t >= T) break;
     float v[NV];
     bool bad = false;
@@ -352,7 +355,7 @@ int launch_route(const float *logits, int T, int E, int K, int mode, const moe_r
   const size_t hist_smem = (size_t)E * 4;
   const int nv = (E + 31) / 32;
 #define MOE_TOPK_LAUNCH(NV)                                                                                       \
-  route_topk_kernel<NV><<<w.nchunks, 256, hist_smem, stream>>>(logits, T, E, K, want_member, r->topk_idx,          \
+  route_topk_kernel<NV><<<w.nchunks, kTopkThreads, hist_smem, stream>>>(logits, T, E, K, want_member, r->topk_idx,          \
                                                                r->topk_score, w.tok_max, w.tok_den, w.chunk_cnt, \
                                                                w.member, w.member_words, r->status)
   prof_begin("route_topk", stream);
