@@ -133,6 +133,21 @@ int make_tmap_bf16(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t r
   return r == CUDA_SUCCESS ? MOE_OK : record_cu_error(r);
 }
 
+int make_tmap_bf16_epi(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return record_cuda_error(cudaErrorNotSupported);
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : record_cu_error(r);
+}
+
+static void fill_unused(TensorMaps &tm) { tm.h = tm.dh = tm.sa = tm.b; }
+
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 static int check_route_shape(int T, int E, int K, int mode) {
@@ -259,7 +274,7 @@ int moe_forward(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const
   a.Kdim = d;
   a.out0 = H;
   a.out1 = A;
-  if ((rc = launch_up(a, tm, s)) != MOE_OK) return rc;
+  if ((rc = (fill_unused(tm), launch_up(a, tm, s))) != MOE_OK) return rc;
   // down-projection + aggregation: O32[tok] += s * A W2_e (N = d, K = n)
   if ((rc = make_tmap_bf16(&tm.a, A, n, p_cap, 128)) != MOE_OK) return rc;
   if ((rc = make_tmap_bf16(&tm.b, W2, d, (uint64_t)E * n, 64)) != MOE_OK) return rc;
@@ -269,7 +284,7 @@ int moe_forward(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const
   a.out1 = nullptr;
   a.gsrc = nullptr;
   a.out_f32 = O32;
-  if ((rc = launch_down(a, tm, s)) != MOE_OK) return rc;
+  if ((rc = (fill_unused(tm), launch_down(a, tm, s))) != MOE_OK) return rc;
   return launch_f32_to_bf16(O32, O, (size_t)T * d, s);
 }
 
@@ -316,6 +331,9 @@ int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, cons
   a.out1 = sA;
   a.dS = dS;
   a.Hin = H;
+  if ((rc = make_tmap_bf16_epi(&tm.h, H, 2 * (uint64_t)n, p_cap)) != MOE_OK) return rc;
+  if ((rc = make_tmap_bf16_epi(&tm.dh, dH, 2 * (uint64_t)n, p_cap)) != MOE_OK) return rc;
+  if ((rc = make_tmap_bf16_epi(&tm.sa, sA, n, p_cap)) != MOE_OK) return rc;
   if ((rc = launch_dh(a, tm, s, bn)) != MOE_OK) return rc;
   // dX~: dX32[tok] += dH W1_e^T (N = d, K = 2n)
   if ((rc = make_tmap_bf16(&tm.a, dH, 2 * (uint64_t)n, p_cap, 128)) != MOE_OK) return rc;
@@ -324,7 +342,7 @@ int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, cons
   ax.Ndim = d;
   ax.Kdim = 2 * n;
   ax.out_f32 = dX32;
-  if ((rc = launch_dx(ax, tm, s)) != MOE_OK) return rc;
+  if ((rc = (fill_unused(tm), launch_dx(ax, tm, s))) != MOE_OK) return rc;
   if ((rc = launch_f32_to_bf16(dX32, dX, (size_t)T * d, s)) != MOE_OK) return rc;
   // rows [P, P_cap) of dH and s*A are read as the zero tail of the last expert's k-blocks
   if ((rc = launch_zero_tail(dH, sA, r->offsets, E, p_cap, 2 * n, n, s)) != MOE_OK) return rc;
@@ -337,7 +355,7 @@ int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, cons
   aw.out0 = dW1;
   aw.gsrc = X;
   aw.gld = d;
-  if ((rc = launch_dw1(aw, tm, s)) != MOE_OK) return rc;
+  if ((rc = (fill_unused(tm), launch_dw1(aw, tm, s))) != MOE_OK) return rc;
   // dW2_e = (s*A)_e^T dO[tok] (M = n, N = d, K = rows of e); dO rows gathered with cp.async
   if ((rc = make_tmap_bf16(&tm.a, sA, n, p_cap, 64)) != MOE_OK) return rc;
   tm.b = tm.a;
@@ -346,7 +364,7 @@ int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, cons
   aw.out0 = dW2;
   aw.gsrc = dO;
   aw.gld = d;
-  return launch_dw2(aw, tm, s);
+  return (fill_unused(tm), launch_dw2(aw, tm, s));
 }
 
 int moe_get_status(const moe_routing *r, int32_t *code, int32_t *P, void *stream) {

@@ -95,6 +95,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm,
       : "memory");
 }
 
+// 2D tiled store of a shared-memory box to (c0, c1) of the tensor map (bulk async group of this thread).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *tm, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tm), "r"(src),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
 // Gather of four rows (r0..r3, each one box-width wide starting at element c0) of a 2D tensor into four
 // consecutive box rows of shared memory.  A row index outside the tensor reads the zero fill.
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *tm, int c0, int r0, int r1, int r2,
@@ -234,6 +241,25 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
+}
+
+// Bulk (TMA engine) element-wise fp32 add of `bytes` from shared memory into global memory.
+__device__ __forceinline__ void bulk_reduce_add_f32(float *gdst, uint32_t ssrc, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.L2::cache_hint.add.f32 [%0], [%1], %2, %3;" ::"l"(gdst),
+               "r"(ssrc), "r"(bytes), "l"(policy)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {

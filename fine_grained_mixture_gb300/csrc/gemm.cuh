@@ -55,15 +55,25 @@ constexpr int kGatherLag = 2;  // stages a gather thread keeps in flight before 
 // red.v4 instruction covers four whole 128-byte rows; rows are padded by 16 bytes against bank conflicts.
 constexpr int kStgRowFloats = 36;
 constexpr int kStgWarpBytes = 32 * kStgRowFloats * 4;
+constexpr int kStgBytes = 4 * kStgWarpBytes;
 
-template <int BN, int STAGES, bool SCATTER>
+// dH epilogue, per warp: two 4 KB buffers of cached H (gate | up, 32 rows x 32 columns each) filled by TMA one
+// chunk ahead, and a 6 KB staging tile (dH gate | dH up | s*A) drained by TMA stores; 64-byte swizzle.
+constexpr int kDhWarpBytes = 2 * 4096 + 6144;
+
+template <int BN, int STAGES, int EPI_BYTES>
 struct Smem {
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStgOff = STAGES * kStageBytes;
-  static constexpr int kBarOff = kStgOff + (SCATTER ? 4 * kStgWarpBytes : 0);
+  static constexpr int kBarOff = kStgOff + EPI_BYTES;
   static constexpr int kBytes = kBarOff + 256 + 1024;  // + barriers/flags + alignment slack
 };
+
+template <int MODE>
+__host__ __device__ constexpr int epi_bytes() {
+  return Traits<MODE>::nt_outer ? kStgBytes : (MODE == kDH ? 4 * kDhWarpBytes : 0);
+}
 
 struct Tile {
   int e, m0, n0, row0, row_end, kblocks;
@@ -137,10 +147,11 @@ __device__ __forceinline__ int token_or_oob(const GemmArgs &a, int r, int row_en
 
 template <int MODE, int BN, int STAGES>
 __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
-    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const GemmArgs a) {
+    moe_gemm_kernel(const __grid_constant__ TensorMaps tm, const GemmArgs a) {
+  const CUtensorMap &tmA = tm.a;
+  const CUtensorMap &tmB = tm.b;
   using TR = Traits<MODE>;
-  using SM = Smem<BN, STAGES, TR::nt_outer>;
+  using SM = Smem<BN, STAGES, epi_bytes<MODE>()>;
   constexpr uint32_t kTmemCols = 2 * BN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -154,6 +165,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
   auto tfull_bar = [&](int b) { return bar + 8u * (2 * STAGES + b); };
   auto tempty_bar = [&](int b) { return bar + 8u * (2 * STAGES + 2 + b); };
   const uint32_t drain_bar = bar + 8u * (2 * STAGES + 4);
+  auto hin_bar = [&](int w, int b) { return bar + 8u * (2 * STAGES + 6 + 2 * w + b); };  // dH epilogue
   volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + SM::kBarOff + 8 * (2 * STAGES + 5));
   volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + SM::kBarOff + 8 * (2 * STAGES + 5) + 4);
 
@@ -170,6 +182,8 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
       mbar_init(tempty_bar(b), 4);
     }
     mbar_init(drain_bar, 1);
+    if (MODE == kDH)
+      for (int i = 0; i < 8; ++i) mbar_init(hin_bar(i >> 1, i & 1), 1);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -177,6 +191,11 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (MODE == kDH) {
+      tma_prefetch_desc(&tm.h);
+      tma_prefetch_desc(&tm.dh);
+      tma_prefetch_desc(&tm.sa);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
@@ -399,6 +418,8 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     const int row = q * 32 + lane;
     int buf = 0;
     uint32_t bph = 0;
+    uint32_t hin_par = 0u;                       // dH epilogue: bit b = parity of H buffer b's next fill
+    const uint64_t pol_stream = policy_evict_first();  // cached H is read exactly once
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const Tile t = decode_tile<MODE, BN>(a, tile, total_m);
       if (t.kblocks == 0) {
@@ -494,57 +515,98 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
       } else if (MODE == kDH) {
         const int r = t.row0 + row;
         const bool valid = r < t.row_end;
+        const bool full_warp = t.row0 + q * 32 + 31 < t.row_end;  // all 32 rows belong to this expert
         const float sc = valid ? __ldg(&a.row_score[r]) : 0.f;
-        const uint8_t *hrow = static_cast<const uint8_t *>(a.Hin) + (size_t)(valid ? r : t.row0) * (2 * a.n) * 2;
+        const int wrow = t.row0 + q * 32;                          // first row of this warp's 32
+        const uint32_t wbase = base + SM::kStgOff + q * kDhWarpBytes;
+        const uint32_t out_st = wbase + 8192;                      // dH gate | dH up | s*A staging
+        // 64-byte swizzle: 16-byte piece p of row `lane` sits at piece p ^ ((lane >> 1) & 3)
+        const int sw = (lane >> 1) & 3;
+        auto issue_h = [&](int c, int b) {
+          const uint32_t hb = hin_bar(q, b);
+          mbar_arrive_expect_tx(hb, 4096);
+          tma_load_2d(wbase + b * 4096, &tm.h, t.n0 + c * 32, wrow, hb, pol_stream);
+          tma_load_2d(wbase + b * 4096 + 2048, &tm.h, a.n + t.n0 + c * 32, wrow, hb, pol_stream);
+        };
+        if (lane == 0) issue_h(0, 0);
         uint8_t *dhrow = static_cast<uint8_t *>(a.out0) + (size_t)r * (2 * a.n) * 2;
         uint8_t *sarow = static_cast<uint8_t *>(a.out1) + (size_t)r * a.n * 2;
         float ds = 0.f;
-        // the cached H of chunk c+1 is fetched while chunk c is computed
-        uint4 hg4[4], hu4[4];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          hg4[w] = __ldg(reinterpret_cast<const uint4 *>(hrow + (size_t)t.n0 * 2) + w);
-          hu4[w] = __ldg(reinterpret_cast<const uint4 *>(hrow + (size_t)(a.n + t.n0) * 2) + w);
-        }
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
+          const int b = c & 1;
+          if (c + 1 < BN / 32 && lane == 0) {
+            fence_proxy_async_smem();  // this warp's reads of the other buffer are ordered before the refill
+            issue_h(c + 1, b ^ 1);
+          }
           uint32_t v[32];
           tmem_ld32(tacc + c * 32, v);
-          const int j = t.n0 + c * 32;
-          uint4 ng4[4], nu4[4];
-          if (c + 1 < BN / 32) {
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              ng4[w] = __ldg(reinterpret_cast<const uint4 *>(hrow + (size_t)(j + 32) * 2) + w);
-              nu4[w] = __ldg(reinterpret_cast<const uint4 *>(hrow + (size_t)(a.n + j + 32) * 2) + w);
-            }
+          const bool got = mbar_wait(hin_bar(q, b), (hin_par >> b) & 1u);
+          hin_par ^= 1u << b;
+          if (!got) {
+            set_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
           }
           tmem_ld_wait();
-          if (valid) {
-            const uint32_t *hg = reinterpret_cast<const uint32_t *>(hg4);
-            const uint32_t *hu = reinterpret_cast<const uint32_t *>(hu4);
-            uint32_t dg[16], du[16], sa[16];
+          uint32_t hg[16], hu[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float o_g[2], o_u[2], o_a[2];
+          for (int p = 0; p < 4; ++p) {
+            const float4 g4 = ld_shared_v4(wbase + b * 4096 + lane * 64 + ((p ^ sw) << 4));
+            const float4 u4 = ld_shared_v4(wbase + b * 4096 + 2048 + lane * 64 + ((p ^ sw) << 4));
+            hg[4 * p] = __float_as_uint(g4.x);
+            hg[4 * p + 1] = __float_as_uint(g4.y);
+            hg[4 * p + 2] = __float_as_uint(g4.z);
+            hg[4 * p + 3] = __float_as_uint(g4.w);
+            hu[4 * p] = __float_as_uint(u4.x);
+            hu[4 * p + 1] = __float_as_uint(u4.y);
+            hu[4 * p + 2] = __float_as_uint(u4.z);
+            hu[4 * p + 3] = __float_as_uint(u4.w);
+          }
+          uint32_t dg[16], du[16], sa[16];
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const float gg = h ? bf16_hi(hg[i]) : bf16_lo(hg[i]);
-                const float uu = h ? bf16_hi(hu[i]) : bf16_lo(hu[i]);
-                const float dap = __uint_as_float(v[2 * i + h]);
-                const float sig = 1.f / (1.f + __expf(-gg));
-                const float silu = gg * sig;
-                const float act = silu * uu;
-                ds += dap * act;
-                const float da = sc * dap;
-                o_g[h] = da * uu * sig * (1.f + gg * (1.f - sig));
-                o_u[h] = da * silu;
-                o_a[h] = sc * act;
-              }
-              dg[i] = pack_bf16x2(o_g[0], o_g[1]);
-              du[i] = pack_bf16x2(o_u[0], o_u[1]);
-              sa[i] = pack_bf16x2(o_a[0], o_a[1]);
+          for (int i = 0; i < 16; ++i) {
+            float o_g[2], o_u[2], o_a[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const float gg = h ? bf16_hi(hg[i]) : bf16_lo(hg[i]);
+              const float uu = h ? bf16_hi(hu[i]) : bf16_lo(hu[i]);
+              const float dap = __uint_as_float(v[2 * i + h]);
+              const float sig = 1.f / (1.f + __expf(-gg));
+              const float silu = gg * sig;
+              const float act = silu * uu;
+              ds += dap * act;
+              const float da = sc * dap;
+              o_g[h] = da * uu * sig * (1.f + gg * (1.f - sig));
+              o_u[h] = da * silu;
+              o_a[h] = sc * act;
             }
+            dg[i] = pack_bf16x2(o_g[0], o_g[1]);
+            du[i] = pack_bf16x2(o_u[0], o_u[1]);
+            sa[i] = pack_bf16x2(o_a[0], o_a[1]);
+          }
+          const int j = t.n0 + c * 32;
+          if (full_warp) {
+            if (lane == 0) bulk_wait_read<0>();  // the previous chunk's stores have read the staging tile
+            __syncwarp();
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+              const uint32_t o = lane * 64 + ((p ^ sw) << 4);
+              st_shared_v4(out_st + o, __uint_as_float(dg[4 * p]), __uint_as_float(dg[4 * p + 1]),
+                           __uint_as_float(dg[4 * p + 2]), __uint_as_float(dg[4 * p + 3]));
+              st_shared_v4(out_st + 2048 + o, __uint_as_float(du[4 * p]), __uint_as_float(du[4 * p + 1]),
+                           __uint_as_float(du[4 * p + 2]), __uint_as_float(du[4 * p + 3]));
+              st_shared_v4(out_st + 4096 + o, __uint_as_float(sa[4 * p]), __uint_as_float(sa[4 * p + 1]),
+                           __uint_as_float(sa[4 * p + 2]), __uint_as_float(sa[4 * p + 3]));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tm.dh, out_st, j, wrow);
+              tma_store_2d(&tm.dh, out_st + 2048, a.n + j, wrow);
+              tma_store_2d(&tm.sa, out_st + 4096, j, wrow);
+              bulk_commit();
+            }
+          } else if (valid) {
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
               st_v4(dhrow + (size_t)j * 2 + w * 16, dg[4 * w], dg[4 * w + 1], dg[4 * w + 2], dg[4 * w + 3]);
@@ -552,13 +614,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
               st_v4(sarow + (size_t)j * 2 + w * 16, sa[4 * w], sa[4 * w + 1], sa[4 * w + 2], sa[4 * w + 3]);
             }
           }
-          if (c + 1 < BN / 32) {
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              hg4[w] = ng4[w];
-              hu4[w] = nu4[w];
-            }
-          }
+          __syncwarp();
         }
         if (valid) atomicAdd(&a.dS[r], ds);
       } else {
@@ -584,6 +640,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
         bph ^= 1u;
       }
     }
+    if (MODE == kDH) bulk_wait<0>();  // every TMA store has landed before the kernel ends
   }
 
   __syncthreads();
@@ -601,7 +658,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
 // Host launcher for one instantiation.
 template <int MODE, int BN, int STAGES>
 int launch_gemm(const GemmArgs &a, const TensorMaps &tm, cudaStream_t stream) {
-  using SM = Smem<BN, STAGES, Traits<MODE>::nt_outer>;
+  using SM = Smem<BN, STAGES, epi_bytes<MODE>()>;
   static int attr_dev = -1;
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -614,7 +671,7 @@ int launch_gemm(const GemmArgs &a, const TensorMaps &tm, cudaStream_t stream) {
   }
   static const char *const kNames[] = {"gemm_up", "gemm_down", "gemm_dh", "gemm_dx", "gemm_dw1", "gemm_dw2"};
   prof_begin(kNames[MODE], stream);
-  moe_gemm_kernel<MODE, BN, STAGES><<<num_sms(), Traits<MODE>::threads, SM::kBytes, stream>>>(tm.a, tm.b, a);
+  moe_gemm_kernel<MODE, BN, STAGES><<<num_sms(), Traits<MODE>::threads, SM::kBytes, stream>>>(tm, a);
   prof_end(stream);
   count_launch();
   err = cudaGetLastError();

@@ -49,12 +49,16 @@ struct GemmArgs {
   int gld;           // its row length in elements
 };
 
+// Tensor maps of one GEMM launch: a/b are the operands; h, dh, sa are the dH epilogue's cached-H input and
+// dH / s*A outputs (32 x 32 boxes, 64-byte swizzle).  Unused maps are copies of `b`.
 struct TensorMaps {
-  CUtensorMap a, b;
+  CUtensorMap a, b, h, dh, sa;
 };
 
 // Encodes a 2D bf16 tensor map over [rows, inner] (row-major) with a {64, box_rows} box, 128-byte swizzle.
 int make_tmap_bf16(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t rows, uint32_t box_rows);
+// Same with a {32, 32} box and 64-byte swizzle (the dH epilogue's per-warp tiles).
+int make_tmap_bf16_epi(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t rows);
 
 int num_sms();
 
