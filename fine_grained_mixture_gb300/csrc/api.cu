@@ -321,7 +321,7 @@ int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, cons
   TensorMaps tm;
   // dH: dA' = dO[tok] W2_e^T (N = n, K = d); epilogue dSwiGLU, dS, s*A
   const int bn = (n % 256 == 0) ? 256 : 128;
-  if ((rc = make_tmap_bf16(&tm.b, W2, d, (uint64_t)E * n, bn)) != MOE_OK) return rc;
+  if ((rc = make_tmap_bf16(&tm.b, W2, d, (uint64_t)E * n, bn / 2)) != MOE_OK) return rc;  // two N halves
   tm.a = tm.b;  // unused: dO rows are gathered with cp.async
   a.gsrc = dO;
   a.gld = d;
@@ -337,7 +337,7 @@ int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, cons
   if ((rc = launch_dh(a, tm, s, bn)) != MOE_OK) return rc;
   // dX~: dX32[tok] += dH W1_e^T (N = d, K = 2n)
   if ((rc = make_tmap_bf16(&tm.a, dH, 2 * (uint64_t)n, p_cap, 128)) != MOE_OK) return rc;
-  if ((rc = make_tmap_bf16(&tm.b, W1, 2 * (uint64_t)n, (uint64_t)E * d, 256)) != MOE_OK) return rc;
+  if ((rc = make_tmap_bf16(&tm.b, W1, 2 * (uint64_t)n, (uint64_t)E * d, 128)) != MOE_OK) return rc;  // two N halves
   GemmArgs ax = base_args(r, T, d, n, E, p_cap);
   ax.Ndim = d;
   ax.Kdim = 2 * n;

@@ -20,6 +20,9 @@
 // (a TMA gather costs one request per 128-byte row, which starves the tensor cores here; the LSU path
 // moves the same rows at a fraction of the issue cost).
 // Tiles: 128 x BN x 64, STAGES-deep shared-memory ring, two TMEM accumulators of BN fp32 columns.
+// CTAs run in clusters of two on neighbouring tiles that need the same TMA-loaded operand (the expert's
+// weight tile, or the s*A tile of dW2): each CTA loads half of it and multicasts it to both, halving the
+// L2 -> SM traffic of that operand; a stage is released to both producers by a multicast commit.
 // Every wait is bounded; on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT, drains its own copies and
 // MMAs, frees TMEM and returns.
 #pragma once
@@ -77,6 +80,7 @@ __host__ __device__ constexpr int epi_bytes() {
 
 struct Tile {
   int e, m0, n0, row0, row_end, kblocks;
+  bool shared;  // both CTAs of the cluster need the same shared-operand tile (load halves + multicast)
 };
 
 // Largest e in [0, E) with tile_offsets[e] <= mt.
@@ -90,24 +94,40 @@ __device__ __forceinline__ int find_expert(const int32_t *__restrict__ tile_offs
   return lo;
 }
 
+// Number of cluster work items (pairs of tiles).
 template <int MODE, int BN>
-__device__ __forceinline__ int total_tiles(const GemmArgs &a) {
-  if (Traits<MODE>::varlen_k) return a.E * (a.Mdim / kBM) * (a.Ndim / BN);
-  return __ldg(&a.tile_offsets[a.E]) * (a.Ndim / BN);
+__device__ __forceinline__ int total_pairs(const GemmArgs &a, int total_m) {
+  const int n_tiles = a.Ndim / BN;
+  const int m_tiles = a.Mdim / kBM;
+  if (MODE == kDW1) return a.E * (m_tiles / 2) * n_tiles;        // pairs along M (d % 256 == 0)
+  if (MODE == kDW2) return a.E * m_tiles * ((n_tiles + 1) / 2);  // pairs along N
+  return ((total_m + 1) / 2) * n_tiles;                           // pairs of consecutive m-tiles
 }
 
 template <int MODE, int BN>
-__device__ __forceinline__ Tile decode_tile(const GemmArgs &a, int tile, int total_m) {
+__device__ __forceinline__ Tile decode_tile(const GemmArgs &a, int pair, int rank, int total_m) {
   Tile t;
   const int n_tiles = a.Ndim / BN;
+  t.shared = true;
   if (Traits<MODE>::varlen_k) {
     const int m_tiles = a.Mdim / kBM;
-    const int per_e = m_tiles * n_tiles;
-    t.e = tile / per_e;
-    const int rem = tile - t.e * per_e;
-    const int mt = rem / n_tiles;
+    int mt, nt;
+    if (MODE == kDW1) {
+      const int per_e = (m_tiles / 2) * n_tiles;
+      t.e = pair / per_e;
+      const int rem = pair - t.e * per_e;
+      mt = 2 * (rem / n_tiles) + rank;
+      nt = rem % n_tiles;
+    } else {
+      const int np = (n_tiles + 1) / 2;
+      const int per_e = m_tiles * np;
+      t.e = pair / per_e;
+      const int rem = pair - t.e * per_e;
+      mt = rem / np;
+      nt = min(2 * (rem % np) + rank, n_tiles - 1);  // an odd last column pair computes its tile twice
+    }
     t.m0 = mt * kBM;
-    t.n0 = (rem - mt * n_tiles) * BN;
+    t.n0 = nt * BN;
     t.row0 = __ldg(&a.offsets[t.e]);
     t.row_end = __ldg(&a.offsets[t.e + 1]);
     if (t.row0 < 0 || t.row_end < t.row0 || t.row_end > a.p_cap) {
@@ -116,23 +136,29 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &a, int tile, int tot
     }
     t.kblocks = (t.row_end - t.row0 + kBK - 1) / kBK;
   } else {
-    int mt, nt;
+    const int n_pairs_m = (total_m + 1) / 2;
+    int mp, nt;
     if (Traits<MODE>::nt_outer) {
-      nt = tile / total_m;
-      mt = tile - nt * total_m;
+      nt = pair / n_pairs_m;
+      mp = pair - nt * n_pairs_m;
     } else {
-      mt = tile / n_tiles;
-      nt = tile - mt * n_tiles;
+      mp = pair / n_tiles;
+      nt = pair - mp * n_tiles;
     }
+    const int mt = 2 * mp + rank;
     t.e = find_expert(a.tile_offsets, a.E, mt);
+    // the partner tile shares this weight tile only if it exists and belongs to the same expert
+    const int partner = 2 * mp + (rank ^ 1);
+    t.shared = (2 * mp + 1 < total_m) && find_expert(a.tile_offsets, a.E, partner) == t.e;
     t.m0 = 0;
     t.n0 = nt * BN;
+    // a missing last tile (odd tile count) runs on rows past the last expert: zero operands, no output
     t.row0 = __ldg(&a.offsets[t.e]) + (mt - __ldg(&a.tile_offsets[t.e])) * kBM;
     t.row_end = __ldg(&a.offsets[t.e + 1]);
-    t.kblocks = a.Kdim / kBK;
-    if (t.row0 < 0 || t.row_end > a.p_cap || t.row0 >= t.row_end) {
+    t.kblocks = a.Kdim / kBK;  // every tile runs the full k-loop so both CTAs stay in step
+    if (mt < total_m && (t.row0 < 0 || t.row_end > a.p_cap || t.row0 >= t.row_end)) {
       set_status(a.status, MOE_ERR_BAD_METADATA);
-      t.kblocks = 0;
+      t.row_end = t.row0;  // nothing is written
     }
   }
   return t;
@@ -175,7 +201,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), TR::gather ? 1 + kGatherThreads : 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), 2);  // released by the MMA issuers of both CTAs
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -202,12 +228,15 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // barriers of both CTAs initialised before any multicast lands in them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int total = total_tiles<MODE, BN>(a);
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int first_pair = static_cast<int>(cluster_id_x());
+  const int pair_step = static_cast<int>(num_clusters_x());
   const int total_m = TR::varlen_k ? 0 : __ldg(&a.tile_offsets[a.E]);
+  const int total = total_pairs<MODE, BN>(a, total_m);
 
   if (warp == 0) {
     // ------------------------------------------------------------------------------ TMA producer
@@ -225,8 +254,8 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     int issued = 0;
     bool aborted = false;
     if (lane == 0) {
-      for (int tile = blockIdx.x; tile < total && !aborted; tile += gridDim.x) {
-        const Tile t = decode_tile<MODE, BN>(a, tile, total_m);
+      for (int pair = first_pair; pair < total && !aborted; pair += pair_step) {
+        const Tile t = decode_tile<MODE, BN>(a, pair, rank, total_m);
         for (int kb = 0; kb < t.kblocks; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u) || *abort_flag) {
             set_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
@@ -238,34 +267,44 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
           const uint32_t a_dst = sA + s * kABytes;
           const uint32_t b_dst = sB + s * SM::kBBytes;
           const uint32_t fb = full_bar(s);
+          // the shared operand: this CTA's half (multicast to both) or, when the partner needs a
+          // different tile, the whole tile locally
+          auto shared_box = [&](uint32_t dst, const CUtensorMap *tmap, int c0, int c1, bool mine) {
+            if (!t.shared) tma_load_2d(dst, tmap, c0, c1, fb, pol_w);
+            else if (mine) tma_load_2d_mc(dst, tmap, c0, c1, fb, 0x3, pol_w);
+          };
           if (MODE == kUp) {
             // W1_e rows [kb*64, +64): gate columns [n0/2, +128) and up columns [n + n0/2, +128)
             const int hcol = t.n0 / 2;
             const int wrow = t.e * a.d + kb * kBK;
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-              tma_load_2d(b_dst + c * 8192, &tmB, (c < 2 ? 0 : a.n) + hcol + (c & 1) * 64, wrow, fb, pol_w);
+              shared_box(b_dst + c * 8192, &tmB, (c < 2 ? 0 : a.n) + hcol + (c & 1) * 64, wrow, (c >> 1) == rank);
           } else if (MODE == kDH) {
-            // K-major W2_e: N index = rows n0..n0+BN of W2_e, K-elements [kb*64, +64)
-            tma_load_2d(b_dst, &tmB, kb * kBK, t.e * a.n + t.n0, fb, pol_w);
+            // K-major W2_e: N index = rows n0..n0+BN of W2_e (two halves), K-elements [kb*64, +64)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              shared_box(b_dst + h * (BN / 2) * 128, &tmB, kb * kBK, t.e * a.n + t.n0 + h * (BN / 2), h == rank);
           } else if (MODE == kDown) {
             tma_load_2d(a_dst, &tmA, kb * kBK, t.row0, fb, pol_x);
 #pragma unroll
             for (int c = 0; c < BN / 64; ++c)
-              tma_load_2d(b_dst + c * 8192, &tmB, t.n0 + c * 64, t.e * a.n + kb * kBK, fb, pol_w);
+              shared_box(b_dst + c * 8192, &tmB, t.n0 + c * 64, t.e * a.n + kb * kBK, (c * 2) / (BN / 64) == rank);
           } else if (MODE == kDX) {
             tma_load_2d(a_dst, &tmA, kb * kBK, t.row0, fb, pol_x);
-            tma_load_2d(b_dst, &tmB, kb * kBK, t.e * a.d + t.n0, fb, pol_w);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              shared_box(b_dst + h * (BN / 2) * 128, &tmB, kb * kBK, t.e * a.d + t.n0 + h * (BN / 2), h == rank);
           } else if (MODE == kDW1) {
             // B = dH rows [rb, rb+64) (MN-major); rows past the expert meet zero A rows
 #pragma unroll
             for (int c = 0; c < BN / 64; ++c)
-              tma_load_2d(b_dst + c * 8192, &tmB, t.n0 + c * 64, t.row0 + kb * kBK, fb, pol_x);
+              shared_box(b_dst + c * 8192, &tmB, t.n0 + c * 64, t.row0 + kb * kBK, (c * 2) / (BN / 64) == rank);
           } else {
             // kDW2: A = (s*A) rows [rb, rb+64) (MN-major); rows past the expert meet zero B rows
 #pragma unroll
             for (int c = 0; c < kBM / 64; ++c)
-              tma_load_2d(a_dst + c * 8192, &tmA, t.m0 + c * 64, t.row0 + kb * kBK, fb, pol_x);
+              shared_box(a_dst + c * 8192, &tmA, t.m0 + c * 64, t.row0 + kb * kBK, c == rank);
           }
           ++issued;
           if (++s == STAGES) {
@@ -294,8 +333,8 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     uint32_t ph = 0;
     int pending = 0, sig = 0;
     bool aborted = false;
-    for (int tile = blockIdx.x; tile < total && !aborted; tile += gridDim.x) {
-      const Tile t = decode_tile<MODE, BN>(a, tile, total_m);
+    for (int pair = first_pair; pair < total && !aborted; pair += pair_step) {
+      const Tile t = decode_tile<MODE, BN>(a, pair, rank, total_m);
       if (t.kblocks == 0) continue;
       const uint8_t *rowp[8];
       uint32_t rown[8];
@@ -369,8 +408,8 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
       int buf = 0;
       uint32_t bph = 0;
       bool aborted = false;
-      for (int tile = blockIdx.x; tile < total && !aborted; tile += gridDim.x) {
-        const Tile t = decode_tile<MODE, BN>(a, tile, total_m);
+      for (int pair = first_pair; pair < total && !aborted; pair += pair_step) {
+        const Tile t = decode_tile<MODE, BN>(a, pair, rank, total_m);
         if (t.kblocks == 0) continue;
         if (!mbar_wait(tempty_bar(buf), bph ^ 1u) || *abort_flag) {
           aborted = true;
@@ -394,7 +433,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
                                          : smem_desc_sw128(b_st + k * 32, 16, 1024);
             umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
-          umma_commit(empty_bar(s));
+          umma_commit_mc(empty_bar(s), 0x3);  // the stage is free for the producers of both CTAs
           if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
@@ -420,8 +459,8 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     uint32_t bph = 0;
     uint32_t hin_par = 0u;                       // dH epilogue: bit b = parity of H buffer b's next fill
     const uint64_t pol_stream = policy_evict_first();  // cached H is read exactly once
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const Tile t = decode_tile<MODE, BN>(a, tile, total_m);
+    for (int pair = first_pair; pair < total; pair += pair_step) {
+      const Tile t = decode_tile<MODE, BN>(a, pair, rank, total_m);
       if (t.kblocks == 0) {
         if (TR::varlen_k) {  // an expert without rows has an exactly zero weight gradient
           uint8_t *dst = static_cast<uint8_t *>(a.out0) +
@@ -653,28 +692,47 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+  cluster_sync();  // the partner's multicasts and stage releases into this CTA are all done
 }
 
-// Host launcher for one instantiation.
+// Host launcher for one instantiation: clusters of two CTAs, one CTA per SM, as many clusters as fit.
 template <int MODE, int BN, int STAGES>
 int launch_gemm(const GemmArgs &a, const TensorMaps &tm, cudaStream_t stream) {
   using SM = Smem<BN, STAGES, epi_bytes<MODE>()>;
   static int attr_dev = -1;
+  static int grid_cache = 0;
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return record_cuda_error(err);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(Traits<MODE>::threads, 1, 1);
+  cfg.dynamicSmemBytes = SM::kBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (attr_dev != dev) {
     err = cudaFuncSetAttribute(moe_gemm_kernel<MODE, BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                SM::kBytes);
     if (err != cudaSuccess) return record_cuda_error(err);
+    int clusters = 0;
+    cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+    err = cudaOccupancyMaxActiveClusters(&clusters, moe_gemm_kernel<MODE, BN, STAGES>, &cfg);
+    if (err != cudaSuccess || clusters <= 0) clusters = num_sms() / 2;
+    grid_cache = 2 * clusters;
     attr_dev = dev;
   }
+  cfg.gridDim = dim3(grid_cache, 1, 1);
   static const char *const kNames[] = {"gemm_up", "gemm_down", "gemm_dh", "gemm_dx", "gemm_dw1", "gemm_dw2"};
   prof_begin(kNames[MODE], stream);
-  moe_gemm_kernel<MODE, BN, STAGES><<<num_sms(), Traits<MODE>::threads, SM::kBytes, stream>>>(tm, a);
+  err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<MODE, BN, STAGES>, tm, a);
   prof_end(stream);
   count_launch();
-  err = cudaGetLastError();
+  if (err == cudaSuccess) err = cudaGetLastError();
   if (err != cudaSuccess) return record_cuda_error(err);
   return MOE_OK;
 }
