@@ -150,6 +150,12 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint3
                : "memory");
 }
 
+// The mbarrier receives one arrival once every cp.async this thread issued so far has landed (the
+// barrier's expected count already includes that arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
 template <int N>

@@ -52,7 +52,6 @@ struct Traits {
 };
 
 constexpr int kGatherThreads = 128;
-constexpr int kGatherLag = 2;  // stages a gather thread keeps in flight before it signals the oldest
 
 // Scatter-add epilogues transpose each warp's 32 x 32 fp32 chunk through shared memory so that one
 // red.v4 instruction covers four whole 128-byte rows; rows are padded by 16 bytes against bank conflicts.
@@ -331,7 +330,6 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     const size_t ld_bytes = static_cast<size_t>(a.gld) * 2;
     int s = 0;
     uint32_t ph = 0;
-    int pending = 0, sig = 0;
     bool aborted = false;
     for (int pair = first_pair; pair < total && !aborted; pair += pair_step) {
       const Tile t = decode_tile<MODE, BN>(a, pair, rank, total_m);
@@ -379,14 +377,9 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
             for (int c = 0; c < kChunks; ++c)
               cp_async_16(base_dst + q * 2048 + c * 8192, rowp[q] + static_cast<size_t>(mn0 + c * 64) * 2, rown[q]);
         }
-        cp_async_commit();
-        if (++pending > kGatherLag) {
-          cp_async_wait<kGatherLag>();
-          fence_proxy_async_smem();
-          mbar_arrive(full_bar(sig));
-          if (++sig == STAGES) sig = 0;
-          --pending;
-        }
+        // the stage's barrier counts this thread's arrival when its copies have landed; the MMA issuer
+        // fences the async proxy after the barrier before the tensor cores read the stage
+        cp_async_arrive_noinc(full_bar(s));
         if (++s == STAGES) {
           s = 0;
           ph ^= 1u;
@@ -394,11 +387,6 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
       }
     }
     cp_async_wait<0>();
-    fence_proxy_async_smem();
-    for (; pending > 0; --pending) {
-      mbar_arrive(full_bar(sig));
-      if (++sig == STAGES) sig = 0;
-    }
   } else if (warp == 1) {
     // -------------------------------------------------------------------------------- MMA issuer
     if (lane == 0) {
@@ -422,6 +410,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
             aborted = true;
             break;
           }
+          if (TR::gather) fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tensor-core reads
           tc_fence_after();
           const uint32_t a_st = sA + s * kABytes;
           const uint32_t b_st = sB + s * SM::kBBytes;
