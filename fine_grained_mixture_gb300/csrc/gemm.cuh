@@ -45,7 +45,10 @@ struct Traits {
   static constexpr bool gather_a_mn = (MODE == kDW1);                // A: token rows along K, MN-major
   static constexpr bool gather_b_mn = (MODE == kDW2);                // B: token rows along K, MN-major
   static constexpr bool gather = gather_a_k || gather_a_mn || gather_b_mn;
-  static constexpr int threads = gather ? 320 : 192;
+  static constexpr bool nt_outer_ = (MODE == kDown || MODE == kDX);
+  // the scatter-add GEMMs drain TMEM with eight warps (two per TMEM lane quarter, half the columns each)
+  static constexpr int epi_warps = nt_outer_ ? 8 : 4;
+  static constexpr int threads = gather ? 320 : 64 + 32 * epi_warps;
   static constexpr bool a_mn = varlen_k;  // A operand MN-major in shared memory
   static constexpr bool b_mn = (MODE == kUp || MODE == kDown || varlen_k);
   static constexpr bool nt_outer = (MODE == kDown || MODE == kDX);  // keep one fp32 column slab hot in L2
@@ -53,11 +56,11 @@ struct Traits {
 
 constexpr int kGatherThreads = 128;
 
-// Scatter-add epilogues transpose each warp's 32 x 32 fp32 chunk through shared memory so that one
-// red.v4 instruction covers four whole 128-byte rows; rows are padded by 16 bytes against bank conflicts.
-constexpr int kStgRowFloats = 36;
-constexpr int kStgWarpBytes = 32 * kStgRowFloats * 4;
-constexpr int kStgBytes = 4 * kStgWarpBytes;
+// Scatter-add epilogues: every thread stages 64 fp32 of its row (256 B, padded to 272 B against bank
+// conflicts) and hands it to the TMA engine as one bulk reduce-add into the fp32 accumulator row of its
+// token.  256-byte bulk adds reach about 1.6x the L2 reduction rate of per-lane red.v4.
+constexpr int kStgRowBytes = 272;
+constexpr int kStgBytes = 256 * kStgRowBytes;  // eight epilogue warps x 32 threads
 
 // dH epilogue, per warp: two 4 KB buffers of cached H (gate | up, 32 rows x 32 columns each) filled by TMA one
 // chunk ahead, and a 6 KB staging tile (dH gate | dH up | s*A) drained by TMA stores; 64-byte swizzle.
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), 4);
+      mbar_init(tempty_bar(b), TR::epi_warps);
     }
     mbar_init(drain_bar, 1);
     if (MODE == kDH)
@@ -440,13 +443,14 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
         *abort_flag = 1;
       }
     }
-  } else if (warp >= 2 && warp < 6) {
+  } else if (warp >= 2 && warp < 2 + TR::epi_warps) {
     // ---------------------------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     int buf = 0;
     uint32_t bph = 0;
     uint32_t hin_par = 0u;                       // dH epilogue: bit b = parity of H buffer b's next fill
+    const uint64_t pol_acc = policy_evict_last();  // keep the fp32 accumulator slab in L2
     const uint64_t pol_stream = policy_evict_first();  // cached H is read exactly once
     for (int pair = first_pair; pair < total; pair += pair_step) {
       const Tile t = decode_tile<MODE, BN>(a, pair, rank, total_m);
@@ -516,29 +520,28 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
           }
           if (MODE == kDown) sc = __ldg(&a.row_score[r]);
         }
-        const uint32_t stg = base + SM::kStgOff + q * kStgWarpBytes;
-        const uint32_t my_row = stg + lane * (kStgRowFloats * 4);
-        // read-back role: 8 lanes per row, 4 rows per instruction
-        const int sub_row = lane >> 3;
-        const int sub_col = (lane & 7) * 4;
+        const int half = (warp - 2) >> 2;  // which half of the BN columns this warp drains
+        float *grow = a.out_f32 + (size_t)(tok >= 0 ? tok : 0) * a.d + t.n0 + half * (BN / 2);
+        const uint32_t stg = base + SM::kStgOff + ((warp - 2) * 32 + lane) * kStgRowBytes;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tacc + c * 32, v);
+        for (int c = 0; c < BN / 128; ++c) {
+          uint32_t v0[32], v1[32];
+          const uint32_t col = half * (BN / 2) + c * 64;
+          tmem_ld32(tacc + col, v0);
+          tmem_ld32(tacc + col + 32, v1);
           tmem_ld_wait();
+          bulk_wait_read<0>();  // the previous bulk add has read the staging row
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            st_shared_v4(my_row + i * 16, sc * __uint_as_float(v[4 * i]), sc * __uint_as_float(v[4 * i + 1]),
-                         sc * __uint_as_float(v[4 * i + 2]), sc * __uint_as_float(v[4 * i + 3]));
-          __syncwarp();
+            st_shared_v4(stg + i * 16, sc * __uint_as_float(v0[4 * i]), sc * __uint_as_float(v0[4 * i + 1]),
+                         sc * __uint_as_float(v0[4 * i + 2]), sc * __uint_as_float(v0[4 * i + 3]));
 #pragma unroll
-          for (int rd = 0; rd < 8; ++rd) {
-            const int rr = rd * 4 + sub_row;
-            const int trr = __shfl_sync(0xffffffffu, tok, rr);
-            const float4 x = ld_shared_v4(stg + rr * (kStgRowFloats * 4) + sub_col * 4);
-            if (trr >= 0) red_add_v4(a.out_f32 + (size_t)trr * a.d + t.n0 + c * 32 + sub_col, x.x, x.y, x.z, x.w);
-          }
-          __syncwarp();
+          for (int i = 0; i < 8; ++i)
+            st_shared_v4(stg + 128 + i * 16, sc * __uint_as_float(v1[4 * i]), sc * __uint_as_float(v1[4 * i + 1]),
+                         sc * __uint_as_float(v1[4 * i + 2]), sc * __uint_as_float(v1[4 * i + 3]));
+          fence_proxy_async_smem();
+          if (tok >= 0) bulk_reduce_add_f32(grow + c * 64, stg, 256, pol_acc);
+          bulk_commit();
         }
       } else if (MODE == kDH) {
         const int r = t.row0 + row;
@@ -668,7 +671,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
         bph ^= 1u;
       }
     }
-    if (MODE == kDH) bulk_wait<0>();  // every TMA store has landed before the kernel ends
+    if (MODE == kDH || TR::nt_outer) bulk_wait<0>();  // every bulk store / add has landed before the end
   }
 
   __syncthreads();

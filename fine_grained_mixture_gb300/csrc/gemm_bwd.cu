@@ -9,7 +9,7 @@ int launch_dh(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, int bn) {
   return launch_gemm<kDH, 128, 4>(a, tm, s);
 }
 
-int launch_dx(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) { return launch_gemm<kDX, 256, 4>(a, tm, s); }
+int launch_dx(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) { return launch_gemm<kDX, 256, 3>(a, tm, s); }
 
 int launch_dw1(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) {
   return launch_gemm<kDW1, 256, 4>(a, tm, s);

@@ -7,7 +7,7 @@ namespace moe {
 int launch_up(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) { return launch_gemm<kUp, 256, 4>(a, tm, s); }
 
 int launch_down(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) {
-  return launch_gemm<kDown, 256, 4>(a, tm, s);
+  return launch_gemm<kDown, 256, 3>(a, tm, s);
 }
 
 }  // namespace moe

@@ -8,7 +8,7 @@
 // smaller than the distance down, and drops its weakest token-choice tokens otherwise.
 //
 // Pipeline (one stream, no host synchronisation):
-//   route_topk_kernel   one warp per token (32 warps per chunk): top-K by (logit desc, expert asc), softmax over the K,
+//   route_topk_kernel   one warp per token (32 tokens per CTA): top-K by (logit desc, expert asc), softmax over the K,
 //                       per-chunk (256 tokens) expert histograms, membership bitmap (TR only)
 //   route_scan_kernel   one CTA: per-chunk bases, counts (TC f_e or TR r_e), offsets, tile offsets
 //   route_fill_tc       one CTA per 256-token chunk: rows in ascending token order via bitmap ranks
@@ -30,8 +30,10 @@ __device__ __forceinline__ uint32_t order_key(float z) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-constexpr int kTopkThreads = 1024;                   // 32 warps per 256-token chunk
-constexpr int kTokensPerWarp = kChunk / (kTopkThreads / 32);
+constexpr int kTopkThreads = 256;                    // 8 warps, 4 tokens each: 32 tokens per CTA
+constexpr int kTokensPerWarp = 4;
+constexpr int kTopkTokens = (kTopkThreads / 32) * kTokensPerWarp;
+static_assert(kChunk % kTopkTokens == 0, "a top-K CTA must not straddle two histogram chunks");
 
 template <int NV>  // NV = logits held per lane = ceil(E / 32)
 __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float *__restrict__ logits, int T, int E, int K,
@@ -45,9 +47,10 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float *_
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int chunk = blockIdx.x;
+  const int t_first = blockIdx.x * kTopkTokens;
+  const int chunk = t_first / kChunk;
   for (int i = 0; i < kTokensPerWarp; ++i) {
-    const int t = chunk * kChunk + warp * kTokensPerWarp + i;
+    const int t = t_first + warp * kTokensPerWarp + i;
     if (t >= T) break;
     float v[NV];
     bool bad = false;
@@ -109,7 +112,8 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float *_
     }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_cnt[(size_t)chunk * E + e] = hist[e];
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    if (hist[e]) atomicAdd(&chunk_cnt[(size_t)chunk * E + e], hist[e]);
 }
 
 // Exclusive scan of one value per thread across a block of 1024 threads; returns the exclusive prefix and
@@ -346,6 +350,7 @@ int launch_route(const float *logits, int T, int E, int K, int mode, const moe_r
   RouteWs w = carve(ws, T, E, mode);
   cudaError_t err;
   err = cudaMemsetAsync(r->status, 0, MOE_STATUS_WORDS * sizeof(int32_t), stream);
+  if (err == cudaSuccess) err = cudaMemsetAsync(w.chunk_cnt, 0, (size_t)w.nchunks * E * 4, stream);
   if (err != cudaSuccess) return record_cuda_error(err);
   if (mode == MOE_ROUTE_TR) {
     err = cudaMemsetAsync(w.member, 0, (size_t)w.member_words * E * 4, stream);
@@ -355,7 +360,7 @@ int launch_route(const float *logits, int T, int E, int K, int mode, const moe_r
   const size_t hist_smem = (size_t)E * 4;
   const int nv = (E + 31) / 32;
 #define MOE_TOPK_LAUNCH(NV)                                                                                       \
-  route_topk_kernel<NV><<<w.nchunks, kTopkThreads, hist_smem, stream>>>(logits, T, E, K, want_member, r->topk_idx,          \
+  route_topk_kernel<NV><<<(T + kTopkTokens - 1) / kTopkTokens, kTopkThreads, hist_smem, stream>>>(logits, T, E, K, want_member, r->topk_idx,          \
                                                                r->topk_score, w.tok_max, w.tok_den, w.chunk_cnt, \
                                                                w.member, w.member_words, r->status)
   prof_begin("route_topk", stream);
