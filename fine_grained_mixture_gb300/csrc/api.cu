@@ -181,6 +181,16 @@ static size_t bwd_ws_bytes(int T, int d, int n, size_t p_cap) {
   return align256(p_cap * 2 * n * 2) + align256(p_cap * n * 2) + align256((size_t)T * d * 4);
 }
 
+// Column tiles (of 256) per pass of a scatter-add GEMM: the largest divisor of d/256 whose fp32 slab
+// T x (256 * group) stays within 64 MiB (about half of L2), so A is re-read d / (256 * group) times.
+static int scatter_nt_group(int T, int d) {
+  const int n_tiles = d / 256;
+  int best = 1;
+  for (int g = 1; g <= n_tiles; ++g)
+    if (n_tiles % g == 0 && (size_t)T * 256 * g * 4 <= ((size_t)64 << 20)) best = g;
+  return best;
+}
+
 static GemmArgs base_args(const moe_routing *r, int T, int d, int n, int E, size_t p_cap) {
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -194,6 +204,7 @@ static GemmArgs base_args(const moe_routing *r, int T, int d, int n, int E, size
   a.n = n;
   a.E = E;
   a.p_cap = static_cast<int>(p_cap);
+  a.nt_group = scatter_nt_group(T, d);
   return a;
 }
 

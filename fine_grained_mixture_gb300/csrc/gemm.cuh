@@ -141,8 +141,12 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &a, int pair, int ran
     const int n_pairs_m = (total_m + 1) / 2;
     int mp, nt;
     if (Traits<MODE>::nt_outer) {
-      nt = pair / n_pairs_m;
-      mp = pair - nt * n_pairs_m;
+      // passes over all m-tile pairs, nt_group column tiles per pass (neighbours share the A tile in L2)
+      const int per_pass = n_pairs_m * a.nt_group;
+      const int g = pair / per_pass;
+      const int rem = pair - g * per_pass;
+      mp = rem / a.nt_group;
+      nt = g * a.nt_group + (rem - mp * a.nt_group);
     } else {
       mp = pair / n_tiles;
       nt = pair - mp * n_tiles;
