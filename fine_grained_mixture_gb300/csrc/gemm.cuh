@@ -66,10 +66,14 @@ constexpr int kStgBytes = 256 * kStgRowBytes;  // eight epilogue warps x 32 thre
 // chunk ahead, and a 6 KB staging tile (dH gate | dH up | s*A) drained by TMA stores; 64-byte swizzle.
 constexpr int kDhWarpBytes = 2 * 4096 + 6144;
 
-template <int BN, int STAGES, int EPI_BYTES>
+// MB = 128-row M blocks per CTA.  The weight-gradient GEMMs (long K loop, light epilogue) use MB = 2: two
+// M=128 MMAs per k-step share the B tile, halving shared-memory bytes per FLOP so the same shared memory
+// covers twice the load latency; both accumulators fill TMEM (512 columns), so there is one buffer.
+template <int BN, int STAGES, int EPI_BYTES, int MB = 1>
 struct Smem {
+  static constexpr int kABytesMB = MB * kABytes;
   static constexpr int kBBytes = BN * kBK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStageBytes = kABytesMB + kBBytes;
   static constexpr int kStgOff = STAGES * kStageBytes;
   static constexpr int kBarOff = kStgOff + EPI_BYTES;
   static constexpr int kBytes = kBarOff + 256 + 1024;  // + barriers/flags + alignment slack
@@ -97,28 +101,29 @@ __device__ __forceinline__ int find_expert(const int32_t *__restrict__ tile_offs
 }
 
 // Number of cluster work items (pairs of tiles).
-template <int MODE, int BN>
+template <int MODE, int BN, int MB>
 __device__ __forceinline__ int total_pairs(const GemmArgs &a, int total_m) {
   const int n_tiles = a.Ndim / BN;
-  const int m_tiles = a.Mdim / kBM;
-  if (MODE == kDW1) return a.E * (m_tiles / 2) * n_tiles;        // pairs along M (d % 256 == 0)
+  const int m_tiles = a.Mdim / (kBM * MB);
+  if (MODE == kDW1) return a.E * ((m_tiles + 1) / 2) * n_tiles;  // pairs along M
   if (MODE == kDW2) return a.E * m_tiles * ((n_tiles + 1) / 2);  // pairs along N
   return ((total_m + 1) / 2) * n_tiles;                           // pairs of consecutive m-tiles
 }
 
-template <int MODE, int BN>
+template <int MODE, int BN, int MB>
 __device__ __forceinline__ Tile decode_tile(const GemmArgs &a, int pair, int rank, int total_m) {
   Tile t;
   const int n_tiles = a.Ndim / BN;
   t.shared = true;
   if (Traits<MODE>::varlen_k) {
-    const int m_tiles = a.Mdim / kBM;
+    const int m_tiles = a.Mdim / (kBM * MB);
     int mt, nt;
     if (MODE == kDW1) {
-      const int per_e = (m_tiles / 2) * n_tiles;
+      const int mp = (m_tiles + 1) / 2;
+      const int per_e = mp * n_tiles;
       t.e = pair / per_e;
       const int rem = pair - t.e * per_e;
-      mt = 2 * (rem / n_tiles) + rank;
+      mt = min(2 * (rem / n_tiles) + rank, m_tiles - 1);  // an odd last row pair computes its tile twice
       nt = rem % n_tiles;
     } else {
       const int np = (n_tiles + 1) / 2;
@@ -128,7 +133,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &a, int pair, int ran
       mt = rem / np;
       nt = min(2 * (rem % np) + rank, n_tiles - 1);  // an odd last column pair computes its tile twice
     }
-    t.m0 = mt * kBM;
+    t.m0 = mt * kBM * MB;
     t.n0 = nt * BN;
     t.row0 = __ldg(&a.offsets[t.e]);
     t.row_end = __ldg(&a.offsets[t.e + 1]);
@@ -177,20 +182,22 @@ __device__ __forceinline__ int token_or_oob(const GemmArgs &a, int r, int row_en
   return (t >= 0 && t < a.T) ? t : a.T;
 }
 
-template <int MODE, int BN, int STAGES>
+template <int MODE, int BN, int STAGES, int MB>
 __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     moe_gemm_kernel(const __grid_constant__ TensorMaps tm, const GemmArgs a) {
   const CUtensorMap &tmA = tm.a;
   const CUtensorMap &tmB = tm.b;
   using TR = Traits<MODE>;
-  using SM = Smem<BN, STAGES, epi_bytes<MODE>()>;
-  constexpr uint32_t kTmemCols = 2 * BN;
+  using SM = Smem<BN, STAGES, epi_bytes<MODE>(), MB>;
+  constexpr int kBufs = MB == 1 ? 2 : 1;           // TMEM accumulator buffers (double-buffered when MB = 1)
+  constexpr uint32_t kTmemCols = 2 * BN;            // MB * BN * kBufs == 2 * BN in both layouts
+  static_assert(MB * kBufs == 2, "TMEM holds two BN-column accumulators");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *gbase = smem_raw + (base - raw);
   const uint32_t sA = base;
-  const uint32_t sB = base + STAGES * kABytes;
+  const uint32_t sB = base + STAGES * SM::kABytesMB;
   const uint32_t bar = base + SM::kBarOff;
   auto full_bar = [&](int s) { return bar + 8u * s; };
   auto empty_bar = [&](int s) { return bar + 8u * (STAGES + s); };
@@ -242,7 +249,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
   const int first_pair = static_cast<int>(cluster_id_x());
   const int pair_step = static_cast<int>(num_clusters_x());
   const int total_m = TR::varlen_k ? 0 : __ldg(&a.tile_offsets[a.E]);
-  const int total = total_pairs<MODE, BN>(a, total_m);
+  const int total = total_pairs<MODE, BN, MB>(a, total_m);
 
   if (warp == 0) {
     // ------------------------------------------------------------------------------ TMA producer
@@ -253,7 +260,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     constexpr uint32_t kTmaBytes = MODE == kUp ? SM::kBBytes
                                    : MODE == kDH ? SM::kBBytes
                                    : MODE == kDW1 ? SM::kBBytes
-                                   : MODE == kDW2 ? kABytes
+                                   : MODE == kDW2 ? SM::kABytesMB
                                                   : SM::kStageBytes;
     int s = 0;
     uint32_t ph = 0;
@@ -261,7 +268,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     bool aborted = false;
     if (lane == 0) {
       for (int pair = first_pair; pair < total && !aborted; pair += pair_step) {
-        const Tile t = decode_tile<MODE, BN>(a, pair, rank, total_m);
+        const Tile t = decode_tile<MODE, BN, MB>(a, pair, rank, total_m);
         for (int kb = 0; kb < t.kblocks; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u) || *abort_flag) {
             set_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
@@ -270,7 +277,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
             break;
           }
           mbar_arrive_expect_tx(full_bar(s), kTmaBytes);
-          const uint32_t a_dst = sA + s * kABytes;
+          const uint32_t a_dst = sA + s * SM::kABytesMB;
           const uint32_t b_dst = sB + s * SM::kBBytes;
           const uint32_t fb = full_bar(s);
           // the shared operand: this CTA's half (multicast to both) or, when the partner needs a
@@ -309,8 +316,8 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
           } else {
             // kDW2: A = (s*A) rows [rb, rb+64) (MN-major); rows past the expert meet zero B rows
 #pragma unroll
-            for (int c = 0; c < kBM / 64; ++c)
-              shared_box(a_dst + c * 8192, &tmA, t.m0 + c * 64, t.row0 + kb * kBK, c == rank);
+            for (int c = 0; c < MB * kBM / 64; ++c)
+              shared_box(a_dst + c * 8192, &tmA, t.m0 + c * 64, t.row0 + kb * kBK, c / MB == rank);
           }
           ++issued;
           if (++s == STAGES) {
@@ -339,7 +346,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     uint32_t ph = 0;
     bool aborted = false;
     for (int pair = first_pair; pair < total && !aborted; pair += pair_step) {
-      const Tile t = decode_tile<MODE, BN>(a, pair, rank, total_m);
+      const Tile t = decode_tile<MODE, BN, MB>(a, pair, rank, total_m);
       if (t.kblocks == 0) continue;
       const uint8_t *rowp[8];
       uint32_t rown[8];
@@ -369,14 +376,14 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
           break;
         }
         if (TR::gather_a_k) {
-          const uint32_t dst = sA + s * kABytes + rsub * 128 + swz;
+          const uint32_t dst = sA + s * SM::kABytesMB + rsub * 128 + swz;
           const size_t koff = static_cast<size_t>(kb) * kBK * 2;
 #pragma unroll
           for (int q = 0; q < 8; ++q) cp_async_16(dst + q * 2048, rowp[q] + koff, rown[q]);
         } else {
           // MN-major: K-row k = rsub + 16q at byte k*128 of each 64-column chunk c (8 KB apart)
-          constexpr int kChunks = TR::gather_a_mn ? kBM / 64 : BN / 64;
-          const uint32_t base_dst = (TR::gather_a_mn ? sA + s * kABytes : sB + s * SM::kBBytes) + rsub * 128 + swz;
+          constexpr int kChunks = TR::gather_a_mn ? MB * kBM / 64 : BN / 64;
+          const uint32_t base_dst = (TR::gather_a_mn ? sA + s * SM::kABytesMB : sB + s * SM::kBBytes) + rsub * 128 + swz;
           const int mn0 = TR::gather_a_mn ? t.m0 : t.n0;
 #pragma unroll
           for (int q = 0; q < 4; ++q)
@@ -404,7 +411,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
       uint32_t bph = 0;
       bool aborted = false;
       for (int pair = first_pair; pair < total && !aborted; pair += pair_step) {
-        const Tile t = decode_tile<MODE, BN>(a, pair, rank, total_m);
+        const Tile t = decode_tile<MODE, BN, MB>(a, pair, rank, total_m);
         if (t.kblocks == 0) continue;
         if (!mbar_wait(tempty_bar(buf), bph ^ 1u) || *abort_flag) {
           aborted = true;
@@ -419,15 +426,19 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
           }
           if (TR::gather) fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tensor-core reads
           tc_fence_after();
-          const uint32_t a_st = sA + s * kABytes;
+          const uint32_t a_st = sA + s * SM::kABytesMB;
           const uint32_t b_st = sB + s * SM::kBBytes;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
-            const uint64_t ad = TR::a_mn ? smem_desc_sw128(a_st + k * 2048, 8192, 1024)
-                                         : smem_desc_sw128(a_st + k * 32, 16, 1024);
             const uint64_t bd = TR::b_mn ? smem_desc_sw128(b_st + k * 2048, 8192, 1024)
                                          : smem_desc_sw128(b_st + k * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+#pragma unroll
+            for (int mb = 0; mb < MB; ++mb) {
+              const uint32_t a_blk = a_st + mb * kABytes;
+              const uint64_t ad = TR::a_mn ? smem_desc_sw128(a_blk + k * 2048, 8192, 1024)
+                                           : smem_desc_sw128(a_blk + k * 32, 16, 1024);
+              umma_bf16(d_tmem + mb * BN, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            }
           }
           umma_commit_mc(empty_bar(s), 0x3);  // the stage is free for the producers of both CTAs
           if (++s == STAGES) {
@@ -437,7 +448,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
         }
         if (aborted) break;
         umma_commit(tfull_bar(buf));
-        if (++buf == 2) {
+        if (++buf == kBufs) {
           buf = 0;
           bph ^= 1u;
         }
@@ -457,12 +468,14 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     const uint64_t pol_acc = policy_evict_last();  // keep the fp32 accumulator slab in L2
     const uint64_t pol_stream = policy_evict_first();  // cached H is read exactly once
     for (int pair = first_pair; pair < total; pair += pair_step) {
-      const Tile t = decode_tile<MODE, BN>(a, pair, rank, total_m);
+      const Tile t = decode_tile<MODE, BN, MB>(a, pair, rank, total_m);
       if (t.kblocks == 0) {
         if (TR::varlen_k) {  // an expert without rows has an exactly zero weight gradient
-          uint8_t *dst = static_cast<uint8_t *>(a.out0) +
-                         (((size_t)t.e * a.Mdim + t.m0 + row) * a.Ndim + t.n0) * 2;
-          for (int c = 0; c < BN * 2; c += 16) st_v4(dst + c, 0u, 0u, 0u, 0u);
+          for (int mb = 0; mb < MB; ++mb) {
+            uint8_t *dst = static_cast<uint8_t *>(a.out0) +
+                           (((size_t)t.e * a.Mdim + t.m0 + mb * kBM + row) * a.Ndim + t.n0) * 2;
+            for (int c = 0; c < BN * 2; c += 16) st_v4(dst + c, 0u, 0u, 0u, 0u);
+          }
         }
         continue;
       }
@@ -497,8 +510,8 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
             for (int i = 0; i < 16; ++i) {
               const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
               const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
-              const float a0 = g0 / (1.f + __expf(-g0)) * u0;
-              const float a1 = g1 / (1.f + __expf(-g1)) * u1;
+              const float a0 = __fdividef(g0, 1.f + __expf(-g0)) * u0;
+              const float a1 = __fdividef(g1, 1.f + __expf(-g1)) * u1;
               hg[i] = pack_bf16x2(g0, g1);
               hu[i] = pack_bf16x2(u0, u1);
               av[i] = pack_bf16x2(a0, a1);
@@ -606,7 +619,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
               const float gg = h ? bf16_hi(hg[i]) : bf16_lo(hg[i]);
               const float uu = h ? bf16_hi(hu[i]) : bf16_lo(hu[i]);
               const float dap = __uint_as_float(v[2 * i + h]);
-              const float sig = 1.f / (1.f + __expf(-gg));
+              const float sig = __fdividef(1.f, 1.f + __expf(-gg));
               const float silu = gg * sig;
               const float act = silu * uu;
               ds += dap * act;
@@ -653,12 +666,14 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
         }
         if (valid) atomicAdd(&a.dS[r], ds);
       } else {
-        // weight gradients: bf16 rows of dW_e
-        uint8_t *dst = static_cast<uint8_t *>(a.out0) + (((size_t)t.e * a.Mdim + t.m0 + row) * a.Ndim + t.n0) * 2;
+        // weight gradients: bf16 rows of dW_e (M block mb sits in TMEM columns [mb * BN, (mb + 1) * BN))
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int cc = 0; cc < MB * (BN / 32); ++cc) {
+          const int mb = cc / (BN / 32), c = cc % (BN / 32);
+          uint8_t *dst = static_cast<uint8_t *>(a.out0) +
+                         (((size_t)t.e * a.Mdim + t.m0 + mb * kBM + row) * a.Ndim + t.n0) * 2;
           uint32_t v[32];
-          tmem_ld32(tacc + c * 32, v);
+          tmem_ld32(tacc + mb * BN + c * 32, v);
           tmem_ld_wait();
           uint32_t p[16];
 #pragma unroll
@@ -670,7 +685,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(buf));
-      if (++buf == 2) {
+      if (++buf == kBufs) {
         buf = 0;
         bph ^= 1u;
       }
@@ -692,9 +707,9 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
 }
 
 // Host launcher for one instantiation: clusters of two CTAs, one CTA per SM, as many clusters as fit.
-template <int MODE, int BN, int STAGES>
+template <int MODE, int BN, int STAGES, int MB = 1>
 int launch_gemm(const GemmArgs &a, const TensorMaps &tm, cudaStream_t stream) {
-  using SM = Smem<BN, STAGES, epi_bytes<MODE>()>;
+  using SM = Smem<BN, STAGES, epi_bytes<MODE>(), MB>;
   static int attr_dev = -1;
   static int grid_cache = 0;
   int dev = 0;
@@ -712,12 +727,12 @@ int launch_gemm(const GemmArgs &a, const TensorMaps &tm, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (attr_dev != dev) {
-    err = cudaFuncSetAttribute(moe_gemm_kernel<MODE, BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(moe_gemm_kernel<MODE, BN, STAGES, MB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                SM::kBytes);
     if (err != cudaSuccess) return record_cuda_error(err);
     int clusters = 0;
     cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
-    err = cudaOccupancyMaxActiveClusters(&clusters, moe_gemm_kernel<MODE, BN, STAGES>, &cfg);
+    err = cudaOccupancyMaxActiveClusters(&clusters, moe_gemm_kernel<MODE, BN, STAGES, MB>, &cfg);
     if (err != cudaSuccess || clusters <= 0) clusters = num_sms() / 2;
     grid_cache = 2 * clusters;
     attr_dev = dev;
@@ -725,7 +740,7 @@ int launch_gemm(const GemmArgs &a, const TensorMaps &tm, cudaStream_t stream) {
   cfg.gridDim = dim3(grid_cache, 1, 1);
   static const char *const kNames[] = {"gemm_up", "gemm_down", "gemm_dh", "gemm_dx", "gemm_dw1", "gemm_dw2"};
   prof_begin(kNames[MODE], stream);
-  err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<MODE, BN, STAGES>, tm, a);
+  err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<MODE, BN, STAGES, MB>, tm, a);
   prof_end(stream);
   count_launch();
   if (err == cudaSuccess) err = cudaGetLastError();
