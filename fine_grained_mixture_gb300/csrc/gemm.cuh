@@ -345,8 +345,19 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     int s = 0;
     uint32_t ph = 0;
     bool aborted = false;
+    // token ids of the next tile are fetched while the current tile's rows are copied
+    int tok_next[8];
+    auto fetch_tokens = [&](const Tile &tt) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) tok_next[q] = token_or_oob(a, tt.row0 + rsub + 16 * q, tt.row_end);
+    };
+    Tile t_next;
+    if (TR::gather_a_k && first_pair < total) {
+      t_next = decode_tile<MODE, BN, MB>(a, first_pair, rank, total_m);
+      fetch_tokens(t_next);
+    }
     for (int pair = first_pair; pair < total && !aborted; pair += pair_step) {
-      const Tile t = decode_tile<MODE, BN, MB>(a, pair, rank, total_m);
+      const Tile t = TR::gather_a_k ? t_next : decode_tile<MODE, BN, MB>(a, pair, rank, total_m);
       if (t.kblocks == 0) continue;
       const uint8_t *rowp[8];
       uint32_t rown[8];
@@ -354,9 +365,13 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
         // this thread copies piece j of rows rsub + 16q (q = 0..7) of the 128-row tile at every k-block
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          const int tok = token_or_oob(a, t.row0 + rsub + 16 * q, t.row_end);
+          const int tok = tok_next[q];
           rown[q] = tok < a.T ? 16u : 0u;
           rowp[q] = src_base + (tok < a.T ? tok : 0) * ld_bytes + j * 16;
+        }
+        if (pair + pair_step < total) {
+          t_next = decode_tile<MODE, BN, MB>(a, pair + pair_step, rank, total_m);
+          fetch_tokens(t_next);
         }
       }
       for (int kb = 0; kb < t.kblocks; ++kb) {

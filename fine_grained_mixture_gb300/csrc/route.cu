@@ -35,6 +35,11 @@ constexpr int kTokensPerWarp = 4;
 constexpr int kTopkTokens = (kTopkThreads / 32) * kTokensPerWarp;
 static_assert(kChunk % kTopkTokens == 0, "a top-K CTA must not straddle two histogram chunks");
 
+// Inverse of order_key.
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 template <int NV>  // NV = logits held per lane = ceil(E / 32)
 __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float *__restrict__ logits, int T, int E, int K,
                                                          int want_member, int32_t *__restrict__ topk_idx,
@@ -66,34 +71,78 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float *_
       for (int j = 0; j < NV; ++j)
         if (!isfinite(v[j])) v[j] = -INFINITY;
     }
-    uint32_t taken = 0;  // bit j: v[j] already selected
-    int my_e = -1;       // lane k keeps the k-th selection
+    int my_e = -1;  // lane k keeps the k-th selection
     float my_z = 0.f, z0 = 0.f;
-    for (int k = 0; k < K; ++k) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
+    if (NV <= 8) {
+      // each lane sorts its NV logits once (key descending; equal keys keep the lower expert first), then
+      // every round is two warp reductions: the largest key, then the lowest expert holding it
+      uint32_t key[NV];
+      int ex[NV];
 #pragma unroll
       for (int j = 0; j < NV; ++j) {
         const int e = lane + 32 * j;
-        if (e < E && !((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < be) || be == 0x7fffffff)) {
-          bv = v[j];
-          be = e;
-        }
+        key[j] = (e < E) ? order_key(v[j]) : 0u;
+        ex[j] = (e < E) ? e : 0x7fffffff;
       }
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
+      for (int i = 1; i < NV; ++i)
+#pragma unroll
+        for (int j = i; j > 0; --j)
+          if (key[j] > key[j - 1]) {
+            const uint32_t tk = key[j];
+            key[j] = key[j - 1];
+            key[j - 1] = tk;
+            const int te = ex[j];
+            ex[j] = ex[j - 1];
+            ex[j - 1] = te;
+          }
+      for (int k = 0; k < K; ++k) {
+        const uint32_t mx = __reduce_max_sync(0xffffffffu, key[0]);
+        const uint32_t we = __reduce_min_sync(0xffffffffu, key[0] == mx ? static_cast<uint32_t>(ex[0]) : 0xffffffffu);
+        if (static_cast<uint32_t>(ex[0]) == we) {
+#pragma unroll
+          for (int j = 0; j + 1 < NV; ++j) {
+            key[j] = key[j + 1];
+            ex[j] = ex[j + 1];
+          }
+          key[NV - 1] = 0u;
+          ex[NV - 1] = 0x7fffffff;
+        }
+        const float z = key_to_float(mx);
+        if (k == 0) z0 = z;
+        if (lane == k) {
+          my_e = static_cast<int>(we);
+          my_z = z;
         }
       }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (k == 0) z0 = bv;
-      if (lane == k) {
-        my_e = be;
-        my_z = bv;
+    } else {
+      uint32_t taken = 0;  // bit j: v[j] already selected
+      for (int k = 0; k < K; ++k) {
+        float bv = -INFINITY;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+          const int e = lane + 32 * j;
+          if (e < E && !((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < be) || be == 0x7fffffff)) {
+            bv = v[j];
+            be = e;
+          }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+          const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+          if (ov > bv || (ov == bv && oe < be)) {
+            bv = ov;
+            be = oe;
+          }
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        if (k == 0) z0 = bv;
+        if (lane == k) {
+          my_e = be;
+          my_z = bv;
+        }
       }
     }
     // softmax over the K selected logits, in selection order
