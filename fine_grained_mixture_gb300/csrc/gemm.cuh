@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     // ------------------------------------------------------------------------------ TMA producer
     // weights: reused by the m-tiles of one expert, which run close together -> normal priority;
     // the dense activation operand of the scatter-add GEMMs streams through once per column slab -> first
-    const uint64_t pol_w = policy_evict_normal();
+    const uint64_t pol_w = TR::gather ? policy_evict_first() : policy_evict_normal();
     const uint64_t pol_x = TR::nt_outer ? policy_evict_first() : policy_evict_normal();
     constexpr uint32_t kTmaBytes = MODE == kUp ? SM::kBBytes
                                    : MODE == kDH ? SM::kBBytes
@@ -342,6 +342,8 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     const uint32_t swz = static_cast<uint32_t>((j ^ (rsub & 7)) << 4);
     const uint8_t *src_base = static_cast<const uint8_t *>(a.gsrc);
     const size_t ld_bytes = static_cast<size_t>(a.gld) * 2;
+    // token rows (X or dO) are gathered about K times each: keep them in L2 ahead of the streamed weights
+    const uint64_t pol_rows = policy_evict_last();
     int s = 0;
     uint32_t ph = 0;
     bool aborted = false;
@@ -394,7 +396,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
           const uint32_t dst = sA + s * SM::kABytesMB + rsub * 128 + swz;
           const size_t koff = static_cast<size_t>(kb) * kBK * 2;
 #pragma unroll
-          for (int q = 0; q < 8; ++q) cp_async_16(dst + q * 2048, rowp[q] + koff, rown[q]);
+          for (int q = 0; q < 8; ++q) cp_async_16_hint(dst + q * 2048, rowp[q] + koff, rown[q], pol_rows);
         } else {
           // MN-major: K-row k = rsub + 16q at byte k*128 of each 64-column chunk c (8 KB apart)
           constexpr int kChunks = TR::gather_a_mn ? MB * kBM / 64 : BN / 64;
@@ -404,7 +406,8 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
           for (int q = 0; q < 4; ++q)
 #pragma unroll
             for (int c = 0; c < kChunks; ++c)
-              cp_async_16(base_dst + q * 2048 + c * 8192, rowp[q] + static_cast<size_t>(mn0 + c * 64) * 2, rown[q]);
+              cp_async_16_hint(base_dst + q * 2048 + c * 8192, rowp[q] + static_cast<size_t>(mn0 + c * 64) * 2, rown[q],
+                               pol_rows);
         }
         // the stage's barrier counts this thread's arrival when its copies have landed; the MMA issuer
         // fences the async proxy after the barrier before the tensor cores read the stage
