@@ -63,6 +63,21 @@ def peaks():
         return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
 
 
+def reduce_max(x: float, world: int, device) -> float:
+    """Max of a per-rank scalar over all ranks (the slowest replica sets the step time)."""
+    if world <= 1:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_tflops(flops_per_rank: float, ms_max: float, world: int) -> float:
+    """Whole-job throughput of N independent replicas: all ranks' FLOPs over the slowest rank's time."""
+    return world * flops_per_rank / (ms_max * 1e-3) / 1e12
+
+
 def layer_flops(w, P=None):
     rows = w.T * w.K if P is None else P
     return 6.0 * rows * w.n * w.d, 12.0 * rows * w.n * w.d
@@ -374,14 +389,9 @@ def main():
     clocks = sampler.stop(t0, t1)
     prof = moe.profile_summary()
 
-    ms_local = total_ms / args.steps
-    ms = ms_local
-    if world > 1:
-        t = torch.tensor([ms_local], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(total_ms / args.steps, world, dev)
     ff, fb = layer_flops(w)
-    value = world * (ff + fb) / (ms * 1e-3) / 1e12
+    value = weak_scaling_tflops(ff + fb, ms, world)
     cache = layer.cached_bytes()
     P = cache["P"]
 
@@ -471,13 +481,9 @@ def e2e_measure(layer, inp, args, world, dev):
         one()
     e1.record()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(e0.elapsed_time(e1) / args.steps, world, dev)
     ff, fb = layer_flops(w)
-    return {"value": world * (ff + fb) / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
+    return {"value": weak_scaling_tflops(ff + fb, ms, world), "unit": UNIT, "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "note": "weights and weight gradients stay resident in HBM; activations cross PCIe/C2C each step"}
 
