@@ -205,6 +205,7 @@ static GemmArgs base_args(const moe_routing *r, int T, int d, int n, int E, size
   a.E = E;
   a.p_cap = static_cast<int>(p_cap);
   a.nt_group = scatter_nt_group(T, d);
+  a.wide_m = 0;
   return a;
 }
 
@@ -361,6 +362,7 @@ int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, cons
   if ((rc = make_tmap_bf16(&tm.b, dH, 2 * (uint64_t)n, p_cap, 64)) != MOE_OK) return rc;
   tm.a = tm.b;
   GemmArgs aw = base_args(r, T, d, n, E, p_cap);
+  aw.wide_m = (int64_t)T * K >= (int64_t)1024 * E;  // experts average >= 1024 rows: >= 16 k-blocks per tile
   aw.Mdim = d;
   aw.Ndim = 2 * n;
   aw.out0 = dW1;

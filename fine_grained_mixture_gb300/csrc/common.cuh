@@ -107,9 +107,9 @@ __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *
 }
 
 // 2D tiled store of a shared-memory box to (c0, c1) of the tensor map (bulk async group of this thread).
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap *tm, uint32_t src, int c0, int c1) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tm), "r"(src),
-               "r"(c0), "r"(c1)
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *tm, uint32_t src, int c0, int c1, uint64_t policy) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(tm),
+               "r"(src), "r"(c0), "r"(c1), "l"(policy)
                : "memory");
 }
 
@@ -328,6 +328,13 @@ __device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
                : "memory");
   return v;
+}
+
+// 16-byte store with an L2 eviction-priority hint (streamed outputs should not displace reused inputs).
+__device__ __forceinline__ void st_v4_hint(void *addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(addr), "r"(a), "r"(b), "r"(c), "r"(d),
+               "l"(policy)
+               : "memory");
 }
 
 __device__ __forceinline__ void st_v4(void *addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {

@@ -484,7 +484,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     uint32_t bph = 0;
     uint32_t hin_par = 0u;                       // dH epilogue: bit b = parity of H buffer b's next fill
     const uint64_t pol_acc = policy_evict_last();  // keep the fp32 accumulator slab in L2
-    const uint64_t pol_stream = policy_evict_first();  // cached H is read exactly once
+    const uint64_t pol_stream = policy_evict_first();  // streamed epilogue traffic (H, A, dH, s*A) is touched once here
     for (int pair = first_pair; pair < total; pair += pair_step) {
       const Tile t = decode_tile<MODE, BN, MB>(a, pair, rank, total_m);
       if (t.kblocks == 0) {
@@ -537,9 +537,12 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
             const int j = j0 + c * 32;
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-              st_v4(hrow + (size_t)j * 2 + v * 16, hg[4 * v], hg[4 * v + 1], hg[4 * v + 2], hg[4 * v + 3]);
-              st_v4(hrow + (size_t)(a.n + j) * 2 + v * 16, hu[4 * v], hu[4 * v + 1], hu[4 * v + 2], hu[4 * v + 3]);
-              st_v4(arow + (size_t)j * 2 + v * 16, av[4 * v], av[4 * v + 1], av[4 * v + 2], av[4 * v + 3]);
+              st_v4_hint(hrow + (size_t)j * 2 + v * 16, hg[4 * v], hg[4 * v + 1], hg[4 * v + 2], hg[4 * v + 3],
+                         pol_stream);
+              st_v4_hint(hrow + (size_t)(a.n + j) * 2 + v * 16, hu[4 * v], hu[4 * v + 1], hu[4 * v + 2], hu[4 * v + 3],
+                         pol_stream);
+              st_v4_hint(arow + (size_t)j * 2 + v * 16, av[4 * v], av[4 * v + 1], av[4 * v + 2], av[4 * v + 3],
+                         pol_stream);
             }
           }
         }
@@ -667,9 +670,9 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&tm.dh, out_st, j, wrow);
-              tma_store_2d(&tm.dh, out_st + 2048, a.n + j, wrow);
-              tma_store_2d(&tm.sa, out_st + 4096, j, wrow);
+              tma_store_2d(&tm.dh, out_st, j, wrow, pol_stream);
+              tma_store_2d(&tm.dh, out_st + 2048, a.n + j, wrow, pol_stream);
+              tma_store_2d(&tm.sa, out_st + 4096, j, wrow, pol_stream);
               bulk_commit();
             }
           } else if (valid) {

@@ -11,14 +11,15 @@ int launch_dh(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, int bn) {
 
 int launch_dx(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) { return launch_gemm<kDX, 256, 3>(a, tm, s); }
 
-// 256-row M blocks when the weight's row count allows it (see Smem), else 128.
+// 256-row M blocks (see Smem) when the weight's row count allows it and the experts' K loops are long
+// enough to hide the unoverlapped epilogue; else 128-row blocks with double-buffered TMEM.
 int launch_dw1(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) {
-  if (a.Mdim % 256 == 0) return launch_gemm<kDW1, 256, 3, 2>(a, tm, s);
+  if (a.wide_m && a.Mdim % 256 == 0) return launch_gemm<kDW1, 256, 3, 2>(a, tm, s);
   return launch_gemm<kDW1, 256, 4, 1>(a, tm, s);
 }
 
 int launch_dw2(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) {
-  if (a.Mdim % 256 == 0) return launch_gemm<kDW2, 256, 3, 2>(a, tm, s);
+  if (a.wide_m && a.Mdim % 256 == 0) return launch_gemm<kDW2, 256, 3, 2>(a, tm, s);
   return launch_gemm<kDW2, 256, 4, 1>(a, tm, s);
 }
 

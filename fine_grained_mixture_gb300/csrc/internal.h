@@ -41,6 +41,7 @@ struct GemmArgs {
   int Ndim;  // output columns
   int Kdim;  // varlen-M: reduction length
   int nt_group;  // scatter-add GEMMs: column tiles per pass over all m-tiles (the fp32 slab kept in L2)
+  int wide_m;    // weight-gradient GEMMs: 256-row blocks (experts average >= 1024 rows) instead of 128
   void *out0;        // up: H;  dH: dH;  dW1/dW2: the weight gradient
   void *out1;        // up: A;  dH: s*A
   float *out_f32;    // down: fp32 O;  dX~: fp32 dX

@@ -262,18 +262,42 @@ __global__ void __launch_bounds__(kChunk) route_fill_tc_kernel(int T, int E, int
 }
 
 // One CTA (1024 threads) per expert.  Keys of all T tokens for this expert live in shared memory.
-__global__ void __launch_bounds__(1024) route_fill_tr_kernel(
+//   selection: a 4-pass radix select (8 bits per pass, most significant first) over the candidates finds the
+//              key of the R-th best candidate; each group of four warps fills its own 256-bin histogram and one
+//              warp scans the bins; candidates equal to that key are kept lowest token first
+//   output:    each warp owns a contiguous token range; ballots give in-order ranks, so the whole pass needs
+//              two block-wide scans (tie ranks, row positions)
+constexpr int kTrThreads = 1024;
+constexpr int kTrWarps = kTrThreads / 32;
+constexpr int kTrHists = 8;
+
+__device__ __forceinline__ int warp_scan_exclusive(int v, int *total) {
+  const int lane = threadIdx.x & 31;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  *total = __shfl_sync(0xffffffffu, x, 31);
+  return x - v;
+}
+
+__global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
     const float *__restrict__ logits, int T, int E, int K, const int32_t *__restrict__ topk_idx,
     const float *__restrict__ topk_score, const float *__restrict__ tok_max, const float *__restrict__ tok_den,
     const uint32_t *__restrict__ member, int member_words, const int32_t *__restrict__ tc_counts,
     const int32_t *__restrict__ counts, const int32_t *__restrict__ offsets, int32_t *__restrict__ row_token,
     int32_t *__restrict__ row_slot, float *__restrict__ row_score) {
   extern __shared__ uint32_t sm[];
-  uint32_t *key = sm;                        // [T]
-  uint32_t *mem = sm + T;                    // [member_words]
-  int *hist = reinterpret_cast<int *>(mem + member_words);  // [256]
-  __shared__ int scratch[32];
-  __shared__ int sel_state[3];
+  uint32_t *key = sm;                                       // [T]
+  uint32_t *mem = sm + T;                                   // [member_words]
+  int *hist = reinterpret_cast<int *>(mem + member_words);  // [kTrHists][256]
+  uint32_t *keep_bits = reinterpret_cast<uint32_t *>(hist + kTrHists * 256);  // [member_words]
+  __shared__ int warp_tot[kTrWarps];
+  __shared__ int warp_base[kTrWarps];
+  __shared__ int sel_state[2];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int e = blockIdx.x;
   const int f = tc_counts[e], r = counts[e], base = offsets[e];
   if (r == 0) return;
@@ -286,68 +310,130 @@ __global__ void __launch_bounds__(1024) route_fill_tr_kernel(
   uint32_t prefix = 0u, mask = 0u;
   int remaining = R;
   if (r != f) {
+    int *my_hist = hist + (warp >> 2) * 256;
     for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+      for (int i = threadIdx.x; i < kTrHists * 256; i += blockDim.x) hist[i] = 0;
       __syncthreads();
       for (int t = threadIdx.x; t < T; t += blockDim.x) {
         const bool tc = (mem[t >> 5] >> (t & 31)) & 1u;
-        if (tc == drop && (key[t] & mask) == prefix) atomicAdd(&hist[(key[t] >> shift) & 255u], 1);
+        const uint32_t k = key[t];
+        if (tc == drop && (k & mask) == prefix) atomicAdd(&my_hist[(k >> shift) & 255u], 1);
       }
       __syncthreads();
-      if (threadIdx.x == 0) {
-        int acc = 0, b = 255;
-        for (; b > 0; --b) {
-          if (acc + hist[b] >= remaining) break;
-          acc += hist[b];
+      if (warp == 0) {
+        // lane l owns bins 255 - 8l - i (i = 0..7), i.e. lane 0 the highest bins
+        int c[8], lane_sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int b = 255 - (lane * 8 + i);
+          int v = 0;
+#pragma unroll
+          for (int g = 0; g < kTrHists; ++g) v += hist[g * 256 + b];
+          c[i] = v;
+          lane_sum += v;
         }
-        sel_state[0] = b;
-        sel_state[1] = remaining - acc;
+        int tot;
+        const int before = warp_scan_exclusive(lane_sum, &tot);
+        if (before < remaining && remaining <= before + lane_sum) {
+          int acc = before;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (acc + c[i] >= remaining) {
+              sel_state[0] = 255 - (lane * 8 + i);
+              sel_state[1] = remaining - acc;
+              break;
+            }
+            acc += c[i];
+          }
+        }
       }
       __syncthreads();
       prefix |= static_cast<uint32_t>(sel_state[0]) << shift;
       mask |= 255u << shift;
       remaining = sel_state[1];
-      __syncthreads();
     }
   }
-  // prefix = key of the R-th best candidate; `remaining` candidates equal to it are kept, lowest token first
-  int eq_carry = 0, row_carry = 0;
-  for (int t0 = 0; t0 < T; t0 += blockDim.x) {
-    const int t = t0 + threadIdx.x;
-    bool tc = false, cand = false, eq = false, gt = false;
+  // prefix = key of the R-th best candidate; `remaining` candidates equal to it are kept, lowest token first.
+  const int span = ((T + kTrThreads - 1) / kTrThreads) * 32;  // tokens per warp, a multiple of 32
+  const int t_lo = warp * span;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  // pass 1: ties (candidates whose key equals the boundary key) per warp
+  int eq_count = 0;
+  if (r != f) {
+    for (int t0 = t_lo; t0 < t_lo + span && t0 < T; t0 += 32) {
+      const int t = t0 + lane;
+      bool eq = false;
+      if (t < T) {
+        const bool tc = (mem[t >> 5] >> (t & 31)) & 1u;
+        eq = (tc == drop) && key[t] == prefix;
+      }
+      eq_count += __popc(__ballot_sync(0xffffffffu, eq));
+    }
+  }
+  if (lane == 0) warp_tot[warp] = eq_count;
+  __syncthreads();
+  if (warp == 0) {
+    int tot;
+    const int b = warp_scan_exclusive(warp_tot[lane], &tot);
+    warp_base[lane] = b;
+  }
+  __syncthreads();
+  // pass 2: keep decisions in token order; the kept bits of each 32-token group go to shared memory
+  int eq_run = warp_base[warp];
+  int keep_count = 0;
+  for (int t0 = t_lo; t0 < t_lo + span && t0 < T; t0 += 32) {
+    const int t = t0 + lane;
+    bool tc = false, gt = false, eq = false;
     if (t < T) {
       tc = (mem[t >> 5] >> (t & 31)) & 1u;
-      cand = (r != f) && (tc == drop);
-      gt = cand && key[t] > prefix;
-      eq = cand && key[t] == prefix;
+      if (r != f && tc == drop) {
+        const uint32_t k = key[t];
+        gt = k > prefix;
+        eq = k == prefix;
+      }
     }
-    int eq_total;
-    const int eq_rank = block_exclusive_scan_1024(eq ? 1 : 0, scratch, &eq_total) + eq_carry;
-    eq_carry += eq_total;
+    const uint32_t eq_bal = __ballot_sync(0xffffffffu, eq);
+    const int eq_rank = eq_run + __popc(eq_bal & lt_mask);
+    eq_run += __popc(eq_bal);
     bool keep;
-    if (r == f) keep = tc;
-    else if (drop) keep = gt || (eq && eq_rank < remaining);
-    else keep = tc || gt || (eq && eq_rank < remaining);
-    int kept_total;
-    const int pos = block_exclusive_scan_1024(keep ? 1 : 0, scratch, &kept_total) + row_carry;
-    row_carry += kept_total;
-    if (keep) {
-      const int row = base + pos;
+    if (r == f) {
+      keep = tc;
+    } else {
+      const bool take = gt || (eq && eq_rank < remaining);
+      keep = drop ? take : (tc || take);
+    }
+    const uint32_t kb = __ballot_sync(0xffffffffu, keep);
+    if (lane == 0) keep_bits[t0 >> 5] = kb;
+    keep_count += __popc(kb);
+  }
+  __syncthreads();
+  if (lane == 0) warp_tot[warp] = keep_count;
+  __syncthreads();
+  if (warp == 0) {
+    int tot;
+    const int b = warp_scan_exclusive(warp_tot[lane], &tot);
+    warp_base[lane] = b;
+  }
+  __syncthreads();
+  // pass 3: rows in ascending token order
+  int row = base + warp_base[warp];
+  for (int t0 = t_lo; t0 < t_lo + span && t0 < T; t0 += 32) {
+    const uint32_t kb = keep_bits[t0 >> 5];
+    const int t = t0 + lane;
+    if ((kb >> lane) & 1u) {
+      const int pos = row + __popc(kb & lt_mask);
       int slot = -1;
-      float s;
-      if (tc) {
+      if ((mem[t >> 5] >> (t & 31)) & 1u) {
         for (int k = 0; k < K; ++k)
           if (topk_idx[(size_t)t * K + k] == e) slot = k;
       }
-      if (slot >= 0) {
-        s = topk_score[(size_t)t * K + slot];
-      } else {
-        s = expf(logits[(size_t)t * E + e] - tok_max[t]) / tok_den[t];
-      }
-      row_token[row] = t;
-      row_slot[row] = slot;
-      row_score[row] = s;
+      const float sc = slot >= 0 ? topk_score[(size_t)t * K + slot]
+                                 : expf(logits[(size_t)t * E + e] - tok_max[t]) / tok_den[t];
+      row_token[pos] = t;
+      row_slot[pos] = slot;
+      row_score[pos] = sc;
     }
+    row += __popc(kb);
   }
 }
 
@@ -392,7 +478,9 @@ static RouteWs carve(void *ws, int T, int E, int mode) {
   return w;
 }
 
-size_t route_tr_smem_bytes(int T) { return (size_t)T * 4 + (size_t)((T + 31) / 32) * 4 + 256 * 4; }
+size_t route_tr_smem_bytes(int T) {
+  return (size_t)T * 4 + (size_t)((T + 31) / 32) * 4 * 2 + kTrHists * 256 * 4;
+}
 
 int launch_route(const float *logits, int T, int E, int K, int mode, const moe_routing *r, void *ws,
                  cudaStream_t stream) {
@@ -443,7 +531,7 @@ int launch_route(const float *logits, int T, int E, int K, int mode, const moe_r
       attr_set_dev = dev;
     }
     prof_begin("route_fill_tr", stream);
-    route_fill_tr_kernel<<<E, 1024, smem, stream>>>(logits, T, E, K, r->topk_idx, r->topk_score, w.tok_max, w.tok_den,
+    route_fill_tr_kernel<<<E, kTrThreads, smem, stream>>>(logits, T, E, K, r->topk_idx, r->topk_score, w.tok_max, w.tok_den,
                                                     w.member, w.member_words, r->tc_counts, r->counts, r->offsets,
                                                     r->row_token, r->row_slot, r->row_score);
   }
