@@ -378,14 +378,18 @@ def main():
         torch.distributed.barrier()
     torch.cuda.synchronize()
     launches0 = moe.kernel_launch_count()
-    moe.profile_enable(True)
     t0 = time.time()
     total_ms, parts = time_steps(layer, args.steps, split=True)
     t1 = time.time()
-    moe.profile_enable(False)
     launches = moe.kernel_launch_count() - launches0
     if world > 1:
         torch.distributed.barrier()
+    # per-kernel CUDA events on the launch stream, over the same number of steps: a second pass, because
+    # events between kernels would serialise the programmatic overlap of consecutive kernels
+    torch.cuda.synchronize()
+    moe.profile_enable(True)
+    time_steps(layer, args.steps)
+    moe.profile_enable(False)
     clocks = sampler.stop(t0, t1)
     prof = moe.profile_summary()
 

@@ -7,6 +7,8 @@ namespace moe {
 
 __global__ void __launch_bounds__(256) f32_to_bf16_kernel(const float4 *__restrict__ src, uint2 *__restrict__ dst,
                                                           size_t n4) {
+  griddep_wait();
+  griddep_launch_dependents();
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
     const float4 v = __ldcs(src + i);
     uint2 o;
@@ -20,16 +22,19 @@ int launch_f32_to_bf16(const float *src, void *dst, size_t count, cudaStream_t s
   const size_t n4 = count / 4;  // count is a multiple of 256 (d % 256 == 0)
   const int blocks = num_sms() * 8;
   prof_begin("cast_f32_bf16", s);
-  f32_to_bf16_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4 *>(src), reinterpret_cast<uint2 *>(dst), n4);
+  cudaError_t err = launch_pdl(f32_to_bf16_kernel, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const float4 *>(src),
+                               reinterpret_cast<uint2 *>(dst), n4);
   prof_end(s);
   count_launch();
-  const cudaError_t err = cudaGetLastError();
+  if (err == cudaSuccess) err = cudaGetLastError();
   return err == cudaSuccess ? MOE_OK : record_cuda_error(err);
 }
 
 __global__ void __launch_bounds__(256) zero_tail_kernel(uint4 *__restrict__ a, uint4 *__restrict__ b,
                                                         const int32_t *__restrict__ offsets, int E, size_t p_cap,
                                                         int ld_a, int ld_b) {
+  griddep_wait();
+  griddep_launch_dependents();
   const size_t P = static_cast<size_t>(offsets[E]);
   if (P >= p_cap) return;
   const size_t va = ld_a / 8, vb = ld_b / 8;  // uint4 per row
@@ -44,11 +49,11 @@ __global__ void __launch_bounds__(256) zero_tail_kernel(uint4 *__restrict__ a, u
 int launch_zero_tail(void *a, void *b, const int32_t *offsets, int E, size_t p_cap, int ld_a, int ld_b,
                      cudaStream_t s) {
   prof_begin("zero_tail", s);
-  zero_tail_kernel<<<num_sms(), 256, 0, s>>>(static_cast<uint4 *>(a), static_cast<uint4 *>(b), offsets, E, p_cap,
-                                             ld_a, ld_b);
+  cudaError_t err = launch_pdl(zero_tail_kernel, dim3(num_sms()), dim3(256), 0, s, static_cast<uint4 *>(a),
+                               static_cast<uint4 *>(b), offsets, E, p_cap, ld_a, ld_b);
   prof_end(s);
   count_launch();
-  const cudaError_t err = cudaGetLastError();
+  if (err == cudaSuccess) err = cudaGetLastError();
   return err == cudaSuccess ? MOE_OK : record_cuda_error(err);
 }
 

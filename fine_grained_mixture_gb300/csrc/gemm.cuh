@@ -244,6 +244,9 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
   cluster_sync();  // barriers of both CTAs initialised before any multicast lands in them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // everything above overlaps the previous kernel's tail; its outputs are read only after this wait
+  griddep_wait();
+  griddep_launch_dependents();
 
   const int rank = static_cast<int>(cluster_ctarank());
   const int first_pair = static_cast<int>(cluster_id_x());
@@ -737,16 +740,18 @@ int launch_gemm(const GemmArgs &a, const TensorMaps &tm, cudaStream_t stream) {
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return record_cuda_error(err);
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(Traits<MODE>::threads, 1, 1);
   cfg.dynamicSmemBytes = SM::kBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;  // occupancy query with the cluster shape only
   if (attr_dev != dev) {
     err = cudaFuncSetAttribute(moe_gemm_kernel<MODE, BN, STAGES, MB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                SM::kBytes);
@@ -759,6 +764,7 @@ int launch_gemm(const GemmArgs &a, const TensorMaps &tm, cudaStream_t stream) {
     attr_dev = dev;
   }
   cfg.gridDim = dim3(grid_cache, 1, 1);
+  cfg.numAttrs = 2;
   static const char *const kNames[] = {"gemm_up", "gemm_down", "gemm_dh", "gemm_dx", "gemm_dw1", "gemm_dw2"};
   prof_begin(kNames[MODE], stream);
   err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<MODE, BN, STAGES, MB>, tm, a);

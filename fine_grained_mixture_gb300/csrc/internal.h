@@ -23,6 +23,24 @@ void count_launch();
 void prof_begin(const char *name, cudaStream_t s);
 void prof_end(cudaStream_t s);
 
+// Launches `kernel` with programmatic stream serialization, so that it may start while the previous kernel
+// in the stream drains; the kernel calls griddep_wait() before reading that kernel's results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // routing (route.cu)
 size_t route_workspace_bytes(int T, int E, int K, int mode);
 int launch_route(const float *logits, int T, int E, int K, int mode, const moe_routing *r, void *ws,

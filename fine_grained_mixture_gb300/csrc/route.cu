@@ -199,6 +199,8 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int T, int E, int nchu
                                                           int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                                                           int32_t *__restrict__ tile_offsets, int32_t *__restrict__ status) {
   __shared__ int scratch[32];
+  griddep_wait();
+  griddep_launch_dependents();
   const int e = threadIdx.x;
   int f = 0;
   if (e < E) {
@@ -239,6 +241,8 @@ __global__ void __launch_bounds__(kChunk) route_fill_tc_kernel(int T, int E, int
                                                                int32_t *__restrict__ row_token, int32_t *__restrict__ row_slot,
                                                                float *__restrict__ row_score) {
   extern __shared__ uint32_t bm[];  // [E][8]: bit i of word w = token chunk*256 + 32w + i chose the expert
+  griddep_wait();
+  griddep_launch_dependents();
   const int chunk = blockIdx.x;
   for (int i = threadIdx.x; i < E * 8; i += blockDim.x) bm[i] = 0u;
   __syncthreads();
@@ -297,6 +301,8 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
   __shared__ int warp_tot[kTrWarps];
   __shared__ int warp_base[kTrWarps];
   __shared__ int sel_state[2];
+  griddep_wait();
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int e = blockIdx.x;
   const int f = tc_counts[e], r = counts[e], base = offsets[e];
@@ -511,14 +517,16 @@ int launch_route(const float *logits, int T, int E, int K, int mode, const moe_r
   prof_end(stream);
   count_launch();
   prof_begin("route_scan", stream);
-  route_scan_kernel<<<1, 1024, 0, stream>>>(T, E, w.nchunks, mode, MOE_M_TILE, w.chunk_cnt, w.chunk_base,
-                                            r->tc_counts, r->counts, r->offsets, r->tile_offsets, r->status);
+  err = launch_pdl(route_scan_kernel, dim3(1), dim3(1024), 0, stream, T, E, w.nchunks, mode, MOE_M_TILE, w.chunk_cnt,
+                   w.chunk_base, r->tc_counts, r->counts, r->offsets, r->tile_offsets, r->status);
+  if (err != cudaSuccess) return record_cuda_error(err);
   prof_end(stream);
   count_launch();
   if (mode == MOE_ROUTE_TC) {
     prof_begin("route_fill_tc", stream);
-    route_fill_tc_kernel<<<w.nchunks, kChunk, (size_t)E * 8 * 4, stream>>>(
-        T, E, K, r->topk_idx, r->topk_score, w.chunk_base, r->offsets, r->row_token, r->row_slot, r->row_score);
+    err = launch_pdl(route_fill_tc_kernel, dim3(w.nchunks), dim3(kChunk), (size_t)E * 8 * 4, stream, T, E, K, r->topk_idx,
+                     r->topk_score, w.chunk_base, r->offsets, r->row_token, r->row_slot, r->row_score);
+    if (err != cudaSuccess) return record_cuda_error(err);
   } else {
     const size_t smem = route_tr_smem_bytes(T);
     static int attr_set_dev = -1;
@@ -531,9 +539,10 @@ int launch_route(const float *logits, int T, int E, int K, int mode, const moe_r
       attr_set_dev = dev;
     }
     prof_begin("route_fill_tr", stream);
-    route_fill_tr_kernel<<<E, kTrThreads, smem, stream>>>(logits, T, E, K, r->topk_idx, r->topk_score, w.tok_max, w.tok_den,
-                                                    w.member, w.member_words, r->tc_counts, r->counts, r->offsets,
-                                                    r->row_token, r->row_slot, r->row_score);
+    err = launch_pdl(route_fill_tr_kernel, dim3(E), dim3(kTrThreads), smem, stream, logits, T, E, K, r->topk_idx,
+                     r->topk_score, w.tok_max, w.tok_den, w.member, w.member_words, r->tc_counts, r->counts, r->offsets,
+                     r->row_token, r->row_slot, r->row_score);
+    if (err != cudaSuccess) return record_cuda_error(err);
   }
   prof_end(stream);
   count_launch();
