@@ -182,12 +182,12 @@ static size_t bwd_ws_bytes(int T, int d, int n, size_t p_cap) {
 }
 
 // Column tiles (of 256) per pass of a scatter-add GEMM: the largest divisor of d/256 whose fp32 slab
-// T x (256 * group) stays within 64 MiB (about half of L2), so A is re-read d / (256 * group) times.
+// T x (256 * group) stays within 80 MiB (about two thirds of L2), so A is re-read d / (256 * group) times.
 static int scatter_nt_group(int T, int d) {
   const int n_tiles = d / 256;
   int best = 1;
   for (int g = 1; g <= n_tiles; ++g)
-    if (n_tiles % g == 0 && (size_t)T * 256 * g * 4 <= ((size_t)64 << 20)) best = g;
+    if (n_tiles % g == 0 && (size_t)T * 256 * g * 4 <= ((size_t)80 << 20)) best = g;
   return best;
 }
 
