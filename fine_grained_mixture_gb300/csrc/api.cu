@@ -104,6 +104,74 @@ static int check_device() {
   return cache[dev] == 1 ? MOE_OK : MOE_ERR_DEVICE;
 }
 
+// Memory-bound steps that do not feed the next GEMM (zeroing an fp32 accumulator, the final cast of dX)
+// run on a library-owned side stream of the current device, so that they overlap the operand-feed-bound
+// GEMMs.  A Fork makes the side stream wait for the caller's stream; join() makes the caller's stream
+// wait for the side stream, and the destructor joins whatever is still open, so every call returns with
+// all of its work ordered before whatever the caller enqueues next on its own stream.  The per-device
+// mutex is held for the whole call: the two events are reused, and cudaStreamWaitEvent takes the latest
+// record at the time it is enqueued.
+namespace {
+struct SideStream {
+  std::mutex mu;
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+SideStream g_side[kMaxDevices];
+
+class Fork {
+ public:
+  Fork() = default;
+  Fork(const Fork &) = delete;
+  Fork &operator=(const Fork &) = delete;
+  ~Fork() {
+    if (open_) join();
+  }
+  // side waits for the work enqueued on s so far
+  int open(cudaStream_t s) {
+    if (!sd_) {
+      int dev = 0;
+      cudaError_t err = cudaGetDevice(&dev);
+      if (err != cudaSuccess) return record_cuda_error(err);
+      if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_DEVICE;
+      sd_ = &g_side[dev];
+      lk_ = std::unique_lock<std::mutex>(sd_->mu);
+      if (!sd_->stream) {
+        err = cudaStreamCreateWithFlags(&sd_->stream, cudaStreamNonBlocking);
+        if (err == cudaSuccess) err = cudaEventCreateWithFlags(&sd_->fork, cudaEventDisableTiming);
+        if (err == cudaSuccess) err = cudaEventCreateWithFlags(&sd_->join, cudaEventDisableTiming);
+        if (err != cudaSuccess) {
+          sd_->stream = nullptr;  // retried on the next call; a partial creation leaks at most two handles
+          sd_ = nullptr;
+          lk_.unlock();
+          return record_cuda_error(err);
+        }
+      }
+    }
+    s_ = s;
+    cudaError_t err = cudaEventRecord(sd_->fork, s);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(sd_->stream, sd_->fork, 0);
+    if (err != cudaSuccess) return record_cuda_error(err);
+    open_ = true;
+    return MOE_OK;
+  }
+  // s waits for the work enqueued on the side stream so far
+  int join() {
+    open_ = false;
+    cudaError_t err = cudaEventRecord(sd_->join, sd_->stream);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(s_, sd_->join, 0);
+    return err == cudaSuccess ? MOE_OK : record_cuda_error(err);
+  }
+  cudaStream_t side() const { return sd_->stream; }
+
+ private:
+  SideStream *sd_ = nullptr;
+  std::unique_lock<std::mutex> lk_;
+  cudaStream_t s_ = nullptr;
+  bool open_ = false;
+};
+}  // namespace
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -272,7 +340,9 @@ int moe_forward(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const
   p += align256(p_cap * n * 2);
   float *O32 = reinterpret_cast<float *>(p);
 
-  cudaError_t err = cudaMemsetAsync(O32, 0, (size_t)T * d * 4, s);
+  Fork side;
+  if ((rc = side.open(s)) != MOE_OK) return rc;
+  cudaError_t err = cudaMemsetAsync(O32, 0, (size_t)T * d * 4, side.side());
   if (err != cudaSuccess) return record_cuda_error(err);
 
   GemmArgs a = base_args(r, T, d, n, E, p_cap);
@@ -296,6 +366,7 @@ int moe_forward(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const
   a.out1 = nullptr;
   a.gsrc = nullptr;
   a.out_f32 = O32;
+  if ((rc = side.join()) != MOE_OK) return rc;
   if ((rc = (fill_unused(tm), launch_down(a, tm, s))) != MOE_OK) return rc;
   return launch_f32_to_bf16(O32, O, (size_t)T * d, s);
 }
@@ -325,7 +396,9 @@ int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, cons
   p += align256(p_cap * n * 2);
   float *dX32 = reinterpret_cast<float *>(p);
 
-  cudaError_t err = cudaMemsetAsync(dX32, 0, (size_t)T * d * 4, s);
+  Fork side;
+  if ((rc = side.open(s)) != MOE_OK) return rc;
+  cudaError_t err = cudaMemsetAsync(dX32, 0, (size_t)T * d * 4, side.side());
   if (err == cudaSuccess) err = cudaMemsetAsync(dS, 0, p_cap * 4, s);
   if (err != cudaSuccess) return record_cuda_error(err);
 
@@ -354,8 +427,11 @@ int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, cons
   ax.Ndim = d;
   ax.Kdim = 2 * n;
   ax.out_f32 = dX32;
+  if ((rc = side.join()) != MOE_OK) return rc;
   if ((rc = (fill_unused(tm), launch_dx(ax, tm, s))) != MOE_OK) return rc;
-  if ((rc = launch_f32_to_bf16(dX32, dX, (size_t)T * d, s)) != MOE_OK) return rc;
+  // the cast of dX overlaps the weight-gradient GEMMs, which read neither dX32 nor dX
+  if ((rc = side.open(s)) != MOE_OK) return rc;
+  if ((rc = launch_f32_to_bf16(dX32, dX, (size_t)T * d, side.side())) != MOE_OK) return rc;
   // rows [P, P_cap) of dH and s*A are read as the zero tail of the last expert's k-blocks
   if ((rc = launch_zero_tail(dH, sA, r->offsets, E, p_cap, 2 * n, n, s)) != MOE_OK) return rc;
   // dW1_e = X[tok]^T dH_e (M = d, N = 2n, K = rows of e); X rows gathered with cp.async
@@ -377,7 +453,8 @@ int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, cons
   aw.out0 = dW2;
   aw.gsrc = dO;
   aw.gld = d;
-  return (fill_unused(tm), launch_dw2(aw, tm, s));
+  if ((rc = (fill_unused(tm), launch_dw2(aw, tm, s))) != MOE_OK) return rc;
+  return side.join();
 }
 
 int moe_get_status(const moe_routing *r, int32_t *code, int32_t *P, void *stream) {
