@@ -62,9 +62,10 @@ constexpr int kGatherThreads = 128;
 constexpr int kStgRowBytes = 272;
 constexpr int kStgBytes = 256 * kStgRowBytes;  // eight epilogue warps x 32 threads
 
-// dH epilogue, per warp: two 4 KB buffers of cached H (gate | up, 32 rows x 32 columns each) filled by TMA one
-// chunk ahead, and a 6 KB staging tile (dH gate | dH up | s*A) drained by TMA stores; 64-byte swizzle.
-constexpr int kDhWarpBytes = 2 * 4096 + 6144;
+// dH epilogue, per warp: one 4 KB buffer of cached H (gate | up, 32 rows x 32 columns each), refilled by TMA as
+// soon as the warp has read the current chunk, and a 4 KB staging tile (dH gate | dH up) drained by TMA stores;
+// 64-byte swizzle.  s*A leaves from registers.  This keeps the epilogue to 32 KB, so the mainloop gets four stages.
+constexpr int kDhWarpBytes = 4096 + 4096;
 
 // MB = 128-row M blocks per CTA.  The weight-gradient GEMMs (long K loop, light epilogue) use MB = 2: two
 // M=128 MMAs per k-step share the B tile, halving shared-memory bytes per FLOP so the same shared memory
@@ -591,7 +592,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
         const float sc = valid ? __ldg(&a.row_score[r]) : 0.f;
         const int wrow = t.row0 + q * 32;                          // first row of this warp's 32
         const uint32_t wbase = base + SM::kStgOff + q * kDhWarpBytes;
-        const uint32_t out_st = wbase + 8192;                      // dH gate | dH up | s*A staging
+        const uint32_t out_st = wbase + 4096;                      // dH gate | dH up staging
         // 64-byte swizzle: 16-byte piece p of row `lane` sits at piece p ^ ((lane >> 1) & 3)
         const int sw = (lane >> 1) & 3;
         auto issue_h = [&](int c, int b) {
@@ -600,17 +601,16 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
           tma_load_2d(wbase + b * 4096, &tm.h, t.n0 + c * 32, wrow, hb, pol_stream);
           tma_load_2d(wbase + b * 4096 + 2048, &tm.h, a.n + t.n0 + c * 32, wrow, hb, pol_stream);
         };
-        if (lane == 0) issue_h(0, 0);
+        if (lane == 0) {
+          fence_proxy_async_smem();  // the previous tile's reads of the buffer come before this refill
+          issue_h(0, 0);
+        }
         uint8_t *dhrow = static_cast<uint8_t *>(a.out0) + (size_t)r * (2 * a.n) * 2;
         uint8_t *sarow = static_cast<uint8_t *>(a.out1) + (size_t)r * a.n * 2;
         float ds = 0.f;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
-          const int b = c & 1;
-          if (c + 1 < BN / 32 && lane == 0) {
-            fence_proxy_async_smem();  // this warp's reads of the other buffer are ordered before the refill
-            issue_h(c + 1, b ^ 1);
-          }
+          const int b = 0;
           uint32_t v[32];
           tmem_ld32(tacc + c * 32, v);
           const bool got = mbar_wait(hin_bar(q, b), (hin_par >> b) & 1u);
@@ -633,6 +633,11 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
             hu[4 * p + 1] = __float_as_uint(u4.y);
             hu[4 * p + 2] = __float_as_uint(u4.z);
             hu[4 * p + 3] = __float_as_uint(u4.w);
+          }
+          __syncwarp();  // every lane has read this chunk of H: the buffer can be refilled
+          if (c + 1 < BN / 32 && lane == 0) {
+            fence_proxy_async_smem();  // the warp's generic-proxy reads are ordered before the TMA refill
+            issue_h(c + 1, 0);
           }
           uint32_t dg[16], du[16], sa[16];
 #pragma unroll
@@ -667,17 +672,18 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
                            __uint_as_float(dg[4 * p + 2]), __uint_as_float(dg[4 * p + 3]));
               st_shared_v4(out_st + 2048 + o, __uint_as_float(du[4 * p]), __uint_as_float(du[4 * p + 1]),
                            __uint_as_float(du[4 * p + 2]), __uint_as_float(du[4 * p + 3]));
-              st_shared_v4(out_st + 4096 + o, __uint_as_float(sa[4 * p]), __uint_as_float(sa[4 * p + 1]),
-                           __uint_as_float(sa[4 * p + 2]), __uint_as_float(sa[4 * p + 3]));
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
               tma_store_2d(&tm.dh, out_st, j, wrow, pol_stream);
               tma_store_2d(&tm.dh, out_st + 2048, a.n + j, wrow, pol_stream);
-              tma_store_2d(&tm.sa, out_st + 4096, j, wrow, pol_stream);
               bulk_commit();
             }
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+              st_v4_hint(sarow + (size_t)j * 2 + w * 16, sa[4 * w], sa[4 * w + 1], sa[4 * w + 2], sa[4 * w + 3],
+                         pol_stream);
           } else if (valid) {
 #pragma unroll
             for (int w = 0; w < 4; ++w) {

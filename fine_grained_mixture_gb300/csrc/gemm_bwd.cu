@@ -5,7 +5,7 @@
 namespace moe {
 
 int launch_dh(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, int bn) {
-  if (bn == 256) return launch_gemm<kDH, 256, 3>(a, tm, s);
+  if (bn == 256) return launch_gemm<kDH, 256, 4>(a, tm, s);
   return launch_gemm<kDH, 128, 4>(a, tm, s);
 }
 

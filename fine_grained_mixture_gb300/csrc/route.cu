@@ -9,10 +9,12 @@
 //
 // Pipeline (one stream, no host synchronisation):
 //   route_topk_kernel   one warp per token (32 tokens per CTA): top-K by (logit desc, expert asc), softmax over the K,
-//                       per-chunk (256 tokens) expert histograms, membership bitmap (TR only)
-//   route_scan_kernel   one CTA: per-chunk bases, counts (TC f_e or TR r_e), offsets, tile offsets
+//                       the CTA's expert histogram; TR only: the CTA's word of the membership bitmap and its 32
+//                       columns of the expert-major key matrix, both written whole (no zero fill needed)
+//   route_scan_kernel   one CTA per expert: per-chunk (256 tokens) bases, counts (TC f_e or TR r_e)
 //   route_fill_tc       one CTA per 256-token chunk: rows in ascending token order via bitmap ranks
 //   route_fill_tr       one CTA per expert: radix selection of the kept set, rows in token order
+//                       (each fill CTA scans the E counts into offsets; CTA 0 publishes them)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -33,36 +35,72 @@ __device__ __forceinline__ uint32_t order_key(float z) {
 constexpr int kTopkThreads = 256;                    // 8 warps, 4 tokens each: 32 tokens per CTA
 constexpr int kTokensPerWarp = 4;
 constexpr int kTopkTokens = (kTopkThreads / 32) * kTokensPerWarp;
-static_assert(kChunk % kTopkTokens == 0, "a top-K CTA must not straddle two histogram chunks");
+static_assert(kTopkTokens == 32, "a top-K CTA covers exactly one 32-token word of the membership bitmap");
+constexpr int kCtasPerChunk = kChunk / kTopkTokens;  // top-K histograms summed into one routing chunk
 
 // Inverse of order_key.
 __device__ __forceinline__ float key_to_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-template <int NV>  // NV = logits held per lane = ceil(E / 32)
+constexpr int kKeyStride = 33;  // words per expert row of the TR key tile (odd: conflict-free transpose)
+
+// Dynamic shared memory of route_topk_kernel: the CTA histogram, plus for TR the membership words and the
+// [E][32] key tile.
+size_t route_topk_smem_bytes(int E, int mode) {
+  return (size_t)E * 4 + (mode == MOE_ROUTE_TR ? (size_t)E * 4 + (size_t)E * kKeyStride * 4 : 0);
+}
+
+template <int NV, bool TR>  // NV = logits held per lane = ceil(E / 32)
 __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float *__restrict__ logits, int T, int E, int K,
-                                                         int want_member, int32_t *__restrict__ topk_idx,
+                                                         int32_t *__restrict__ topk_idx,
                                                          float *__restrict__ topk_score, float *__restrict__ tok_max,
-                                                         float *__restrict__ tok_den, int32_t *__restrict__ chunk_cnt,
+                                                         float *__restrict__ tok_den, int32_t *__restrict__ cta_hist,
                                                          uint32_t *__restrict__ member, int member_words,
-                                                         int32_t *__restrict__ status) {
-  extern __shared__ int32_t hist[];  // [E]
-  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+                                                         uint32_t *__restrict__ keys_em, int32_t *__restrict__ status) {
+  extern __shared__ int32_t hist[];                                      // [E]
+  uint32_t *mbits = reinterpret_cast<uint32_t *>(hist + E);             // [E]     TR: bit i = token t_first + i chose e
+  uint32_t *ktile = mbits + E;                                           // [E][33] TR: order keys of the 32 tokens
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    hist[e] = 0;
+    if (TR) mbits[e] = 0u;
+  }
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int t_first = blockIdx.x * kTopkTokens;
-  const int chunk = t_first / kChunk;
+  // the warp's logit rows are loaded up front so that their latencies overlap (only while they fit in
+  // registers); rows past T read as -inf and are skipped
+  constexpr int kPre = NV <= 8 ? kTokensPerWarp : 1;
+  float vpre[kPre][NV];
+  if (kPre > 1) {
+#pragma unroll
+    for (int i = 0; i < kPre; ++i) {
+      const int t = t_first + warp * kTokensPerWarp + i;
+#pragma unroll
+      for (int j = 0; j < NV; ++j) {
+        const int e = lane + 32 * j;
+        vpre[i][j] = (t < T && e < E) ? __ldcs(&logits[(size_t)t * E + e]) : -INFINITY;
+      }
+    }
+  }
+#pragma unroll
   for (int i = 0; i < kTokensPerWarp; ++i) {
-    const int t = t_first + warp * kTokensPerWarp + i;
+    const int tl = warp * kTokensPerWarp + i;  // token within the CTA
+    const int t = t_first + tl;
     if (t >= T) break;
     float v[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int e = lane + 32 * j;
+      if (kPre > 1) v[j] = vpre[kPre > 1 ? i : 0][j];
+      else v[j] = (e < E) ? __ldcs(&logits[(size_t)t * E + e]) : -INFINITY;
+    }
     bool bad = false;
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
       const int e = lane + 32 * j;
-      v[j] = (e < E) ? logits[(size_t)t * E + e] : -INFINITY;
+      if (TR && e < E) ktile[e * kKeyStride + tl] = order_key(v[j]);
       if (e < E && !isfinite(v[j])) bad = true;
     }
     if (__any_sync(0xffffffffu, bad)) {
@@ -153,7 +191,7 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float *_
       topk_idx[(size_t)t * K + lane] = my_e;
       topk_score[(size_t)t * K + lane] = w / den;
       atomicAdd(&hist[my_e], 1);
-      if (want_member) atomicOr(&member[(size_t)my_e * member_words + (t >> 5)], 1u << (t & 31));
+      if (TR) atomicOr(&mbits[my_e], 1u << tl);
     }
     if (lane == 0) {
       tok_max[t] = z0;
@@ -161,14 +199,22 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float *_
     }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x)
-    if (hist[e]) atomicAdd(&chunk_cnt[(size_t)chunk * E + e], hist[e]);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    cta_hist[(size_t)blockIdx.x * E + e] = hist[e];
+    if (TR) member[(size_t)e * member_words + blockIdx.x] = mbits[e];  // a CTA covers one 32-token word
+  }
+  if (TR) {
+    // expert-major keys: each warp writes whole 32-token rows (128 bytes) of experts warp, warp + 8, ...
+    const int t = t_first + lane;
+    for (int e = warp; e < E; e += kTopkThreads / 32)
+      if (t < T) keys_em[(size_t)e * T + t] = ktile[e * kKeyStride + lane];
+  }
 }
 
-// Exclusive scan of one value per thread across a block of 1024 threads; returns the exclusive prefix and
-// writes the block total to *total.
-__device__ __forceinline__ int block_exclusive_scan_1024(int v, int *scratch /*[32]*/, int *total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Exclusive scan of one value per thread across the block (blockDim.x a multiple of 32); returns the
+// exclusive prefix and writes the block total to *total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int *scratch /*[32]*/, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   int x = v;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -178,7 +224,7 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int *scratch /*[
   if (lane == 31) scratch[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int s = scratch[lane];
+    int s = lane < nwarps ? scratch[lane] : 0;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, s, off);
@@ -188,64 +234,118 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int *scratch /*[
   }
   __syncthreads();
   const int before = (warp > 0 ? scratch[warp - 1] : 0);
-  *total = scratch[31];
+  *total = scratch[nwarps - 1];
   __syncthreads();
   return before + x - v;
 }
 
-__global__ void __launch_bounds__(1024) route_scan_kernel(int T, int E, int nchunks, int mode, int m_tile,
-                                                          const int32_t *__restrict__ chunk_cnt,
-                                                          int32_t *__restrict__ chunk_base, int32_t *__restrict__ tc_counts,
-                                                          int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
-                                                          int32_t *__restrict__ tile_offsets, int32_t *__restrict__ status) {
-  __shared__ int scratch[32];
-  griddep_wait();
-  griddep_launch_dependents();
-  const int e = threadIdx.x;
-  int f = 0;
-  if (e < E) {
-    for (int c = 0; c < nchunks; ++c) {
-      chunk_base[(size_t)c * E + e] = f;
-      f += chunk_cnt[(size_t)c * E + e];
-    }
+
+// Row offsets and m-tile offsets of every expert (exclusive scans of counts[0..E) and of their tile counts)
+// into shared memory, entries 0..E.  Thread i takes a contiguous run of experts.
+__device__ void expert_offsets(const int32_t *__restrict__ counts, int E, int m_tile, int *s_off, int *s_toff,
+                               int *scratch) {
+  const int per = (E + blockDim.x - 1) / blockDim.x;
+  const int e0 = threadIdx.x * per, e1 = min(E, e0 + per);
+  int c = 0, tl = 0;
+  for (int e = e0; e < e1; ++e) {
+    const int v = counts[e];
+    c += v;
+    tl += (v + m_tile - 1) / m_tile;
   }
-  int cnt = f;
-  if (mode == MOE_ROUTE_TR && e < E) {
-    const int lo = (f / m_tile) * m_tile;
-    const int hi = ((f + m_tile - 1) / m_tile) * m_tile;
-    cnt = ((hi - f) < (f - lo) && hi <= T) ? hi : lo;
+  int P, tiles;
+  int o = block_exclusive_scan(c, scratch, &P);
+  int to = block_exclusive_scan(tl, scratch, &tiles);
+  for (int e = e0; e < e1; ++e) {
+    const int v = counts[e];
+    s_off[e] = o;
+    s_toff[e] = to;
+    o += v;
+    to += (v + m_tile - 1) / m_tile;
   }
-  if (e >= E) cnt = 0;
-  const int tiles = (cnt + m_tile - 1) / m_tile;
-  int P = 0, total_tiles = 0;
-  const int off = block_exclusive_scan_1024(cnt, scratch, &P);
-  const int toff = block_exclusive_scan_1024(tiles, scratch, &total_tiles);
-  if (e < E) {
-    tc_counts[e] = f;
-    counts[e] = cnt;
-    offsets[e] = off;
-    tile_offsets[e] = toff;
+  if (threadIdx.x == 0) {
+    s_off[E] = P;
+    s_toff[E] = tiles;
   }
-  if (e == 0) {
-    offsets[E] = P;
-    tile_offsets[E] = total_tiles;
-    status[1] = P;
-    status[2] = total_tiles;
+  __syncthreads();
+}
+
+// CTA 0 of a fill kernel publishes the offsets (read by the GEMMs once the fill kernel has finished).
+__device__ void publish_offsets(int E, const int *s_off, const int *s_toff, int32_t *__restrict__ offsets,
+                                int32_t *__restrict__ tile_offsets, int32_t *__restrict__ status) {
+  if (blockIdx.x != 0) return;
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    offsets[e] = s_off[e];
+    tile_offsets[e] = s_toff[e];
+  }
+  if (threadIdx.x == 0) {
+    status[1] = s_off[E];
+    status[2] = s_toff[E];
   }
 }
 
-__global__ void __launch_bounds__(kChunk) route_fill_tc_kernel(int T, int E, int K, const int32_t *__restrict__ topk_idx,
+// One CTA per expert: the expert's count in every 256-token chunk (the sum of its top-K CTAs' histograms),
+// their exclusive prefix (chunk_base), the token-choice count f_e and the routed count (f_e, or r_e after
+// rounding).  Thread i takes a contiguous run of chunks.
+constexpr int kScanThreads = 256;
+__global__ void __launch_bounds__(kScanThreads) route_scan_kernel(int T, int E, int nctas, int mode, int m_tile,
+                                                                  const int32_t *__restrict__ cta_hist,
+                                                                  int32_t *__restrict__ chunk_base,
+                                                                  int32_t *__restrict__ tc_counts,
+                                                                  int32_t *__restrict__ counts) {
+  __shared__ int scratch[32];
+  griddep_wait();
+  griddep_launch_dependents();
+  const int e = blockIdx.x;
+  const int nchunks = (nctas + kCtasPerChunk - 1) / kCtasPerChunk;
+  const int per = (nchunks + kScanThreads - 1) / kScanThreads;
+  const int c0 = threadIdx.x * per, c1 = min(nchunks, c0 + per);
+  auto chunk_sum = [&](int c) {
+    int v = 0;
+#pragma unroll
+    for (int i = 0; i < kCtasPerChunk; ++i) {
+      const int b = c * kCtasPerChunk + i;
+      if (b < nctas) v += cta_hist[(size_t)b * E + e];
+    }
+    return v;
+  };
+  int run = 0;
+  for (int c = c0; c < c1; ++c) run += chunk_sum(c);
+  int f;
+  int base = block_exclusive_scan(run, scratch, &f);
+  for (int c = c0; c < c1; ++c) {
+    chunk_base[(size_t)c * E + e] = base;
+    base += chunk_sum(c);
+  }
+  if (threadIdx.x == 0) {
+    int cnt = f;
+    if (mode == MOE_ROUTE_TR) {
+      const int lo = (f / m_tile) * m_tile;
+      const int hi = ((f + m_tile - 1) / m_tile) * m_tile;
+      cnt = ((hi - f) < (f - lo) && hi <= T) ? hi : lo;
+    }
+    tc_counts[e] = f;
+    counts[e] = cnt;
+  }
+}
+
+__global__ void __launch_bounds__(kChunk) route_fill_tc_kernel(int T, int E, int K, int m_tile,
+                                                               const int32_t *__restrict__ topk_idx,
                                                                const float *__restrict__ topk_score,
                                                                const int32_t *__restrict__ chunk_base,
-                                                               const int32_t *__restrict__ offsets,
+                                                               const int32_t *__restrict__ counts,
+                                                               int32_t *__restrict__ offsets,
+                                                               int32_t *__restrict__ tile_offsets,
+                                                               int32_t *__restrict__ status,
                                                                int32_t *__restrict__ row_token, int32_t *__restrict__ row_slot,
                                                                float *__restrict__ row_score) {
   extern __shared__ uint32_t bm[];  // [E][8]: bit i of word w = token chunk*256 + 32w + i chose the expert
-  griddep_wait();
-  griddep_launch_dependents();
+  __shared__ int s_off[kMaxExperts + 1], s_toff[kMaxExperts + 1], scratch[32];
   const int chunk = blockIdx.x;
   for (int i = threadIdx.x; i < E * 8; i += blockDim.x) bm[i] = 0u;
-  __syncthreads();
+  griddep_wait();
+  griddep_launch_dependents();
+  expert_offsets(counts, E, m_tile, s_off, s_toff, scratch);
+  publish_offsets(E, s_off, s_toff, offsets, tile_offsets, status);
   const int tl = threadIdx.x;
   const int t = chunk * kChunk + tl;
   const bool live = t < T;
@@ -258,7 +358,7 @@ __global__ void __launch_bounds__(kChunk) route_fill_tc_kernel(int T, int E, int
     const uint32_t *w = &bm[e * 8];
     int rank = __popc(w[tl >> 5] & ((1u << (tl & 31)) - 1u));
     for (int j = 0; j < (tl >> 5); ++j) rank += __popc(w[j]);
-    const int row = offsets[e] + chunk_base[(size_t)chunk * E + e] + rank;
+    const int row = s_off[e] + chunk_base[(size_t)chunk * E + e] + rank;
     row_token[row] = t;
     row_slot[row] = k;
     row_score[row] = topk_score[(size_t)t * K + k];
@@ -288,11 +388,12 @@ __device__ __forceinline__ int warp_scan_exclusive(int v, int *total) {
 }
 
 __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
-    const float *__restrict__ logits, int T, int E, int K, const int32_t *__restrict__ topk_idx,
+    const uint32_t *__restrict__ keys_em, int T, int E, int K, const int32_t *__restrict__ topk_idx,
     const float *__restrict__ topk_score, const float *__restrict__ tok_max, const float *__restrict__ tok_den,
-    const uint32_t *__restrict__ member, int member_words, const int32_t *__restrict__ tc_counts,
-    const int32_t *__restrict__ counts, const int32_t *__restrict__ offsets, int32_t *__restrict__ row_token,
-    int32_t *__restrict__ row_slot, float *__restrict__ row_score) {
+    const uint32_t *__restrict__ member, int member_words, int m_tile, const int32_t *__restrict__ tc_counts,
+    const int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ tile_offsets,
+    int32_t *__restrict__ status, int32_t *__restrict__ row_token, int32_t *__restrict__ row_slot,
+    float *__restrict__ row_score) {
   extern __shared__ uint32_t sm[];
   uint32_t *key = sm;                                       // [T]
   uint32_t *mem = sm + T;                                   // [member_words]
@@ -301,14 +402,17 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
   __shared__ int warp_tot[kTrWarps];
   __shared__ int warp_base[kTrWarps];
   __shared__ int sel_state[2];
+  __shared__ int s_off[kMaxExperts + 1], s_toff[kMaxExperts + 1], scratch[32];
   griddep_wait();
   griddep_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int e = blockIdx.x;
-  const int f = tc_counts[e], r = counts[e], base = offsets[e];
+  expert_offsets(counts, E, m_tile, s_off, s_toff, scratch);
+  publish_offsets(E, s_off, s_toff, offsets, tile_offsets, status);
+  const int f = tc_counts[e], r = counts[e], base = s_off[e];
   if (r == 0) return;
   for (int w = threadIdx.x; w < member_words; w += blockDim.x) mem[w] = member[(size_t)e * member_words + w];
-  for (int t = threadIdx.x; t < T; t += blockDim.x) key[t] = order_key(logits[(size_t)t * E + e]);
+  for (int t = threadIdx.x; t < T; t += blockDim.x) key[t] = __ldcs(&keys_em[(size_t)e * T + t]);
   __syncthreads();
   // candidates: token-choice tokens when dropping, the other tokens when padding
   const bool drop = r < f;
@@ -320,10 +424,17 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
     for (int shift = 24; shift >= 0; shift -= 8) {
       for (int i = threadIdx.x; i < kTrHists * 256; i += blockDim.x) hist[i] = 0;
       __syncthreads();
-      for (int t = threadIdx.x; t < T; t += blockDim.x) {
-        const bool tc = (mem[t >> 5] >> (t & 31)) & 1u;
-        const uint32_t k = key[t];
-        if (tc == drop && (k & mask) == prefix) atomicAdd(&my_hist[(k >> shift) & 255u], 1);
+      // lanes that fall in the same bin add once (many keys share their leading bits)
+      for (int t0 = 0; t0 < T; t0 += blockDim.x) {
+        const int t = t0 + threadIdx.x;
+        uint32_t bin = 256u;
+        if (t < T) {
+          const bool tc = (mem[t >> 5] >> (t & 31)) & 1u;
+          const uint32_t k = key[t];
+          if (tc == drop && (k & mask) == prefix) bin = (k >> shift) & 255u;
+        }
+        const uint32_t same = __match_any_sync(0xffffffffu, bin);
+        if (bin < 256u && lane == __ffs(same) - 1) atomicAdd(&my_hist[bin], __popc(same));
       }
       __syncthreads();
       if (warp == 0) {
@@ -434,7 +545,7 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
           if (topk_idx[(size_t)t * K + k] == e) slot = k;
       }
       const float sc = slot >= 0 ? topk_score[(size_t)t * K + slot]
-                                 : expf(logits[(size_t)t * E + e] - tok_max[t]) / tok_den[t];
+                                 : expf(key_to_float(key[t]) - tok_max[t]) / tok_den[t];
       row_token[pos] = t;
       row_slot[pos] = slot;
       row_score[pos] = sc;
@@ -446,37 +557,41 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
 // ------------------------------------------------------------------------------------------- host
 
 struct RouteWs {
-  int32_t *chunk_cnt, *chunk_base;
-  uint32_t *member;
+  int32_t *cta_hist, *chunk_base;
+  uint32_t *member, *keys_em;
   float *tok_max, *tok_den;
-  int nchunks, member_words;
+  int nctas, nchunks, member_words;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// cta_hist [nctas][E] | chunk_base [nchunks][E] | TR: member [E][words], keys_em [E][T] | tok_max [T] | tok_den [T]
 size_t route_workspace_bytes(int T, int E, int K, int mode) {
   (void)K;
+  const size_t nctas = (T + kTopkTokens - 1) / kTopkTokens;
   const size_t nchunks = (T + kChunk - 1) / kChunk;
   const size_t words = (T + 31) / 32;
-  size_t b = 0;
-  b += align256(nchunks * E * 4) * 2;
-  b += (mode == MOE_ROUTE_TR) ? align256(words * E * 4) : 0;
+  size_t b = align256(nctas * E * 4) + align256(nchunks * E * 4);
+  if (mode == MOE_ROUTE_TR) b += align256(words * E * 4) + align256((size_t)T * E * 4);
   b += align256((size_t)T * 4) * 2;
   return b;
 }
 
 static RouteWs carve(void *ws, int T, int E, int mode) {
   RouteWs w{};
+  w.nctas = (T + kTopkTokens - 1) / kTopkTokens;
   w.nchunks = (T + kChunk - 1) / kChunk;
   w.member_words = (T + 31) / 32;
   char *p = static_cast<char *>(ws);
-  w.chunk_cnt = reinterpret_cast<int32_t *>(p);
-  p += align256((size_t)w.nchunks * E * 4);
+  w.cta_hist = reinterpret_cast<int32_t *>(p);
+  p += align256((size_t)w.nctas * E * 4);
   w.chunk_base = reinterpret_cast<int32_t *>(p);
   p += align256((size_t)w.nchunks * E * 4);
   if (mode == MOE_ROUTE_TR) {
     w.member = reinterpret_cast<uint32_t *>(p);
     p += align256((size_t)w.member_words * E * 4);
+    w.keys_em = reinterpret_cast<uint32_t *>(p);
+    p += align256((size_t)T * E * 4);
   }
   w.tok_max = reinterpret_cast<float *>(p);
   p += align256((size_t)T * 4);
@@ -491,21 +606,39 @@ size_t route_tr_smem_bytes(int T) {
 int launch_route(const float *logits, int T, int E, int K, int mode, const moe_routing *r, void *ws,
                  cudaStream_t stream) {
   RouteWs w = carve(ws, T, E, mode);
-  cudaError_t err;
-  err = cudaMemsetAsync(r->status, 0, MOE_STATUS_WORDS * sizeof(int32_t), stream);
-  if (err == cudaSuccess) err = cudaMemsetAsync(w.chunk_cnt, 0, (size_t)w.nchunks * E * 4, stream);
+  cudaError_t err = cudaMemsetAsync(r->status, 0, MOE_STATUS_WORDS * sizeof(int32_t), stream);
   if (err != cudaSuccess) return record_cuda_error(err);
-  if (mode == MOE_ROUTE_TR) {
-    err = cudaMemsetAsync(w.member, 0, (size_t)w.member_words * E * 4, stream);
-    if (err != cudaSuccess) return record_cuda_error(err);
-  }
-  const int want_member = mode == MOE_ROUTE_TR;
-  const size_t hist_smem = (size_t)E * 4;
+  const bool tr = mode == MOE_ROUTE_TR;
+  const size_t topk_smem = route_topk_smem_bytes(E, mode);
   const int nv = (E + 31) / 32;
+  // the key tile of E = 1024 needs more than the default 48 KB of dynamic shared memory
+  static int attr_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+#define MOE_TOPK_KERNEL(NV, TRB) route_topk_kernel<NV, TRB>
+#define MOE_TOPK_EACH(F)                                                                                          \
+  F(1, false) F(2, false) F(4, false) F(8, false) F(16, false) F(32, false) F(1, true) F(2, true) F(4, true)      \
+      F(8, true) F(16, true) F(32, true)
+  if (attr_dev != dev) {
+#define MOE_TOPK_ATTR(NV, TRB)                                                                                    \
+  if (err == cudaSuccess)                                                                                         \
+    err = cudaFuncSetAttribute(MOE_TOPK_KERNEL(NV, TRB), cudaFuncAttributeMaxDynamicSharedMemorySize,             \
+                               static_cast<int>(route_topk_smem_bytes(1024, TRB ? MOE_ROUTE_TR : MOE_ROUTE_TC)));
+    MOE_TOPK_EACH(MOE_TOPK_ATTR)
+#undef MOE_TOPK_ATTR
+    if (err == cudaSuccess) err = cudaFuncSetAttribute(route_fill_tr_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       static_cast<int>(route_tr_smem_bytes(kMaxTrTokens)));
+    if (err != cudaSuccess) return record_cuda_error(err);
+    attr_dev = dev;
+  }
+#undef MOE_TOPK_EACH
 #define MOE_TOPK_LAUNCH(NV)                                                                                       \
-  route_topk_kernel<NV><<<(T + kTopkTokens - 1) / kTopkTokens, kTopkThreads, hist_smem, stream>>>(logits, T, E, K, want_member, r->topk_idx,          \
-                                                               r->topk_score, w.tok_max, w.tok_den, w.chunk_cnt, \
-                                                               w.member, w.member_words, r->status)
+  do {                                                                                                            \
+    auto kern = tr ? MOE_TOPK_KERNEL(NV, true) : MOE_TOPK_KERNEL(NV, false);                                      \
+    kern<<<w.nctas, kTopkThreads, topk_smem, stream>>>(logits, T, E, K, r->topk_idx, r->topk_score, w.tok_max,    \
+                                                       w.tok_den, w.cta_hist, w.member, w.member_words, w.keys_em, \
+                                                       r->status);                                                \
+  } while (0)
   prof_begin("route_topk", stream);
   if (nv <= 1) MOE_TOPK_LAUNCH(1);
   else if (nv <= 2) MOE_TOPK_LAUNCH(2);
@@ -514,34 +647,27 @@ int launch_route(const float *logits, int T, int E, int K, int mode, const moe_r
   else if (nv <= 16) MOE_TOPK_LAUNCH(16);
   else MOE_TOPK_LAUNCH(32);
 #undef MOE_TOPK_LAUNCH
+#undef MOE_TOPK_KERNEL
   prof_end(stream);
   count_launch();
   prof_begin("route_scan", stream);
-  err = launch_pdl(route_scan_kernel, dim3(1), dim3(1024), 0, stream, T, E, w.nchunks, mode, MOE_M_TILE, w.chunk_cnt,
-                   w.chunk_base, r->tc_counts, r->counts, r->offsets, r->tile_offsets, r->status);
+  err = launch_pdl(route_scan_kernel, dim3(E), dim3(kScanThreads), 0, stream, T, E, w.nctas, mode, MOE_M_TILE,
+                   w.cta_hist, w.chunk_base, r->tc_counts, r->counts);
   if (err != cudaSuccess) return record_cuda_error(err);
   prof_end(stream);
   count_launch();
   if (mode == MOE_ROUTE_TC) {
     prof_begin("route_fill_tc", stream);
-    err = launch_pdl(route_fill_tc_kernel, dim3(w.nchunks), dim3(kChunk), (size_t)E * 8 * 4, stream, T, E, K, r->topk_idx,
-                     r->topk_score, w.chunk_base, r->offsets, r->row_token, r->row_slot, r->row_score);
+    err = launch_pdl(route_fill_tc_kernel, dim3(w.nchunks), dim3(kChunk), (size_t)E * 8 * 4, stream, T, E, K,
+                     MOE_M_TILE, r->topk_idx, r->topk_score, w.chunk_base, r->counts, r->offsets, r->tile_offsets,
+                     r->status, r->row_token, r->row_slot, r->row_score);
     if (err != cudaSuccess) return record_cuda_error(err);
   } else {
     const size_t smem = route_tr_smem_bytes(T);
-    static int attr_set_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (attr_set_dev != dev) {
-      err = cudaFuncSetAttribute(route_fill_tr_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(route_tr_smem_bytes(kMaxTrTokens)));
-      if (err != cudaSuccess) return record_cuda_error(err);
-      attr_set_dev = dev;
-    }
     prof_begin("route_fill_tr", stream);
-    err = launch_pdl(route_fill_tr_kernel, dim3(E), dim3(kTrThreads), smem, stream, logits, T, E, K, r->topk_idx,
-                     r->topk_score, w.tok_max, w.tok_den, w.member, w.member_words, r->tc_counts, r->counts, r->offsets,
-                     r->row_token, r->row_slot, r->row_score);
+    err = launch_pdl(route_fill_tr_kernel, dim3(E), dim3(kTrThreads), smem, stream, w.keys_em, T, E, K, r->topk_idx,
+                     r->topk_score, w.tok_max, w.tok_den, w.member, w.member_words, MOE_M_TILE, r->tc_counts, r->counts,
+                     r->offsets, r->tile_offsets, r->status, r->row_token, r->row_slot, r->row_score);
     if (err != cudaSuccess) return record_cuda_error(err);
   }
   prof_end(stream);

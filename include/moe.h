@@ -86,7 +86,8 @@ typedef struct moe_routing {
 /* Upper bound on P: T*K for TC; T*K + E*M_tile/2 for TR (rounding pads an expert by < M_tile/2 rows). */
 int moe_route_capacity(int T, int E, int K, int mode, size_t *p_cap);
 
-/* Bytes of scratch moe_route needs (per-chunk histograms, membership bitmap, per-token normalisers). */
+/* Bytes of scratch moe_route needs (per-CTA and per-chunk expert histograms, per-token normalisers; token
+ * rounding adds the membership bitmap and an expert-major copy of the logit order keys, 4*T*E bytes). */
 int moe_route_workspace_size(int T, int E, int K, int mode, size_t *bytes);
 
 /*
