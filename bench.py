@@ -311,7 +311,8 @@ def kernel_flops_bytes(name, w, P):
     """Algorithmic FLOPs (GEMM kernels) or bytes (memory-bound kernels) of one launch."""
     n, d, T, E, K = w.n, w.d, w.T, w.E, w.K
     flops = {"gemm_up": 4.0 * P * n * d, "gemm_down": 2.0 * P * n * d, "gemm_dh": 2.0 * P * n * d,
-             "gemm_dx": 4.0 * P * n * d, "gemm_dw1": 4.0 * P * n * d, "gemm_dw2": 2.0 * P * n * d}
+             "gemm_dx": 4.0 * P * n * d, "gemm_dw1": 4.0 * P * n * d, "gemm_dw2": 2.0 * P * n * d,
+             "gemm_dw": 6.0 * P * n * d}
     if name in flops:
         return "tensor", flops[name]
     nbytes = {"cast_f32_bf16": T * d * 6.0, "route_topk": T * E * 4.0 + T * K * 8.0 + T * 8.0,

@@ -434,11 +434,24 @@ int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, cons
   if ((rc = launch_f32_to_bf16(dX32, dX, (size_t)T * d, side.side())) != MOE_OK) return rc;
   // rows [P, P_cap) of dH and s*A are read as the zero tail of the last expert's k-blocks
   if ((rc = launch_zero_tail(dH, sA, r->offsets, E, p_cap, 2 * n, n, s)) != MOE_OK) return rc;
+  GemmArgs aw = base_args(r, T, d, n, E, p_cap);
+  aw.wide_m = (int64_t)T * K >= (int64_t)1024 * E;  // experts average >= 1024 rows: >= 16 k-blocks per tile
+  if (aw.wide_m && d % 256 == 0 && n % 256 == 0) {
+    // both weight gradients in one launch: dW1 tiles gather X into A and load dH as B, dW2 tiles load s*A
+    // as A and gather dO into B (one wave quantisation instead of two)
+    if ((rc = make_tmap_bf16(&tm.b, dH, 2 * (uint64_t)n, p_cap, 64)) != MOE_OK) return rc;
+    if ((rc = make_tmap_bf16(&tm.a, sA, n, p_cap, 64)) != MOE_OK) return rc;
+    aw.out0 = dW1;
+    aw.out1 = dW2;
+    aw.gsrc = X;
+    aw.gsrc2 = dO;
+    aw.gld = d;
+    if ((rc = (fill_unused(tm), launch_dw12(aw, tm, s))) != MOE_OK) return rc;
+    return side.join();
+  }
   // dW1_e = X[tok]^T dH_e (M = d, N = 2n, K = rows of e); X rows gathered with cp.async
   if ((rc = make_tmap_bf16(&tm.b, dH, 2 * (uint64_t)n, p_cap, 64)) != MOE_OK) return rc;
   tm.a = tm.b;
-  GemmArgs aw = base_args(r, T, d, n, E, p_cap);
-  aw.wide_m = (int64_t)T * K >= (int64_t)1024 * E;  // experts average >= 1024 rows: >= 16 k-blocks per tile
   aw.Mdim = d;
   aw.Ndim = 2 * n;
   aw.out0 = dW1;

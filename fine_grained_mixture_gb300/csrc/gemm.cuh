@@ -13,6 +13,7 @@
 //   kDX   dX32[tok] += dH W1_e^T                                                    M=rows  N=d   K=2n
 //   kDW1  dW1_e = X[tok]^T dH   (reduction over the expert's rows)                  M=d     N=2n  K=rows
 //   kDW2  dW2_e = (sA)^T dO[tok]                                                    M=n     N=d   K=rows
+//   kDW   both weight gradients in one launch: each expert's dW1 pairs, then its dW2 pairs (256-row blocks)
 //
 // CTA = 6 or 10 warps: warp 0 issues TMA tiled loads of the dense operands, warp 1 owns TMEM and one
 // elected lane issues tcgen05.mma, warps 2..5 drain TMEM in the epilogue, and in the four GEMMs that read
@@ -32,7 +33,7 @@
 
 namespace moe {
 
-enum GemmMode : int { kUp = 0, kDown = 1, kDH = 2, kDX = 3, kDW1 = 4, kDW2 = 5 };
+enum GemmMode : int { kUp = 0, kDown = 1, kDH = 2, kDX = 3, kDW1 = 4, kDW2 = 5, kDW = 6 };
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
@@ -40,11 +41,11 @@ constexpr int kABytes = kBM * kBK * 2;  // 16 KB per stage
 
 template <int MODE>
 struct Traits {
-  static constexpr bool varlen_k = (MODE == kDW1 || MODE == kDW2);
+  static constexpr bool varlen_k = (MODE == kDW1 || MODE == kDW2 || MODE == kDW);
   static constexpr bool gather_a_k = (MODE == kUp || MODE == kDH);  // A: token rows, K-major
   static constexpr bool gather_a_mn = (MODE == kDW1);                // A: token rows along K, MN-major
   static constexpr bool gather_b_mn = (MODE == kDW2);                // B: token rows along K, MN-major
-  static constexpr bool gather = gather_a_k || gather_a_mn || gather_b_mn;
+  static constexpr bool gather = gather_a_k || gather_a_mn || gather_b_mn || MODE == kDW;  // kDW: A or B per tile
   static constexpr bool nt_outer_ = (MODE == kDown || MODE == kDX);
   // the scatter-add GEMMs drain TMEM with eight warps (two per TMEM lane quarter, half the columns each)
   static constexpr int epi_warps = nt_outer_ ? 8 : 4;
@@ -88,7 +89,16 @@ __host__ __device__ constexpr int epi_bytes() {
 struct Tile {
   int e, m0, n0, row0, row_end, kblocks;
   bool shared;  // both CTAs of the cluster need the same shared-operand tile (load halves + multicast)
+  bool w2;      // weight gradients: a dW2 tile (gathered B, TMA-loaded A) rather than a dW1 tile
 };
+
+// Pairs of one expert's weight-gradient tiles: dW1 pairs along M (they share the dH tile), dW2 pairs along N
+// (they share the s*A tile).
+template <int BN, int MB>
+__device__ __forceinline__ int dw_pairs(int Mdim, int Ndim, bool w2) {
+  const int m_tiles = Mdim / (kBM * MB), n_tiles = Ndim / BN;
+  return w2 ? m_tiles * ((n_tiles + 1) / 2) : ((m_tiles + 1) / 2) * n_tiles;
+}
 
 // Largest e in [0, E) with tile_offsets[e] <= mt.
 __device__ __forceinline__ int find_expert(const int32_t *__restrict__ tile_offsets, int E, int mt) {
@@ -108,6 +118,7 @@ __device__ __forceinline__ int total_pairs(const GemmArgs &a, int total_m) {
   const int m_tiles = a.Mdim / (kBM * MB);
   if (MODE == kDW1) return a.E * ((m_tiles + 1) / 2) * n_tiles;  // pairs along M
   if (MODE == kDW2) return a.E * m_tiles * ((n_tiles + 1) / 2);  // pairs along N
+  if (MODE == kDW) return a.E * (dw_pairs<BN, MB>(a.d, 2 * a.n, false) + dw_pairs<BN, MB>(a.n, a.d, true));
   return ((total_m + 1) / 2) * n_tiles;                           // pairs of consecutive m-tiles
 }
 
@@ -116,23 +127,39 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &a, int pair, int ran
   Tile t;
   const int n_tiles = a.Ndim / BN;
   t.shared = true;
+  t.w2 = false;
   if (Traits<MODE>::varlen_k) {
-    const int m_tiles = a.Mdim / (kBM * MB);
-    int mt, nt;
-    if (MODE == kDW1) {
-      const int mp = (m_tiles + 1) / 2;
-      const int per_e = mp * n_tiles;
+    bool w2 = MODE == kDW2;
+    int Md = a.Mdim, Nd = a.Ndim, rem;
+    if (MODE == kDW) {
+      const int p1 = dw_pairs<BN, MB>(a.d, 2 * a.n, false);
+      const int per_e = p1 + dw_pairs<BN, MB>(a.n, a.d, true);
       t.e = pair / per_e;
-      const int rem = pair - t.e * per_e;
-      mt = min(2 * (rem / n_tiles) + rank, m_tiles - 1);  // an odd last row pair computes its tile twice
-      nt = rem % n_tiles;
+      rem = pair - t.e * per_e;
+      w2 = rem >= p1;
+      if (w2) {
+        rem -= p1;
+        Md = a.n;
+        Nd = a.d;
+      } else {
+        Md = a.d;
+        Nd = 2 * a.n;
+      }
     } else {
-      const int np = (n_tiles + 1) / 2;
-      const int per_e = m_tiles * np;
+      const int per_e = dw_pairs<BN, MB>(Md, Nd, w2);
       t.e = pair / per_e;
-      const int rem = pair - t.e * per_e;
+      rem = pair - t.e * per_e;
+    }
+    t.w2 = w2;
+    const int m_tiles = Md / (kBM * MB), nt_count = Nd / BN;
+    int mt, nt;
+    if (!w2) {
+      mt = min(2 * (rem / nt_count) + rank, m_tiles - 1);  // an odd last row pair computes its tile twice
+      nt = rem % nt_count;
+    } else {
+      const int np = (nt_count + 1) / 2;
       mt = rem / np;
-      nt = min(2 * (rem % np) + rank, n_tiles - 1);  // an odd last column pair computes its tile twice
+      nt = min(2 * (rem % np) + rank, nt_count - 1);  // an odd last column pair computes its tile twice
     }
     t.m0 = mt * kBM * MB;
     t.n0 = nt * BN;
@@ -190,6 +217,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
   const CUtensorMap &tmB = tm.b;
   using TR = Traits<MODE>;
   using SM = Smem<BN, STAGES, epi_bytes<MODE>(), MB>;
+  static_assert(MODE != kDW || (MB == 2 && BN == 256), "merged weight gradients: A and B stages of equal size");
   constexpr int kBufs = MB == 1 ? 2 : 1;           // TMEM accumulator buffers (double-buffered when MB = 1)
   constexpr uint32_t kTmemCols = 2 * BN;            // MB * BN * kBufs == 2 * BN in both layouts
   static_assert(MB * kBufs == 2, "TMEM holds two BN-column accumulators");
@@ -265,6 +293,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
                                    : MODE == kDH ? SM::kBBytes
                                    : MODE == kDW1 ? SM::kBBytes
                                    : MODE == kDW2 ? SM::kABytesMB
+                                   : MODE == kDW ? SM::kBBytes
                                                   : SM::kStageBytes;
     int s = 0;
     uint32_t ph = 0;
@@ -312,7 +341,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
 #pragma unroll
             for (int h = 0; h < 2; ++h)
               shared_box(b_dst + h * (BN / 2) * 128, &tmB, kb * kBK, t.e * a.d + t.n0 + h * (BN / 2), h == rank);
-          } else if (MODE == kDW1) {
+          } else if (MODE == kDW1 || (MODE == kDW && !t.w2)) {
             // B = dH rows [rb, rb+64) (MN-major); rows past the expert meet zero A rows
 #pragma unroll
             for (int c = 0; c < BN / 64; ++c)
@@ -344,7 +373,8 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     const int j = gt & 7;              // 16-byte piece of a 128-byte row segment
     const int rsub = gt >> 3;          // 0..15
     const uint32_t swz = static_cast<uint32_t>((j ^ (rsub & 7)) << 4);
-    const uint8_t *src_base = static_cast<const uint8_t *>(a.gsrc);
+    const uint8_t *src_a = static_cast<const uint8_t *>(a.gsrc);
+    const uint8_t *src_b = static_cast<const uint8_t *>(MODE == kDW ? a.gsrc2 : a.gsrc);
     const size_t ld_bytes = static_cast<size_t>(a.gld) * 2;
     // token rows (X or dO) are gathered about K times each: keep them in L2 ahead of the streamed weights
     const uint64_t pol_rows = policy_evict_last();
@@ -373,13 +403,16 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
         for (int q = 0; q < 8; ++q) {
           const int tok = tok_next[q];
           rown[q] = tok < a.T ? 16u : 0u;
-          rowp[q] = src_base + (tok < a.T ? tok : 0) * ld_bytes + j * 16;
+          rowp[q] = src_a + (tok < a.T ? tok : 0) * ld_bytes + j * 16;
         }
         if (pair + pair_step < total) {
           t_next = decode_tile<MODE, BN, MB>(a, pair + pair_step, rank, total_m);
           fetch_tokens(t_next);
         }
       }
+      // weight gradients: dW1 tiles gather X into A, dW2 tiles gather dO into B
+      const bool into_a = TR::gather_a_mn || (MODE == kDW && !t.w2);
+      const uint8_t *src_base = (MODE == kDW && t.w2) ? src_b : src_a;
       for (int kb = 0; kb < t.kblocks; ++kb) {
         if (!TR::gather_a_k) {
           // varlen-K: rows rb + rsub + 16q (q = 0..3) of this k-block, by token id
@@ -403,9 +436,9 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
           for (int q = 0; q < 8; ++q) cp_async_16_hint(dst + q * 2048, rowp[q] + koff, rown[q], pol_rows);
         } else {
           // MN-major: K-row k = rsub + 16q at byte k*128 of each 64-column chunk c (8 KB apart)
-          constexpr int kChunks = TR::gather_a_mn ? MB * kBM / 64 : BN / 64;
-          const uint32_t base_dst = (TR::gather_a_mn ? sA + s * SM::kABytesMB : sB + s * SM::kBBytes) + rsub * 128 + swz;
-          const int mn0 = TR::gather_a_mn ? t.m0 : t.n0;
+          constexpr int kChunks = TR::gather_a_mn ? MB * kBM / 64 : BN / 64;  // equal for kDW
+          const uint32_t base_dst = (into_a ? sA + s * SM::kABytesMB : sB + s * SM::kBBytes) + rsub * 128 + swz;
+          const int mn0 = into_a ? t.m0 : t.n0;
 #pragma unroll
           for (int q = 0; q < 4; ++q)
 #pragma unroll
@@ -491,11 +524,14 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     const uint64_t pol_stream = policy_evict_first();  // streamed epilogue traffic (H, A, dH, s*A) is touched once here
     for (int pair = first_pair; pair < total; pair += pair_step) {
       const Tile t = decode_tile<MODE, BN, MB>(a, pair, rank, total_m);
+      // weight gradients: the output of this tile and its row length
+      const int dw_m = MODE == kDW ? (t.w2 ? a.n : a.d) : a.Mdim;
+      const int dw_n = MODE == kDW ? (t.w2 ? a.d : 2 * a.n) : a.Ndim;
+      uint8_t *dw_out = static_cast<uint8_t *>((MODE == kDW && t.w2) ? a.out1 : a.out0);
       if (t.kblocks == 0) {
         if (TR::varlen_k) {  // an expert without rows has an exactly zero weight gradient
           for (int mb = 0; mb < MB; ++mb) {
-            uint8_t *dst = static_cast<uint8_t *>(a.out0) +
-                           (((size_t)t.e * a.Mdim + t.m0 + mb * kBM + row) * a.Ndim + t.n0) * 2;
+            uint8_t *dst = dw_out + (((size_t)t.e * dw_m + t.m0 + mb * kBM + row) * dw_n + t.n0) * 2;
             for (int c = 0; c < BN * 2; c += 16) st_v4(dst + c, 0u, 0u, 0u, 0u);
           }
         }
@@ -700,8 +736,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
 #pragma unroll 1
         for (int cc = 0; cc < MB * (BN / 32); ++cc) {
           const int mb = cc / (BN / 32), c = cc % (BN / 32);
-          uint8_t *dst = static_cast<uint8_t *>(a.out0) +
-                         (((size_t)t.e * a.Mdim + t.m0 + mb * kBM + row) * a.Ndim + t.n0) * 2;
+          uint8_t *dst = dw_out + (((size_t)t.e * dw_m + t.m0 + mb * kBM + row) * dw_n + t.n0) * 2;
           uint32_t v[32];
           tmem_ld32(tacc + mb * BN + c * 32, v);
           tmem_ld_wait();
@@ -771,7 +806,7 @@ int launch_gemm(const GemmArgs &a, const TensorMaps &tm, cudaStream_t stream) {
   }
   cfg.gridDim = dim3(grid_cache, 1, 1);
   cfg.numAttrs = 2;
-  static const char *const kNames[] = {"gemm_up", "gemm_down", "gemm_dh", "gemm_dx", "gemm_dw1", "gemm_dw2"};
+  static const char *const kNames[] = {"gemm_up", "gemm_down", "gemm_dh", "gemm_dx", "gemm_dw1", "gemm_dw2", "gemm_dw"};
   prof_begin(kNames[MODE], stream);
   err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<MODE, BN, STAGES, MB>, tm, a);
   prof_end(stream);

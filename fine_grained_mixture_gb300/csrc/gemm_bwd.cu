@@ -23,4 +23,8 @@ int launch_dw2(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) {
   return launch_gemm<kDW2, 256, 4, 1>(a, tm, s);
 }
 
+int launch_dw12(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) {
+  return launch_gemm<kDW, 256, 3, 2>(a, tm, s);
+}
+
 }  // namespace moe

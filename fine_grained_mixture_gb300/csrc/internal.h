@@ -60,13 +60,14 @@ struct GemmArgs {
   int Kdim;  // varlen-M: reduction length
   int nt_group;  // scatter-add GEMMs: column tiles per pass over all m-tiles (the fp32 slab kept in L2)
   int wide_m;    // weight-gradient GEMMs: 256-row blocks (experts average >= 1024 rows) instead of 128
-  void *out0;        // up: H;  dH: dH;  dW1/dW2: the weight gradient
-  void *out1;        // up: A;  dH: s*A
+  void *out0;        // up: H;  dH: dH;  dW1/dW2: the weight gradient (both in one launch: dW1)
+  void *out1;        // up: A;  dH: s*A;  both weight gradients in one launch: dW2
   float *out_f32;    // down: fp32 O;  dX~: fp32 dX
   float *dS;         // dH: per-row dS
   const void *Hin;   // dH: cached H
   const void *gsrc;  // the operand gathered by token id: X (up, dW1) or dO (dH, dW2), bf16 rows
-  int gld;           // its row length in elements
+  const void *gsrc2; // both weight gradients in one launch: dO (gsrc is X)
+  int gld;           // row length of the gathered operands in elements
 };
 
 // Tensor maps of one GEMM launch: a/b are the operands; h, dh, sa are the dH epilogue's cached-H input and
@@ -88,6 +89,8 @@ int launch_dh(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, int bn);
 int launch_dx(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s);
 int launch_dw1(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s);
 int launch_dw2(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s);
+// Both weight gradients in one launch (256-row blocks; d and n multiples of 256).
+int launch_dw12(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s);
 
 // elementwise (elementwise.cu)
 int launch_f32_to_bf16(const float *src, void *dst, size_t count, cudaStream_t s);
