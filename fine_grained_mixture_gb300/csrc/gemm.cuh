@@ -53,6 +53,11 @@ struct Traits {
   static constexpr bool a_mn = varlen_k;  // A operand MN-major in shared memory
   static constexpr bool b_mn = (MODE == kUp || MODE == kDown || varlen_k);
   static constexpr bool nt_outer = (MODE == kDown || MODE == kDX);  // keep one fp32 column slab hot in L2
+  // Paired CTAs of a cluster split the shared operand and multicast it, so each stage is released only when
+  // both CTAs' MMAs are done with it.  That lockstep costs more than the saved L2 reads where the CTAs' load
+  // latencies differ most (the X gather of the up-projection, the dense dH stream of dX~): there each CTA
+  // loads its whole tile and releases its own stages.
+  static constexpr bool paired = !(MODE == kUp || MODE == kDX);
 };
 
 constexpr int kGatherThreads = 128;
@@ -188,7 +193,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &a, int pair, int ran
     t.e = find_expert(a.tile_offsets, a.E, mt);
     // the partner tile shares this weight tile only if it exists and belongs to the same expert
     const int partner = 2 * mp + (rank ^ 1);
-    t.shared = (2 * mp + 1 < total_m) && find_expert(a.tile_offsets, a.E, partner) == t.e;
+    t.shared = Traits<MODE>::paired && (2 * mp + 1 < total_m) && find_expert(a.tile_offsets, a.E, partner) == t.e;
     t.m0 = 0;
     t.n0 = nt * BN;
     // a missing last tile (odd tile count) runs on rows past the last expert: zero operands, no output
@@ -200,6 +205,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &a, int pair, int ran
       t.row_end = t.row0;  // nothing is written
     }
   }
+  if (!Traits<MODE>::paired) t.shared = false;
   return t;
 }
 
@@ -243,7 +249,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), TR::gather ? 1 + kGatherThreads : 1);
-      mbar_init(empty_bar(s), 2);  // released by the MMA issuers of both CTAs
+      mbar_init(empty_bar(s), TR::paired ? 2 : 1);  // released by the MMA issuers of both CTAs (paired)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -495,7 +501,8 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
               umma_bf16(d_tmem + mb * BN, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
             }
           }
-          umma_commit_mc(empty_bar(s), 0x3);  // the stage is free for the producers of both CTAs
+          if (TR::paired) umma_commit_mc(empty_bar(s), 0x3);  // the stage is free for the producers of both CTAs
+          else umma_commit(empty_bar(s));
           if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
