@@ -76,14 +76,15 @@ constexpr int kDhWarpBytes = 4096 + 4096;
 // MB = 128-row M blocks per CTA.  The weight-gradient GEMMs (long K loop, light epilogue) use MB = 2: two
 // M=128 MMAs per k-step share the B tile, halving shared-memory bytes per FLOP so the same shared memory
 // covers twice the load latency; both accumulators fill TMEM (512 columns), so there is one buffer.
-template <int BN, int STAGES, int EPI_BYTES, int MB = 1>
+template <int BN, int STAGES, int EPI_BYTES, int MB = 1, int CACHE_BYTES = 0>
 struct Smem {
   static constexpr int kABytesMB = MB * kABytes;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytesMB + kBBytes;
   static constexpr int kStgOff = STAGES * kStageBytes;
   static constexpr int kBarOff = kStgOff + EPI_BYTES;
-  static constexpr int kBytes = kBarOff + 256 + 1024;  // + barriers/flags + alignment slack
+  static constexpr int kCacheOff = kBarOff + 256;                // barriers/flags, then the tile cache
+  static constexpr int kBytes = kCacheOff + CACHE_BYTES + 1024;  // + alignment slack
 };
 
 template <int MODE>
@@ -209,6 +210,36 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &a, int pair, int ran
   return t;
 }
 
+// Varlen-M tiles of one CTA, decoded once after the grid-dependency wait (the expert search over the tile
+// offsets is a chain of dependent loads: done per tile and per role it costs more than a k-block of MMA).
+constexpr int kTileCache = 128;  // tiles per CTA kept in shared memory; later tiles are decoded on the fly
+struct TileRec {
+  int row0, row_end;
+  uint32_t e_nt;  // expert (bits 0-15) | n-tile (bits 16-30) | shared (bit 31)
+};
+template <int MODE>
+__host__ __device__ constexpr int tile_cache_bytes() {
+  return Traits<MODE>::varlen_k ? 0 : kTileCache * static_cast<int>(sizeof(TileRec));
+}
+
+// Tile i of this CTA (pair = first_pair + i * pair_step): from the cache when it holds it.
+template <int MODE, int BN, int MB>
+__device__ __forceinline__ Tile tile_at(const GemmArgs &a, const TileRec *cache, int i, int pair, int rank,
+                                        int total_m) {
+  if (Traits<MODE>::varlen_k || i >= kTileCache) return decode_tile<MODE, BN, MB>(a, pair, rank, total_m);
+  const TileRec r = cache[i];
+  Tile t;
+  t.e = static_cast<int>(r.e_nt & 0xffffu);
+  t.n0 = static_cast<int>((r.e_nt >> 16) & 0x7fffu) * BN;
+  t.shared = (r.e_nt >> 31) != 0u;
+  t.w2 = false;
+  t.m0 = 0;
+  t.row0 = r.row0;
+  t.row_end = r.row_end;
+  t.kblocks = a.Kdim / kBK;
+  return t;
+}
+
 // Token id of row r, or an out-of-range row (zero fill) when r is past the expert or the id is invalid.
 __device__ __forceinline__ int token_or_oob(const GemmArgs &a, int r, int row_end) {
   if (r >= row_end) return a.T;
@@ -222,7 +253,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
   const CUtensorMap &tmA = tm.a;
   const CUtensorMap &tmB = tm.b;
   using TR = Traits<MODE>;
-  using SM = Smem<BN, STAGES, epi_bytes<MODE>(), MB>;
+  using SM = Smem<BN, STAGES, epi_bytes<MODE>(), MB, tile_cache_bytes<MODE>()>;
   static_assert(MODE != kDW || (MB == 2 && BN == 256), "merged weight gradients: A and B stages of equal size");
   constexpr int kBufs = MB == 1 ? 2 : 1;           // TMEM accumulator buffers (double-buffered when MB = 1)
   constexpr uint32_t kTmemCols = 2 * BN;            // MB * BN * kBufs == 2 * BN in both layouts
@@ -288,6 +319,18 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
   const int pair_step = static_cast<int>(num_clusters_x());
   const int total_m = TR::varlen_k ? 0 : __ldg(&a.tile_offsets[a.E]);
   const int total = total_pairs<MODE, BN, MB>(a, total_m);
+  TileRec *tile_cache = reinterpret_cast<TileRec *>(gbase + SM::kCacheOff);
+  if (!TR::varlen_k) {
+    const int mine = first_pair < total ? (total - first_pair + pair_step - 1) / pair_step : 0;
+    for (int i = threadIdx.x; i < min(mine, kTileCache); i += blockDim.x) {
+      const int pair = first_pair + i * pair_step;
+      const Tile t = decode_tile<MODE, BN, MB>(a, pair, rank, total_m);
+      tile_cache[i] = TileRec{t.row0, t.row_end,
+                              static_cast<uint32_t>(t.e) | (static_cast<uint32_t>(t.n0 / BN) << 16) |
+                                  (t.shared ? 0x80000000u : 0u)};
+    }
+    __syncthreads();
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------------------------ TMA producer
@@ -306,8 +349,8 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     int issued = 0;
     bool aborted = false;
     if (lane == 0) {
-      for (int pair = first_pair; pair < total && !aborted; pair += pair_step) {
-        const Tile t = decode_tile<MODE, BN, MB>(a, pair, rank, total_m);
+      for (int pair = first_pair, ti = 0; pair < total && !aborted; pair += pair_step, ++ti) {
+        const Tile t = tile_at<MODE, BN, MB>(a, tile_cache, ti, pair, rank, total_m);
         for (int kb = 0; kb < t.kblocks; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u) || *abort_flag) {
             set_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
@@ -395,11 +438,11 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     };
     Tile t_next;
     if (TR::gather_a_k && first_pair < total) {
-      t_next = decode_tile<MODE, BN, MB>(a, first_pair, rank, total_m);
+      t_next = tile_at<MODE, BN, MB>(a, tile_cache, 0, first_pair, rank, total_m);
       fetch_tokens(t_next);
     }
-    for (int pair = first_pair; pair < total && !aborted; pair += pair_step) {
-      const Tile t = TR::gather_a_k ? t_next : decode_tile<MODE, BN, MB>(a, pair, rank, total_m);
+    for (int pair = first_pair, ti = 0; pair < total && !aborted; pair += pair_step, ++ti) {
+      const Tile t = TR::gather_a_k ? t_next : tile_at<MODE, BN, MB>(a, tile_cache, ti, pair, rank, total_m);
       if (t.kblocks == 0) continue;
       const uint8_t *rowp[8];
       uint32_t rown[8];
@@ -412,7 +455,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
           rowp[q] = src_a + (tok < a.T ? tok : 0) * ld_bytes + j * 16;
         }
         if (pair + pair_step < total) {
-          t_next = decode_tile<MODE, BN, MB>(a, pair + pair_step, rank, total_m);
+          t_next = tile_at<MODE, BN, MB>(a, tile_cache, ti + 1, pair + pair_step, rank, total_m);
           fetch_tokens(t_next);
         }
       }
@@ -471,8 +514,8 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
       int buf = 0;
       uint32_t bph = 0;
       bool aborted = false;
-      for (int pair = first_pair; pair < total && !aborted; pair += pair_step) {
-        const Tile t = decode_tile<MODE, BN, MB>(a, pair, rank, total_m);
+      for (int pair = first_pair, ti = 0; pair < total && !aborted; pair += pair_step, ++ti) {
+        const Tile t = tile_at<MODE, BN, MB>(a, tile_cache, ti, pair, rank, total_m);
         if (t.kblocks == 0) continue;
         if (!mbar_wait(tempty_bar(buf), bph ^ 1u) || *abort_flag) {
           aborted = true;
@@ -529,8 +572,8 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     uint32_t hin_par = 0u;                       // dH epilogue: bit b = parity of H buffer b's next fill
     const uint64_t pol_acc = policy_evict_last();  // keep the fp32 accumulator slab in L2
     const uint64_t pol_stream = policy_evict_first();  // streamed epilogue traffic (H, A, dH, s*A) is touched once here
-    for (int pair = first_pair; pair < total; pair += pair_step) {
-      const Tile t = decode_tile<MODE, BN, MB>(a, pair, rank, total_m);
+    for (int pair = first_pair, ti = 0; pair < total; pair += pair_step, ++ti) {
+      const Tile t = tile_at<MODE, BN, MB>(a, tile_cache, ti, pair, rank, total_m);
       // weight gradients: the output of this tile and its row length
       const int dw_m = MODE == kDW ? (t.w2 ? a.n : a.d) : a.Mdim;
       const int dw_n = MODE == kDW ? (t.w2 ? a.d : 2 * a.n) : a.Ndim;
@@ -781,7 +824,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
 // Host launcher for one instantiation: clusters of two CTAs, one CTA per SM, as many clusters as fit.
 template <int MODE, int BN, int STAGES, int MB = 1>
 int launch_gemm(const GemmArgs &a, const TensorMaps &tm, cudaStream_t stream) {
-  using SM = Smem<BN, STAGES, epi_bytes<MODE>(), MB>;
+  using SM = Smem<BN, STAGES, epi_bytes<MODE>(), MB, tile_cache_bytes<MODE>()>;
   static int attr_dev = -1;
   static int grid_cache = 0;
   int dev = 0;
