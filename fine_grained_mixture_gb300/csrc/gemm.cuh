@@ -13,7 +13,7 @@
 //   kDX   dX32[tok] += dH W1_e^T                                                    M=rows  N=d   K=2n
 //   kDW1  dW1_e = X[tok]^T dH   (reduction over the expert's rows)                  M=d     N=2n  K=rows
 //   kDW2  dW2_e = (sA)^T dO[tok]                                                    M=n     N=d   K=rows
-//   kDW   both weight gradients in one launch: each expert's dW1 pairs, then its dW2 pairs (256-row blocks)
+//   kDW   both weight gradients in one launch: the dW1 pairs of every expert, then the dW2 pairs (256-row blocks)
 //
 // CTA = 6 or 10 warps: warp 0 issues TMA tiled loads of the dense operands, warp 1 owns TMEM and one
 // elected lane issues tcgen05.mma, warps 2..5 drain TMEM in the epilogue, and in the four GEMMs that read
@@ -138,16 +138,20 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &a, int pair, int ran
     bool w2 = MODE == kDW2;
     int Md = a.Mdim, Nd = a.Ndim, rem;
     if (MODE == kDW) {
+      // all dW1 pairs (expert by expert), then all dW2 pairs: the gathered rows in flight come from X, then
+      // from dO, rather than from both at once
       const int p1 = dw_pairs<BN, MB>(a.d, 2 * a.n, false);
-      const int per_e = p1 + dw_pairs<BN, MB>(a.n, a.d, true);
-      t.e = pair / per_e;
-      rem = pair - t.e * per_e;
-      w2 = rem >= p1;
+      w2 = pair >= a.E * p1;
       if (w2) {
-        rem -= p1;
+        const int p2 = dw_pairs<BN, MB>(a.n, a.d, true);
+        const int q = pair - a.E * p1;
+        t.e = q / p2;
+        rem = q - t.e * p2;
         Md = a.n;
         Nd = a.d;
       } else {
+        t.e = pair / p1;
+        rem = pair - t.e * p1;
         Md = a.d;
         Nd = 2 * a.n;
       }
