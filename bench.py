@@ -18,6 +18,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import re
 import math
 import os
 import statistics
@@ -50,6 +51,8 @@ def parse():
     p.add_argument("--mode", default="tc", choices=["tc", "tr"])
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle baseline sample")
     p.add_argument("--no-extras", action="store_true", help="skip the TR-vs-TC and e2e side measurements")
+    p.add_argument("--ingest-ncu", metavar="CSV", help="record per-launch DRAM bytes from an ncu --csv log "
+                   "(dram__bytes_read.sum, dram__bytes_write.sum) in profiles/dram_traffic.json and exit")
     return p.parse_args()
 
 
@@ -337,6 +340,65 @@ def load_traffic(kernel, workload):
     return ent.get("bytes_per_launch")
 
 
+GEMM_NAMES = ["gemm_up", "gemm_down", "gemm_dh", "gemm_dx", "gemm_dw1", "gemm_dw2", "gemm_dw"]
+NCU_NAMES = [("route_topk_kernel", "route_topk"), ("route_scan_kernel", "route_scan"),
+             ("route_fill_tc_kernel", "route_fill_tc"), ("route_fill_tr_kernel", "route_fill_tr"),
+             ("f32_to_bf16_kernel", "cast_f32_bf16"), ("zero_tail_kernel", "zero_tail")]
+UNIT_SCALE = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12, "ns": 1e-3, "us": 1.0, "ms": 1e3,
+              "nsecond": 1e-3, "usecond": 1.0, "msecond": 1e3, "second": 1e6}
+
+
+def bench_kernel_name(ncu_name):
+    m = re.search(r"moe_gemm_kernel<\(?(?:int\))?(\d+)", ncu_name)
+    if m:
+        return GEMM_NAMES[int(m.group(1))]
+    for key, name in NCU_NAMES:
+        if key in ncu_name:
+            return name
+    return None
+
+
+def ingest_ncu(csv_path, workload):
+    """Average per-launch DRAM bytes per kernel from an ncu --csv log into profiles/dram_traffic.json."""
+    import csv
+    rows = []
+    with open(csv_path) as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    per = {}  # launch id -> {name, metrics}
+    for r in csv.DictReader(lines):
+        name = bench_kernel_name(r["Kernel Name"])
+        if name is None:
+            continue
+        ent = per.setdefault(r["ID"], {"name": name})
+        ent[r["Metric Name"]] = float(r["Metric Value"].replace(",", "")) * UNIT_SCALE.get(r["Metric Unit"], 1.0)
+    agg = {}
+    for ent in per.values():
+        if "dram__bytes_read.sum" not in ent:
+            continue
+        a = agg.setdefault(ent["name"], {"read": 0.0, "write": 0.0, "us": 0.0, "n": 0})
+        a["read"] += ent["dram__bytes_read.sum"]
+        a["write"] += ent.get("dram__bytes_write.sum", 0.0)
+        a["us"] += ent.get("gpu__time_duration.sum", 0.0)
+        a["n"] += 1
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            table = json.load(f)
+    except Exception:
+        table = {}
+    sha = source_sha()
+    for name, a in sorted(agg.items()):
+        n = a["n"]
+        table.setdefault(name, {})[workload] = {
+            "bytes_per_launch": (a["read"] + a["write"]) / n, "read": a["read"] / n, "write": a["write"] / n,
+            "launches": n, "ncu_time_us": a["us"] / n, "source_sha": sha}
+    with open(path, "w") as f:
+        json.dump(table, f, indent=1, sort_keys=True)
+        f.write("\n")
+    print(json.dumps({k: round(v[workload]["bytes_per_launch"] / 1e6, 1) for k, v in table.items() if workload in v}))
+    return 0
+
+
 def source_sha():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fine_grained_mixture_gb300", "csrc")
@@ -349,6 +411,8 @@ def source_sha():
 
 def main():
     args = parse()
+    if args.ingest_ncu:
+        return ingest_ncu(args.ingest_ncu, args.workload)
     if args.impl == "reference":
         return run_reference(args)
 
