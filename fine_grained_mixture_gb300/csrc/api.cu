@@ -277,6 +277,25 @@ static GemmArgs base_args(const moe_routing *r, int T, int d, int n, int E, size
   return a;
 }
 
+int route_call(const float *logits, int T, int E, int K, int mode, const moe_routing *r, void *ws, size_t ws_bytes,
+               int32_t *P_host, void *stream, bool em_keys) {
+  int rc = check_route_shape(T, E, K, mode);
+  if (rc != MOE_OK) return rc;
+  if (!logits || !routing_ok(r)) return MOE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < route_workspace_bytes(T, E, K, mode, em_keys)) return MOE_ERR_WORKSPACE;
+  rc = check_device();
+  if (rc != MOE_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = launch_route(logits, T, E, K, mode, r, ws, s, em_keys);
+  if (rc != MOE_OK) return rc;
+  if (P_host) {
+    cudaError_t err = cudaMemcpyAsync(P_host, r->status + 1, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(s);
+    if (err != cudaSuccess) return record_cuda_error(err);
+  }
+  return MOE_OK;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -301,22 +320,9 @@ int moe_route_workspace_size(int T, int E, int K, int mode, size_t *bytes) {
 
 int moe_route(const float *logits, int T, int E, int K, int mode, const moe_routing *r, void *ws, size_t ws_bytes,
               int32_t *P_host, void *stream) {
-  int rc = check_route_shape(T, E, K, mode);
-  if (rc != MOE_OK) return rc;
-  if (!logits || !routing_ok(r)) return MOE_ERR_INVALID_ARG;
-  if (!ws || ws_bytes < route_workspace_bytes(T, E, K, mode)) return MOE_ERR_WORKSPACE;
-  rc = check_device();
-  if (rc != MOE_OK) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  rc = launch_route(logits, T, E, K, mode, r, ws, s);
-  if (rc != MOE_OK) return rc;
-  if (P_host) {
-    cudaError_t err = cudaMemcpyAsync(P_host, r->status + 1, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
-    if (err == cudaSuccess) err = cudaStreamSynchronize(s);
-    if (err != cudaSuccess) return record_cuda_error(err);
-  }
-  return MOE_OK;
+  return moe::route_call(logits, T, E, K, mode, r, ws, ws_bytes, P_host, stream, true);
 }
+
 
 int moe_forward_workspace_size(int T, int d, int n, int E, int K, size_t p_cap, size_t *bytes) {
   if (!bytes) return MOE_ERR_INVALID_ARG;

@@ -42,9 +42,15 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 // routing (route.cu)
-size_t route_workspace_bytes(int T, int E, int K, int mode);
+// Routing scratch.  em_keys: token rounding keeps an expert-major copy of the logit order keys (4*T*E bytes)
+// so that its per-expert selection reads them coalesced; without it the selection reads the logits in place.
+size_t route_workspace_bytes(int T, int E, int K, int mode, bool em_keys = true);
 int launch_route(const float *logits, int T, int E, int K, int mode, const moe_routing *r, void *ws,
-                 cudaStream_t stream);
+                 cudaStream_t stream, bool em_keys = true);
+// moe_route with the scratch layout chosen by the caller (moe_route_noalloc drops the expert-major keys when
+// they would not fit its static array).
+int route_call(const float *logits, int T, int E, int K, int mode, const moe_routing *r, void *ws, size_t ws_bytes,
+               int32_t *P_host, void *stream, bool em_keys);
 
 // grouped GEMMs (gemm_fwd.cu, gemm_bwd.cu)
 struct GemmArgs {

@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float *_
     cta_hist[(size_t)blockIdx.x * E + e] = hist[e];
     if (TR) member[(size_t)e * member_words + blockIdx.x] = mbits[e];  // a CTA covers one 32-token word
   }
-  if (TR) {
+  if (TR && keys_em) {
     // expert-major keys: each warp writes whole 32-token rows (128 bytes) of experts warp, warp + 8, ...
     const int t = t_first + lane;
     for (int e = warp; e < E; e += kTopkThreads / 32)
@@ -388,7 +388,8 @@ __device__ __forceinline__ int warp_scan_exclusive(int v, int *total) {
 }
 
 __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
-    const uint32_t *__restrict__ keys_em, int T, int E, int K, const int32_t *__restrict__ topk_idx,
+    const uint32_t *__restrict__ keys_em, const float *__restrict__ logits, int T, int E, int K,
+    const int32_t *__restrict__ topk_idx,
     const float *__restrict__ topk_score, const float *__restrict__ tok_max, const float *__restrict__ tok_den,
     const uint32_t *__restrict__ member, int member_words, int m_tile, const int32_t *__restrict__ tc_counts,
     const int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ tile_offsets,
@@ -412,7 +413,11 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
   const int f = tc_counts[e], r = counts[e], base = s_off[e];
   if (r == 0) return;
   for (int w = threadIdx.x; w < member_words; w += blockDim.x) mem[w] = member[(size_t)e * member_words + w];
-  for (int t = threadIdx.x; t < T; t += blockDim.x) key[t] = __ldcs(&keys_em[(size_t)e * T + t]);
+  if (keys_em) {
+    for (int t = threadIdx.x; t < T; t += blockDim.x) key[t] = __ldcs(&keys_em[(size_t)e * T + t]);
+  } else {  // compact scratch: the expert's column of the logits, one strided word per token
+    for (int t = threadIdx.x; t < T; t += blockDim.x) key[t] = order_key(logits[(size_t)t * E + e]);
+  }
   __syncthreads();
   // candidates: token-choice tokens when dropping, the other tokens when padding
   const bool drop = r < f;
@@ -566,18 +571,18 @@ struct RouteWs {
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // cta_hist [nctas][E] | chunk_base [nchunks][E] | TR: member [E][words], keys_em [E][T] | tok_max [T] | tok_den [T]
-size_t route_workspace_bytes(int T, int E, int K, int mode) {
+size_t route_workspace_bytes(int T, int E, int K, int mode, bool em_keys) {
   (void)K;
   const size_t nctas = (T + kTopkTokens - 1) / kTopkTokens;
   const size_t nchunks = (T + kChunk - 1) / kChunk;
   const size_t words = (T + 31) / 32;
   size_t b = align256(nctas * E * 4) + align256(nchunks * E * 4);
-  if (mode == MOE_ROUTE_TR) b += align256(words * E * 4) + align256((size_t)T * E * 4);
+  if (mode == MOE_ROUTE_TR) b += align256(words * E * 4) + (em_keys ? align256((size_t)T * E * 4) : 0);
   b += align256((size_t)T * 4) * 2;
   return b;
 }
 
-static RouteWs carve(void *ws, int T, int E, int mode) {
+static RouteWs carve(void *ws, int T, int E, int mode, bool em_keys) {
   RouteWs w{};
   w.nctas = (T + kTopkTokens - 1) / kTopkTokens;
   w.nchunks = (T + kChunk - 1) / kChunk;
@@ -590,8 +595,10 @@ static RouteWs carve(void *ws, int T, int E, int mode) {
   if (mode == MOE_ROUTE_TR) {
     w.member = reinterpret_cast<uint32_t *>(p);
     p += align256((size_t)w.member_words * E * 4);
-    w.keys_em = reinterpret_cast<uint32_t *>(p);
-    p += align256((size_t)T * E * 4);
+    if (em_keys) {
+      w.keys_em = reinterpret_cast<uint32_t *>(p);
+      p += align256((size_t)T * E * 4);
+    }
   }
   w.tok_max = reinterpret_cast<float *>(p);
   p += align256((size_t)T * 4);
@@ -604,8 +611,8 @@ size_t route_tr_smem_bytes(int T) {
 }
 
 int launch_route(const float *logits, int T, int E, int K, int mode, const moe_routing *r, void *ws,
-                 cudaStream_t stream) {
-  RouteWs w = carve(ws, T, E, mode);
+                 cudaStream_t stream, bool em_keys) {
+  RouteWs w = carve(ws, T, E, mode, em_keys);
   cudaError_t err = cudaMemsetAsync(r->status, 0, MOE_STATUS_WORDS * sizeof(int32_t), stream);
   if (err != cudaSuccess) return record_cuda_error(err);
   const bool tr = mode == MOE_ROUTE_TR;
@@ -665,7 +672,8 @@ int launch_route(const float *logits, int T, int E, int K, int mode, const moe_r
   } else {
     const size_t smem = route_tr_smem_bytes(T);
     prof_begin("route_fill_tr", stream);
-    err = launch_pdl(route_fill_tr_kernel, dim3(E), dim3(kTrThreads), smem, stream, w.keys_em, T, E, K, r->topk_idx,
+    err = launch_pdl(route_fill_tr_kernel, dim3(E), dim3(kTrThreads), smem, stream, w.keys_em, logits, T, E, K,
+                     r->topk_idx,
                      r->topk_score, w.tok_max, w.tok_den, w.member, w.member_words, MOE_M_TILE, r->tc_counts, r->counts,
                      r->offsets, r->tile_offsets, r->status, r->row_token, r->row_slot, r->row_score);
     if (err != cudaSuccess) return record_cuda_error(err);

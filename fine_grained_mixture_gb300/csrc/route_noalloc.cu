@@ -47,11 +47,18 @@ extern "C" int moe_route_noalloc(const float *logits, int T, int E, int K, int m
   size_t need = 0;
   int rc = moe_route_workspace_size(T, E, K, mode, &need);
   if (rc != MOE_OK) return rc;
+  // token rounding's expert-major key copy (4*T*E bytes) is a speed-up, not a necessity: drop it when it
+  // would not fit, and the selection reads the logits in place
+  bool em_keys = true;
+  if (need > MOE_ROUTE_NOALLOC_SCRATCH_BYTES) {
+    em_keys = false;
+    need = moe::route_workspace_bytes(T, E, K, mode, false);
+  }
   if (need > MOE_ROUTE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
   void *scratch = nullptr;
   rc = moe::scratch_address(&scratch);
   if (rc != MOE_OK) return rc;
   // Same kernels and validation as moe_route; the scratch is the library's own array instead of the
-  // caller's workspace.  Every per-call scratch word is rewritten (or cleared) before it is read.
-  return moe_route(logits, T, E, K, mode, r, scratch, need, P_host, stream);
+  // caller's workspace.  Every per-call scratch word is rewritten before it is read.
+  return moe::route_call(logits, T, E, K, mode, r, scratch, need, P_host, stream, em_keys);
 }

@@ -108,9 +108,11 @@ int moe_route(const float *logits, int T, int E, int K, int mode, const moe_rout
  *   Who needs it: code embedded in a host program whose allocator owns all device memory (raw cudaMalloc
  *   is forbidden), or a path with a fixed memory budget where no allocation may happen.  Such callers
  *   still pass the logits and the routing outputs (r); only the routing scratch changes hands.
- *   Scratch: a static device array of MOE_ROUTE_NOALLOC_SCRATCH_BYTES (8 MiB) inside the library, which
- *   every GPU that loads the library holds until the process exits.  Shapes whose scratch
- *   (moe_route_workspace_size) exceeds it return MOE_ERR_WORKSPACE before any device work.
+ *   Scratch: a static device array of MOE_ROUTE_NOALLOC_SCRATCH_BYTES (16 MiB) inside the library, which
+ *   every GPU that loads the library holds until the process exits.  When moe_route_workspace_size exceeds
+ *   it, token rounding leaves out its expert-major copy of the logit keys (4*T*E bytes) and reads the logits
+ *   in place (same results, slower selection); shapes that still do not fit return MOE_ERR_WORKSPACE before
+ *   any device work.
  *   Set-up: the first call on a device looks up the array's device address (cudaGetSymbolAddress) with
  *   that device current; make that first call before any stream capture.
  *   Sharing: all calls in the process share the one array per device and it keeps the last call's
@@ -118,7 +120,7 @@ int moe_route(const float *logits, int T, int E, int K, int mode, const moe_rout
  *   streams, or different host threads on one device) race on the array and corrupt each other.
  *   Never calls cudaMalloc, cudaFree or any allocating routine.  Other arguments and results as moe_route.
  */
-#define MOE_ROUTE_NOALLOC_SCRATCH_BYTES (8u << 20)
+#define MOE_ROUTE_NOALLOC_SCRATCH_BYTES (16u << 20)
 int moe_route_noalloc(const float *logits, int T, int E, int K, int mode, const moe_routing *r, int32_t *P_host,
                       void *stream);
 
