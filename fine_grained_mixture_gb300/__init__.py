@@ -4,8 +4,10 @@ The compute runs in libmoe.so (hand-written CUDA); ``moe`` is the thin ctypes bi
 """
 from .moe import (M_TILE, MOE_ROUTE_TC, MOE_ROUTE_TR, MoeError, Routing, kernel_launch_count, library,
                   moe_backward, moe_backward_workspace_size, moe_forward, moe_forward_workspace_size, moe_route,
-                  moe_route_capacity, moe_route_workspace_size, profile_enable, profile_summary)
+                  moe_route_capacity, moe_route_workspace_size, profile_enable, profile_summary,
+                  selftest_bounded_wait)
 
 __all__ = ["M_TILE", "MOE_ROUTE_TC", "MOE_ROUTE_TR", "MoeError", "Routing", "kernel_launch_count", "library",
            "moe_backward", "moe_backward_workspace_size", "moe_forward", "moe_forward_workspace_size", "moe_route",
-           "moe_route_capacity", "moe_route_workspace_size", "profile_enable", "profile_summary"]
+           "moe_route_capacity", "moe_route_workspace_size", "profile_enable", "profile_summary",
+           "selftest_bounded_wait"]

@@ -1,5 +1,6 @@
 // elementwise.cu - the fp32 -> bf16 cast that finishes the fused aggregations (O and dX are accumulated
-// in fp32 by the down-projection and dX~ epilogues, then rounded once to bf16).
+// in fp32 by the down-projection and dX~ epilogues, then rounded once to bf16), the zeroing of the rows past
+// the last expert, and the bounded-wait self-test.
 #include "common.cuh"
 #include "internal.h"
 
@@ -57,4 +58,25 @@ int launch_zero_tail(void *a, void *b, const int32_t *offsets, int E, size_t p_c
   return err == cudaSuccess ? MOE_OK : record_cuda_error(err);
 }
 
+// One CTA waits on an mbarrier that nothing arrives on; the bounded wait ends it with a status code.
+__global__ void __launch_bounds__(32) wait_selftest_kernel(int32_t *status) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = static_cast<uint32_t>(__cvta_generic_to_shared(&bar));
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0 && !mbar_wait(b, 0)) set_status(status, MOE_ERR_DEVICE_TIMEOUT);
+}
+
 }  // namespace moe
+
+extern "C" int moe_selftest_bounded_wait(int32_t *status, void *stream) {
+  if (!status) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  moe::wait_selftest_kernel<<<1, 32, 0, s>>>(status);
+  moe::count_launch();
+  const cudaError_t err = cudaGetLastError();
+  return err == cudaSuccess ? MOE_OK : moe::record_cuda_error(err);
+}

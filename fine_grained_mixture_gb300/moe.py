@@ -71,6 +71,8 @@ def library() -> ctypes.CDLL:
     lib.moe_last_cuda_error.argtypes = []
     lib.moe_kernel_launch_count.argtypes = []
     lib.moe_kernel_launch_count.restype = ctypes.c_uint64
+    lib.moe_selftest_bounded_wait.argtypes = [_vp, _vp]
+    lib.moe_selftest_bounded_wait.restype = _c_int
     lib.moe_profile_enable.argtypes = [_c_int]
     lib.moe_profile_count.argtypes = []
     lib.moe_profile_entry.argtypes = [_c_int, ctypes.c_char_p, _c_size, ctypes.POINTER(_c_int),
@@ -82,6 +84,15 @@ def library() -> ctypes.CDLL:
         getattr(lib, f).restype = _c_int
     _LIB = lib
     return lib
+
+
+def selftest_bounded_wait(stream=None) -> int:
+    """Run the bounded-wait self-test; returns the device status code it wrote (MOE_ERR_DEVICE_TIMEOUT = 6)."""
+    lib = library()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _check(lib.moe_selftest_bounded_wait(_ptr(st), _stream(stream)), "moe_selftest_bounded_wait")
+    torch.cuda.synchronize()
+    return int(st.item())
 
 
 def _check(code: int, where: str):

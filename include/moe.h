@@ -163,6 +163,14 @@ int moe_get_status(const moe_routing *r, int32_t *code, int32_t *P, void *stream
 /* Human-readable text of a status code (static storage). */
 const char *moe_strerror(int code);
 
+/*
+ * Self-test of the bounded device waits (no counterpart in the paper).  Launches one CTA that waits on an
+ * mbarrier nothing will ever arrive on, with the same bounded wait the GEMM pipelines use: after
+ * MOE_WAIT_TIMEOUT_NS (2 s) it gives up, writes MOE_ERR_DEVICE_TIMEOUT to status[0] (a device int32 the
+ * caller zeroes) and returns, leaving the CUDA context usable.  Asynchronous on `stream`.
+ */
+int moe_selftest_bounded_wait(int32_t *status, void *stream);
+
 /* The cudaError_t of the last MOE_ERR_CUDA on this thread (0 if none). */
 int moe_last_cuda_error(void);
 
