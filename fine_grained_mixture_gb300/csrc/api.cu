@@ -362,7 +362,11 @@ int moe_forward(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const
   a.Kdim = d;
   a.out0 = H;
   a.out1 = A;
-  if ((rc = (fill_unused(tm), launch_up(a, tm, s))) != MOE_OK) return rc;
+  fill_unused(tm);
+  // the epilogue stores H and A as 32 x 32 boxes from shared memory
+  if ((rc = make_tmap_bf16_epi(&tm.dh, H, 2 * (uint64_t)n, p_cap)) != MOE_OK) return rc;
+  if ((rc = make_tmap_bf16_epi(&tm.sa, A, n, p_cap)) != MOE_OK) return rc;
+  if ((rc = launch_up(a, tm, s)) != MOE_OK) return rc;
   // down-projection + aggregation: O32[tok] += s * A W2_e (N = d, K = n)
   if ((rc = make_tmap_bf16(&tm.a, A, n, p_cap, 128)) != MOE_OK) return rc;
   if ((rc = make_tmap_bf16(&tm.b, W2, d, (uint64_t)E * n, 64)) != MOE_OK) return rc;

@@ -87,9 +87,14 @@ struct Smem {
   static constexpr int kBytes = kCacheOff + CACHE_BYTES + 1024;  // + alignment slack
 };
 
+// Up-projection epilogue, per warp: one 6 KB staging tile (H gate | H up | A, 32 rows x 32 columns each,
+// 64-byte swizzle) drained by TMA stores.  Per-row stores from registers would send three uncoalesced 64-byte
+// pieces per lane and chunk through L1, twice the requests of the cp.async gather they compete with.
+constexpr int kUpWarpBytes = 6144;
+
 template <int MODE>
 __host__ __device__ constexpr int epi_bytes() {
-  return Traits<MODE>::nt_outer ? kStgBytes : (MODE == kDH ? 4 * kDhWarpBytes : 0);
+  return Traits<MODE>::nt_outer ? kStgBytes : (MODE == kDH ? 4 * kDhWarpBytes : (MODE == kUp ? 4 * kUpWarpBytes : 0));
 }
 
 struct Tile {
@@ -300,8 +305,8 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (MODE == kDH) {
-      tma_prefetch_desc(&tm.h);
+    if (MODE == kDH || MODE == kUp) {
+      if (MODE == kDH) tma_prefetch_desc(&tm.h);
       tma_prefetch_desc(&tm.dh);
       tma_prefetch_desc(&tm.sa);
     }
@@ -607,7 +612,11 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
       if (MODE == kUp) {
         const int r = t.row0 + row;
         const bool valid = r < t.row_end;
+        const bool full_warp = t.row0 + q * 32 + 31 < t.row_end;  // all 32 rows belong to this expert
+        const int wrow = t.row0 + q * 32;
         const int j0 = t.n0 / 2;
+        const uint32_t out_st = base + SM::kStgOff + q * kUpWarpBytes;
+        const int sw = (lane >> 1) & 3;  // 64-byte swizzle: piece p of row `lane` at piece p ^ ((lane >> 1) & 3)
         uint8_t *hrow = static_cast<uint8_t *>(a.out0) + (size_t)r * (2 * a.n) * 2;
         uint8_t *arow = static_cast<uint8_t *>(a.out1) + (size_t)r * a.n * 2;
 #pragma unroll 1
@@ -616,19 +625,41 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
           tmem_ld32(tacc + c * 32, g);
           tmem_ld32(tacc + BN / 2 + c * 32, u);
           tmem_ld_wait();
-          if (valid) {
-            uint32_t hg[16], hu[16], av[16];
+          uint32_t hg[16], hu[16], av[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
-              const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
-              const float a0 = __fdividef(g0, 1.f + __expf(-g0)) * u0;
-              const float a1 = __fdividef(g1, 1.f + __expf(-g1)) * u1;
-              hg[i] = pack_bf16x2(g0, g1);
-              hu[i] = pack_bf16x2(u0, u1);
-              av[i] = pack_bf16x2(a0, a1);
+          for (int i = 0; i < 16; ++i) {
+            const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+            const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+            const float a0 = __fdividef(g0, 1.f + __expf(-g0)) * u0;
+            const float a1 = __fdividef(g1, 1.f + __expf(-g1)) * u1;
+            hg[i] = pack_bf16x2(g0, g1);
+            hu[i] = pack_bf16x2(u0, u1);
+            av[i] = pack_bf16x2(a0, a1);
+          }
+          const int j = j0 + c * 32;
+          if (full_warp) {
+            if (lane == 0) bulk_wait_read<0>();  // the previous chunk's stores have read the staging tile
+            __syncwarp();
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+              const uint32_t o = lane * 64 + ((p ^ sw) << 4);
+              st_shared_v4(out_st + o, __uint_as_float(hg[4 * p]), __uint_as_float(hg[4 * p + 1]),
+                           __uint_as_float(hg[4 * p + 2]), __uint_as_float(hg[4 * p + 3]));
+              st_shared_v4(out_st + 2048 + o, __uint_as_float(hu[4 * p]), __uint_as_float(hu[4 * p + 1]),
+                           __uint_as_float(hu[4 * p + 2]), __uint_as_float(hu[4 * p + 3]));
+              st_shared_v4(out_st + 4096 + o, __uint_as_float(av[4 * p]), __uint_as_float(av[4 * p + 1]),
+                           __uint_as_float(av[4 * p + 2]), __uint_as_float(av[4 * p + 3]));
             }
-            const int j = j0 + c * 32;
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tm.dh, out_st, j, wrow, pol_stream);
+              tma_store_2d(&tm.dh, out_st + 2048, a.n + j, wrow, pol_stream);
+              tma_store_2d(&tm.sa, out_st + 4096, j, wrow, pol_stream);
+              bulk_commit();
+            }
+          } else if (valid) {
+            // a warp whose rows run past the expert: per-row stores keep the next expert's rows intact
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               st_v4_hint(hrow + (size_t)j * 2 + v * 16, hg[4 * v], hg[4 * v + 1], hg[4 * v + 2], hg[4 * v + 3],
@@ -639,6 +670,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
                          pol_stream);
             }
           }
+          __syncwarp();
         }
       } else if (MODE == kDown || MODE == kDX) {
         const int r = t.row0 + row;
@@ -809,7 +841,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
         bph ^= 1u;
       }
     }
-    if (MODE == kDH || TR::nt_outer) bulk_wait<0>();  // every bulk store / add has landed before the end
+    if (MODE == kUp || MODE == kDH || TR::nt_outer) bulk_wait<0>();  // every bulk store / add has landed
   }
 
   __syncthreads();
