@@ -456,7 +456,10 @@ int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, cons
     aw.gsrc = X;
     aw.gsrc2 = dO;
     aw.gld = d;
-    if ((rc = (fill_unused(tm), launch_dw12(aw, tm, s))) != MOE_OK) return rc;
+    fill_unused(tm);
+    if ((rc = make_tmap_bf16_epi(&tm.dh, dW1, 2 * (uint64_t)n, (uint64_t)E * d)) != MOE_OK) return rc;
+    if ((rc = make_tmap_bf16_epi(&tm.sa, dW2, d, (uint64_t)E * n)) != MOE_OK) return rc;
+    if ((rc = launch_dw12(aw, tm, s)) != MOE_OK) return rc;
     return side.join();
   }
   // dW1_e = X[tok]^T dH_e (M = d, N = 2n, K = rows of e); X rows gathered with cp.async
@@ -467,7 +470,9 @@ int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, cons
   aw.out0 = dW1;
   aw.gsrc = X;
   aw.gld = d;
-  if ((rc = (fill_unused(tm), launch_dw1(aw, tm, s))) != MOE_OK) return rc;
+  fill_unused(tm);
+  if ((rc = make_tmap_bf16_epi(&tm.dh, dW1, 2 * (uint64_t)n, (uint64_t)E * d)) != MOE_OK) return rc;
+  if ((rc = launch_dw1(aw, tm, s)) != MOE_OK) return rc;
   // dW2_e = (s*A)_e^T dO[tok] (M = n, N = d, K = rows of e); dO rows gathered with cp.async
   if ((rc = make_tmap_bf16(&tm.a, sA, n, p_cap, 64)) != MOE_OK) return rc;
   tm.b = tm.a;
@@ -476,7 +481,9 @@ int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, cons
   aw.out0 = dW2;
   aw.gsrc = dO;
   aw.gld = d;
-  if ((rc = (fill_unused(tm), launch_dw2(aw, tm, s))) != MOE_OK) return rc;
+  fill_unused(tm);
+  if ((rc = make_tmap_bf16_epi(&tm.dh, dW2, d, (uint64_t)E * n)) != MOE_OK) return rc;
+  if ((rc = launch_dw2(aw, tm, s)) != MOE_OK) return rc;
   return side.join();
 }
 

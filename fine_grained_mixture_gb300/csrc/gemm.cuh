@@ -92,9 +92,17 @@ struct Smem {
 // pieces per lane and chunk through L1, twice the requests of the cp.async gather they compete with.
 constexpr int kUpWarpBytes = 6144;
 
+// Weight-gradient epilogue, per warp: two 2 KB staging tiles (32 rows x 32 columns of dW, 64-byte swizzle)
+// drained by TMA stores, one box in flight while the next is written.
+constexpr int kDwWarpBytes = 2 * 2048;
+
 template <int MODE>
 __host__ __device__ constexpr int epi_bytes() {
-  return Traits<MODE>::nt_outer ? kStgBytes : (MODE == kDH ? 4 * kDhWarpBytes : (MODE == kUp ? 4 * kUpWarpBytes : 0));
+  return Traits<MODE>::nt_outer ? kStgBytes
+         : MODE == kDH          ? 4 * kDhWarpBytes
+         : MODE == kUp          ? 4 * kUpWarpBytes
+         : Traits<MODE>::varlen_k ? 4 * kDwWarpBytes
+                                  : 0;
 }
 
 struct Tile {
@@ -305,7 +313,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (MODE == kDH || MODE == kUp) {
+    if (MODE == kDH || MODE == kUp || TR::varlen_k) {
       if (MODE == kDH) tma_prefetch_desc(&tm.h);
       tma_prefetch_desc(&tm.dh);
       tma_prefetch_desc(&tm.sa);
@@ -818,19 +826,33 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
         }
         if (valid) atomicAdd(&a.dS[r], ds);
       } else {
-        // weight gradients: bf16 rows of dW_e (M block mb sits in TMEM columns [mb * BN, (mb + 1) * BN))
+        // weight gradients: bf16 rows of dW_e (M block mb sits in TMEM columns [mb * BN, (mb + 1) * BN)), stored
+        // as 32 x 32 boxes of the [E * M, N] output view through two staging tiles per warp
+        const CUtensorMap *omap = (MODE == kDW && t.w2) ? &tm.sa : &tm.dh;
+        const uint32_t stg = base + SM::kStgOff + q * kDwWarpBytes;
+        const int sw = (lane >> 1) & 3;  // 64-byte swizzle
 #pragma unroll 1
         for (int cc = 0; cc < MB * (BN / 32); ++cc) {
           const int mb = cc / (BN / 32), c = cc % (BN / 32);
-          uint8_t *dst = dw_out + (((size_t)t.e * dw_m + t.m0 + mb * kBM + row) * dw_n + t.n0) * 2;
           uint32_t v[32];
           tmem_ld32(tacc + mb * BN + c * 32, v);
           tmem_ld_wait();
           uint32_t p[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          const uint32_t buf_st = stg + (cc & 1) * 2048;
+          if (lane == 0) bulk_wait_read<1>();  // the box stored from this tile two chunks ago has been read
+          __syncwarp();
 #pragma unroll
-          for (int w = 0; w < 4; ++w) st_v4(dst + c * 64 + w * 16, p[4 * w], p[4 * w + 1], p[4 * w + 2], p[4 * w + 3]);
+          for (int w = 0; w < 4; ++w)
+            st_shared_v4(buf_st + lane * 64 + ((w ^ sw) << 4), __uint_as_float(p[4 * w]), __uint_as_float(p[4 * w + 1]),
+                         __uint_as_float(p[4 * w + 2]), __uint_as_float(p[4 * w + 3]));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(omap, buf_st, t.n0 + c * 32, t.e * dw_m + t.m0 + mb * kBM + q * 32, policy_evict_first());
+            bulk_commit();
+          }
         }
       }
       tc_fence_before();
@@ -841,7 +863,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
         bph ^= 1u;
       }
     }
-    if (MODE == kUp || MODE == kDH || TR::nt_outer) bulk_wait<0>();  // every bulk store / add has landed
+    bulk_wait<0>();  // every bulk store / reduce-add of this thread has landed before the end
   }
 
   __syncthreads();
