@@ -809,11 +809,19 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
               tma_store_2d(&tm.dh, out_st, j, wrow, pol_stream);
               tma_store_2d(&tm.dh, out_st + 2048, a.n + j, wrow, pol_stream);
               bulk_commit();
+              bulk_wait_read<0>();  // the dH gate tile has been read: s*A reuses its 2 KB
             }
+            __syncwarp();
 #pragma unroll
-            for (int w = 0; w < 4; ++w)
-              st_v4_hint(sarow + (size_t)j * 2 + w * 16, sa[4 * w], sa[4 * w + 1], sa[4 * w + 2], sa[4 * w + 3],
-                         pol_stream);
+            for (int p = 0; p < 4; ++p)
+              st_shared_v4(out_st + lane * 64 + ((p ^ sw) << 4), __uint_as_float(sa[4 * p]),
+                           __uint_as_float(sa[4 * p + 1]), __uint_as_float(sa[4 * p + 2]), __uint_as_float(sa[4 * p + 3]));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tm.sa, out_st, j, wrow, pol_stream);
+              bulk_commit();
+            }
           } else if (valid) {
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
