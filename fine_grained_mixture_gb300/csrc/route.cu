@@ -367,13 +367,15 @@ __global__ void __launch_bounds__(kChunk) route_fill_tc_kernel(int T, int E, int
 
 // One CTA (1024 threads) per expert.  Keys of all T tokens for this expert live in shared memory.
 //   selection: a 4-pass radix select (8 bits per pass, most significant first) over the candidates finds the
-//              key of the R-th best candidate; each group of four warps fills its own 256-bin histogram and one
-//              warp scans the bins; candidates equal to that key are kept lowest token first
+//              key of the R-th best candidate; each group of four warps fills its own 256-bin histogram (lanes
+//              in one bin add once) and one warp scans the bins; after the first pass (or from the start when dropping) the
+//              candidates are listed so the later passes skip the rest of the tokens; candidates equal to the
+//              boundary key are kept lowest token first
 //   output:    each warp owns a contiguous token range; ballots give in-order ranks, so the whole pass needs
 //              two block-wide scans (tie ranks, row positions)
 constexpr int kTrThreads = 1024;
 constexpr int kTrWarps = kTrThreads / 32;
-constexpr int kTrHists = 8;
+constexpr int kTrHists = 8;  // histogram copies, one per four warps
 
 __device__ __forceinline__ int warp_scan_exclusive(int v, int *total) {
   const int lane = threadIdx.x & 31;
@@ -394,12 +396,14 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
     const uint32_t *__restrict__ member, int member_words, int m_tile, const int32_t *__restrict__ tc_counts,
     const int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ tile_offsets,
     int32_t *__restrict__ status, int32_t *__restrict__ row_token, int32_t *__restrict__ row_slot,
-    float *__restrict__ row_score) {
+    float *__restrict__ row_score, int list_cap) {
   extern __shared__ uint32_t sm[];
   uint32_t *key = sm;                                       // [T]
   uint32_t *mem = sm + T;                                   // [member_words]
   int *hist = reinterpret_cast<int *>(mem + member_words);  // [kTrHists][256]
   uint32_t *keep_bits = reinterpret_cast<uint32_t *>(hist + kTrHists * 256);  // [member_words]
+  int *list = reinterpret_cast<int *>(keep_bits + member_words);              // [list_cap] candidate tokens
+  __shared__ int list_n;
   __shared__ int warp_tot[kTrWarps];
   __shared__ int warp_base[kTrWarps];
   __shared__ int sel_state[2];
@@ -424,19 +428,42 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
   const int R = drop ? r : r - f;  // how many candidates to keep
   uint32_t prefix = 0u, mask = 0u;
   int remaining = R;
+  const uint32_t lt = (1u << lane) - 1u;
+  // Tokens satisfying `pred`, in no particular order, into list[]; -1 when there are more than list_cap.
+  auto build_list = [&](auto pred) -> int {
+    if (threadIdx.x == 0) list_n = 0;
+    __syncthreads();
+    for (int t0 = 0; t0 < T; t0 += blockDim.x) {
+      const int t = t0 + threadIdx.x;
+      const bool p = t < T && pred(t);
+      const uint32_t b = __ballot_sync(0xffffffffu, p);
+      int at = 0;
+      if (lane == 0 && b) at = atomicAdd(&list_n, __popc(b));
+      at = __shfl_sync(0xffffffffu, at, 0) + __popc(b & lt);
+      if (p && at < list_cap) list[at] = t;
+    }
+    __syncthreads();
+    return list_n <= list_cap ? list_n : -1;
+  };
+  auto is_tc = [&](int t) { return ((mem[t >> 5] >> (t & 31)) & 1u) != 0u; };
   if (r != f) {
+    // Candidates are few next to T: the expert's token-choice tokens when dropping, and when padding the
+    // other tokens in the top-byte bin of the boundary.  Once they are listed, the remaining radix passes
+    // walk the list instead of all T tokens (all T when the list would overflow its space).
+    int nlist = drop ? build_list(is_tc) : -1;
     int *my_hist = hist + (warp >> 2) * 256;
     for (int shift = 24; shift >= 0; shift -= 8) {
       for (int i = threadIdx.x; i < kTrHists * 256; i += blockDim.x) hist[i] = 0;
       __syncthreads();
       // lanes that fall in the same bin add once (many keys share their leading bits)
-      for (int t0 = 0; t0 < T; t0 += blockDim.x) {
-        const int t = t0 + threadIdx.x;
+      const int n_iter = nlist >= 0 ? nlist : T;
+      for (int i0 = 0; i0 < n_iter; i0 += blockDim.x) {
+        const int i = i0 + threadIdx.x;
         uint32_t bin = 256u;
-        if (t < T) {
-          const bool tc = (mem[t >> 5] >> (t & 31)) & 1u;
+        if (i < n_iter) {
+          const int t = nlist >= 0 ? list[i] : i;
           const uint32_t k = key[t];
-          if (tc == drop && (k & mask) == prefix) bin = (k >> shift) & 255u;
+          if ((nlist >= 0 || is_tc(t) == drop) && (k & mask) == prefix) bin = (k >> shift) & 255u;
         }
         const uint32_t same = __match_any_sync(0xffffffffu, bin);
         if (bin < 256u && lane == __ffs(same) - 1) atomicAdd(&my_hist[bin], __popc(same));
@@ -473,6 +500,10 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
       prefix |= static_cast<uint32_t>(sel_state[0]) << shift;
       mask |= 255u << shift;
       remaining = sel_state[1];
+      if (!drop && shift == 24) {
+        const uint32_t top = prefix;
+        nlist = build_list([&](int t) { return !is_tc(t) && (key[t] & 0xff000000u) == top; });
+      }
     }
   }
   // prefix = key of the R-th best candidate; `remaining` candidates equal to it are kept, lowest token first.
@@ -610,6 +641,15 @@ size_t route_tr_smem_bytes(int T) {
   return (size_t)T * 4 + (size_t)((T + 31) / 32) * 4 * 2 + kTrHists * 256 * 4;
 }
 
+// Candidate-list entries the token-rounding fill gets beside its fixed shared memory: up to 4096 (16 KB keeps
+// two CTAs per SM at T = 16384), less where T leaves less room.
+constexpr size_t kTrDynSmemMax = 218 * 1024;  // + about 8.4 KB of static shared memory stays under 227 KB
+static int route_tr_list_cap(int T) {
+  const size_t fixed = route_tr_smem_bytes(T);
+  const size_t room = fixed < kTrDynSmemMax ? (kTrDynSmemMax - fixed) / 4 : 0;
+  return static_cast<int>(room < 4096 ? room : 4096);
+}
+
 int launch_route(const float *logits, int T, int E, int K, int mode, const moe_routing *r, void *ws,
                  cudaStream_t stream, bool em_keys) {
   RouteWs w = carve(ws, T, E, mode, em_keys);
@@ -634,7 +674,7 @@ int launch_route(const float *logits, int T, int E, int K, int mode, const moe_r
     MOE_TOPK_EACH(MOE_TOPK_ATTR)
 #undef MOE_TOPK_ATTR
     if (err == cudaSuccess) err = cudaFuncSetAttribute(route_fill_tr_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                       static_cast<int>(route_tr_smem_bytes(kMaxTrTokens)));
+                                                       static_cast<int>(kTrDynSmemMax));
     if (err != cudaSuccess) return record_cuda_error(err);
     attr_dev = dev;
   }
@@ -670,12 +710,13 @@ int launch_route(const float *logits, int T, int E, int K, int mode, const moe_r
                      r->status, r->row_token, r->row_slot, r->row_score);
     if (err != cudaSuccess) return record_cuda_error(err);
   } else {
-    const size_t smem = route_tr_smem_bytes(T);
+    const int list_cap = route_tr_list_cap(T);
+    const size_t smem = route_tr_smem_bytes(T) + (size_t)list_cap * 4;
     prof_begin("route_fill_tr", stream);
     err = launch_pdl(route_fill_tr_kernel, dim3(E), dim3(kTrThreads), smem, stream, w.keys_em, logits, T, E, K,
                      r->topk_idx,
                      r->topk_score, w.tok_max, w.tok_den, w.member, w.member_words, MOE_M_TILE, r->tc_counts, r->counts,
-                     r->offsets, r->tile_offsets, r->status, r->row_token, r->row_slot, r->row_score);
+                     r->offsets, r->tile_offsets, r->status, r->row_token, r->row_slot, r->row_score, list_cap);
     if (err != cudaSuccess) return record_cuda_error(err);
   }
   prof_end(stream);
