@@ -1,0 +1,62 @@
+"""The layer inside a CUDA graph.
+
+Every call forks its memory-bound side work (accumulator zeroing, the dX cast) onto a library-owned stream
+and joins it back with events, and launches its kernels with programmatic dependent launch.  Captured on a
+caller stream and replayed, route + forward + backward must give the eager results: routing bit-exact, the
+fp32-accumulated tensors within the parity tolerance (their reduce-add order may differ run to run).
+"""
+import pytest
+import torch
+
+import fine_grained_mixture_gb300 as moe
+from fine_grained_mixture_gb300 import synth
+from gpu_util import assert_close, f64, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name,mode", [("tiny", "tc"), ("tiny", "tr"), ("fine7b", "tc")])
+def test_route_forward_backward_replay_in_a_cuda_graph(name, mode):
+    w = synth.WORKLOADS[name]
+    g = to_dev(synth.make_inputs(w, 3))
+    rt = moe.Routing(w.T, w.E, w.K, mode, "cuda")
+    p = rt.p_cap
+    bf = torch.bfloat16
+    O = torch.empty((w.T, w.d), dtype=bf, device="cuda")
+    H = torch.empty((p, 2 * w.n), dtype=bf, device="cuda")
+    dX = torch.empty((w.T, w.d), dtype=bf, device="cuda")
+    dW1 = torch.empty((w.E, w.d, 2 * w.n), dtype=bf, device="cuda")
+    dW2 = torch.empty((w.E, w.n, w.d), dtype=bf, device="cuda")
+    dS = torch.empty(p, dtype=torch.float32, device="cuda")
+    wsf = torch.empty(moe.moe_forward_workspace_size(w.T, w.d, w.n, w.E, w.K, p), dtype=torch.uint8, device="cuda")
+    wsb = torch.empty(moe.moe_backward_workspace_size(w.T, w.d, w.n, w.E, w.K, p), dtype=torch.uint8, device="cuda")
+
+    def step():
+        moe.moe_route(g["logits"], w.K, mode, routing=rt)
+        moe.moe_forward(g["X"], g["W1"], g["W2"], rt, O=O, H=H, ws=wsf)
+        moe.moe_backward(g["dO"], g["X"], g["W1"], g["W2"], H, rt, dX=dX, dW1=dW1, dW2=dW2, dS=dS, ws=wsb)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # eager: first-use set-up (attributes, side stream, events) happens outside the capture
+    torch.cuda.synchronize()
+    eager = {k: t.clone() for k, t in dict(O=O, H=H, dX=dX, dW1=dW1, dW2=dW2, dS=dS, row_token=rt.row_token,
+                                             offsets=rt.offsets).items()}
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        step()
+    for t in (O, H, dX, dW1, dW2, dS):
+        t.zero_()
+    rt.row_token.fill_(-1)
+    torch.cuda.synchronize()
+    graph.replay()
+    graph.replay()  # twice: nothing from the first replay may leak into the second
+    torch.cuda.synchronize()
+    code, P = rt.device_status()
+    assert code == 0
+    assert torch.equal(rt.offsets, eager["offsets"])
+    assert torch.equal(rt.row_token[:P], eager["row_token"][:P])
+    for k, t in dict(O=O, H=H[:P], dX=dX, dW1=dW1, dW2=dW2, dS=dS[:P]).items():
+        ref = eager[k][:P] if k in ("H", "dS") else eager[k]
+        assert_close(k, f64(t), f64(ref))
