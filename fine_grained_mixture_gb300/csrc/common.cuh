@@ -113,17 +113,6 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *tm, uint32_t src
                : "memory");
 }
 
-// Gather of four rows (r0..r3, each one box-width wide starting at element c0) of a 2D tensor into four
-// consecutive box rows of shared memory.  A row index outside the tensor reads the zero fill.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *tm, int c0, int r0, int r1, int r2,
-                                            int r3, uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
-      "l"(tm), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar), "l"(policy)
-      : "memory");
-}
-
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
@@ -162,8 +151,6 @@ __device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void *src, 
                "l"(policy)
                : "memory");
 }
-
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -304,11 +291,6 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);
-}
-
-__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
 }
 
 // Bulk (TMA engine) element-wise fp32 add of `bytes` from shared memory into global memory.

@@ -6,7 +6,7 @@
 // operand load and elementwise work fused into the epilogue ("Key design 2: IO-aware fused kernels"), and
 // on Blackwell a two-stage TMEM accumulator so one tile's epilogue overlaps the next tile's MMAs.
 //
-// One persistent kernel template serves all six GEMMs of the layer:
+// One persistent kernel template serves the GEMMs of the layer:
 //   kUp   H = X[tok] W1_e, epilogue SwiGLU -> H (bf16, cached) and A (bf16)        M=rows  N=2n  K=d
 //   kDown O32[tok] += s * (A W2_e)  (Y never stored)                              M=rows  N=d   K=n
 //   kDH   dA' = dO[tok] W2_e^T, epilogue: A'=SwiGLU(H), dS=<dA',A'>, dH, s*A'      M=rows  N=n   K=d
@@ -16,14 +16,17 @@
 //   kDW   both weight gradients in one launch: the dW1 pairs of every expert, then the dW2 pairs (256-row blocks)
 //
 // CTA = 6 or 10 warps: warp 0 issues TMA tiled loads of the dense operands, warp 1 owns TMEM and one
-// elected lane issues tcgen05.mma, warps 2..5 drain TMEM in the epilogue, and in the four GEMMs that read
-// rows by token id warps 6..9 gather those rows with 16-byte cp.async into the 128-byte-swizzled layout
-// (a TMA gather costs one request per 128-byte row, which starves the tensor cores here; the LSU path
-// moves the same rows at a fraction of the issue cost).
-// Tiles: 128 x BN x 64, STAGES-deep shared-memory ring, two TMEM accumulators of BN fp32 columns.
-// CTAs run in clusters of two on neighbouring tiles that need the same TMA-loaded operand (the expert's
-// weight tile, or the s*A tile of dW2): each CTA loads half of it and multicasts it to both, halving the
-// L2 -> SM traffic of that operand; a stage is released to both producers by a multicast commit.
+// elected lane issues tcgen05.mma, warps 2..5 (2..9 in the scatter-add GEMMs) drain TMEM in the epilogue,
+// and in the GEMMs that read rows by token id warps 6..9 gather those rows with 16-byte cp.async into the
+// 128-byte-swizzled layout (a TMA gather costs one request per 128-byte row, which starves the tensor cores
+// here; the LSU path moves the same rows at a fraction of the issue cost).  Epilogue outputs leave through
+// TMA stores (or bulk reduce-adds) from shared-memory staging: per-row stores from registers would crowd
+// the gather out of L1.
+// Tiles: 128 x BN x 64 (256-row blocks in the weight gradients), STAGES-deep shared-memory ring, two TMEM
+// accumulators of BN fp32 columns.  Each CTA decodes its tiles once into shared memory.
+// CTAs run in clusters of two on neighbouring tiles.  Where the two tiles need the same TMA-loaded operand
+// (down, dH, the weight gradients) each CTA loads half of it and multicasts it to both, and a stage is
+// released to both producers by a multicast commit; the up-projection and dX~ run unpaired.
 // Every wait is bounded; on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT, drains its own copies and
 // MMAs, frees TMEM and returns.
 #pragma once
