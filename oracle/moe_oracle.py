@@ -30,6 +30,13 @@ Readings taken where the pages are silent (each listed in the design notes of th
     f_e - floor = ceil - f_e rounds down; a pad that would exceed T rounds down; an expert-choice pair
     added by rounding gets the token's token-choice softmax normaliser.
   * Rows of one expert are ordered by ascending token id.
+  * Rounding subroutines other than the nearest multiple (the note, "Loss function / training strategy",
+    says token rounding is robust to which one is used): always up, always down, and stochastic (up with
+    probability (f - floor)/M_tile, from one uniform draw per expert passed in, so the expected count is f).
+    Padding beyond T tokens is impossible under every rule, which then rounds down.
+  * Expert choice (the "EC" rows of the note's ablation table): each expert takes the C = floor(T K / E)
+    tokens with the largest logits in its column (ties to the lower token id); a routed pair's gate is the
+    token's softmax over all E logits.
 """
 from __future__ import annotations
 
@@ -93,13 +100,34 @@ def gate_scores(z: np.ndarray, topk_idx: np.ndarray) -> np.ndarray:
     return np.exp(zs - z0[:, None]) / den[:, None]
 
 
-def round_and_sparsify(f: np.ndarray, m_tile: int, T: int) -> np.ndarray:
-    """Nearest multiple of M_tile: pad up when ceil - f < f - floor (strict), else drop to floor.
-    A pad beyond T tokens is impossible, so it drops instead."""
+ROUNDING_RULES = ("nearest", "up", "down", "stochastic")
+
+
+def round_and_sparsify(f: np.ndarray, m_tile: int, T: int, rule: str = "nearest", u=None) -> np.ndarray:
+    """Each expert's count f rounded to a multiple of M_tile: floor or ceil.
+
+    nearest:     ceil when ceil - f < f - floor (strict), else floor (the pages' rule)
+    up / down:   ceil / floor
+    stochastic:  ceil when u * M_tile < f - floor for the expert's uniform u in [0, 1), so that ceil is taken
+                 with probability (f - floor) / M_tile and the expected count is f
+    A ceil beyond T tokens is impossible, so every rule takes the floor there."""
     f = np.asarray(f, dtype=np.int64)
     lo = (f // m_tile) * m_tile
     hi = -((-f) // m_tile) * m_tile
-    up = ((hi - f) < (f - lo)) & (hi <= T)
+    if rule == "nearest":
+        up = (hi - f) < (f - lo)
+    elif rule == "up":
+        up = hi > f
+    elif rule == "down":
+        up = np.zeros(f.shape, dtype=bool)
+    elif rule == "stochastic":
+        u = np.asarray(u, dtype=np.float64)
+        if u.shape != f.shape:
+            raise ValueError("stochastic rounding needs one uniform per expert")
+        up = u * m_tile < (f - lo)
+    else:
+        raise ValueError(rule)
+    up = up & (hi <= T)
     return np.where(up, hi, lo)
 
 
@@ -147,9 +175,10 @@ def route_tc(z: np.ndarray, K: int, m_tile: int = 128) -> dict:
     return _pack(T, E, K, idx, score, counts, counts.copy(), expert_rows, m_tile)
 
 
-def route_tr(z: np.ndarray, K: int, m_tile: int = 128) -> dict:
+def route_tr(z: np.ndarray, K: int, m_tile: int = 128, rule: str = "nearest", u=None) -> dict:
     """Token rounding [NOTE-TR]: token choice, then per expert an expert-choice ranking of all tokens with
-    token-choice tokens first, then keep the first r_e = round_and_sparsify(f_e) of that ranking."""
+    token-choice tokens first, then keep the first r_e = round_and_sparsify(f_e) of that ranking (under the
+    given rounding rule)."""
     z = np.asarray(z, dtype=np.float64)
     T, E = z.shape
     idx = topk_token_choice(z, K)
@@ -161,7 +190,7 @@ def route_tr(z: np.ndarray, K: int, m_tile: int = 128) -> dict:
         member[np.arange(T), idx[:, k]] = True
         slot_of[np.arange(T), idx[:, k]] = k
     f = member.sum(axis=0).astype(np.int64)
-    r = round_and_sparsify(f, m_tile, T)
+    r = round_and_sparsify(f, m_tile, T, rule, u)
     tok = np.arange(T)
     expert_rows = []
     for e in range(E):
@@ -175,11 +204,60 @@ def route_tr(z: np.ndarray, K: int, m_tile: int = 128) -> dict:
     return out
 
 
-def route(z: np.ndarray, K: int, mode: str = "tc", m_tile: int = 128) -> dict:
+def softmax_all(z: np.ndarray) -> np.ndarray:
+    """Per token: softmax over all E logits."""
+    z = np.asarray(z, dtype=np.float64)
+    ex = np.exp(z - z.max(axis=1, keepdims=True))
+    return ex / ex.sum(axis=1, keepdims=True)
+
+
+def ec_capacity(T: int, E: int, K: int) -> int:
+    """Tokens each expert takes under expert choice: the token-choice average T K / E, rounded down."""
+    return min(T, (T * K) // E)
+
+
+def route_ec(z: np.ndarray, K: int, m_tile: int = 128) -> dict:
+    """Expert choice: every expert takes the C tokens with the largest logits in its column (ties to the
+    lower token id); a pair's gate is the token's softmax over all E logits.  Token choice is still
+    computed (topk_idx, topk_score, tc_counts) and names the slot of a pair that token choice also picked."""
+    z = np.asarray(z, dtype=np.float64)
+    T, E = z.shape
+    idx = topk_token_choice(z, K)
+    score = gate_scores(z, idx)
+    prob = softmax_all(z)
+    slot_of = np.full((T, E), -1, dtype=np.int64)
+    for k in range(K):
+        slot_of[np.arange(T), idx[:, k]] = k
+    f = (slot_of >= 0).sum(axis=0).astype(np.int64)
+    C = ec_capacity(T, E, K)
+    tok = np.arange(T)
+    expert_rows = []
+    for e in range(E):
+        order = np.lexsort((tok, -z[:, e]))            # logit descending, then token ascending
+        kept = np.sort(order[:C])
+        expert_rows.append((kept, slot_of[kept, e], prob[kept, e]))
+    counts = np.full(E, C, dtype=np.int64)
+    return _pack(T, E, K, idx, score, counts, f, expert_rows, m_tile)
+
+
+# routing modes: token choice, token rounding under each rounding rule, expert choice
+ROUTE_MODES = ("tc", "tr", "tr_up", "tr_down", "tr_stoch", "ec")
+
+
+def route(z: np.ndarray, K: int, mode: str = "tc", m_tile: int = 128, u=None) -> dict:
+    """Routing metadata in one of ROUTE_MODES; `u` holds the per-expert uniforms of "tr_stoch"."""
     if mode == "tc":
         return route_tc(z, K, m_tile)
     if mode == "tr":
         return route_tr(z, K, m_tile)
+    if mode == "tr_up":
+        return route_tr(z, K, m_tile, "up")
+    if mode == "tr_down":
+        return route_tr(z, K, m_tile, "down")
+    if mode == "tr_stoch":
+        return route_tr(z, K, m_tile, "stochastic", u)
+    if mode == "ec":
+        return route_ec(z, K, m_tile)
     raise ValueError(mode)
 
 

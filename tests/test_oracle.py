@@ -61,17 +61,25 @@ def test_round_and_sparsify_table(f, M, T, r):
     assert int(orc.round_and_sparsify(np.array([f]), M, T)[0]) == r
 
 
-def _check_tr_invariants(z, K, M):
+def _check_tr_invariants(z, K, M, rule="nearest", u=None):
     tc = orc.route_tc(z, K, M)
-    tr = orc.route_tr(z, K, M)
+    tr = orc.route_tr(z, K, M, rule, u)
     T, E = z.shape
     z64 = z.astype(np.float64)
     f, r = tc["counts"], tr["counts"]
     assert np.array_equal(tr["tc_counts"], f)
     assert np.all(r % M == 0)
     hi = -((-f) // M) * M
-    near = hi <= T                                            # padding possible: nearest multiple
-    assert np.all(np.abs(r - f)[near] <= M // 2)              # never more than half a tile away
+    lo = (f // M) * M
+    near = hi <= T                                            # padding possible
+    if rule == "nearest":
+        assert np.all(np.abs(r - f)[near] <= M // 2)          # never more than half a tile away
+    elif rule == "up":
+        assert np.all(r[near] == hi[near])
+    elif rule == "down":
+        assert np.all(r == lo)
+    else:
+        assert np.all((r == lo) | (r == hi))
     assert np.all(np.abs(r - f) < M)                          # deviation within one tile
     for e in range(E):
         tc_set = tc["row_token"][tc["offsets"][e]:tc["offsets"][e + 1]]
@@ -117,13 +125,75 @@ def test_tr_invariants_random_seeds():
         _check_tr_invariants(z, K, M)
 
 
-def test_tr_bruteforce_tiny():
+@pytest.mark.parametrize("rule", orc.ROUNDING_RULES)
+def test_tr_rule_invariants_random_seeds(rule):
+    rng = np.random.default_rng(13)
+    for seed in range(25):
+        T = int(rng.integers(1, 500))
+        E = int(rng.integers(2, 16))
+        K = int(rng.integers(1, min(E, 5) + 1))
+        M = int(rng.choice([4, 16, 128]))
+        z = rng.standard_normal((T, E)).astype(np.float32)
+        if seed % 3 == 0:
+            z = np.round(z * 2) / 2                          # heavy ties
+        u = rng.random(E).astype(np.float32)
+        _check_tr_invariants(z, K, M, rule, u)
+
+
+@pytest.mark.parametrize("rule,f,M,T,u,r", [
+    ("up", 0, 128, 10**6, 0, 0), ("up", 1, 128, 10**6, 0, 128), ("up", 127, 128, 10**6, 0, 128),
+    ("up", 128, 128, 10**6, 0, 128), ("up", 129, 128, 10**6, 0, 256), ("up", 100, 128, 120, 0, 0),   # ceil > T
+    ("down", 0, 128, 10**6, 0, 0), ("down", 127, 128, 10**6, 0, 0), ("down", 128, 128, 10**6, 0, 128),
+    ("down", 255, 128, 10**6, 0, 128),
+    # stochastic: ceil iff u * M < f - floor; u = 0.5 pads when f - floor > 64, u = 0 whenever f is not a multiple
+    ("stochastic", 64, 128, 10**6, 0.5, 0), ("stochastic", 65, 128, 10**6, 0.5, 128), ("stochastic", 1, 128, 10**6, 0.0, 128),
+    ("stochastic", 128, 128, 10**6, 0.0, 128), ("stochastic", 127, 128, 10**6, 0.9921875, 0),  # 0.9921875*128 = 127
+    ("stochastic", 127, 128, 120, 0.0, 0), ("stochastic", 3, 4, 100, 0.74, 4), ("stochastic", 3, 4, 100, 0.75, 0),
+])
+def test_rounding_rules_table(rule, f, M, T, u, r):
+    got = orc.round_and_sparsify(np.array([f]), M, T, rule, np.array([u], dtype=np.float32))
+    assert int(got[0]) == r
+
+
+@pytest.mark.parametrize("M", [4, 16, 128])
+def test_stochastic_rounding_is_unbiased_over_a_uniform_grid(M):
+    """Closed form: with the uniforms u_i = (i + 1/2)/M, i = 0..M-1, exactly f - floor of them pad, so the mean
+    of the rounded count over the grid is f itself (the expected count equals the token-choice count)."""
+    grid = (np.arange(M) + 0.5) / M
+    for f in range(0, 3 * M + 1):
+        r = [int(orc.round_and_sparsify(np.array([f]), M, 10**6, "stochastic", np.array([u]))[0]) for u in grid]
+        assert sum(r) == f * M
+
+
+def test_ec_per_expert_top_c_is_stable_argsort_and_gate_is_softmax():
+    rng = np.random.default_rng(14)
+    for seed in range(20):
+        T, E, K = int(rng.integers(1, 300)), int(rng.integers(1, 12)), 1
+        K = int(rng.integers(1, E + 1))
+        z = rng.standard_normal((T, E)).astype(np.float32)
+        if seed % 3 == 0:
+            z = np.round(z * 2) / 2                          # heavy ties
+        rt = orc.route_ec(z, K, 16)
+        C = min(T, T * K // E)
+        assert np.all(rt["counts"] == C) and rt["P"] == E * C
+        prob = scipy.special.softmax(z.astype(np.float64), axis=1)
+        for e in range(E):
+            ref = np.sort(np.argsort(-z[:, e].astype(np.float64), kind="stable")[:C])
+            sl = slice(rt["offsets"][e], rt["offsets"][e + 1])
+            assert np.array_equal(rt["row_token"][sl], ref)
+            assert np.allclose(rt["row_score"][sl], prob[ref, e], rtol=1e-14, atol=0)
+            for t, k in zip(rt["row_token"][sl], rt["row_slot"][sl]):
+                assert (k == -1 and e not in rt["topk_idx"][t]) or rt["topk_idx"][t, k] == e
+
+
+@pytest.mark.parametrize("rule", orc.ROUNDING_RULES)
+def test_tr_bruteforce_tiny(rule):
     rng = np.random.default_rng(4)
-    for _ in range(60):
+    for _ in range(40):
         T, E, K, M = int(rng.integers(2, 11)), 3, int(rng.integers(1, 3)), 4
         z = rng.choice([-1.0, -0.5, 0.0, 0.25, 0.5, 1.0], size=(T, E)).astype(np.float32)
         tc = orc.route_tc(z, K, M)
-        tr = orc.route_tr(z, K, M)
+        tr = orc.route_tr(z, K, M, rule, rng.random(E))
         member = np.zeros((T, E), bool)
         for t in range(T):
             member[t, tc["topk_idx"][t]] = True
@@ -156,12 +226,14 @@ def test_tr_expected_total_unchanged():
     assert abs(diffs.mean()) / (T * K) < 0.01
 
 
-@pytest.mark.parametrize("fixture", ["tr_pad_and_drop.txt", "tr_tie_rounds_down.txt"])
+@pytest.mark.parametrize("fixture", ["tr_pad_and_drop.txt", "tr_tie_rounds_down.txt", "tr_rules_and_ec.txt"])
 def test_routing_golden(fixture):
     g = load_golden(fixture)
     z = np.array(g["logits"], dtype=np.float32)
     for mode, exp in g["expect"].items():
-        rt = orc.route(z, g["K"], mode, g["m_tile"])
+        exp = dict(exp)
+        u = np.array(exp.pop("u"), dtype=np.float32) if "u" in exp else None
+        rt = orc.route(z, g["K"], mode, g["m_tile"], u=u)
         for key, val in exp.items():
             got = rt[key]
             if key in ("row_score", "topk_score"):
