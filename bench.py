@@ -48,7 +48,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="fine7b", choices=list(synth.WORKLOADS))
-    p.add_argument("--mode", default="tc", choices=["tc", "tr"])
+    p.add_argument("--mode", default="tc", choices=["tc", "tr", "tr_up", "tr_down", "tr_stoch", "ec"])
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle baseline sample")
     p.add_argument("--no-extras", action="store_true", help="skip the TR-vs-TC and e2e side measurements")
     p.add_argument("--ingest-ncu", metavar="CSV", help="record per-launch DRAM bytes from an ncu --csv log "
@@ -176,7 +176,7 @@ def cpu_threads():
 def prepare_oracle_inputs(w, inp, mode):
     from oracle import moe_oracle as orc
 
-    ref = orc.route(inp["logits"].numpy(), w.K, mode)
+    ref = orc.route(inp["logits"].numpy(), w.K, mode, u=synth.make_uniforms(w.E, 0).numpy())
     ref_inp = {"X_64": inp["X"].double().numpy(), "dO_64": inp["dO"].double().numpy(),
                "W1_64": inp["W1"].double().numpy(), "W2_64": inp["W2"].double().numpy()}
     return ref, ref_inp
@@ -246,6 +246,7 @@ class Layer:
 
         self.moe, self.w, self.mode = moe, w, mode
         self.g = {k: v.to(dev) for k, v in inp.items()}
+        self.u = synth.make_uniforms(w.E, 0).to(dev)  # per-expert draws of stochastic rounding
         self.rt = moe.Routing(w.T, w.E, w.K, mode, dev)
         p = self.rt.p_cap
         bf = torch.bfloat16
@@ -260,7 +261,7 @@ class Layer:
                                device=dev)
 
     def route(self):
-        self.moe.moe_route(self.g["logits"], self.w.K, self.mode, routing=self.rt)
+        self.moe.moe_route(self.g["logits"], self.w.K, self.mode, routing=self.rt, uniforms=self.u)
 
     def forward(self):
         self.moe.moe_forward(self.g["X"], self.g["W1"], self.g["W2"], self.rt, O=self.O, H=self.H, ws=self.wsf)
@@ -596,11 +597,12 @@ def e2e_measure(layer, inp, args, world, dev):
 
 
 def tr_vs_tc(args, dev):
-    """Token rounding vs token choice on the high-sparsity layer (T=16384, d=1536, n=256, E=256, K=4)."""
+    """Token rounding (under each rounding rule) and expert choice vs token choice on the high-sparsity layer
+    (T=16384, d=1536, n=256, E=256, K=4)."""
     w = synth.WORKLOADS["sparse"]
     inp = synth.make_inputs(w, seed=0)
     out = {}
-    for mode in ("tc", "tr"):
+    for mode in ("tc", "tr", "tr_up", "tr_down", "tr_stoch", "ec"):
         layer = Layer(w, inp, mode, dev)
         for _ in range(3):
             layer.step()
@@ -619,6 +621,8 @@ def tr_vs_tc(args, dev):
         del layer
         torch.cuda.empty_cache()
     out["speedup_tr_over_tc"] = out["tc"]["ms_per_step"] / out["tr"]["ms_per_step"]
+    out["speedup_over_tc"] = {m: out["tc"]["ms_per_step"] / out[m]["ms_per_step"]
+                              for m in ("tr", "tr_up", "tr_down", "tr_stoch", "ec")}
     out["workload"] = f"sparse: T={w.T}, d={w.d}, n={w.n}, E={w.E}, K={w.K}"
     return out
 

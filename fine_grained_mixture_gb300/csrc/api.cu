@@ -220,9 +220,9 @@ static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 
 static int check_route_shape(int T, int E, int K, int mode) {
   if (T <= 0 || E <= 0 || K <= 0 || K > E) return MOE_ERR_INVALID_ARG;
-  if (mode != MOE_ROUTE_TC && mode != MOE_ROUTE_TR) return MOE_ERR_INVALID_ARG;
+  if (mode < MOE_ROUTE_TC || mode > MOE_ROUTE_EC) return MOE_ERR_INVALID_ARG;
   if (E > kMaxExperts || K > kMaxTopK) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if (mode == MOE_ROUTE_TR && T > kMaxTrTokens) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (route_selects(mode) && T > kMaxTrTokens) return MOE_ERR_UNSUPPORTED_SHAPE;
   if ((int64_t)T * K > (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED_SHAPE;
   return MOE_OK;
 }
@@ -277,16 +277,17 @@ static GemmArgs base_args(const moe_routing *r, int T, int d, int n, int E, size
   return a;
 }
 
-int route_call(const float *logits, int T, int E, int K, int mode, const moe_routing *r, void *ws, size_t ws_bytes,
-               int32_t *P_host, void *stream, bool em_keys) {
+int route_call(const float *logits, const float *uniforms, int T, int E, int K, int mode, const moe_routing *r,
+               void *ws, size_t ws_bytes, int32_t *P_host, void *stream, bool em_keys) {
   int rc = check_route_shape(T, E, K, mode);
   if (rc != MOE_OK) return rc;
   if (!logits || !routing_ok(r)) return MOE_ERR_INVALID_ARG;
+  if (mode == MOE_ROUTE_TR_STOCHASTIC && !uniforms) return MOE_ERR_INVALID_ARG;
   if (!ws || ws_bytes < route_workspace_bytes(T, E, K, mode, em_keys)) return MOE_ERR_WORKSPACE;
   rc = check_device();
   if (rc != MOE_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  rc = launch_route(logits, T, E, K, mode, r, ws, s, em_keys);
+  rc = launch_route(logits, uniforms, T, E, K, mode, r, ws, s, em_keys);
   if (rc != MOE_OK) return rc;
   if (P_host) {
     cudaError_t err = cudaMemcpyAsync(P_host, r->status + 1, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
@@ -306,7 +307,12 @@ int moe_route_capacity(int T, int E, int K, int mode, size_t *p_cap) {
   if (!p_cap) return MOE_ERR_INVALID_ARG;
   const int rc = check_route_shape(T, E, K, mode);
   if (rc != MOE_OK) return rc;
-  *p_cap = (size_t)T * K + (mode == MOE_ROUTE_TR ? (size_t)E * (MOE_M_TILE / 2) : 0);
+  // padding adds fewer than M_tile/2 rows per expert under the nearest rule, fewer than M_tile under up and
+  // stochastic rounding; token choice, rounding down and expert choice (E * floor(T*K/E) rows) stay within T*K
+  size_t pad = 0;
+  if (mode == MOE_ROUTE_TR) pad = (size_t)E * (MOE_M_TILE / 2);
+  if (mode == MOE_ROUTE_TR_UP || mode == MOE_ROUTE_TR_STOCHASTIC) pad = (size_t)E * (MOE_M_TILE - 1);
+  *p_cap = (size_t)T * K + pad;
   return MOE_OK;
 }
 
@@ -320,7 +326,12 @@ int moe_route_workspace_size(int T, int E, int K, int mode, size_t *bytes) {
 
 int moe_route(const float *logits, int T, int E, int K, int mode, const moe_routing *r, void *ws, size_t ws_bytes,
               int32_t *P_host, void *stream) {
-  return moe::route_call(logits, T, E, K, mode, r, ws, ws_bytes, P_host, stream, true);
+  return moe::route_call(logits, nullptr, T, E, K, mode, r, ws, ws_bytes, P_host, stream, true);
+}
+
+int moe_route_ex(const float *logits, const float *uniforms, int T, int E, int K, int mode, const moe_routing *r,
+                 void *ws, size_t ws_bytes, int32_t *P_host, void *stream) {
+  return moe::route_call(logits, uniforms, T, E, K, mode, r, ws, ws_bytes, P_host, stream, true);
 }
 
 

@@ -42,15 +42,18 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 // routing (route.cu)
-// Routing scratch.  em_keys: token rounding keeps an expert-major copy of the logit order keys (4*T*E bytes)
-// so that its per-expert selection reads them coalesced; without it the selection reads the logits in place.
+// Every mode but token choice selects each expert's rows from a per-expert ranking of all tokens.
+inline bool route_selects(int mode) { return mode != MOE_ROUTE_TC; }
+// Routing scratch.  em_keys: the selection modes keep an expert-major copy of the logit order keys (4*T*E bytes)
+// so that the per-expert selection reads them coalesced; without it the selection reads the logits in place.
 size_t route_workspace_bytes(int T, int E, int K, int mode, bool em_keys = true);
-int launch_route(const float *logits, int T, int E, int K, int mode, const moe_routing *r, void *ws,
-                 cudaStream_t stream, bool em_keys = true);
-// moe_route with the scratch layout chosen by the caller (moe_route_noalloc drops the expert-major keys when
+// uniforms: per-expert draws of stochastic rounding (device fp32 [E]); unused by the other modes.
+int launch_route(const float *logits, const float *uniforms, int T, int E, int K, int mode, const moe_routing *r,
+                 void *ws, cudaStream_t stream, bool em_keys = true);
+// moe_route_ex with the scratch layout chosen by the caller (moe_route_noalloc drops the expert-major keys when
 // they would not fit its static array).
-int route_call(const float *logits, int T, int E, int K, int mode, const moe_routing *r, void *ws, size_t ws_bytes,
-               int32_t *P_host, void *stream, bool em_keys);
+int route_call(const float *logits, const float *uniforms, int T, int E, int K, int mode, const moe_routing *r,
+               void *ws, size_t ws_bytes, int32_t *P_host, void *stream, bool em_keys);
 
 // grouped GEMMs (gemm_fwd.cu, gemm_bwd.cu)
 struct GemmArgs {

@@ -7,16 +7,23 @@
 // expert with expert-choice tokens when the distance up to the next multiple of M_tile is strictly
 // smaller than the distance down, and drops its weakest token-choice tokens otherwise.
 //
+// The rounding subroutine is a free choice ("Loss function / training strategy": token rounding is robust to
+// it): nearest (the default above), always up, always down, or stochastic (up with probability
+// (f - floor)/M_tile, from one caller-drawn uniform per expert).  Expert choice (the "EC" rows of the ablation
+// table) reuses the same per-expert selection: every token is a candidate and each expert keeps C of them.
+//
 // Pipeline (one stream, no host synchronisation):
 //   route_topk_kernel   one warp per token (32 tokens per CTA): top-K by (logit desc, expert asc), softmax over the K,
-//                       the CTA's expert histogram; TR only: the CTA's word of the membership bitmap and its 32
-//                       columns of the expert-major key matrix, both written whole (no zero fill needed)
-//   route_scan_kernel   one CTA per expert: per-chunk (256 tokens) bases, counts (TC f_e or TR r_e)
+//                       the CTA's expert histogram; selection modes (all but TC): the CTA's word of the membership
+//                       bitmap and its 32 columns of the expert-major key matrix, both written whole (no zero fill)
+//   route_scan_kernel   one CTA per expert: per-chunk (256 tokens) bases, counts (f_e, rounded r_e, or C)
 //   route_fill_tc       one CTA per 256-token chunk: rows in ascending token order via bitmap ranks
 //   route_fill_tr       one CTA per expert: radix selection of the kept set, rows in token order
 //                       (each fill CTA scans the E counts into offsets; CTA 0 publishes them)
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "internal.h"
@@ -48,7 +55,7 @@ constexpr int kKeyStride = 33;  // words per expert row of the TR key tile (odd:
 // Dynamic shared memory of route_topk_kernel: the CTA histogram, plus for TR the membership words and the
 // [E][32] key tile.
 size_t route_topk_smem_bytes(int E, int mode) {
-  return (size_t)E * 4 + (mode == MOE_ROUTE_TR ? (size_t)E * 4 + (size_t)E * kKeyStride * 4 : 0);
+  return (size_t)E * 4 + (route_selects(mode) ? (size_t)E * 4 + (size_t)E * kKeyStride * 4 : 0);
 }
 
 template <int NV, bool TR>  // NV = logits held per lane = ceil(E / 32)
@@ -57,7 +64,9 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float *_
                                                          float *__restrict__ topk_score, float *__restrict__ tok_max,
                                                          float *__restrict__ tok_den, int32_t *__restrict__ cta_hist,
                                                          uint32_t *__restrict__ member, int member_words,
-                                                         uint32_t *__restrict__ keys_em, int32_t *__restrict__ status) {
+                                                         uint32_t *__restrict__ keys_em, int32_t *__restrict__ status,
+                                                         int den_all) {
+  // den_all (expert choice): tok_den holds the softmax denominator over all E logits instead of the K selected
   extern __shared__ int32_t hist[];                                      // [E]
   uint32_t *mbits = reinterpret_cast<uint32_t *>(hist + E);             // [E]     TR: bit i = token t_first + i chose e
   uint32_t *ktile = mbits + E;                                           // [E][33] TR: order keys of the 32 tokens
@@ -187,6 +196,15 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float *_
     const float w = (lane < K) ? expf(my_z - z0) : 0.f;
     float den = 0.f;
     for (int k = 0; k < K; ++k) den += __shfl_sync(0xffffffffu, w, k);
+    // expert choice: sum over all E of exp(z - z0), accumulated in fp64 so that up to 1024 terms round once
+    double den_e = 0.0;
+    if (den_all) {
+#pragma unroll
+      for (int j = 0; j < NV; ++j)
+        if (lane + 32 * j < E) den_e += static_cast<double>(expf(v[j] - z0));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) den_e += __shfl_xor_sync(0xffffffffu, den_e, off);
+    }
     if (lane < K) {
       topk_idx[(size_t)t * K + lane] = my_e;
       topk_score[(size_t)t * K + lane] = w / den;
@@ -195,7 +213,7 @@ __global__ void __launch_bounds__(kTopkThreads) route_topk_kernel(const float *_
     }
     if (lane == 0) {
       tok_max[t] = z0;
-      tok_den[t] = den;
+      tok_den[t] = den_all ? static_cast<float>(den_e) : den;
     }
   }
   __syncthreads();
@@ -288,6 +306,7 @@ __device__ void publish_offsets(int E, const int *s_off, const int *s_toff, int3
 // rounding).  Thread i takes a contiguous run of chunks.
 constexpr int kScanThreads = 256;
 __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(int T, int E, int nctas, int mode, int m_tile,
+                                                                  const float *__restrict__ uniforms, int ec_cap,
                                                                   const int32_t *__restrict__ cta_hist,
                                                                   int32_t *__restrict__ chunk_base,
                                                                   int32_t *__restrict__ tc_counts,
@@ -318,10 +337,17 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(int T, int E, 
   }
   if (threadIdx.x == 0) {
     int cnt = f;
-    if (mode == MOE_ROUTE_TR) {
+    if (mode == MOE_ROUTE_EC) {
+      cnt = ec_cap;
+    } else if (mode != MOE_ROUTE_TC) {
       const int lo = (f / m_tile) * m_tile;
       const int hi = ((f + m_tile - 1) / m_tile) * m_tile;
-      cnt = ((hi - f) < (f - lo) && hi <= T) ? hi : lo;
+      bool up;
+      if (mode == MOE_ROUTE_TR) up = (hi - f) < (f - lo);  // nearest; a tie takes the floor
+      else if (mode == MOE_ROUTE_TR_UP) up = hi > f;
+      else if (mode == MOE_ROUTE_TR_DOWN) up = false;
+      else up = uniforms[e] * static_cast<float>(m_tile) < static_cast<float>(f - lo);  // both sides exact in fp32
+      cnt = (up && hi <= T) ? hi : lo;  // no padding beyond the T tokens there are
     }
     tc_counts[e] = f;
     counts[e] = cnt;
@@ -396,7 +422,9 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
     const uint32_t *__restrict__ member, int member_words, int m_tile, const int32_t *__restrict__ tc_counts,
     const int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ tile_offsets,
     int32_t *__restrict__ status, int32_t *__restrict__ row_token, int32_t *__restrict__ row_slot,
-    float *__restrict__ row_score, int list_cap) {
+    float *__restrict__ row_score, int list_cap, int ec) {
+  // ec (expert choice): every token is a candidate (as if all had chosen the expert) and a row's gate is the
+  // token's softmax over all E logits (tok_den holds that denominator)
   extern __shared__ uint32_t sm[];
   uint32_t *key = sm;                                       // [T]
   uint32_t *mem = sm + T;                                   // [member_words]
@@ -414,7 +442,7 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
   const int e = blockIdx.x;
   expert_offsets(counts, E, m_tile, s_off, s_toff, scratch);
   publish_offsets(E, s_off, s_toff, offsets, tile_offsets, status);
-  const int f = tc_counts[e], r = counts[e], base = s_off[e];
+  const int f = ec ? T : tc_counts[e], r = counts[e], base = s_off[e];
   if (r == 0) return;
   for (int w = threadIdx.x; w < member_words; w += blockDim.x) mem[w] = member[(size_t)e * member_words + w];
   if (keys_em) {
@@ -446,11 +474,13 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
     return list_n <= list_cap ? list_n : -1;
   };
   auto is_tc = [&](int t) { return ((mem[t >> 5] >> (t & 31)) & 1u) != 0u; };
+  auto first = [&](int t) { return ec || is_tc(t); };  // ranked ahead of the other tokens
   if (r != f) {
     // Candidates are few next to T: the expert's token-choice tokens when dropping, and when padding the
     // other tokens in the top-byte bin of the boundary.  Once they are listed, the remaining radix passes
-    // walk the list instead of all T tokens (all T when the list would overflow its space).
-    int nlist = drop ? build_list(is_tc) : -1;
+    // walk the list instead of all T tokens (all T when the list would overflow its space, or under expert
+    // choice, where every token is a candidate).
+    int nlist = (drop && !ec) ? build_list(is_tc) : -1;
     int *my_hist = hist + (warp >> 2) * 256;
     for (int shift = 24; shift >= 0; shift -= 8) {
       for (int i = threadIdx.x; i < kTrHists * 256; i += blockDim.x) hist[i] = 0;
@@ -463,7 +493,7 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
         if (i < n_iter) {
           const int t = nlist >= 0 ? list[i] : i;
           const uint32_t k = key[t];
-          if ((nlist >= 0 || is_tc(t) == drop) && (k & mask) == prefix) bin = (k >> shift) & 255u;
+          if ((nlist >= 0 || first(t) == drop) && (k & mask) == prefix) bin = (k >> shift) & 255u;
         }
         const uint32_t same = __match_any_sync(0xffffffffu, bin);
         if (bin < 256u && lane == __ffs(same) - 1) atomicAdd(&my_hist[bin], __popc(same));
@@ -502,7 +532,7 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
       remaining = sel_state[1];
       if (!drop && shift == 24) {
         const uint32_t top = prefix;
-        nlist = build_list([&](int t) { return !is_tc(t) && (key[t] & 0xff000000u) == top; });
+        nlist = build_list([&](int t) { return !first(t) && (key[t] & 0xff000000u) == top; });
       }
     }
   }
@@ -516,10 +546,7 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
     for (int t0 = t_lo; t0 < t_lo + span && t0 < T; t0 += 32) {
       const int t = t0 + lane;
       bool eq = false;
-      if (t < T) {
-        const bool tc = (mem[t >> 5] >> (t & 31)) & 1u;
-        eq = (tc == drop) && key[t] == prefix;
-      }
+      if (t < T) eq = (first(t) == drop) && key[t] == prefix;
       eq_count += __popc(__ballot_sync(0xffffffffu, eq));
     }
   }
@@ -538,7 +565,7 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
     const int t = t0 + lane;
     bool tc = false, gt = false, eq = false;
     if (t < T) {
-      tc = (mem[t >> 5] >> (t & 31)) & 1u;
+      tc = first(t);
       if (r != f && tc == drop) {
         const uint32_t k = key[t];
         gt = k > prefix;
@@ -580,8 +607,8 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
         for (int k = 0; k < K; ++k)
           if (topk_idx[(size_t)t * K + k] == e) slot = k;
       }
-      const float sc = slot >= 0 ? topk_score[(size_t)t * K + slot]
-                                 : expf(key_to_float(key[t]) - tok_max[t]) / tok_den[t];
+      const float sc = (slot >= 0 && !ec) ? topk_score[(size_t)t * K + slot]
+                                          : expf(key_to_float(key[t]) - tok_max[t]) / tok_den[t];
       row_token[pos] = t;
       row_slot[pos] = slot;
       row_score[pos] = sc;
@@ -608,7 +635,7 @@ size_t route_workspace_bytes(int T, int E, int K, int mode, bool em_keys) {
   const size_t nchunks = (T + kChunk - 1) / kChunk;
   const size_t words = (T + 31) / 32;
   size_t b = align256(nctas * E * 4) + align256(nchunks * E * 4);
-  if (mode == MOE_ROUTE_TR) b += align256(words * E * 4) + (em_keys ? align256((size_t)T * E * 4) : 0);
+  if (route_selects(mode)) b += align256(words * E * 4) + (em_keys ? align256((size_t)T * E * 4) : 0);
   b += align256((size_t)T * 4) * 2;
   return b;
 }
@@ -623,7 +650,7 @@ static RouteWs carve(void *ws, int T, int E, int mode, bool em_keys) {
   p += align256((size_t)w.nctas * E * 4);
   w.chunk_base = reinterpret_cast<int32_t *>(p);
   p += align256((size_t)w.nchunks * E * 4);
-  if (mode == MOE_ROUTE_TR) {
+  if (route_selects(mode)) {
     w.member = reinterpret_cast<uint32_t *>(p);
     p += align256((size_t)w.member_words * E * 4);
     if (em_keys) {
@@ -650,12 +677,13 @@ static int route_tr_list_cap(int T) {
   return static_cast<int>(room < 4096 ? room : 4096);
 }
 
-int launch_route(const float *logits, int T, int E, int K, int mode, const moe_routing *r, void *ws,
-                 cudaStream_t stream, bool em_keys) {
+int launch_route(const float *logits, const float *uniforms, int T, int E, int K, int mode, const moe_routing *r,
+                 void *ws, cudaStream_t stream, bool em_keys) {
   RouteWs w = carve(ws, T, E, mode, em_keys);
   cudaError_t err = cudaMemsetAsync(r->status, 0, MOE_STATUS_WORDS * sizeof(int32_t), stream);
   if (err != cudaSuccess) return record_cuda_error(err);
-  const bool tr = mode == MOE_ROUTE_TR;
+  const bool tr = route_selects(mode);
+  const int den_all = mode == MOE_ROUTE_EC ? 1 : 0;
   const size_t topk_smem = route_topk_smem_bytes(E, mode);
   const int nv = (E + 31) / 32;
   // the key tile of E = 1024 needs more than the default 48 KB of dynamic shared memory
@@ -684,7 +712,7 @@ int launch_route(const float *logits, int T, int E, int K, int mode, const moe_r
     auto kern = tr ? MOE_TOPK_KERNEL(NV, true) : MOE_TOPK_KERNEL(NV, false);                                      \
     kern<<<w.nctas, kTopkThreads, topk_smem, stream>>>(logits, T, E, K, r->topk_idx, r->topk_score, w.tok_max,    \
                                                        w.tok_den, w.cta_hist, w.member, w.member_words, w.keys_em, \
-                                                       r->status);                                                \
+                                                       r->status, den_all);                                       \
   } while (0)
   prof_begin("route_topk", stream);
   if (nv <= 1) MOE_TOPK_LAUNCH(1);
@@ -698,8 +726,9 @@ int launch_route(const float *logits, int T, int E, int K, int mode, const moe_r
   prof_end(stream);
   count_launch();
   prof_begin("route_scan", stream);
+  const int ec_cap = static_cast<int>(std::min<int64_t>(T, (int64_t)T * K / E));
   err = launch_pdl(route_scan_kernel, dim3(E), dim3(kScanThreads), 0, stream, T, E, w.nctas, mode, MOE_M_TILE,
-                   w.cta_hist, w.chunk_base, r->tc_counts, r->counts);
+                   uniforms, ec_cap, w.cta_hist, w.chunk_base, r->tc_counts, r->counts);
   if (err != cudaSuccess) return record_cuda_error(err);
   prof_end(stream);
   count_launch();
@@ -716,7 +745,8 @@ int launch_route(const float *logits, int T, int E, int K, int mode, const moe_r
     err = launch_pdl(route_fill_tr_kernel, dim3(E), dim3(kTrThreads), smem, stream, w.keys_em, logits, T, E, K,
                      r->topk_idx,
                      r->topk_score, w.tok_max, w.tok_den, w.member, w.member_words, MOE_M_TILE, r->tc_counts, r->counts,
-                     r->offsets, r->tile_offsets, r->status, r->row_token, r->row_slot, r->row_score, list_cap);
+                     r->offsets, r->tile_offsets, r->status, r->row_token, r->row_slot, r->row_score, list_cap,
+                     den_all);
     if (err != cudaSuccess) return record_cuda_error(err);
   }
   prof_end(stream);

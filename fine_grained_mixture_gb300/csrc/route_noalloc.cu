@@ -60,5 +60,5 @@ extern "C" int moe_route_noalloc(const float *logits, int T, int E, int K, int m
   if (rc != MOE_OK) return rc;
   // Same kernels and validation as moe_route; the scratch is the library's own array instead of the
   // caller's workspace.  Every per-call scratch word is rewritten before it is read.
-  return moe::route_call(logits, T, E, K, mode, r, scratch, need, P_host, stream, em_keys);
+  return moe::route_call(logits, nullptr, T, E, K, mode, r, scratch, need, P_host, stream, em_keys);
 }

@@ -15,9 +15,15 @@ from . import build as _build
 
 MOE_ROUTE_TC = 0
 MOE_ROUTE_TR = 1
+MOE_ROUTE_TR_UP = 2
+MOE_ROUTE_TR_DOWN = 3
+MOE_ROUTE_TR_STOCHASTIC = 4
+MOE_ROUTE_EC = 5
 M_TILE = 128
 STATUS_WORDS = 4
-MODES = {"tc": MOE_ROUTE_TC, "tr": MOE_ROUTE_TR}
+# token choice; token rounding to the nearest tile, always up, always down, stochastically; expert choice
+MODES = {"tc": MOE_ROUTE_TC, "tr": MOE_ROUTE_TR, "tr_up": MOE_ROUTE_TR_UP, "tr_down": MOE_ROUTE_TR_DOWN,
+         "tr_stoch": MOE_ROUTE_TR_STOCHASTIC, "ec": MOE_ROUTE_EC}
 
 ERRORS = {
     0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_WORKSPACE",
@@ -58,6 +64,8 @@ def library() -> ctypes.CDLL:
     lib.moe_route_workspace_size.argtypes = [_c_int, _c_int, _c_int, _c_int, sz]
     lib.moe_route.argtypes = [_vp, _c_int, _c_int, _c_int, _c_int, ctypes.POINTER(moe_routing), _vp, _c_size,
                               ctypes.POINTER(ctypes.c_int32), _vp]
+    lib.moe_route_ex.argtypes = [_vp, _vp, _c_int, _c_int, _c_int, _c_int, ctypes.POINTER(moe_routing), _vp, _c_size,
+                                 ctypes.POINTER(ctypes.c_int32), _vp]
     lib.moe_forward_workspace_size.argtypes = [_c_int] * 5 + [_c_size, sz]
     lib.moe_forward.argtypes = [_vp, _vp, _vp, ctypes.POINTER(moe_routing)] + [_c_int] * 5 + [_c_size, _vp, _vp, _vp,
                                                                                               _c_size, _vp]
@@ -79,7 +87,7 @@ def library() -> ctypes.CDLL:
                                       ctypes.POINTER(ctypes.c_double)]
     for f in ("moe_profile_enable", "moe_profile_count", "moe_profile_entry"):
         getattr(lib, f).restype = _c_int
-    for f in ("moe_route_capacity", "moe_route_workspace_size", "moe_route", "moe_forward_workspace_size",
+    for f in ("moe_route_capacity", "moe_route_workspace_size", "moe_route", "moe_route_ex", "moe_forward_workspace_size",
               "moe_forward", "moe_backward_workspace_size", "moe_backward", "moe_get_status", "moe_last_cuda_error"):
         getattr(lib, f).restype = _c_int
     _LIB = lib
@@ -176,16 +184,21 @@ class Routing:
         return code.value, P.value
 
 
-def moe_route(logits: torch.Tensor, K: int, mode="tc", routing: Routing | None = None, want_P=False, stream=None):
-    """Routing metadata for fp32 logits [T, E]; returns the Routing (and P when want_P)."""
+def moe_route(logits: torch.Tensor, K: int, mode="tc", routing: Routing | None = None, want_P=False, stream=None,
+              uniforms: torch.Tensor | None = None):
+    """Routing metadata for fp32 logits [T, E]; returns the Routing (and P when want_P).
+
+    uniforms: fp32 [E] draws in [0, 1) for stochastic rounding ("tr_stoch"); other modes ignore them."""
     T, E = logits.shape
     _need(logits, "logits", torch.float32)
     if routing is None:
         routing = Routing(T, E, K, mode, logits.device)
+    if uniforms is not None:
+        _need(uniforms, "uniforms", torch.float32, E)
     P = ctypes.c_int32(0)
-    _check(library().moe_route(_ptr(logits), T, E, K, routing.mode, ctypes.byref(routing.struct),
-                               _ptr(routing.ws), routing.ws.numel(), ctypes.byref(P) if want_P else None,
-                               _stream(stream)), "moe_route")
+    _check(library().moe_route_ex(_ptr(logits), _ptr(uniforms), T, E, K, routing.mode, ctypes.byref(routing.struct),
+                                  _ptr(routing.ws), routing.ws.numel(), ctypes.byref(P) if want_P else None,
+                                  _stream(stream)), "moe_route_ex")
     return (routing, P.value) if want_P else routing
 
 

@@ -14,6 +14,9 @@ Recipe (per workload, one ``torch.Generator('cpu')`` seeded with ``seed``), draw
 * ``W2`` [E, n, d] ~ N(0, 1/n), drawn one expert at a time, bf16;
 * ``dO`` [T, d] ~ N(0, 1), bf16.
 
+Stochastic rounding draws one uniform per expert; ``make_uniforms`` takes them from a generator of their own
+(seeded with ``seed + 0x5EED``) so the tensors above are the same whichever routing mode is run.
+
 The workloads are the layer shapes SonicMoE is evaluated on in spirit (a fine-grained 7B-class layer,
 a coarser layer, a high-sparsity layer and a skewed-load layer); the pages list no public dataset,
 so these seeded draws stand in for real activations.
@@ -88,3 +91,10 @@ def make_logits_only(w: Workload, seed: int = 0) -> torch.Tensor:
     gen = torch.Generator(device="cpu")
     gen.manual_seed(seed)
     return make_logits(w, gen)
+
+
+def make_uniforms(E: int, seed: int = 0) -> torch.Tensor:
+    """Per-expert uniforms in [0, 1) for stochastic rounding (fp32, host)."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed + 0x5EED)
+    return torch.rand((E,), generator=gen, dtype=torch.float32)

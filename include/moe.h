@@ -36,7 +36,7 @@ typedef uint16_t moe_bf16;
 
 enum moe_status_code {
   MOE_OK = 0,
-  MOE_ERR_INVALID_ARG = 1,        /* null pointer, T/E/K <= 0, K > E, unknown mode                       */
+  MOE_ERR_INVALID_ARG = 1,        /* null pointer, T/E/K <= 0, K > E, unknown mode, missing uniforms     */
   MOE_ERR_UNSUPPORTED_SHAPE = 2,  /* shape outside the limits above                                     */
   MOE_ERR_WORKSPACE = 3,          /* workspace pointer null or smaller than the *_workspace_size query  */
   MOE_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed (moe_last_cuda_error() has it)   */
@@ -46,9 +46,23 @@ enum moe_status_code {
   MOE_ERR_DEVICE = 8              /* current device is not compute capability 10.3 (GB300)              */
 };
 
+/*
+ * Routing modes.  Token rounding ("Key design 1") rounds each expert's token-choice count f_e to a multiple of
+ * M_tile and then keeps token-choice tokens ahead of expert-choice candidates; the rounding subroutine is a
+ * choice the method is robust to ("Loss function / training strategy"), so every rule below is offered.  A
+ * rounding that would need more than T tokens takes the floor under every rule.  Expert choice is the "EC"
+ * baseline of the ablation table.
+ */
 enum moe_route_mode {
-  MOE_ROUTE_TC = 0,  /* token choice: each token's top-K experts                                   */
-  MOE_ROUTE_TR = 1   /* token rounding: token choice, then each expert's count rounded to M_tile   */
+  MOE_ROUTE_TC = 0,               /* token choice: each token's top-K experts                                 */
+  MOE_ROUTE_TR = 1,               /* token rounding, nearest multiple (ceil only when strictly closer)        */
+  MOE_ROUTE_TR_UP = 2,            /* token rounding, always the ceiling                                       */
+  MOE_ROUTE_TR_DOWN = 3,          /* token rounding, always the floor                                         */
+  MOE_ROUTE_TR_STOCHASTIC = 4,    /* token rounding, ceiling iff u_e * M_tile < f_e - floor (u_e per expert,  */
+                                  /* uniform in [0,1), passed to moe_route_ex): expected count f_e            */
+  MOE_ROUTE_EC = 5                /* expert choice: each expert's C = min(T, floor(T*K/E)) tokens with the    */
+                                  /* largest logits (ties to the lower token id); gate = the token's softmax  */
+                                  /* over all E logits                                                        */
 };
 
 #define MOE_M_TILE 128
@@ -59,14 +73,14 @@ enum moe_route_mode {
  *   topk_idx   int32 [T*K]   token t's k-th expert, best first (logit descending, expert ascending on ties)
  *   topk_score fp32  [T*K]   softmax over the token's K selected logits
  *   tc_counts  int32 [E]     token-choice count f_e of each expert
- *   counts     int32 [E]     rows per expert (TC: f_e; TR: r_e = round_and_sparsify(f_e))
+ *   counts     int32 [E]     rows per expert (TC: f_e; TR modes: r_e = f_e rounded to M_tile; EC: C)
  *   offsets    int32 [E+1]   exclusive prefix sum of counts; offsets[E] = P (rows of expert e are
  *                            [offsets[e], offsets[e+1]), ordered by ascending token id)
  *   tile_offsets int32 [E+1] exclusive prefix sum of ceil(counts/M_tile) (the grouped-GEMM schedule)
  *   row_token  int32 [P_cap] token of each row
  *   row_slot   int32 [P_cap] k with topk_idx[token*K+k] == expert, or -1 for a pair added by rounding
  *   row_score  fp32  [P_cap] the row's gate score s_r (a pair added by rounding uses its token's
- *                            token-choice softmax normaliser)
+ *                            token-choice softmax normaliser; EC: softmax over all E logits)
  *   status     int32 [MOE_STATUS_WORDS]  [0] device error code, [1] P, [2] total M-tiles, [3] reserved
  * Rows at and beyond P are left untouched.
  */
@@ -83,24 +97,37 @@ typedef struct moe_routing {
   int32_t *status;
 } moe_routing;
 
-/* Upper bound on P: T*K for TC; T*K + E*M_tile/2 for TR (rounding pads an expert by < M_tile/2 rows). */
+/* Upper bound on P: T*K for TC, TR_DOWN and EC; T*K + E*M_tile/2 for TR (the nearest rule pads an expert by
+ * less than M_tile/2 rows); T*K + E*(M_tile-1) for TR_UP and TR_STOCHASTIC. */
 int moe_route_capacity(int T, int E, int K, int mode, size_t *p_cap);
 
-/* Bytes of scratch moe_route needs (per-CTA and per-chunk expert histograms, per-token normalisers; token
- * rounding adds the membership bitmap and an expert-major copy of the logit order keys, 4*T*E bytes). */
+/* Bytes of scratch moe_route needs (per-CTA and per-chunk expert histograms, per-token normalisers; every
+ * mode but TC adds the membership bitmap and an expert-major copy of the logit order keys, 4*T*E bytes). */
 int moe_route_workspace_size(int T, int E, int K, int mode, size_t *bytes);
 
 /*
  * moe_route - routing metadata from router logits ("Key design 1: Token Rounding routing").
  *   logits  fp32 [T, E] device.  Must be finite (else MOE_ERR_NONFINITE_LOGITS in status[0]).
- *   mode    MOE_ROUTE_TC or MOE_ROUTE_TR.  TR supports T <= 49152.
+ *   mode    a moe_route_mode other than MOE_ROUTE_TR_STOCHASTIC (which needs moe_route_ex).  Every mode but TC
+ *           supports T <= 49152.
  *   r       filled routing struct; every pointer non-null.  status is cleared by this call.
  *   ws      device scratch of at least moe_route_workspace_size() bytes (contents need not be zero).
  *   P_host  optional host pointer: if non-null, the call synchronises `stream` and stores P there.
- * Bit-exact and deterministic: same logits give the same metadata on every run.
+ * Bit-exact and deterministic: same logits give the same metadata on every run.  Under EC, row_slot names the
+ * token-choice slot of a pair that token choice also picked (-1 otherwise) and tc_counts still holds f_e.
  */
 int moe_route(const float *logits, int T, int E, int K, int mode, const moe_routing *r, void *ws,
               size_t ws_bytes, int32_t *P_host, void *stream);
+
+/*
+ * moe_route_ex - moe_route with the random draws of stochastic rounding.
+ *   uniforms  fp32 [E] device, one uniform draw in [0, 1) per expert (the caller's generator): expert e pads
+ *             to the ceiling iff uniforms[e] * M_tile < f_e - floor.  Required for MOE_ROUTE_TR_STOCHASTIC
+ *             (MOE_ERR_INVALID_ARG when NULL), ignored by the other modes.
+ * Every other argument and result as moe_route; same uniforms and logits give the same metadata.
+ */
+int moe_route_ex(const float *logits, const float *uniforms, int T, int E, int K, int mode, const moe_routing *r,
+                 void *ws, size_t ws_bytes, int32_t *P_host, void *stream);
 
 /*
  * moe_route_noalloc - moe_route for callers that may not allocate device memory.  The paper has no
@@ -118,7 +145,8 @@ int moe_route(const float *logits, int T, int E, int K, int mode, const moe_rout
  *   Sharing: all calls in the process share the one array per device and it keeps the last call's
  *   contents (this call clears whatever must start at zero).  Calls that overlap on the GPU (different
  *   streams, or different host threads on one device) race on the array and corrupt each other.
- *   Never calls cudaMalloc, cudaFree or any allocating routine.  Other arguments and results as moe_route.
+ *   Never calls cudaMalloc, cudaFree or any allocating routine.  Other arguments and results as moe_route
+ *   (MOE_ROUTE_TR_STOCHASTIC is not available here: it needs the uniforms of moe_route_ex).
  */
 #define MOE_ROUTE_NOALLOC_SCRATCH_BYTES (16u << 20)
 int moe_route_noalloc(const float *logits, int T, int E, int K, int mode, const moe_routing *r, int32_t *P_host,

@@ -40,8 +40,9 @@ def to_dev(inp: dict, dev="cuda") -> dict:
     return {k: v.to(dev) for k, v in inp.items()}
 
 
-def run_gpu(g: dict, K: int, mode: str, backward=True):
-    rt = moe.moe_route(g["logits"], K, mode)
+def run_gpu(g: dict, K: int, mode: str, backward=True, uniforms=None):
+    u = None if uniforms is None else uniforms.to(g["logits"].device)
+    rt = moe.moe_route(g["logits"], K, mode, uniforms=u)
     O, H = moe.moe_forward(g["X"], g["W1"], g["W2"], rt)
     out = dict(rt=rt, O=O, H=H)
     if backward:

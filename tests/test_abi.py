@@ -38,6 +38,13 @@ def test_every_declared_symbol_is_exported(lib):
 def test_capacity_and_workspace_queries(lib):
     assert moe.moe_route_capacity(24576, 128, 8, "tc") == 24576 * 8
     assert moe.moe_route_capacity(24576, 128, 8, "tr") == 24576 * 8 + 128 * 64
+    for mode in ("tr_up", "tr_stoch"):
+        assert moe.moe_route_capacity(24576, 128, 8, mode) == 24576 * 8 + 128 * 127
+    for mode in ("tr_down", "ec"):
+        assert moe.moe_route_capacity(24576, 128, 8, mode) == 24576 * 8
+    tc_ws = moe.moe_route_workspace_size(4096, 64, 8, "tc")
+    for mode in ("tr", "tr_up", "tr_down", "tr_stoch", "ec"):
+        assert moe.moe_route_workspace_size(4096, 64, 8, mode) >= tc_ws + 4096 * 64 * 4   # + expert-major keys
     p = moe.moe_route_capacity(512, 8, 2, "tc")
     fw = moe.moe_forward_workspace_size(512, 256, 128, 8, 2, p)
     assert fw >= p * 128 * 2 + 512 * 256 * 4
@@ -46,8 +53,8 @@ def test_capacity_and_workspace_queries(lib):
 
 
 @pytest.mark.parametrize("args,code", [
-    ((0, 8, 2, 0), 1), ((16, 8, 9, 0), 1), ((16, 8, 2, 7), 1), ((16, 2000, 2, 0), 2), ((16, 64, 40, 0), 2),
-    ((60000, 8, 2, 1), 2),
+    ((0, 8, 2, 0), 1), ((16, 8, 9, 0), 1), ((16, 8, 2, 7), 1), ((16, 8, 2, 6), 1), ((16, 8, 2, -1), 1),
+    ((16, 2000, 2, 0), 2), ((16, 64, 40, 0), 2), ((60000, 8, 2, 1), 2), ((60000, 8, 2, 5), 2),
 ])
 def test_route_validation(lib, args, code):
     out = ctypes.c_size_t(0)
@@ -69,6 +76,10 @@ def test_layer_validation(lib, shape, code):
 def test_null_arguments_rejected_before_any_device_work(lib):
     r = moe.moe.moe_routing()
     assert lib.moe_route(None, 16, 8, 2, 0, ctypes.byref(r), None, 0, None, None) == 1
+    # stochastic rounding without its uniforms: rejected on the host (the pointers are never dereferenced)
+    dummy = moe.moe.moe_routing(*([16] * 10))
+    assert lib.moe_route_ex(ctypes.c_void_p(16), None, 16, 8, 2, 4, ctypes.byref(dummy), None, 0, None, None) == 1
+    assert lib.moe_route(ctypes.c_void_p(16), 16, 8, 2, 4, ctypes.byref(dummy), None, 0, None, None) == 1
     assert lib.moe_forward(None, None, None, ctypes.byref(r), 512, 256, 128, 8, 2, 1024, None, None, None, 0,
                            None) == 1
     assert lib.moe_strerror(6) == b"device pipeline wait timed out"

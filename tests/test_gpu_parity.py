@@ -14,32 +14,49 @@ from oracle import moe_oracle as orc
 
 pytestmark = pytest.mark.gpu
 
-ROUTE_CASES = [(name, "tc") for name in synth.WORKLOADS] + [(name, "tr") for name in synth.WORKLOADS]
+# token choice, token rounding under each rounding rule, expert choice
+MODES = ["tc", "tr", "tr_up", "tr_down", "tr_stoch", "ec"]
+ROUTE_CASES = [(name, mode) for mode in MODES for name in synth.WORKLOADS]
+
+
+def _route_both(z, K, mode, seed=0):
+    """GPU routing through the C ABI and the oracle's, on the same logits (and uniforms for tr_stoch)."""
+    import fine_grained_mixture_gb300 as moe
+    u = synth.make_uniforms(z.shape[1], seed)
+    rt, P = moe.moe_route(z.cuda(), K, mode, want_P=True, uniforms=u.cuda())
+    return rt, P, orc.route(z.numpy(), K, mode, u=u.numpy())
 
 
 @pytest.mark.parametrize("name,mode", ROUTE_CASES)
 def test_routing_workloads(name, mode):
     w = synth.WORKLOADS[name]
     z = synth.make_logits_only(w, 0)
-    import fine_grained_mixture_gb300 as moe
-    rt, P = moe.moe_route(z.cuda(), w.K, mode, want_P=True)
+    rt, P, ref = _route_both(z, w.K, mode)
     code, P2 = rt.device_status()
     assert code == 0 and P2 == P
-    check_routing(rt, orc.route(z.numpy(), w.K, mode), P)
+    check_routing(rt, ref, P)
 
 
-@pytest.mark.parametrize("T,E,K,mode,ties", [
-    (2048, 1024, 32, "tc", False), (2048, 1024, 32, "tr", False), (1, 8, 2, "tc", False), (1, 8, 2, "tr", False),
-    (777, 33, 5, "tc", True), (777, 33, 5, "tr", True), (300, 1, 1, "tr", False), (4099, 64, 8, "tr", True),
-])
-def test_routing_edge_shapes(T, E, K, mode, ties):
-    import fine_grained_mixture_gb300 as moe
+EDGE_SHAPES = [(2048, 1024, 32, False), (1, 8, 2, False), (777, 33, 5, True), (300, 1, 1, False), (4099, 64, 8, True),
+               (200, 256, 1, False)]
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("T,E,K,ties", EDGE_SHAPES)
+def test_routing_edge_shapes(T, E, K, ties, mode):
     gen = torch.Generator().manual_seed(T * 7 + E)
     z = torch.randn((T, E), generator=gen)
     if ties:
         z = torch.round(z * 2) / 2          # many equal logits: exercises every tie-break rule
-    rt, P = moe.moe_route(z.cuda(), K, mode, want_P=True)
-    check_routing(rt, orc.route(z.numpy(), K, mode), P)
+    rt, P, ref = _route_both(z, K, mode, seed=T)
+    check_routing(rt, ref, P)
+
+
+def test_stochastic_rounding_without_uniforms_is_rejected():
+    import fine_grained_mixture_gb300 as moe
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_route(torch.randn((64, 8)).cuda(), 2, "tr_stoch")
+    assert ei.value.code == 1
 
 
 def test_routing_nonfinite_logits_flagged():
@@ -53,9 +70,10 @@ def test_routing_nonfinite_logits_flagged():
 
 def _full_compare(inp, K, mode):
     g = to_dev(inp)
-    out = run_gpu(g, K, mode)
+    u = synth.make_uniforms(inp["logits"].shape[1], 0)
+    out = run_gpu(g, K, mode, uniforms=u)
     assert out["code"] == 0
-    ref = orc.route(inp["logits"].numpy(), K, mode)
+    ref = orc.route(inp["logits"].numpy(), K, mode, u=u.numpy())
     check_routing(out["rt"], ref, out["P"])
     X, W1, W2, dO = (f64(inp[k]) for k in ("X", "W1", "W2", "dO"))
     fwd, bwd = orc.layer(X, W1, W2, dO, ref)
@@ -72,7 +90,7 @@ def _full_compare(inp, K, mode):
         assert float(out["dW2"][torch.from_numpy(empty).cuda()].abs().max()) == 0.0
 
 
-@pytest.mark.parametrize("mode", ["tc", "tr"])
+@pytest.mark.parametrize("mode", MODES)
 def test_layer_tiny_full(mode):
     w = synth.WORKLOADS["tiny"]
     _full_compare(synth.make_inputs(w, 0), w.K, mode)
@@ -86,6 +104,10 @@ def test_layer_tiny_full(mode):
     (1, 256, 128, 4, 2, False, "tc"),        # a single token
     (260, 256, 384, 1, 1, False, "tc"),      # one expert holds every token; n = 3 x 128
     (640, 768, 128, 3, 3, False, "tc"),      # K = E: every token visits every expert
+    (1000, 512, 256, 16, 4, True, "tr_up"),  # skewed, every expert padded up
+    (1000, 512, 256, 16, 4, True, "ec"),     # expert choice: equal counts whatever the skew
+    (300, 256, 128, 5, 2, False, "tr_stoch"),
+    (100, 256, 128, 64, 1, False, "ec"),     # T K < E: C = 1 row per expert
 ])
 def test_layer_small_shapes(T, d, n, E, K, skew, mode):
     w = synth.custom(T, d, n, E, K, skew=skew)
@@ -93,14 +115,16 @@ def test_layer_small_shapes(T, d, n, E, K, skew, mode):
 
 
 @pytest.mark.parametrize("name,mode", [("fine7b", "tc"), ("fine7b", "tr"), ("coarse", "tc"), ("sparse", "tc"),
-                                       ("sparse", "tr"), ("skew", "tc"), ("skew", "tr")])
+                                       ("sparse", "tr"), ("skew", "tc"), ("skew", "tr"), ("sparse", "tr_stoch"),
+                                       ("skew", "ec")])
 def test_layer_full_size_sampled(name, mode):
     w = synth.WORKLOADS[name]
     inp = synth.make_inputs(w, 0)
     g = to_dev(inp)
-    out = run_gpu(g, w.K, mode)
+    u = synth.make_uniforms(w.E, 0)
+    out = run_gpu(g, w.K, mode, uniforms=u)
     assert out["code"] == 0
-    ref = orc.route(inp["logits"].numpy(), w.K, mode)
+    ref = orc.route(inp["logits"].numpy(), w.K, mode, u=u.numpy())
     check_routing(out["rt"], ref, out["P"])
     rng = np.random.default_rng(0)
     # tokens: O and dX of sampled tokens need exactly the rows of those tokens
