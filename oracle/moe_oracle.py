@@ -34,6 +34,8 @@ Readings taken where the pages are silent (each listed in the design notes of th
     says token rounding is robust to which one is used): always up, always down, and stochastic (up with
     probability (f - floor)/M_tile, from one uniform draw per expert passed in, so the expected count is f).
     Padding beyond T tokens is impossible under every rule, which then rounds down.
+  * The router (the flowchart's "router scoring") is z = X W_r with W_r [d, E]; its backward holds the routing
+    fixed and differentiates only the gates (selection is piecewise constant in z).
   * Expert choice (the "EC" rows of the note's ablation table): each expert takes the C = floor(T K / E)
     tokens with the largest logits in its column (ties to the lower token id); a routed pair's gate is the
     token's softmax over all E logits.
@@ -355,6 +357,56 @@ def ds_via_h(dO, W2, row_token, row_expert, H):
         a = silu(H[sel, :n]) * H[sel, n:]
         dS[sel] = (dA * a).sum(axis=1)
     return dS
+
+
+# --------------------------------------------------------------------------------------------------
+# router  [NOTE-FW] (flowchart: input tokens and router scoring feed the routing step)
+# --------------------------------------------------------------------------------------------------
+
+
+def router_logits(X, Wr):
+    """The router's scores: z = X W_r, [T, d] x [d, E] -> [T, E]."""
+    return _matmul(np.asarray(X, np.float64), np.asarray(Wr, np.float64))
+
+
+def router_dz(z, rt: dict, dS, mode: str, tokens=None):
+    """Gradient of L = sum_r dS_r s_r with respect to the logits, the routing held fixed.
+
+    A row r = (t, e) has the gate s_r = exp(z_te) / sum_{j in N(t)} exp(z_tj), where the normaliser set N(t) is
+    the token's K token-choice experts (token choice and every token-rounding rule: a pair added by rounding
+    shares its token's token-choice normaliser) or all E experts (expert choice).  By the chain rule
+    dz_tj = sum over the token's rows r of dS_r * s_r * ([j = e_r] - [j in N(t)] * s(t, j)).
+    Returns dz [T, E] (rows outside `tokens`, when given, stay zero)."""
+    z = np.asarray(z, np.float64)
+    dS = np.asarray(dS, np.float64)
+    T, E = z.shape
+    dz = np.zeros((T, E))
+    tokens = np.arange(T) if tokens is None else np.asarray(tokens, np.int64)
+    want = np.zeros(T, dtype=bool)
+    want[tokens] = True
+    rows_of = {}
+    for r in np.nonzero(want[rt["row_token"]])[0]:
+        rows_of.setdefault(int(rt["row_token"][r]), []).append(int(r))
+    for t in tokens:
+        t = int(t)
+        N = np.arange(E) if mode == "ec" else np.asarray(rt["topk_idx"][t])
+        m = z[t, N].max()
+        den = np.exp(z[t, N] - m).sum()
+        s_N = np.exp(z[t, N] - m) / den
+        for r in rows_of.get(t, []):
+            e = int(rt["row_expert"][r])
+            s_r = np.exp(z[t, e] - m) / den
+            dz[t, e] += dS[r] * s_r
+            dz[t, N] -= dS[r] * s_r * s_N
+    return dz
+
+
+def router_backward(z, rt: dict, dS, X, Wr, mode: str):
+    """Router gradients: dz (router_dz), its contribution to dX (dz W_r^T) and dW_r = X^T dz."""
+    dz = router_dz(z, rt, dS, mode)
+    dX = _matmul(dz, np.asarray(Wr, np.float64).T)
+    dWr = _matmul(np.asarray(X, np.float64).T, dz)
+    return dict(dz=dz, dX=dX, dWr=dWr)
 
 
 # --------------------------------------------------------------------------------------------------

@@ -415,3 +415,90 @@ def test_planted_transposed_tie_break_is_caught(monkeypatch):
     monkeypatch.setattr(orc, "topk_token_choice", last_max)
     rt = orc.route_tc(z, g["K"], g["m_tile"])
     assert list(rt["topk_idx"].ravel()) != [int(v) for v in g["expect"]["tc"]["topk_idx"]]
+
+
+# ------------------------------------------------------------------------------------------------ router
+
+
+def _gate_loss(z, rt, dS, mode):
+    """L = sum_r dS_r s_r, each gate exp(z_te - logsumexp of the token's normaliser set) via scipy."""
+    L = 0.0
+    for r in range(rt["P"]):
+        t, e = int(rt["row_token"][r]), int(rt["row_expert"][r])
+        N = np.arange(z.shape[1]) if mode == "ec" else rt["topk_idx"][t]
+        L += dS[r] * np.exp(z[t, e] - scipy.special.logsumexp(z[t, N]))
+    return L
+
+
+def _router_problem(seed, mode, T=10, d=6, E=5, K=2, M=4):
+    rng = np.random.default_rng(seed)
+    X = rng.standard_normal((T, d))
+    Wr = rng.standard_normal((d, E)) / np.sqrt(d)
+    z = orc.router_logits(X, Wr)
+    rt = orc.route(z.astype(np.float32), K, mode, M, u=rng.random(E))
+    dS = rng.standard_normal(rt["P"])
+    return X, Wr, z, rt, dS
+
+
+@pytest.mark.parametrize("mode", ["tc", "tr", "tr_up", "ec"])
+def test_router_dz_matches_finite_differences(mode):
+    X, Wr, z, rt, dS = _router_problem(21, mode)
+    dz = orc.router_dz(z, rt, dS, mode)
+    h = 1e-6
+    g = np.zeros_like(z)
+    for i in np.ndindex(z.shape):
+        zp, zm = z.copy(), z.copy()
+        zp[i] += h
+        zm[i] -= h
+        g[i] = (_gate_loss(zp, rt, dS, mode) - _gate_loss(zm, rt, dS, mode)) / (2 * h)
+    assert np.abs(g - dz).max() <= 1e-7 * max(np.abs(dz).max(), 1.0)
+
+
+@pytest.mark.parametrize("mode", ["tc", "ec"])
+def test_router_dz_equals_torch_softmax_autograd(mode):
+    X, Wr, z, rt, dS = _router_problem(22, mode, T=24, E=7, K=3)
+    zt = torch.tensor(z, requires_grad=True)
+    if mode == "ec":
+        s = torch.softmax(zt, dim=1)
+        gates = s[torch.tensor(rt["row_token"]), torch.tensor(rt["row_expert"])]
+    else:
+        idx = torch.tensor(rt["topk_idx"])
+        s = torch.softmax(torch.gather(zt, 1, idx), dim=1)
+        gates = s[torch.tensor(rt["row_token"]), torch.tensor(rt["row_slot"])]
+    (gates * torch.tensor(dS)).sum().backward()
+    assert np.allclose(zt.grad.numpy(), orc.router_dz(z, rt, dS, mode), rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("mode", orc.ROUTE_MODES)
+def test_router_dz_rows_sum_to_zero(mode):
+    """Adding a constant to all of a token's logits leaves every gate unchanged, so each row of dz sums to 0."""
+    X, Wr, z, rt, dS = _router_problem(23, mode, T=64, E=8, K=3, M=8)
+    dz = orc.router_dz(z, rt, dS, mode)
+    assert np.abs(dz.sum(axis=1)).max() <= 1e-14 * max(np.abs(dz).max(), 1.0)
+    assert np.abs(dz).max() > 0
+
+
+def test_router_dz_is_zero_for_top1_token_choice():
+    """K = 1: every gate is exp(z_te)/exp(z_te) = 1, whatever the logits."""
+    X, Wr, z, rt, dS = _router_problem(24, "tc", K=1)
+    assert np.all(orc.router_dz(z, rt, dS, "tc") == 0.0)
+
+
+@pytest.mark.parametrize("mode", ["tc", "tr_down", "ec"])
+def test_router_backward_through_x_and_wr(mode):
+    X, Wr, z, rt, dS = _router_problem(25, mode, T=8, d=5, E=4, K=2)
+    out = orc.router_backward(z, rt, dS, X, Wr, mode)
+    assert np.allclose(orc.router_logits(X, Wr), torch.nn.functional.linear(torch.tensor(X), torch.tensor(Wr.T)).numpy(),
+                       rtol=1e-14, atol=1e-15)
+    h = 1e-6
+    for name, arr in (("dX", X), ("dWr", Wr)):
+        g = np.zeros_like(arr)
+        for i in np.ndindex(arr.shape):
+            old = arr[i]
+            arr[i] = old + h
+            lp = _gate_loss(orc.router_logits(X, Wr), rt, dS, mode)
+            arr[i] = old - h
+            lm = _gate_loss(orc.router_logits(X, Wr), rt, dS, mode)
+            arr[i] = old
+            g[i] = (lp - lm) / (2 * h)
+        assert np.abs(g - out[name]).max() <= 1e-7 * max(np.abs(out[name]).max(), 1.0), name
