@@ -515,6 +515,7 @@ def main():
         line["e2e"] = e2e_measure(layer, inp, args, world, dev)
         if rank == 0 and world == 1:
             line["tr_vs_tc"] = tr_vs_tc(args, dev)
+            line["router"] = router_timing(args, dev)
     if rank == 0 and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, inp, args.mode, args.cpu_seconds)
     if rank == 0:
@@ -624,6 +625,41 @@ def tr_vs_tc(args, dev):
     out["speedup_over_tc"] = {m: out["tc"]["ms_per_step"] / out[m]["ms_per_step"]
                               for m in ("tr", "tr_up", "tr_down", "tr_stoch", "ec")}
     out["workload"] = f"sparse: T={w.T}, d={w.d}, n={w.n}, E={w.E}, K={w.K}"
+    return out
+
+
+def router_timing(args, dev):
+    """The router either side of the layer on the metric's workload: logits = X W_r, then the gate backward
+    (dz, dX += dz W_r^T, dW_r = X^T dz) on that workload's token-choice routing."""
+    import fine_grained_mixture_gb300 as moe
+
+    w = synth.WORKLOADS[args.workload]
+    gen = torch.Generator().manual_seed(0)
+    X = torch.randn((w.T, w.d), generator=gen).to(torch.bfloat16).to(dev)
+    Wr = synth.make_router_weights(w.d, w.E, 0).to(dev)
+    z = moe.moe_router_forward(X, Wr)
+    rt = moe.moe_route(z, w.K, "tc")
+    dS = synth.make_row_grads(rt.p_cap, 0).to(dev)
+    dX = torch.zeros((w.T, w.d), dtype=torch.bfloat16, device=dev)
+    dlogits = torch.empty((w.T, w.E), dtype=torch.float32, device=dev)
+    dWr = torch.empty((w.d, w.E), dtype=torch.float32, device=dev)
+    n = max(args.steps, 20)
+    out = {}
+    for name, fn in (("forward", lambda: moe.moe_router_forward(X, Wr, logits=z)),
+                     ("backward", lambda: moe.moe_router_backward(dS, rt, z, X, Wr, dX, dlogits=dlogits, dWr=dWr))):
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n
+        flops = 2.0 * w.T * w.d * w.E * (1 if name == "forward" else 2)
+        out[name] = {"us": 1e3 * ms, "tflops": flops / (ms * 1e-3) / 1e12}
+    out["workload"] = f"{w.name}: T={w.T}, d={w.d}, E={w.E}, K={w.K}"
     return out
 
 

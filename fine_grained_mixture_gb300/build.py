@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe.so")
 
-SOURCES = ["api.cu", "route.cu", "gemm_fwd.cu", "gemm_bwd.cu", "elementwise.cu", "route_noalloc.cu"]
+SOURCES = ["api.cu", "route.cu", "gemm_fwd.cu", "gemm_bwd.cu", "elementwise.cu", "route_noalloc.cu", "router.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

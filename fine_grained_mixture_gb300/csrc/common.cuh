@@ -300,6 +300,12 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float *gdst, uint32_t ssrc, 
                : "memory");
 }
 
+// Bulk (TMA engine) copy of `bytes` from shared memory to global memory (both 16-byte aligned, bytes % 16 == 0).
+__device__ __forceinline__ void bulk_store(void *gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 template <int N>

@@ -72,6 +72,10 @@ def library() -> ctypes.CDLL:
     lib.moe_backward_workspace_size.argtypes = [_c_int] * 5 + [_c_size, sz]
     lib.moe_backward.argtypes = [_vp] * 5 + [ctypes.POINTER(moe_routing)] + [_c_int] * 5 + [_c_size] + [_vp] * 5 + [
         _c_size, _vp]
+    lib.moe_router_forward.argtypes = [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp]
+    lib.moe_router_backward_workspace_size.argtypes = [_c_int, _c_int, sz]
+    lib.moe_router_backward.argtypes = [_vp, ctypes.POINTER(moe_routing), _vp, _vp, _vp] + [_c_int] * 5 + [
+        _c_size, _vp, _vp, _vp, _vp, _c_size, _vp]
     lib.moe_get_status.argtypes = [ctypes.POINTER(moe_routing), ctypes.POINTER(ctypes.c_int32),
                                    ctypes.POINTER(ctypes.c_int32), _vp]
     lib.moe_strerror.argtypes = [_c_int]
@@ -88,7 +92,8 @@ def library() -> ctypes.CDLL:
     for f in ("moe_profile_enable", "moe_profile_count", "moe_profile_entry"):
         getattr(lib, f).restype = _c_int
     for f in ("moe_route_capacity", "moe_route_workspace_size", "moe_route", "moe_route_ex", "moe_forward_workspace_size",
-              "moe_forward", "moe_backward_workspace_size", "moe_backward", "moe_get_status", "moe_last_cuda_error"):
+              "moe_forward", "moe_backward_workspace_size", "moe_backward", "moe_get_status", "moe_last_cuda_error",
+              "moe_router_forward", "moe_router_backward_workspace_size", "moe_router_backward"):
         getattr(lib, f).restype = _c_int
     _LIB = lib
     return lib
@@ -243,6 +248,40 @@ def moe_backward(dO, X, W1, W2, H, routing: Routing, dX=None, dW1=None, dW2=None
                                   T, d, n, E, K, p_cap, _ptr(dX), _ptr(dW1), _ptr(dW2), _ptr(dS), _ptr(ws),
                                   ws.numel(), _stream(stream)), "moe_backward")
     return dX, dW1, dW2, dS
+
+
+def moe_router_forward(X, Wr, logits=None, status=None, stream=None):
+    """Router logits = X W_r (X bf16 [T, d], W_r bf16 [d, E]); returns fp32 logits [T, E]."""
+    T, d = X.shape
+    E = Wr.shape[1]
+    _need(X, "X", torch.bfloat16, T * d)
+    _need(Wr, "Wr", torch.bfloat16, d * E)
+    logits = torch.empty((T, E), dtype=torch.float32, device=X.device) if logits is None else logits
+    _need(logits, "logits", torch.float32, T * E)
+    _check(library().moe_router_forward(_ptr(X), _ptr(Wr), T, d, E, _ptr(logits), _ptr(status), _stream(stream)),
+           "moe_router_forward")
+    return logits
+
+
+def moe_router_backward(dS, routing: Routing, logits, X, Wr, dX, dlogits=None, dWr=None, ws=None, stream=None):
+    """Router gradients through the gates (routing held fixed): returns (dlogits [T, E] fp32, dWr [d, E] fp32).
+
+    dX (bf16 [T, d], the layer's input gradient from moe_backward) is updated in place with dz W_r^T."""
+    T, d = X.shape
+    E = Wr.shape[1]
+    for t, name, dt in ((dS, "dS", torch.float32), (logits, "logits", torch.float32), (X, "X", torch.bfloat16),
+                        (Wr, "Wr", torch.bfloat16), (dX, "dX", torch.bfloat16)):
+        _need(t, name, dt)
+    dev = X.device
+    dlogits = torch.empty((T, E), dtype=torch.float32, device=dev) if dlogits is None else dlogits
+    dWr = torch.empty((d, E), dtype=torch.float32, device=dev) if dWr is None else dWr
+    out = _c_size(0)
+    _check(library().moe_router_backward_workspace_size(T, E, ctypes.byref(out)), "moe_router_backward_workspace_size")
+    ws = torch.empty(out.value, dtype=torch.uint8, device=dev) if ws is None else ws
+    _check(library().moe_router_backward(_ptr(dS), ctypes.byref(routing.struct), _ptr(logits), _ptr(X), _ptr(Wr), T, d,
+                                         E, routing.K, routing.mode, routing.p_cap, _ptr(dlogits), _ptr(dX), _ptr(dWr),
+                                         _ptr(ws), ws.numel(), _stream(stream)), "moe_router_backward")
+    return dlogits, dWr
 
 
 def kernel_launch_count() -> int:

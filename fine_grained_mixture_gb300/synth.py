@@ -14,7 +14,8 @@ Recipe (per workload, one ``torch.Generator('cpu')`` seeded with ``seed``), draw
 * ``W2`` [E, n, d] ~ N(0, 1/n), drawn one expert at a time, bf16;
 * ``dO`` [T, d] ~ N(0, 1), bf16.
 
-Stochastic rounding draws one uniform per expert; ``make_uniforms`` takes them from a generator of their own
+The router weights W_r [d, E] ~ N(0, 1/d) (bf16) and synthetic per-row gradients dS come from generators of their
+own as well.  Stochastic rounding draws one uniform per expert; ``make_uniforms`` takes them from a generator of their own
 (seeded with ``seed + 0x5EED``) so the tensors above are the same whichever routing mode is run.
 
 The workloads are the layer shapes SonicMoE is evaluated on in spirit (a fine-grained 7B-class layer,
@@ -98,3 +99,26 @@ def make_uniforms(E: int, seed: int = 0) -> torch.Tensor:
     gen = torch.Generator(device="cpu")
     gen.manual_seed(seed + 0x5EED)
     return torch.rand((E,), generator=gen, dtype=torch.float32)
+
+
+def make_router_weights(d: int, E: int, seed: int = 0) -> torch.Tensor:
+    """Router weights W_r [d, E] ~ N(0, 1/d), bf16, from a generator of their own (seed + 0x2047)."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed + 0x2047)
+    return (torch.randn((d, E), generator=gen, dtype=torch.float32) / math.sqrt(d)).to(torch.bfloat16)
+
+
+def make_row_grads(P: int, seed: int = 0) -> torch.Tensor:
+    """Per-row upstream gradients dS [P] ~ N(0, 1), fp32, from a generator of their own (seed + 0xD5)."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed + 0xD5)
+    return torch.randn((P,), generator=gen, dtype=torch.float32)
+
+
+def quantize_for_exact_logits(X: torch.Tensor, Wr: torch.Tensor):
+    """X on a grid of 1/4 in [-2, 2] and W_r on a grid of 2^-10 in [-1/2, 1/2] (both stay on their grids in bf16):
+    every product of z = X W_r is a multiple of 2^-12 and, for d <= 2048, every partial sum stays below 2^12 in
+    magnitude, so fp32 accumulation in any order gives z exactly and the routing cannot depend on the order."""
+    Xq = torch.clamp(torch.round(X.float() * 4) / 4, -2, 2).to(torch.bfloat16)
+    Wq = torch.clamp(torch.round(Wr.float() * 1024) / 1024, -0.5, 0.5).to(torch.bfloat16)
+    return Xq, Wq

@@ -185,6 +185,38 @@ int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, cons
                  moe_bf16 *dX, moe_bf16 *dW1, moe_bf16 *dW2, float *dS, void *ws, size_t ws_bytes,
                  void *stream);
 
+/*
+ * The router on either side of the layer ("Method details / overall framework": router scoring of the input
+ * tokens feeds the routing step).  Shapes: E % 8 == 0, E <= 1024, d % 256 == 0.
+ *
+ * moe_router_forward - logits = X W_r on the tensor cores, fp32 accumulation.
+ *   X  bf16 [T, d];  W_r bf16 [d, E];  logits fp32 [T, E] output (the input of moe_route / moe_route_ex)
+ *   status  optional device int32: a bounded wait that ran out writes MOE_ERR_DEVICE_TIMEOUT there
+ */
+int moe_router_forward(const moe_bf16 *X, const moe_bf16 *Wr, int T, int d, int E, float *logits, int32_t *status,
+                       void *stream);
+
+/* Router backward scratch: dz in bf16 [T, E] and the per-token sums G [T]. */
+int moe_router_backward_workspace_size(int T, int E, size_t *bytes);
+
+/*
+ * moe_router_backward - gradients through the gates, the routing held fixed (selection is piecewise constant).
+ * A row r = (t, e) has the gate s_r = exp(z_te) / sum_{j in N(t)} exp(z_tj), N(t) = the token's K token-choice
+ * experts (MOE_ROUTE_TC and every token-rounding mode) or all E experts (MOE_ROUTE_EC), so
+ *     dz_tj = [a row (t, j) exists] dS_tj s_tj - [j in N(t)] s_tj G_t,   G_t = sum over the token's rows of dS_r s_r.
+ *   dS       fp32 [P_cap] from moe_backward (dL/ds_r per row);  r, K, mode, p_cap: the routing call's
+ *   logits   fp32 [T, E], the routing call's input (read under MOE_ROUTE_EC only)
+ *   X, W_r   as in moe_router_forward
+ *   dlogits  fp32 [T, E] output: dz
+ *   dX       bf16 [T, d] in/out: the layer's dX from moe_backward; dz W_r^T is added to it
+ *   dWr      fp32 [d, E] output: X^T dz
+ *   ws       scratch of moe_router_backward_workspace_size() bytes
+ * Row metadata out of range is skipped and reported as MOE_ERR_BAD_METADATA in the routing status block.
+ */
+int moe_router_backward(const float *dS, const moe_routing *r, const float *logits, const moe_bf16 *X,
+                        const moe_bf16 *Wr, int T, int d, int E, int K, int mode, size_t p_cap, float *dlogits,
+                        moe_bf16 *dX, float *dWr, void *ws, size_t ws_bytes, void *stream);
+
 /* Synchronise `stream` and read the routing status block: device error code and P (either may be NULL). */
 int moe_get_status(const moe_routing *r, int32_t *code, int32_t *P, void *stream);
 
