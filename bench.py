@@ -241,10 +241,11 @@ def run_reference(args):
 class Layer:
     """Resident device buffers for one workload and the step = route + forward + backward."""
 
-    def __init__(self, w, inp, mode, dev):
+    def __init__(self, w, inp, mode, dev, det=False):
         import fine_grained_mixture_gb300 as moe
 
-        self.moe, self.w, self.mode = moe, w, mode
+        self.moe, self.w, self.mode, self.det = moe, w, mode, det
+        flags = moe.MOE_FLAG_DETERMINISTIC if det else 0
         self.g = {k: v.to(dev) for k, v in inp.items()}
         self.u = synth.make_uniforms(w.E, 0).to(dev)  # per-expert draws of stochastic rounding
         self.rt = moe.Routing(w.T, w.E, w.K, mode, dev)
@@ -256,19 +257,21 @@ class Layer:
         self.dW1 = torch.empty((w.E, w.d, 2 * w.n), dtype=bf, device=dev)
         self.dW2 = torch.empty((w.E, w.n, w.d), dtype=bf, device=dev)
         self.dS = torch.empty(p, dtype=torch.float32, device=dev)
-        self.wsf = torch.empty(moe.moe_forward_workspace_size(w.T, w.d, w.n, w.E, w.K, p), dtype=torch.uint8, device=dev)
-        self.wsb = torch.empty(moe.moe_backward_workspace_size(w.T, w.d, w.n, w.E, w.K, p), dtype=torch.uint8,
+        self.wsf = torch.empty(moe.moe_forward_workspace_size(w.T, w.d, w.n, w.E, w.K, p, flags), dtype=torch.uint8,
+                               device=dev)
+        self.wsb = torch.empty(moe.moe_backward_workspace_size(w.T, w.d, w.n, w.E, w.K, p, flags), dtype=torch.uint8,
                                device=dev)
 
     def route(self):
         self.moe.moe_route(self.g["logits"], self.w.K, self.mode, routing=self.rt, uniforms=self.u)
 
     def forward(self):
-        self.moe.moe_forward(self.g["X"], self.g["W1"], self.g["W2"], self.rt, O=self.O, H=self.H, ws=self.wsf)
+        self.moe.moe_forward(self.g["X"], self.g["W1"], self.g["W2"], self.rt, O=self.O, H=self.H, ws=self.wsf,
+                             deterministic=self.det)
 
     def backward(self):
         self.moe.moe_backward(self.g["dO"], self.g["X"], self.g["W1"], self.g["W2"], self.H, self.rt, dX=self.dX,
-                              dW1=self.dW1, dW2=self.dW2, dS=self.dS, ws=self.wsb)
+                              dW1=self.dW1, dW2=self.dW2, dS=self.dS, ws=self.wsb, deterministic=self.det)
 
     def step(self):
         self.route()
@@ -516,6 +519,7 @@ def main():
         if rank == 0 and world == 1:
             line["tr_vs_tc"] = tr_vs_tc(args, dev)
             line["router"] = router_timing(args, dev)
+            line["deterministic"] = deterministic_timing(args, w, inp, line["ms_per_step"], dev)
     if rank == 0 and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, inp, args.mode, args.cpu_seconds)
     if rank == 0:
@@ -626,6 +630,21 @@ def tr_vs_tc(args, dev):
                               for m in ("tr", "tr_up", "tr_down", "tr_stoch", "ec")}
     out["workload"] = f"sparse: T={w.T}, d={w.d}, n={w.n}, E={w.E}, K={w.K}"
     return out
+
+
+def deterministic_timing(args, w, inp, ms_default, dev):
+    """The same step with MOE_FLAG_DETERMINISTIC (fixed-point aggregation: bitwise-reproducible O, dX and dS)."""
+    layer = Layer(w, inp, args.mode, dev, det=True)
+    for _ in range(3):
+        layer.step()
+    torch.cuda.synchronize()
+    n = max(args.steps, 20)
+    total, _ = time_steps(layer, n)
+    ms = total / n
+    ff, fb = layer_flops(w)
+    del layer
+    torch.cuda.empty_cache()
+    return {"ms_per_step": ms, "tflops": (ff + fb) / (ms * 1e-3) / 1e12, "slowdown_vs_default": ms / ms_default}
 
 
 def router_timing(args, dev):

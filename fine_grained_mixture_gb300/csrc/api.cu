@@ -241,12 +241,22 @@ static bool routing_ok(const moe_routing *r) {
          r->row_token && r->row_slot && r->row_score && r->status;
 }
 
-static size_t fwd_ws_bytes(int T, int d, int n, size_t p_cap) {
-  return align256(p_cap * n * 2) + align256((size_t)T * d * 4);
+static bool det_flag(unsigned flags) { return (flags & MOE_FLAG_DETERMINISTIC) != 0u; }
+
+// Column tile of the dH GEMM (n = 256 * k uses 256-wide tiles, else 128).
+static int dh_bn(int n) { return (n % 256 == 0) ? 256 : 128; }
+
+// A [P_cap, n] bf16, then the accumulator of O: fp32, or 64-bit fixed point when deterministic.
+static size_t fwd_ws_bytes(int T, int d, int n, size_t p_cap, unsigned flags) {
+  return align256(p_cap * n * 2) + align256((size_t)T * d * (det_flag(flags) ? 8 : 4));
 }
 
-static size_t bwd_ws_bytes(int T, int d, int n, size_t p_cap) {
-  return align256(p_cap * 2 * n * 2) + align256(p_cap * n * 2) + align256((size_t)T * d * 4);
+// dH [P_cap, 2n], s*A [P_cap, n], the accumulator of dX (fp32 or fixed point); deterministic mode adds the
+// per-column-tile dS partials [P_cap, n / BN].
+static size_t bwd_ws_bytes(int T, int d, int n, size_t p_cap, unsigned flags) {
+  const bool det = det_flag(flags);
+  return align256(p_cap * 2 * n * 2) + align256(p_cap * n * 2) + align256((size_t)T * d * (det ? 8 : 4)) +
+         (det ? align256(p_cap * (n / dh_bn(n)) * 4) : 0);
 }
 
 // Column tiles (of 256) per pass of a scatter-add GEMM: the largest divisor of d/256 whose fp32 slab
@@ -335,31 +345,37 @@ int moe_route_ex(const float *logits, const float *uniforms, int T, int E, int K
 }
 
 
-int moe_forward_workspace_size(int T, int d, int n, int E, int K, size_t p_cap, size_t *bytes) {
-  if (!bytes) return MOE_ERR_INVALID_ARG;
+int moe_forward_workspace_size_ex(int T, int d, int n, int E, int K, size_t p_cap, unsigned flags, size_t *bytes) {
+  if (!bytes || (flags & ~MOE_FLAG_DETERMINISTIC)) return MOE_ERR_INVALID_ARG;
   const int rc = check_layer_shape(T, d, n, E, K, p_cap);
   if (rc != MOE_OK) return rc;
-  *bytes = fwd_ws_bytes(T, d, n, p_cap);
+  *bytes = fwd_ws_bytes(T, d, n, p_cap, flags);
   return MOE_OK;
 }
 
-int moe_forward(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const moe_routing *r, int T, int d, int n,
-                int E, int K, size_t p_cap, moe_bf16 *O, moe_bf16 *H, void *ws, size_t ws_bytes, void *stream) {
+int moe_forward_workspace_size(int T, int d, int n, int E, int K, size_t p_cap, size_t *bytes) {
+  return moe_forward_workspace_size_ex(T, d, n, E, K, p_cap, 0u, bytes);
+}
+
+int moe_forward_ex(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const moe_routing *r, int T, int d,
+                   int n, int E, int K, size_t p_cap, moe_bf16 *O, moe_bf16 *H, void *ws, size_t ws_bytes,
+                   unsigned flags, void *stream) {
   int rc = check_layer_shape(T, d, n, E, K, p_cap);
   if (rc != MOE_OK) return rc;
-  if (!X || !W1 || !W2 || !O || !H || !routing_ok(r)) return MOE_ERR_INVALID_ARG;
-  if (!ws || ws_bytes < fwd_ws_bytes(T, d, n, p_cap)) return MOE_ERR_WORKSPACE;
+  if (!X || !W1 || !W2 || !O || !H || !routing_ok(r) || (flags & ~MOE_FLAG_DETERMINISTIC)) return MOE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < fwd_ws_bytes(T, d, n, p_cap, flags)) return MOE_ERR_WORKSPACE;
   rc = check_device();
   if (rc != MOE_OK) return rc;
+  const bool det = det_flag(flags);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char *p = static_cast<char *>(ws);
   moe_bf16 *A = reinterpret_cast<moe_bf16 *>(p);
   p += align256(p_cap * n * 2);
-  float *O32 = reinterpret_cast<float *>(p);
+  void *Oacc = p;  // fp32, or 64-bit fixed point when deterministic
 
   Fork side;
   if ((rc = side.open(s)) != MOE_OK) return rc;
-  cudaError_t err = cudaMemsetAsync(O32, 0, (size_t)T * d * 4, side.side());
+  cudaError_t err = cudaMemsetAsync(Oacc, 0, (size_t)T * d * (det ? 8 : 4), side.side());
   if (err != cudaSuccess) return record_cuda_error(err);
 
   GemmArgs a = base_args(r, T, d, n, E, p_cap);
@@ -386,47 +402,63 @@ int moe_forward(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const
   a.out0 = nullptr;
   a.out1 = nullptr;
   a.gsrc = nullptr;
-  a.out_f32 = O32;
+  a.out_f32 = det ? nullptr : static_cast<float *>(Oacc);
+  a.out_i64 = det ? static_cast<long long *>(Oacc) : nullptr;
   if ((rc = side.join()) != MOE_OK) return rc;
-  if ((rc = (fill_unused(tm), launch_down(a, tm, s))) != MOE_OK) return rc;
-  return launch_f32_to_bf16(O32, O, (size_t)T * d, s);
+  if ((rc = (fill_unused(tm), launch_down(a, tm, s, det))) != MOE_OK) return rc;
+  if (det) return launch_fixed_to_bf16(static_cast<long long *>(Oacc), O, (size_t)T * d, s);
+  return launch_f32_to_bf16(static_cast<float *>(Oacc), O, (size_t)T * d, s);
 }
 
-int moe_backward_workspace_size(int T, int d, int n, int E, int K, size_t p_cap, size_t *bytes) {
-  if (!bytes) return MOE_ERR_INVALID_ARG;
+int moe_forward(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const moe_routing *r, int T, int d, int n,
+                int E, int K, size_t p_cap, moe_bf16 *O, moe_bf16 *H, void *ws, size_t ws_bytes, void *stream) {
+  return moe_forward_ex(X, W1, W2, r, T, d, n, E, K, p_cap, O, H, ws, ws_bytes, 0u, stream);
+}
+
+int moe_backward_workspace_size_ex(int T, int d, int n, int E, int K, size_t p_cap, unsigned flags, size_t *bytes) {
+  if (!bytes || (flags & ~MOE_FLAG_DETERMINISTIC)) return MOE_ERR_INVALID_ARG;
   const int rc = check_layer_shape(T, d, n, E, K, p_cap);
   if (rc != MOE_OK) return rc;
-  *bytes = bwd_ws_bytes(T, d, n, p_cap);
+  *bytes = bwd_ws_bytes(T, d, n, p_cap, flags);
   return MOE_OK;
 }
 
-int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const moe_bf16 *H,
-                 const moe_routing *r, int T, int d, int n, int E, int K, size_t p_cap, moe_bf16 *dX, moe_bf16 *dW1,
-                 moe_bf16 *dW2, float *dS, void *ws, size_t ws_bytes, void *stream) {
+int moe_backward_workspace_size(int T, int d, int n, int E, int K, size_t p_cap, size_t *bytes) {
+  return moe_backward_workspace_size_ex(T, d, n, E, K, p_cap, 0u, bytes);
+}
+
+int moe_backward_ex(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const moe_bf16 *H,
+                    const moe_routing *r, int T, int d, int n, int E, int K, size_t p_cap, moe_bf16 *dX, moe_bf16 *dW1,
+                    moe_bf16 *dW2, float *dS, void *ws, size_t ws_bytes, unsigned flags, void *stream) {
   int rc = check_layer_shape(T, d, n, E, K, p_cap);
   if (rc != MOE_OK) return rc;
-  if (!dO || !X || !W1 || !W2 || !H || !dX || !dW1 || !dW2 || !dS || !routing_ok(r)) return MOE_ERR_INVALID_ARG;
-  if (!ws || ws_bytes < bwd_ws_bytes(T, d, n, p_cap)) return MOE_ERR_WORKSPACE;
+  if (!dO || !X || !W1 || !W2 || !H || !dX || !dW1 || !dW2 || !dS || !routing_ok(r) ||
+      (flags & ~MOE_FLAG_DETERMINISTIC))
+    return MOE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < bwd_ws_bytes(T, d, n, p_cap, flags)) return MOE_ERR_WORKSPACE;
   rc = check_device();
   if (rc != MOE_OK) return rc;
+  const bool det = det_flag(flags);
+  const int bn = dh_bn(n);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char *p = static_cast<char *>(ws);
   moe_bf16 *dH = reinterpret_cast<moe_bf16 *>(p);
   p += align256(p_cap * 2 * n * 2);
   moe_bf16 *sA = reinterpret_cast<moe_bf16 *>(p);
   p += align256(p_cap * n * 2);
-  float *dX32 = reinterpret_cast<float *>(p);
+  void *dXacc = p;  // fp32, or 64-bit fixed point when deterministic
+  p += align256((size_t)T * d * (det ? 8 : 4));
+  float *dS_part = det ? reinterpret_cast<float *>(p) : nullptr;
 
   Fork side;
   if ((rc = side.open(s)) != MOE_OK) return rc;
-  cudaError_t err = cudaMemsetAsync(dX32, 0, (size_t)T * d * 4, side.side());
+  cudaError_t err = cudaMemsetAsync(dXacc, 0, (size_t)T * d * (det ? 8 : 4), side.side());
   if (err == cudaSuccess) err = cudaMemsetAsync(dS, 0, p_cap * 4, s);
   if (err != cudaSuccess) return record_cuda_error(err);
 
   GemmArgs a = base_args(r, T, d, n, E, p_cap);
   TensorMaps tm;
   // dH: dA' = dO[tok] W2_e^T (N = n, K = d); epilogue dSwiGLU, dS, s*A
-  const int bn = (n % 256 == 0) ? 256 : 128;
   if ((rc = make_tmap_bf16(&tm.b, W2, d, (uint64_t)E * n, bn / 2)) != MOE_OK) return rc;  // two N halves
   tm.a = tm.b;  // unused: dO rows are gathered with cp.async
   a.gsrc = dO;
@@ -436,23 +468,28 @@ int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, cons
   a.out0 = dH;
   a.out1 = sA;
   a.dS = dS;
+  a.dS_part = dS_part;
   a.Hin = H;
   if ((rc = make_tmap_bf16_epi(&tm.h, H, 2 * (uint64_t)n, p_cap)) != MOE_OK) return rc;
   if ((rc = make_tmap_bf16_epi(&tm.dh, dH, 2 * (uint64_t)n, p_cap)) != MOE_OK) return rc;
   if ((rc = make_tmap_bf16_epi(&tm.sa, sA, n, p_cap)) != MOE_OK) return rc;
-  if ((rc = launch_dh(a, tm, s, bn)) != MOE_OK) return rc;
+  if ((rc = launch_dh(a, tm, s, bn, det)) != MOE_OK) return rc;
+  if (det && (rc = launch_ds_sum(dS_part, n / bn, r->offsets, E, dS, s)) != MOE_OK) return rc;
   // dX~: dX32[tok] += dH W1_e^T (N = d, K = 2n)
   if ((rc = make_tmap_bf16(&tm.a, dH, 2 * (uint64_t)n, p_cap, 128)) != MOE_OK) return rc;
   if ((rc = make_tmap_bf16(&tm.b, W1, 2 * (uint64_t)n, (uint64_t)E * d, 128)) != MOE_OK) return rc;  // two N halves
   GemmArgs ax = base_args(r, T, d, n, E, p_cap);
   ax.Ndim = d;
   ax.Kdim = 2 * n;
-  ax.out_f32 = dX32;
+  ax.out_f32 = det ? nullptr : static_cast<float *>(dXacc);
+  ax.out_i64 = det ? static_cast<long long *>(dXacc) : nullptr;
   if ((rc = side.join()) != MOE_OK) return rc;
-  if ((rc = (fill_unused(tm), launch_dx(ax, tm, s))) != MOE_OK) return rc;
-  // the cast of dX overlaps the weight-gradient GEMMs, which read neither dX32 nor dX
+  if ((rc = (fill_unused(tm), launch_dx(ax, tm, s, det))) != MOE_OK) return rc;
+  // the cast of dX overlaps the weight-gradient GEMMs, which read neither the accumulator nor dX
   if ((rc = side.open(s)) != MOE_OK) return rc;
-  if ((rc = launch_f32_to_bf16(dX32, dX, (size_t)T * d, side.side())) != MOE_OK) return rc;
+  rc = det ? launch_fixed_to_bf16(static_cast<long long *>(dXacc), dX, (size_t)T * d, side.side())
+           : launch_f32_to_bf16(static_cast<float *>(dXacc), dX, (size_t)T * d, side.side());
+  if (rc != MOE_OK) return rc;
   // rows [P, P_cap) of dH and s*A are read as the zero tail of the last expert's k-blocks
   if ((rc = launch_zero_tail(dH, sA, r->offsets, E, p_cap, 2 * n, n, s)) != MOE_OK) return rc;
   GemmArgs aw = base_args(r, T, d, n, E, p_cap);
@@ -498,6 +535,12 @@ int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, cons
   return side.join();
 }
 
+int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const moe_bf16 *H,
+                 const moe_routing *r, int T, int d, int n, int E, int K, size_t p_cap, moe_bf16 *dX, moe_bf16 *dW1,
+                 moe_bf16 *dW2, float *dS, void *ws, size_t ws_bytes, void *stream) {
+  return moe_backward_ex(dO, X, W1, W2, H, r, T, d, n, E, K, p_cap, dX, dW1, dW2, dS, ws, ws_bytes, 0u, stream);
+}
+
 int moe_get_status(const moe_routing *r, int32_t *code, int32_t *P, void *stream) {
   if (!r || !r->status) return MOE_ERR_INVALID_ARG;
   int32_t words[MOE_STATUS_WORDS];
@@ -521,6 +564,7 @@ const char *moe_strerror(int code) {
     case MOE_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
     case MOE_ERR_BAD_METADATA: return "routing metadata out of range";
     case MOE_ERR_DEVICE: return "device is not compute capability 10.3";
+    case MOE_ERR_RANGE: return "value beyond the deterministic accumulator's range";
     default: return "unknown status";
   }
 }

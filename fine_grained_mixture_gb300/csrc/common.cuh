@@ -300,6 +300,17 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float *gdst, uint32_t ssrc, 
                : "memory");
 }
 
+// Bulk (TMA engine) element-wise 64-bit integer add (two's complement, so signed values add correctly).
+__device__ __forceinline__ void bulk_reduce_add_u64(long long *gdst, uint32_t ssrc, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.L2::cache_hint.add.u64 [%0], [%1], %2, %3;" ::"l"(gdst),
+               "r"(ssrc), "r"(bytes), "l"(policy)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v2_u64(uint32_t addr, unsigned long long a, unsigned long long b) {
+  asm volatile("st.shared.v2.u64 [%0], {%1, %2};" ::"r"(addr), "l"(a), "l"(b) : "memory");
+}
+
 // Bulk (TMA engine) copy of `bytes` from shared memory to global memory (both 16-byte aligned, bytes % 16 == 0).
 __device__ __forceinline__ void bulk_store(void *gdst, uint32_t ssrc, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)

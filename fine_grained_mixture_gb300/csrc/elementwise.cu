@@ -1,6 +1,7 @@
 // elementwise.cu - the fp32 -> bf16 cast that finishes the fused aggregations (O and dX are accumulated
-// in fp32 by the down-projection and dX~ epilogues, then rounded once to bf16), the zeroing of the rows past
-// the last expert, and the bounded-wait self-test.
+// in fp32 by the down-projection and dX~ epilogues, then rounded once to bf16), its fixed-point counterpart and
+// the ordered dS sum of the deterministic mode, the zeroing of the rows past the last expert, and the
+// bounded-wait self-test.
 #include "common.cuh"
 #include "internal.h"
 
@@ -25,6 +26,56 @@ int launch_f32_to_bf16(const float *src, void *dst, size_t count, cudaStream_t s
   prof_begin("cast_f32_bf16", s);
   cudaError_t err = launch_pdl(f32_to_bf16_kernel, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const float4 *>(src),
                                reinterpret_cast<uint2 *>(dst), n4);
+  prof_end(s);
+  count_launch();
+  if (err == cudaSuccess) err = cudaGetLastError();
+  return err == cudaSuccess ? MOE_OK : record_cuda_error(err);
+}
+
+// Fixed-point accumulator (32 fractional bits) of the deterministic aggregation -> bf16, four elements per step.
+__global__ void __launch_bounds__(256) fixed_to_bf16_kernel(const longlong2 *__restrict__ src, uint2 *__restrict__ dst,
+                                                            size_t n4) {
+  griddep_wait();
+  griddep_launch_dependents();
+  constexpr float kInv = 2.3283064365386962890625e-10f;  // 2^-32
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+    const longlong2 a = __ldcs(src + 2 * i), b = __ldcs(src + 2 * i + 1);
+    uint2 o;
+    o.x = pack_bf16x2(__ll2float_rn(a.x) * kInv, __ll2float_rn(a.y) * kInv);
+    o.y = pack_bf16x2(__ll2float_rn(b.x) * kInv, __ll2float_rn(b.y) * kInv);
+    __stcs(dst + i, o);
+  }
+}
+
+int launch_fixed_to_bf16(const long long *src, void *dst, size_t count, cudaStream_t s) {
+  const size_t n4 = count / 4;  // count is a multiple of 256 (d % 256 == 0)
+  const int blocks = num_sms() * 8;
+  prof_begin("cast_fixed_bf16", s);
+  cudaError_t err = launch_pdl(fixed_to_bf16_kernel, dim3(blocks), dim3(256), 0, s,
+                               reinterpret_cast<const longlong2 *>(src), reinterpret_cast<uint2 *>(dst), n4);
+  prof_end(s);
+  count_launch();
+  if (err == cudaSuccess) err = cudaGetLastError();
+  return err == cudaSuccess ? MOE_OK : record_cuda_error(err);
+}
+
+// dS[r] for r < P: the deterministic dH epilogue's per-column-tile partials added in tile order.
+__global__ void __launch_bounds__(256) ds_sum_kernel(const float *__restrict__ part, int tiles,
+                                                     const int32_t *__restrict__ offsets, int E,
+                                                     float *__restrict__ dS) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const size_t P = static_cast<size_t>(offsets[E]);
+  for (size_t r = blockIdx.x * (size_t)blockDim.x + threadIdx.x; r < P; r += (size_t)gridDim.x * blockDim.x) {
+    float v = 0.f;
+    for (int j = 0; j < tiles; ++j) v += part[r * tiles + j];
+    dS[r] = v;
+  }
+}
+
+int launch_ds_sum(const float *part, int tiles, const int32_t *offsets, int E, float *dS, cudaStream_t s) {
+  prof_begin("ds_sum", s);
+  cudaError_t err = launch_pdl(ds_sum_kernel, dim3(num_sms() * 2), dim3(256), 0, s, part, tiles, offsets, E, dS);
   prof_end(s);
   count_launch();
   if (err == cudaSuccess) err = cudaGetLastError();

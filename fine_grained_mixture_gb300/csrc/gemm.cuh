@@ -267,7 +267,21 @@ __device__ __forceinline__ int token_or_oob(const GemmArgs &a, int r, int row_en
   return (t >= 0 && t < a.T) ? t : a.T;
 }
 
-template <int MODE, int BN, int STAGES, int MB>
+// Deterministic aggregation: a row's contribution enters the accumulator as a 64-bit fixed-point integer with
+// 32 fractional bits, so the sum is the same whatever order the reduce-adds land in.  One contribution may not
+// exceed 2^21 in magnitude (a token has at most 1024 rows, so no sum leaves the +-2^31 range).
+constexpr float kFixScale = 4294967296.0f;  // 2^32
+constexpr float kFixLimit = 2097152.0f;     // 2^21
+
+__device__ __forceinline__ long long to_fixed(float x, bool &range_ok) {
+  if (!(fabsf(x) < kFixLimit)) {  // also catches NaN
+    range_ok = false;
+    return 0;
+  }
+  return __float2ll_rn(x * kFixScale);
+}
+
+template <int MODE, int BN, int STAGES, int MB, bool DET>
 __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     moe_gemm_kernel(const __grid_constant__ TensorMaps tm, const GemmArgs a) {
   const CUtensorMap &tmA = tm.a;
@@ -696,27 +710,50 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
           if (MODE == kDown) sc = __ldg(&a.row_score[r]);
         }
         const int half = (warp - 2) >> 2;  // which half of the BN columns this warp drains
-        float *grow = a.out_f32 + (size_t)(tok >= 0 ? tok : 0) * a.d + t.n0 + half * (BN / 2);
         const uint32_t stg = base + SM::kStgOff + ((warp - 2) * 32 + lane) * kStgRowBytes;
+        if (DET) {
+          // 32 columns per bulk add: 32 64-bit integers fill the 256-byte staging row
+          long long *grow = a.out_i64 + (size_t)(tok >= 0 ? tok : 0) * a.d + t.n0 + half * (BN / 2);
+          bool range_ok = true;
 #pragma unroll 1
-        for (int c = 0; c < BN / 128; ++c) {
-          uint32_t v0[32], v1[32];
-          const uint32_t col = half * (BN / 2) + c * 64;
-          tmem_ld32(tacc + col, v0);
-          tmem_ld32(tacc + col + 32, v1);
-          tmem_ld_wait();
-          bulk_wait_read<0>();  // the previous bulk add has read the staging row
+          for (int c = 0; c < BN / 64; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tacc + half * (BN / 2) + c * 32, v);
+            tmem_ld_wait();
+            bulk_wait_read<0>();  // the previous bulk add has read the staging row
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            st_shared_v4(stg + i * 16, sc * __uint_as_float(v0[4 * i]), sc * __uint_as_float(v0[4 * i + 1]),
-                         sc * __uint_as_float(v0[4 * i + 2]), sc * __uint_as_float(v0[4 * i + 3]));
+            for (int i = 0; i < 16; ++i) {
+              const long long q0 = to_fixed(sc * __uint_as_float(v[2 * i]), range_ok);
+              const long long q1 = to_fixed(sc * __uint_as_float(v[2 * i + 1]), range_ok);
+              st_shared_v2_u64(stg + i * 16, static_cast<unsigned long long>(q0), static_cast<unsigned long long>(q1));
+            }
+            fence_proxy_async_smem();
+            if (tok >= 0) bulk_reduce_add_u64(grow + c * 32, stg, 256, pol_acc);
+            bulk_commit();
+          }
+          if (!range_ok) set_status(a.status, MOE_ERR_RANGE);
+        } else {
+          float *grow = a.out_f32 + (size_t)(tok >= 0 ? tok : 0) * a.d + t.n0 + half * (BN / 2);
+#pragma unroll 1
+          for (int c = 0; c < BN / 128; ++c) {
+            uint32_t v0[32], v1[32];
+            const uint32_t col = half * (BN / 2) + c * 64;
+            tmem_ld32(tacc + col, v0);
+            tmem_ld32(tacc + col + 32, v1);
+            tmem_ld_wait();
+            bulk_wait_read<0>();  // the previous bulk add has read the staging row
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            st_shared_v4(stg + 128 + i * 16, sc * __uint_as_float(v1[4 * i]), sc * __uint_as_float(v1[4 * i + 1]),
-                         sc * __uint_as_float(v1[4 * i + 2]), sc * __uint_as_float(v1[4 * i + 3]));
-          fence_proxy_async_smem();
-          if (tok >= 0) bulk_reduce_add_f32(grow + c * 64, stg, 256, pol_acc);
-          bulk_commit();
+            for (int i = 0; i < 8; ++i)
+              st_shared_v4(stg + i * 16, sc * __uint_as_float(v0[4 * i]), sc * __uint_as_float(v0[4 * i + 1]),
+                           sc * __uint_as_float(v0[4 * i + 2]), sc * __uint_as_float(v0[4 * i + 3]));
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              st_shared_v4(stg + 128 + i * 16, sc * __uint_as_float(v1[4 * i]), sc * __uint_as_float(v1[4 * i + 1]),
+                           sc * __uint_as_float(v1[4 * i + 2]), sc * __uint_as_float(v1[4 * i + 3]));
+            fence_proxy_async_smem();
+            if (tok >= 0) bulk_reduce_add_f32(grow + c * 64, stg, 256, pol_acc);
+            bulk_commit();
+          }
         }
       } else if (MODE == kDH) {
         const int r = t.row0 + row;
@@ -835,7 +872,11 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
           }
           __syncwarp();
         }
-        if (valid) atomicAdd(&a.dS[r], ds);
+        if (valid) {
+          // deterministic: one partial per column tile, summed in tile order afterwards
+          if (DET) a.dS_part[(size_t)r * (a.Ndim / BN) + t.n0 / BN] = ds;
+          else atomicAdd(&a.dS[r], ds);
+        }
       } else {
         // weight gradients: bf16 rows of dW_e (M block mb sits in TMEM columns [mb * BN, (mb + 1) * BN)), stored
         // as 32 x 32 boxes of the [E * M, N] output view through two staging tiles per warp
@@ -891,7 +932,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
 }
 
 // Host launcher for one instantiation: clusters of two CTAs, one CTA per SM, as many clusters as fit.
-template <int MODE, int BN, int STAGES, int MB = 1>
+template <int MODE, int BN, int STAGES, int MB = 1, bool DET = false>
 int launch_gemm(const GemmArgs &a, const TensorMaps &tm, cudaStream_t stream) {
   using SM = Smem<BN, STAGES, epi_bytes<MODE>(), MB, tile_cache_bytes<MODE>()>;
   static int attr_dev = -1;
@@ -913,12 +954,12 @@ int launch_gemm(const GemmArgs &a, const TensorMaps &tm, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;  // occupancy query with the cluster shape only
   if (attr_dev != dev) {
-    err = cudaFuncSetAttribute(moe_gemm_kernel<MODE, BN, STAGES, MB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(moe_gemm_kernel<MODE, BN, STAGES, MB, DET>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                SM::kBytes);
     if (err != cudaSuccess) return record_cuda_error(err);
     int clusters = 0;
     cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
-    err = cudaOccupancyMaxActiveClusters(&clusters, moe_gemm_kernel<MODE, BN, STAGES, MB>, &cfg);
+    err = cudaOccupancyMaxActiveClusters(&clusters, moe_gemm_kernel<MODE, BN, STAGES, MB, DET>, &cfg);
     if (err != cudaSuccess || clusters <= 0) clusters = num_sms() / 2;
     grid_cache = 2 * clusters;
     attr_dev = dev;
@@ -927,7 +968,7 @@ int launch_gemm(const GemmArgs &a, const TensorMaps &tm, cudaStream_t stream) {
   cfg.numAttrs = 2;
   static const char *const kNames[] = {"gemm_up", "gemm_down", "gemm_dh", "gemm_dx", "gemm_dw1", "gemm_dw2", "gemm_dw"};
   prof_begin(kNames[MODE], stream);
-  err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<MODE, BN, STAGES, MB>, tm, a);
+  err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<MODE, BN, STAGES, MB, DET>, tm, a);
   prof_end(stream);
   count_launch();
   if (err == cudaSuccess) err = cudaGetLastError();

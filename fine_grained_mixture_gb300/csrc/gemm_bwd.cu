@@ -4,12 +4,19 @@
 
 namespace moe {
 
-int launch_dh(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, int bn) {
+int launch_dh(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, int bn, bool det) {
+  if (det) {
+    if (bn == 256) return launch_gemm<kDH, 256, 4, 1, true>(a, tm, s);
+    return launch_gemm<kDH, 128, 4, 1, true>(a, tm, s);
+  }
   if (bn == 256) return launch_gemm<kDH, 256, 4>(a, tm, s);
   return launch_gemm<kDH, 128, 4>(a, tm, s);
 }
 
-int launch_dx(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) { return launch_gemm<kDX, 256, 3>(a, tm, s); }
+int launch_dx(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, bool det) {
+  if (det) return launch_gemm<kDX, 256, 3, 1, true>(a, tm, s);
+  return launch_gemm<kDX, 256, 3>(a, tm, s);
+}
 
 // 256-row M blocks (see Smem) when the weight's row count allows it and the experts' K loops are long
 // enough to hide the unoverlapped epilogue; else 128-row blocks with double-buffered TMEM.

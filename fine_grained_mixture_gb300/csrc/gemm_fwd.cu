@@ -6,7 +6,8 @@ namespace moe {
 
 int launch_up(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) { return launch_gemm<kUp, 256, 4>(a, tm, s); }
 
-int launch_down(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) {
+int launch_down(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, bool det) {
+  if (det) return launch_gemm<kDown, 256, 3, 1, true>(a, tm, s);
   return launch_gemm<kDown, 256, 3>(a, tm, s);
 }
 

@@ -72,7 +72,9 @@ struct GemmArgs {
   void *out0;        // up: H;  dH: dH;  dW1/dW2: the weight gradient (both in one launch: dW1)
   void *out1;        // up: A;  dH: s*A;  both weight gradients in one launch: dW2
   float *out_f32;    // down: fp32 O;  dX~: fp32 dX
+  long long *out_i64;  // deterministic down / dX~: the fixed-point accumulator of O or dX
   float *dS;         // dH: per-row dS
+  float *dS_part;    // deterministic dH: per-row, per-column-tile partial dS [p_cap][n / BN]
   const void *Hin;   // dH: cached H
   const void *gsrc;  // the operand gathered by token id: X (up, dW1) or dO (dH, dW2), bf16 rows
   const void *gsrc2; // both weight gradients in one launch: dO (gsrc is X)
@@ -92,10 +94,11 @@ int make_tmap_bf16_epi(CUtensorMap *tm, const void *base, uint64_t inner, uint64
 
 int num_sms();
 
+// det: deterministic aggregation (fixed-point accumulators, dS partials per column tile)
 int launch_up(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s);
-int launch_down(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s);
-int launch_dh(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, int bn);
-int launch_dx(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s);
+int launch_down(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, bool det);
+int launch_dh(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, int bn, bool det);
+int launch_dx(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, bool det);
 int launch_dw1(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s);
 int launch_dw2(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s);
 // Both weight gradients in one launch (256-row blocks; d and n multiples of 256).
@@ -103,6 +106,10 @@ int launch_dw12(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s);
 
 // elementwise (elementwise.cu)
 int launch_f32_to_bf16(const float *src, void *dst, size_t count, cudaStream_t s);
+// The fixed-point accumulator of the deterministic aggregation (32 fractional bits) to bf16.
+int launch_fixed_to_bf16(const long long *src, void *dst, size_t count, cudaStream_t s);
+// dS[r] = sum over the column tiles, in tile order, of the deterministic dH epilogue's partials [p_cap][tiles].
+int launch_ds_sum(const float *part, int tiles, const int32_t *offsets, int E, float *dS, cudaStream_t s);
 // Zeroes rows [offsets[E], p_cap) of two bf16 row-major buffers with row lengths ld_a and ld_b.
 int launch_zero_tail(void *a, void *b, const int32_t *offsets, int E, size_t p_cap, int ld_a, int ld_b,
                      cudaStream_t s);

@@ -21,6 +21,7 @@ MOE_ROUTE_TR_STOCHASTIC = 4
 MOE_ROUTE_EC = 5
 M_TILE = 128
 STATUS_WORDS = 4
+MOE_FLAG_DETERMINISTIC = 1  # bitwise-reproducible aggregation (fixed-point accumulators)
 # token choice; token rounding to the nearest tile, always up, always down, stochastically; expert choice
 MODES = {"tc": MOE_ROUTE_TC, "tr": MOE_ROUTE_TR, "tr_up": MOE_ROUTE_TR_UP, "tr_down": MOE_ROUTE_TR_DOWN,
          "tr_stoch": MOE_ROUTE_TR_STOCHASTIC, "ec": MOE_ROUTE_EC}
@@ -28,7 +29,7 @@ MODES = {"tc": MOE_ROUTE_TC, "tr": MOE_ROUTE_TR, "tr_up": MOE_ROUTE_TR_UP, "tr_d
 ERRORS = {
     0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_WORKSPACE",
     4: "MOE_ERR_CUDA", 5: "MOE_ERR_NONFINITE_LOGITS", 6: "MOE_ERR_DEVICE_TIMEOUT", 7: "MOE_ERR_BAD_METADATA",
-    8: "MOE_ERR_DEVICE",
+    8: "MOE_ERR_DEVICE", 9: "MOE_ERR_RANGE",
 }
 
 
@@ -67,6 +68,12 @@ def library() -> ctypes.CDLL:
     lib.moe_route_ex.argtypes = [_vp, _vp, _c_int, _c_int, _c_int, _c_int, ctypes.POINTER(moe_routing), _vp, _c_size,
                                  ctypes.POINTER(ctypes.c_int32), _vp]
     lib.moe_forward_workspace_size.argtypes = [_c_int] * 5 + [_c_size, sz]
+    lib.moe_forward_workspace_size_ex.argtypes = [_c_int] * 5 + [_c_size, ctypes.c_uint, sz]
+    lib.moe_backward_workspace_size_ex.argtypes = [_c_int] * 5 + [_c_size, ctypes.c_uint, sz]
+    lib.moe_forward_ex.argtypes = [_vp, _vp, _vp, ctypes.POINTER(moe_routing)] + [_c_int] * 5 + [
+        _c_size, _vp, _vp, _vp, _c_size, ctypes.c_uint, _vp]
+    lib.moe_backward_ex.argtypes = [_vp] * 5 + [ctypes.POINTER(moe_routing)] + [_c_int] * 5 + [_c_size] + [_vp] * 5 + [
+        _c_size, ctypes.c_uint, _vp]
     lib.moe_forward.argtypes = [_vp, _vp, _vp, ctypes.POINTER(moe_routing)] + [_c_int] * 5 + [_c_size, _vp, _vp, _vp,
                                                                                               _c_size, _vp]
     lib.moe_backward_workspace_size.argtypes = [_c_int] * 5 + [_c_size, sz]
@@ -93,7 +100,8 @@ def library() -> ctypes.CDLL:
         getattr(lib, f).restype = _c_int
     for f in ("moe_route_capacity", "moe_route_workspace_size", "moe_route", "moe_route_ex", "moe_forward_workspace_size",
               "moe_forward", "moe_backward_workspace_size", "moe_backward", "moe_get_status", "moe_last_cuda_error",
-              "moe_router_forward", "moe_router_backward_workspace_size", "moe_router_backward"):
+              "moe_router_forward", "moe_router_backward_workspace_size", "moe_router_backward",
+              "moe_forward_workspace_size_ex", "moe_backward_workspace_size_ex", "moe_forward_ex", "moe_backward_ex"):
         getattr(lib, f).restype = _c_int
     _LIB = lib
     return lib
@@ -145,16 +153,17 @@ def moe_route_workspace_size(T: int, E: int, K: int, mode="tc") -> int:
     return out.value
 
 
-def moe_forward_workspace_size(T, d, n, E, K, p_cap) -> int:
+def moe_forward_workspace_size(T, d, n, E, K, p_cap, flags: int = 0) -> int:
     out = _c_size(0)
-    _check(library().moe_forward_workspace_size(T, d, n, E, K, p_cap, ctypes.byref(out)), "moe_forward_workspace_size")
+    _check(library().moe_forward_workspace_size_ex(T, d, n, E, K, p_cap, flags, ctypes.byref(out)),
+           "moe_forward_workspace_size_ex")
     return out.value
 
 
-def moe_backward_workspace_size(T, d, n, E, K, p_cap) -> int:
+def moe_backward_workspace_size(T, d, n, E, K, p_cap, flags: int = 0) -> int:
     out = _c_size(0)
-    _check(library().moe_backward_workspace_size(T, d, n, E, K, p_cap, ctypes.byref(out)),
-           "moe_backward_workspace_size")
+    _check(library().moe_backward_workspace_size_ex(T, d, n, E, K, p_cap, flags, ctypes.byref(out)),
+           "moe_backward_workspace_size_ex")
     return out.value
 
 
@@ -207,8 +216,10 @@ def moe_route(logits: torch.Tensor, K: int, mode="tc", routing: Routing | None =
     return (routing, P.value) if want_P else routing
 
 
-def moe_forward(X, W1, W2, routing: Routing, O=None, H=None, ws=None, stream=None):
-    """O = sum_k s_k SwiGLU(X W1_e) W2_e; returns (O [T, d] bf16, H [P_cap, 2n] bf16)."""
+def moe_forward(X, W1, W2, routing: Routing, O=None, H=None, ws=None, stream=None, deterministic=False):
+    """O = sum_k s_k SwiGLU(X W1_e) W2_e; returns (O [T, d] bf16, H [P_cap, 2n] bf16).
+
+    deterministic: fixed-point aggregation, bitwise identical results on every run."""
     T, d = X.shape
     E, _, n2 = W1.shape
     n = n2 // 2
@@ -219,17 +230,21 @@ def moe_forward(X, W1, W2, routing: Routing, O=None, H=None, ws=None, stream=Non
     _need(W2, "W2", bf, E * n * d)
     O = torch.empty((T, d), dtype=bf, device=X.device) if O is None else O
     H = torch.empty((p_cap, n2), dtype=bf, device=X.device) if H is None else H
-    need = moe_forward_workspace_size(T, d, n, E, K, p_cap)
+    flags = MOE_FLAG_DETERMINISTIC if deterministic else 0
+    need = moe_forward_workspace_size(T, d, n, E, K, p_cap, flags)
     ws = torch.empty(need, dtype=torch.uint8, device=X.device) if ws is None else ws
     _need(O, "O", bf, T * d)
     _need(H, "H", bf, p_cap * n2)
-    _check(library().moe_forward(_ptr(X), _ptr(W1), _ptr(W2), ctypes.byref(routing.struct), T, d, n, E, K, p_cap,
-                                 _ptr(O), _ptr(H), _ptr(ws), ws.numel(), _stream(stream)), "moe_forward")
+    _check(library().moe_forward_ex(_ptr(X), _ptr(W1), _ptr(W2), ctypes.byref(routing.struct), T, d, n, E, K, p_cap,
+                                    _ptr(O), _ptr(H), _ptr(ws), ws.numel(), flags, _stream(stream)), "moe_forward_ex")
     return O, H
 
 
-def moe_backward(dO, X, W1, W2, H, routing: Routing, dX=None, dW1=None, dW2=None, dS=None, ws=None, stream=None):
-    """Gradients for upstream dO; returns (dX [T, d], dW1 [E, d, 2n], dW2 [E, n, d], dS [P_cap] fp32)."""
+def moe_backward(dO, X, W1, W2, H, routing: Routing, dX=None, dW1=None, dW2=None, dS=None, ws=None, stream=None,
+                 deterministic=False):
+    """Gradients for upstream dO; returns (dX [T, d], dW1 [E, d, 2n], dW2 [E, n, d], dS [P_cap] fp32).
+
+    deterministic: fixed-point aggregation of dX and ordered dS sums, bitwise identical results on every run."""
     T, d = X.shape
     E, _, n2 = W1.shape
     n = n2 // 2
@@ -242,11 +257,12 @@ def moe_backward(dO, X, W1, W2, H, routing: Routing, dX=None, dW1=None, dW2=None
     dW1 = torch.empty((E, d, n2), dtype=bf, device=dev) if dW1 is None else dW1
     dW2 = torch.empty((E, n, d), dtype=bf, device=dev) if dW2 is None else dW2
     dS = torch.empty(p_cap, dtype=torch.float32, device=dev) if dS is None else dS
-    need = moe_backward_workspace_size(T, d, n, E, K, p_cap)
+    flags = MOE_FLAG_DETERMINISTIC if deterministic else 0
+    need = moe_backward_workspace_size(T, d, n, E, K, p_cap, flags)
     ws = torch.empty(need, dtype=torch.uint8, device=dev) if ws is None else ws
-    _check(library().moe_backward(_ptr(dO), _ptr(X), _ptr(W1), _ptr(W2), _ptr(H), ctypes.byref(routing.struct),
-                                  T, d, n, E, K, p_cap, _ptr(dX), _ptr(dW1), _ptr(dW2), _ptr(dS), _ptr(ws),
-                                  ws.numel(), _stream(stream)), "moe_backward")
+    _check(library().moe_backward_ex(_ptr(dO), _ptr(X), _ptr(W1), _ptr(W2), _ptr(H), ctypes.byref(routing.struct),
+                                     T, d, n, E, K, p_cap, _ptr(dX), _ptr(dW1), _ptr(dW2), _ptr(dS), _ptr(ws),
+                                     ws.numel(), flags, _stream(stream)), "moe_backward_ex")
     return dX, dW1, dW2, dS
 
 

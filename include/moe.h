@@ -43,7 +43,8 @@ enum moe_status_code {
   MOE_ERR_NONFINITE_LOGITS = 5,   /* device: a router logit is NaN or +-inf                             */
   MOE_ERR_DEVICE_TIMEOUT = 6,     /* device: a bounded pipeline wait ran out; the kernel returned early */
   MOE_ERR_BAD_METADATA = 7,       /* device: a row's token id or an offset is out of range              */
-  MOE_ERR_DEVICE = 8              /* current device is not compute capability 10.3 (GB300)              */
+  MOE_ERR_DEVICE = 8,             /* current device is not compute capability 10.3 (GB300)              */
+  MOE_ERR_RANGE = 9               /* device: deterministic mode met a contribution of magnitude >= 2^21 */
 };
 
 /*
@@ -154,6 +155,8 @@ int moe_route_noalloc(const float *logits, int T, int E, int K, int mode, const 
 
 /* Forward scratch: A [P_cap, n] bf16 and the fp32 accumulation buffer of O [T, d]. */
 int moe_forward_workspace_size(int T, int d, int n, int E, int K, size_t p_cap, size_t *bytes);
+/* Same for the given flags (MOE_FLAG_DETERMINISTIC: the accumulation buffer of O holds 64-bit integers). */
+int moe_forward_workspace_size_ex(int T, int d, int n, int E, int K, size_t p_cap, unsigned flags, size_t *bytes);
 
 /*
  * moe_forward - O = sum_k s_k SwiGLU(X W1_e) W2_e  ("Method details / overall framework").
@@ -168,9 +171,27 @@ int moe_forward_workspace_size(int T, int d, int n, int E, int K, size_t p_cap, 
 int moe_forward(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const moe_routing *r, int T,
                 int d, int n, int E, int K, size_t p_cap, moe_bf16 *O, moe_bf16 *H, void *ws,
                 size_t ws_bytes, void *stream);
+/* moe_forward with flags (0 or MOE_FLAG_DETERMINISTIC); ws sized by moe_forward_workspace_size_ex. */
+int moe_forward_ex(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const moe_routing *r, int T, int d,
+                   int n, int E, int K, size_t p_cap, moe_bf16 *O, moe_bf16 *H, void *ws, size_t ws_bytes,
+                   unsigned flags, void *stream);
+
+/*
+ * Deterministic aggregation (flag of moe_forward_ex / moe_backward_ex; the pages have no counterpart: they
+ * leave the order of the aggregation's additions open).  O and dX sum a token's rows from different experts,
+ * whose contributions land in whatever order the GPU schedules them; fp32 addition depends on that order, so the
+ * default path can differ in the last bits from run to run.  With this flag every contribution is added as a
+ * 64-bit fixed-point integer with 32 fractional bits (integer addition does not depend on order) and dS sums its
+ * per-column-tile partials in a fixed order: O, H, dX, dW1, dW2 and dS are then bitwise identical on every run.
+ * Cost: twice the reduce-add bytes and accumulator memory.  Range: one contribution s_r * y_r (or a row of
+ * dH W1^T) must stay below 2^21 in magnitude, else MOE_ERR_RANGE in the status block.
+ */
+#define MOE_FLAG_DETERMINISTIC 1u
 
 /* Backward scratch: dH [P_cap, 2n] bf16, s*A [P_cap, n] bf16 and the fp32 accumulation buffer of dX. */
 int moe_backward_workspace_size(int T, int d, int n, int E, int K, size_t p_cap, size_t *bytes);
+/* Same for the given flags (MOE_FLAG_DETERMINISTIC adds the dS partials and a 64-bit dX accumulator). */
+int moe_backward_workspace_size_ex(int T, int d, int n, int E, int K, size_t p_cap, unsigned flags, size_t *bytes);
 
 /*
  * moe_backward - gradients of the layer for upstream gradient dO, routing held fixed
@@ -184,6 +205,10 @@ int moe_backward(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, cons
                  const moe_bf16 *H, const moe_routing *r, int T, int d, int n, int E, int K, size_t p_cap,
                  moe_bf16 *dX, moe_bf16 *dW1, moe_bf16 *dW2, float *dS, void *ws, size_t ws_bytes,
                  void *stream);
+/* moe_backward with flags (0 or MOE_FLAG_DETERMINISTIC); ws sized by moe_backward_workspace_size_ex. */
+int moe_backward_ex(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const moe_bf16 *H,
+                    const moe_routing *r, int T, int d, int n, int E, int K, size_t p_cap, moe_bf16 *dX, moe_bf16 *dW1,
+                    moe_bf16 *dW2, float *dS, void *ws, size_t ws_bytes, unsigned flags, void *stream);
 
 /*
  * The router on either side of the layer ("Method details / overall framework": router scoring of the input

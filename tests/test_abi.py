@@ -73,6 +73,20 @@ def test_layer_validation(lib, shape, code):
     assert lib.moe_backward_workspace_size(*shape, ctypes.byref(out)) == code
 
 
+def test_deterministic_flag_queries(lib):
+    p = moe.moe_route_capacity(512, 8, 2, "tc")
+    base_f = moe.moe_forward_workspace_size(512, 256, 128, 8, 2, p)
+    base_b = moe.moe_backward_workspace_size(512, 256, 512, 8, 2, p)
+    assert moe.moe_forward_workspace_size(512, 256, 128, 8, 2, p, moe.MOE_FLAG_DETERMINISTIC) >= base_f + 512 * 256 * 4
+    # 64-bit dX accumulator and the dS partials of two 256-wide column tiles
+    assert moe.moe_backward_workspace_size(512, 256, 512, 8, 2, p, moe.MOE_FLAG_DETERMINISTIC) >= \
+        base_b + 512 * 256 * 4 + p * 2 * 4
+    out = ctypes.c_size_t(0)
+    assert lib.moe_forward_workspace_size_ex(512, 256, 128, 8, 2, p, 2, ctypes.byref(out)) == 1   # unknown flag
+    assert lib.moe_backward_workspace_size_ex(512, 256, 128, 8, 2, p, 6, ctypes.byref(out)) == 1
+    assert lib.moe_strerror(9) == b"value beyond the deterministic accumulator's range"
+
+
 def test_null_arguments_rejected_before_any_device_work(lib):
     r = moe.moe.moe_routing()
     assert lib.moe_route(None, 16, 8, 2, 0, ctypes.byref(r), None, 0, None, None) == 1
