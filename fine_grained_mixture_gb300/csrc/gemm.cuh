@@ -52,7 +52,6 @@ struct Traits {
   static constexpr bool nt_outer_ = (MODE == kDown || MODE == kDX);
   // the scatter-add GEMMs drain TMEM with eight warps (two per TMEM lane quarter, half the columns each)
   static constexpr int epi_warps = nt_outer_ ? 8 : 4;
-  static constexpr int threads = gather ? 320 : 64 + 32 * epi_warps;
   static constexpr bool a_mn = varlen_k;  // A operand MN-major in shared memory
   static constexpr bool b_mn = (MODE == kUp || MODE == kDown || varlen_k);
   static constexpr bool nt_outer = (MODE == kDown || MODE == kDX);  // keep one fp32 column slab hot in L2
@@ -99,12 +98,24 @@ constexpr int kUpWarpBytes = 6144;
 // drained by TMA stores, one box in flight while the next is written.
 constexpr int kDwWarpBytes = 2 * 2048;
 
-template <int MODE>
+// Epilogue warps: the weight-gradient GEMMs with 256-row blocks drain their single (unoverlapped) 256 x 256
+// accumulator with eight warps, one 128-row block per group of four (warps 2..5 and 10..13).
+template <int MODE, int MB>
+__host__ __device__ constexpr int epi_warps() {
+  return (Traits<MODE>::varlen_k && MB == 2) ? 8 : Traits<MODE>::epi_warps;
+}
+
+template <int MODE, int MB>
+__host__ __device__ constexpr int cta_threads() {
+  return Traits<MODE>::gather ? 192 + 32 * epi_warps<MODE, MB>() : 64 + 32 * epi_warps<MODE, MB>();
+}
+
+template <int MODE, int MB = 1>
 __host__ __device__ constexpr int epi_bytes() {
   return Traits<MODE>::nt_outer ? kStgBytes
          : MODE == kDH          ? 4 * kDhWarpBytes
          : MODE == kUp          ? 4 * kUpWarpBytes
-         : Traits<MODE>::varlen_k ? 4 * kDwWarpBytes
+         : Traits<MODE>::varlen_k ? epi_warps<MODE, MB>() * kDwWarpBytes
                                   : 0;
 }
 
@@ -282,13 +293,15 @@ __device__ __forceinline__ long long to_fixed(float x, bool &range_ok) {
 }
 
 template <int MODE, int BN, int STAGES, int MB, bool DET>
-__global__ void __launch_bounds__(Traits<MODE>::threads, 1)
+__global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
     moe_gemm_kernel(const __grid_constant__ TensorMaps tm, const GemmArgs a) {
   const CUtensorMap &tmA = tm.a;
   const CUtensorMap &tmB = tm.b;
   using TR = Traits<MODE>;
-  using SM = Smem<BN, STAGES, epi_bytes<MODE>(), MB, tile_cache_bytes<MODE>()>;
+  using SM = Smem<BN, STAGES, epi_bytes<MODE, MB>(), MB, tile_cache_bytes<MODE>()>;
   static_assert(MODE != kDW || (MB == 2 && BN == 256), "merged weight gradients: A and B stages of equal size");
+  constexpr int kEpiWarps = epi_warps<MODE, MB>();
+  static_assert(cta_threads<MODE, MB>() <= 448, "one CTA per SM at up to 146 registers a thread");
   constexpr int kBufs = MB == 1 ? 2 : 1;           // TMEM accumulator buffers (double-buffered when MB = 1)
   constexpr uint32_t kTmemCols = 2 * BN;            // MB * BN * kBufs == 2 * BN in both layouts
   static_assert(MB * kBufs == 2, "TMEM holds two BN-column accumulators");
@@ -318,7 +331,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), TR::epi_warps);
+      mbar_init(tempty_bar(b), kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     if (MODE == kDH)
@@ -450,7 +463,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
         }
       }
     }
-  } else if (TR::gather && warp >= 6) {
+  } else if (TR::gather && warp >= 6 && warp < 10) {
     // --------------------------------------------------------------- cp.async token-row gatherers
     const int gt = threadIdx.x - 192;  // 0..127
     const int j = gt & 7;              // 16-byte piece of a 128-byte row segment
@@ -597,9 +610,13 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
         *abort_flag = 1;
       }
     }
-  } else if (warp >= 2 && warp < 2 + TR::epi_warps) {
+  } else if (TR::gather ? ((warp >= 2 && warp < 6) || (kEpiWarps == 8 && warp >= 10 && warp < 14))
+                        : (warp >= 2 && warp < 2 + kEpiWarps)) {
     // ---------------------------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // weight gradients with eight epilogue warps: warps 2..5 drain M block 0, warps 10..13 M block 1
+    const int mb_lo = (TR::varlen_k && kEpiWarps == 8 && warp >= 10) ? 1 : 0;
+    const int mb_hi = (TR::varlen_k && kEpiWarps == 8) ? mb_lo + 1 : MB;
     const int row = q * 32 + lane;
     int buf = 0;
     uint32_t bph = 0;
@@ -614,7 +631,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
       uint8_t *dw_out = static_cast<uint8_t *>((MODE == kDW && t.w2) ? a.out1 : a.out0);
       if (t.kblocks == 0) {
         if (TR::varlen_k) {  // an expert without rows has an exactly zero weight gradient
-          for (int mb = 0; mb < MB; ++mb) {
+          for (int mb = mb_lo; mb < mb_hi; ++mb) {
             uint8_t *dst = dw_out + (((size_t)t.e * dw_m + t.m0 + mb * kBM + row) * dw_n + t.n0) * 2;
             for (int c = 0; c < BN * 2; c += 16) st_v4(dst + c, 0u, 0u, 0u, 0u);
           }
@@ -880,30 +897,43 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
       } else {
         // weight gradients: bf16 rows of dW_e (M block mb sits in TMEM columns [mb * BN, (mb + 1) * BN)), stored
         // as 32 x 32 boxes of the [E * M, N] output view through two staging tiles per warp
+        // Two 32-column chunks per TMEM wait, stored as two boxes from the warp's two staging tiles.
         const CUtensorMap *omap = (MODE == kDW && t.w2) ? &tm.sa : &tm.dh;
-        const uint32_t stg = base + SM::kStgOff + q * kDwWarpBytes;
+        const int ew = (warp >= 10) ? 4 + q : q;  // this warp's staging slot
+        const uint32_t stg = base + SM::kStgOff + ew * kDwWarpBytes;
         const int sw = (lane >> 1) & 3;  // 64-byte swizzle
 #pragma unroll 1
-        for (int cc = 0; cc < MB * (BN / 32); ++cc) {
-          const int mb = cc / (BN / 32), c = cc % (BN / 32);
-          uint32_t v[32];
-          tmem_ld32(tacc + mb * BN + c * 32, v);
-          tmem_ld_wait();
-          uint32_t p[16];
+        for (int mb = mb_lo; mb < mb_hi; ++mb) {
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; c += 2) {
+            uint32_t v0[32], v1[32];
+            tmem_ld32(tacc + mb * BN + c * 32, v0);
+            tmem_ld32(tacc + mb * BN + (c + 1) * 32, v1);
+            tmem_ld_wait();
+            uint32_t p0[16], p1[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-          const uint32_t buf_st = stg + (cc & 1) * 2048;
-          if (lane == 0) bulk_wait_read<1>();  // the box stored from this tile two chunks ago has been read
-          __syncwarp();
+            for (int i = 0; i < 16; ++i) {
+              p0[i] = pack_bf16x2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
+              p1[i] = pack_bf16x2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
+            }
+            if (lane == 0) bulk_wait_read<0>();  // the previous pair of boxes has been read from both tiles
+            __syncwarp();
 #pragma unroll
-          for (int w = 0; w < 4; ++w)
-            st_shared_v4(buf_st + lane * 64 + ((w ^ sw) << 4), __uint_as_float(p[4 * w]), __uint_as_float(p[4 * w + 1]),
-                         __uint_as_float(p[4 * w + 2]), __uint_as_float(p[4 * w + 3]));
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(omap, buf_st, t.n0 + c * 32, t.e * dw_m + t.m0 + mb * kBM + q * 32, policy_evict_first());
-            bulk_commit();
+            for (int w = 0; w < 4; ++w) {
+              const uint32_t o = lane * 64 + ((w ^ sw) << 4);
+              st_shared_v4(stg + o, __uint_as_float(p0[4 * w]), __uint_as_float(p0[4 * w + 1]),
+                           __uint_as_float(p0[4 * w + 2]), __uint_as_float(p0[4 * w + 3]));
+              st_shared_v4(stg + 2048 + o, __uint_as_float(p1[4 * w]), __uint_as_float(p1[4 * w + 1]),
+                           __uint_as_float(p1[4 * w + 2]), __uint_as_float(p1[4 * w + 3]));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const int orow = t.e * dw_m + t.m0 + mb * kBM + q * 32;
+              tma_store_2d(omap, stg, t.n0 + c * 32, orow, policy_evict_first());
+              tma_store_2d(omap, stg + 2048, t.n0 + (c + 1) * 32, orow, policy_evict_first());
+              bulk_commit();
+            }
           }
         }
       }
@@ -934,7 +964,7 @@ __global__ void __launch_bounds__(Traits<MODE>::threads, 1)
 // Host launcher for one instantiation: clusters of two CTAs, one CTA per SM, as many clusters as fit.
 template <int MODE, int BN, int STAGES, int MB = 1, bool DET = false>
 int launch_gemm(const GemmArgs &a, const TensorMaps &tm, cudaStream_t stream) {
-  using SM = Smem<BN, STAGES, epi_bytes<MODE>(), MB, tile_cache_bytes<MODE>()>;
+  using SM = Smem<BN, STAGES, epi_bytes<MODE, MB>(), MB, tile_cache_bytes<MODE>()>;
   static int attr_dev = -1;
   static int grid_cache = 0;
   int dev = 0;
@@ -948,7 +978,7 @@ int launch_gemm(const GemmArgs &a, const TensorMaps &tm, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.blockDim = dim3(Traits<MODE>::threads, 1, 1);
+  cfg.blockDim = dim3(cta_threads<MODE, MB>(), 1, 1);
   cfg.dynamicSmemBytes = SM::kBytes;
   cfg.stream = stream;
   cfg.attrs = attr;

@@ -475,12 +475,13 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
   };
   auto is_tc = [&](int t) { return ((mem[t >> 5] >> (t & 31)) & 1u) != 0u; };
   auto first = [&](int t) { return ec || is_tc(t); };  // ranked ahead of the other tokens
+  int nlist = -1;  // candidates listed in list[] (-1: not listed)
   if (r != f) {
     // Candidates are few next to T: the expert's token-choice tokens when dropping, and when padding the
     // other tokens in the top-byte bin of the boundary.  Once they are listed, the remaining radix passes
     // walk the list instead of all T tokens (all T when the list would overflow its space, or under expert
     // choice, where every token is a candidate).
-    int nlist = (drop && !ec) ? build_list(is_tc) : -1;
+    nlist = (drop && !ec) ? build_list(is_tc) : -1;
     int *my_hist = hist + (warp >> 2) * 256;
     for (int shift = 24; shift >= 0; shift -= 8) {
       for (int i = threadIdx.x; i < kTrHists * 256; i += blockDim.x) hist[i] = 0;
@@ -530,61 +531,115 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
       prefix |= static_cast<uint32_t>(sel_state[0]) << shift;
       mask |= 255u << shift;
       remaining = sel_state[1];
-      if (!drop && shift == 24) {
+      if (shift == 24 && (!drop || nlist < 0)) {
+        // the candidates whose top byte is at or above the boundary's: every candidate that can still be kept
+        // (when padding, or when the first list would not fit or was not built, as under expert choice)
         const uint32_t top = prefix;
-        nlist = build_list([&](int t) { return !first(t) && (key[t] & 0xff000000u) == top; });
+        nlist = build_list([&](int t) { return first(t) == drop && (key[t] & 0xff000000u) >= top; });
       }
     }
   }
   // prefix = key of the R-th best candidate; `remaining` candidates equal to it are kept, lowest token first.
+  // the row of kept token t at position pos: its token-choice slot (if any) and its gate
+  auto write_row = [&](int pos, int t) {
+    int slot = -1;
+    if ((mem[t >> 5] >> (t & 31)) & 1u) {
+      for (int k = 0; k < K; ++k)
+        if (topk_idx[(size_t)t * K + k] == e) slot = k;
+    }
+    const float sc = (slot >= 0 && !ec) ? topk_score[(size_t)t * K + slot]
+                                        : expf(key_to_float(key[t]) - tok_max[t]) / tok_den[t];
+    row_token[pos] = t;
+    row_slot[pos] = slot;
+    row_score[pos] = sc;
+  };
   const int span = ((T + kTrThreads - 1) / kTrThreads) * 32;  // tokens per warp, a multiple of 32
   const int t_lo = warp * span;
   const uint32_t lt_mask = (1u << lane) - 1u;
-  // pass 1: ties (candidates whose key equals the boundary key) per warp
-  int eq_count = 0;
-  if (r != f) {
+  int keep_count = 0;  // kept tokens in this warp's token range
+  if (r == f || nlist >= 0) {
+    // Keep masks word by word (32 tokens a word): tokens ranked first are kept whole unless dropping; listed
+    // candidates above the boundary key are kept; of those equal to it, the first `remaining` in token order.
+    // Each thread owns a contiguous run of words, so one block scan of popcounts ranks the ties.
+    uint32_t *tie = reinterpret_cast<uint32_t *>(hist);  // the radix histograms are free (8 x 256 >= T / 32 words)
+    const int per = (member_words + kTrThreads - 1) / kTrThreads;
+    const int w0 = threadIdx.x * per, w1 = min(member_words, w0 + per);
+    for (int w = w0; w < w1; ++w) {
+      uint32_t m = 0u;
+      if (r == f || !drop) {
+        if (ec) m = (32 * w + 32 <= T) ? 0xffffffffu : ((1u << (T - 32 * w)) - 1u);
+        else m = mem[w];
+      }
+      keep_bits[w] = m;
+      tie[w] = 0u;
+    }
+    __syncthreads();
+    if (r != f) {
+      for (int i = threadIdx.x; i < nlist; i += blockDim.x) {
+        const int t = list[i];
+        const uint32_t k = key[t];
+        if (k > prefix) atomicOr(&keep_bits[t >> 5], 1u << (t & 31));
+        else if (k == prefix) atomicOr(&tie[t >> 5], 1u << (t & 31));
+      }
+      __syncthreads();
+      int ties = 0, total;
+      for (int w = w0; w < w1; ++w) ties += __popc(tie[w]);
+      int rank = block_exclusive_scan(ties, scratch, &total);
+      for (int w = w0; w < w1; ++w) {
+        uint32_t m = tie[w];
+        while (m) {
+          const uint32_t bit = m & (0u - m);
+          if (rank < remaining) keep_bits[w] |= bit;
+          ++rank;
+          m ^= bit;
+        }
+      }
+    }
+    __syncthreads();
+    // this warp's kept tokens: its words' popcounts (lane i takes words i, i + 32, ...)
+    for (int t0 = t_lo + 32 * lane; t0 < t_lo + span && t0 < T; t0 += 32 * 32) keep_count += __popc(keep_bits[t0 >> 5]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) keep_count += __shfl_xor_sync(0xffffffffu, keep_count, off);
+  } else {
+    // Token-order passes, for candidate sets too large for the list.
+    // pass 1: ties (candidates whose key equals the boundary key) per warp
+    int eq_count = 0;
     for (int t0 = t_lo; t0 < t_lo + span && t0 < T; t0 += 32) {
       const int t = t0 + lane;
       bool eq = false;
       if (t < T) eq = (first(t) == drop) && key[t] == prefix;
       eq_count += __popc(__ballot_sync(0xffffffffu, eq));
     }
-  }
-  if (lane == 0) warp_tot[warp] = eq_count;
-  __syncthreads();
-  if (warp == 0) {
-    int tot;
-    const int b = warp_scan_exclusive(warp_tot[lane], &tot);
-    warp_base[lane] = b;
-  }
-  __syncthreads();
-  // pass 2: keep decisions in token order; the kept bits of each 32-token group go to shared memory
-  int eq_run = warp_base[warp];
-  int keep_count = 0;
-  for (int t0 = t_lo; t0 < t_lo + span && t0 < T; t0 += 32) {
-    const int t = t0 + lane;
-    bool tc = false, gt = false, eq = false;
-    if (t < T) {
-      tc = first(t);
-      if (r != f && tc == drop) {
-        const uint32_t k = key[t];
-        gt = k > prefix;
-        eq = k == prefix;
+    if (lane == 0) warp_tot[warp] = eq_count;
+    __syncthreads();
+    if (warp == 0) {
+      int tot;
+      const int b = warp_scan_exclusive(warp_tot[lane], &tot);
+      warp_base[lane] = b;
+    }
+    __syncthreads();
+    // pass 2: keep decisions in token order; the kept bits of each 32-token group go to shared memory
+    int eq_run = warp_base[warp];
+    for (int t0 = t_lo; t0 < t_lo + span && t0 < T; t0 += 32) {
+      const int t = t0 + lane;
+      bool tc = false, gt = false, eq = false;
+      if (t < T) {
+        tc = first(t);
+        if (tc == drop) {
+          const uint32_t k = key[t];
+          gt = k > prefix;
+          eq = k == prefix;
+        }
       }
-    }
-    const uint32_t eq_bal = __ballot_sync(0xffffffffu, eq);
-    const int eq_rank = eq_run + __popc(eq_bal & lt_mask);
-    eq_run += __popc(eq_bal);
-    bool keep;
-    if (r == f) {
-      keep = tc;
-    } else {
+      const uint32_t eq_bal = __ballot_sync(0xffffffffu, eq);
+      const int eq_rank = eq_run + __popc(eq_bal & lt_mask);
+      eq_run += __popc(eq_bal);
       const bool take = gt || (eq && eq_rank < remaining);
-      keep = drop ? take : (tc || take);
+      const bool keep = drop ? take : (tc || take);
+      const uint32_t kb = __ballot_sync(0xffffffffu, keep);
+      if (lane == 0) keep_bits[t0 >> 5] = kb;
+      keep_count += __popc(kb);
     }
-    const uint32_t kb = __ballot_sync(0xffffffffu, keep);
-    if (lane == 0) keep_bits[t0 >> 5] = kb;
-    keep_count += __popc(kb);
   }
   __syncthreads();
   if (lane == 0) warp_tot[warp] = keep_count;
@@ -595,25 +650,25 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
     warp_base[lane] = b;
   }
   __syncthreads();
-  // pass 3: rows in ascending token order
-  int row = base + warp_base[warp];
-  for (int t0 = t_lo; t0 < t_lo + span && t0 < T; t0 += 32) {
-    const uint32_t kb = keep_bits[t0 >> 5];
-    const int t = t0 + lane;
-    if ((kb >> lane) & 1u) {
-      const int pos = row + __popc(kb & lt_mask);
-      int slot = -1;
-      if ((mem[t >> 5] >> (t & 31)) & 1u) {
-        for (int k = 0; k < K; ++k)
-          if (topk_idx[(size_t)t * K + k] == e) slot = k;
-      }
-      const float sc = (slot >= 0 && !ec) ? topk_score[(size_t)t * K + slot]
-                                          : expf(key_to_float(key[t]) - tok_max[t]) / tok_den[t];
-      row_token[pos] = t;
-      row_slot[pos] = slot;
-      row_score[pos] = sc;
+  if (r <= list_cap) {
+    // pass 3: the kept tokens, compacted in token order into the candidate list (free again), then one thread per
+    // row, so the rows' global loads (slot, gate) are all in flight at once rather than chunk after chunk
+    int at = warp_base[warp];
+    for (int t0 = t_lo; t0 < t_lo + span && t0 < T; t0 += 32) {
+      const uint32_t kb = keep_bits[t0 >> 5];
+      if ((kb >> lane) & 1u) list[at + __popc(kb & lt_mask)] = t0 + lane;
+      at += __popc(kb);
     }
-    row += __popc(kb);
+    __syncthreads();
+    for (int i = threadIdx.x; i < r; i += blockDim.x) write_row(base + i, list[i]);
+  } else {
+    // pass 3 for an expert with more rows than the list holds: rows in ascending token order, warp by warp
+    int row = base + warp_base[warp];
+    for (int t0 = t_lo; t0 < t_lo + span && t0 < T; t0 += 32) {
+      const uint32_t kb = keep_bits[t0 >> 5];
+      if ((kb >> lane) & 1u) write_row(row + __popc(kb & lt_mask), t0 + lane);
+      row += __popc(kb);
+    }
   }
 }
 
