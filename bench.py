@@ -347,7 +347,9 @@ def load_traffic(kernel, workload):
 GEMM_NAMES = ["gemm_up", "gemm_down", "gemm_dh", "gemm_dx", "gemm_dw1", "gemm_dw2", "gemm_dw"]
 NCU_NAMES = [("route_topk_kernel", "route_topk"), ("route_scan_kernel", "route_scan"),
              ("route_fill_tc_kernel", "route_fill_tc"), ("route_fill_tr_kernel", "route_fill_tr"),
-             ("f32_to_bf16_kernel", "cast_f32_bf16"), ("zero_tail_kernel", "zero_tail")]
+             ("f32_to_bf16_kernel", "cast_f32_bf16"), ("fixed_to_bf16_kernel", "cast_fixed_bf16"),
+             ("ds_sum_kernel", "ds_sum"), ("router_dz_rows_kernel", "router_dz_rows"),
+             ("router_dz_tokens_kernel", "router_dz_tokens")]
 UNIT_SCALE = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12, "ns": 1e-3, "us": 1.0, "ms": 1e3,
               "nsecond": 1e-3, "usecond": 1.0, "msecond": 1e3, "second": 1e6}
 

@@ -490,8 +490,6 @@ int moe_backward_ex(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, c
   rc = det ? launch_fixed_to_bf16(static_cast<long long *>(dXacc), dX, (size_t)T * d, side.side())
            : launch_f32_to_bf16(static_cast<float *>(dXacc), dX, (size_t)T * d, side.side());
   if (rc != MOE_OK) return rc;
-  // rows [P, P_cap) of dH and s*A are read as the zero tail of the last expert's k-blocks
-  if ((rc = launch_zero_tail(dH, sA, r->offsets, E, p_cap, 2 * n, n, s)) != MOE_OK) return rc;
   GemmArgs aw = base_args(r, T, d, n, E, p_cap);
   aw.wide_m = (int64_t)T * K >= (int64_t)1024 * E;  // experts average >= 1024 rows: >= 16 k-blocks per tile
   if (aw.wide_m && d % 256 == 0 && n % 256 == 0) {

@@ -1,7 +1,6 @@
 // elementwise.cu - the fp32 -> bf16 cast that finishes the fused aggregations (O and dX are accumulated
 // in fp32 by the down-projection and dX~ epilogues, then rounded once to bf16), its fixed-point counterpart and
-// the ordered dS sum of the deterministic mode, the zeroing of the rows past the last expert, and the
-// bounded-wait self-test.
+// the ordered dS sum of the deterministic mode, and the bounded-wait self-test.
 #include "common.cuh"
 #include "internal.h"
 
@@ -76,33 +75,6 @@ __global__ void __launch_bounds__(256) ds_sum_kernel(const float *__restrict__ p
 int launch_ds_sum(const float *part, int tiles, const int32_t *offsets, int E, float *dS, cudaStream_t s) {
   prof_begin("ds_sum", s);
   cudaError_t err = launch_pdl(ds_sum_kernel, dim3(num_sms() * 2), dim3(256), 0, s, part, tiles, offsets, E, dS);
-  prof_end(s);
-  count_launch();
-  if (err == cudaSuccess) err = cudaGetLastError();
-  return err == cudaSuccess ? MOE_OK : record_cuda_error(err);
-}
-
-__global__ void __launch_bounds__(256) zero_tail_kernel(uint4 *__restrict__ a, uint4 *__restrict__ b,
-                                                        const int32_t *__restrict__ offsets, int E, size_t p_cap,
-                                                        int ld_a, int ld_b) {
-  griddep_wait();
-  griddep_launch_dependents();
-  const size_t P = static_cast<size_t>(offsets[E]);
-  if (P >= p_cap) return;
-  const size_t va = ld_a / 8, vb = ld_b / 8;  // uint4 per row
-  const size_t na = (p_cap - P) * va, nb = (p_cap - P) * vb;
-  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < na + nb; i += (size_t)gridDim.x * blockDim.x) {
-    if (i < na) a[P * va + i] = z;
-    else b[P * vb + (i - na)] = z;
-  }
-}
-
-int launch_zero_tail(void *a, void *b, const int32_t *offsets, int E, size_t p_cap, int ld_a, int ld_b,
-                     cudaStream_t s) {
-  prof_begin("zero_tail", s);
-  cudaError_t err = launch_pdl(zero_tail_kernel, dim3(num_sms()), dim3(256), 0, s, static_cast<uint4 *>(a),
-                               static_cast<uint4 *>(b), offsets, E, p_cap, ld_a, ld_b);
   prof_end(s);
   count_launch();
   if (err == cudaSuccess) err = cudaGetLastError();

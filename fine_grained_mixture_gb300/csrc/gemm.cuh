@@ -777,6 +777,9 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
         const bool valid = r < t.row_end;
         const bool full_warp = t.row0 + q * 32 + 31 < t.row_end;  // all 32 rows belong to this expert
         const float sc = valid ? __ldg(&a.row_score[r]) : 0.f;
+        // rows past the last expert (up to the end of its last tile) get zeros: the weight-gradient GEMMs read
+        // them as the zero tail of that expert's last 64-row block
+        const bool zero_row = !valid && t.row_end == __ldg(&a.offsets[a.E]) && r < a.p_cap;
         const int wrow = t.row0 + q * 32;                          // first row of this warp's 32
         const uint32_t wbase = base + SM::kStgOff + q * kDhWarpBytes;
         const uint32_t out_st = wbase + 4096;                      // dH gate | dH up staging
@@ -885,6 +888,13 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
               st_v4(dhrow + (size_t)j * 2 + w * 16, dg[4 * w], dg[4 * w + 1], dg[4 * w + 2], dg[4 * w + 3]);
               st_v4(dhrow + (size_t)(a.n + j) * 2 + w * 16, du[4 * w], du[4 * w + 1], du[4 * w + 2], du[4 * w + 3]);
               st_v4(sarow + (size_t)j * 2 + w * 16, sa[4 * w], sa[4 * w + 1], sa[4 * w + 2], sa[4 * w + 3]);
+            }
+          } else if (zero_row) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              st_v4(dhrow + (size_t)j * 2 + w * 16, 0u, 0u, 0u, 0u);
+              st_v4(dhrow + (size_t)(a.n + j) * 2 + w * 16, 0u, 0u, 0u, 0u);
+              st_v4(sarow + (size_t)j * 2 + w * 16, 0u, 0u, 0u, 0u);
             }
           }
           __syncwarp();

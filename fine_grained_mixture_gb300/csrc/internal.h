@@ -110,8 +110,4 @@ int launch_f32_to_bf16(const float *src, void *dst, size_t count, cudaStream_t s
 int launch_fixed_to_bf16(const long long *src, void *dst, size_t count, cudaStream_t s);
 // dS[r] = sum over the column tiles, in tile order, of the deterministic dH epilogue's partials [p_cap][tiles].
 int launch_ds_sum(const float *part, int tiles, const int32_t *offsets, int E, float *dS, cudaStream_t s);
-// Zeroes rows [offsets[E], p_cap) of two bf16 row-major buffers with row lengths ld_a and ld_b.
-int launch_zero_tail(void *a, void *b, const int32_t *offsets, int E, size_t p_cap, int ld_a, int ld_b,
-                     cudaStream_t s);
-
 }  // namespace moe
