@@ -445,7 +445,21 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
   const int f = ec ? T : tc_counts[e], r = counts[e], base = s_off[e];
   if (r == 0) return;
   for (int w = threadIdx.x; w < member_words; w += blockDim.x) mem[w] = member[(size_t)e * member_words + w];
-  if (keys_em) {
+  if (keys_em && (T & 3) == 0) {
+    // the expert's row of keys, 16 bytes a load and four loads in flight per thread before any store
+    const uint4 *src = reinterpret_cast<const uint4 *>(keys_em + (size_t)e * T);
+    uint4 *dst = reinterpret_cast<uint4 *>(key);
+    const int n4 = T >> 2;
+    for (int i0 = threadIdx.x; i0 < n4; i0 += 4 * kTrThreads) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i0 + u * kTrThreads < n4) v[u] = __ldcs(src + i0 + u * kTrThreads);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i0 + u * kTrThreads < n4) dst[i0 + u * kTrThreads] = v[u];
+    }
+  } else if (keys_em) {
     for (int t = threadIdx.x; t < T; t += blockDim.x) key[t] = __ldcs(&keys_em[(size_t)e * T + t]);
   } else {  // compact scratch: the expert's column of the logits, one strided word per token
     for (int t = threadIdx.x; t < T; t += blockDim.x) key[t] = order_key(logits[(size_t)t * E + e]);
@@ -486,7 +500,8 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
     for (int shift = 24; shift >= 0; shift -= 8) {
       for (int i = threadIdx.x; i < kTrHists * 256; i += blockDim.x) hist[i] = 0;
       __syncthreads();
-      // lanes that fall in the same bin add once (many keys share their leading bits)
+      // lanes that fall in the same bin add once (many keys share their leading bits); grouping the lanes
+      // with __match_any_sync measured faster than ballot rounds on the leading lane's bin
       const int n_iter = nlist >= 0 ? nlist : T;
       for (int i0 = 0; i0 < n_iter; i0 += blockDim.x) {
         const int i = i0 + threadIdx.x;
