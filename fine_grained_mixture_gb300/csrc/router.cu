@@ -12,8 +12,9 @@
 //
 // Kernels:
 //   router_gemm_kernel<kRLogits>  z = X W_r            M = T, N = E (128-column tiles), K = d
-//   router_dz_rows_kernel         one CTA per expert: dS_r s_r into dz[t, e] (each pair is unique) and into G_t
-//   router_dz_tokens_kernel       one warp per token: the normaliser term, dz in fp32 (output) and bf16
+//   router_dz_rows_kernel         one CTA per expert: dS_r s_r into dz[t, e] (each pair is unique)
+//   router_dz_tokens_kernel       one warp per token: G_t as the sum of its dz row (fixed order), the normaliser
+//                                 term, dz in fp32 (output) and bf16
 //   router_gemm_kernel<kRDX>      dX (bf16, read-modify-write) += dz W_r^T   M = T, N = d (256), K = E
 //   router_gemm_kernel<kRDW>      dW_r += X^T dz  (fp32 reduce-add)           M = d, N = E (128), K = T split
 // The GEMMs are dense contractions on tcgen05: operands arrive by TMA (128-byte swizzle, K-major or MN-major),
@@ -309,12 +310,12 @@ __global__ void __launch_bounds__(kRThreads) router_gemm_kernel(const __grid_con
 }
 
 // One CTA per expert: row r = (t, e) of the expert puts dS_r s_r at dz[t, e] (the pair is unique, so a plain
-// store) and adds it into G_t.
+// store into the zeroed dz).
 __global__ void __launch_bounds__(256) router_dz_rows_kernel(const float *__restrict__ dS,
                                                              const int32_t *__restrict__ offsets,
                                                              const int32_t *__restrict__ row_token,
                                                              const float *__restrict__ row_score, int T, int E,
-                                                             int p_cap, float *__restrict__ dz, float *__restrict__ G,
+                                                             int p_cap, float *__restrict__ dz,
                                                              int32_t *__restrict__ status) {
   griddep_wait();
   griddep_launch_dependents();
@@ -330,21 +331,20 @@ __global__ void __launch_bounds__(256) router_dz_rows_kernel(const float *__rest
       set_status(status, MOE_ERR_BAD_METADATA);
       continue;
     }
-    const float v = dS[r] * row_score[r];
-    dz[(size_t)t * E + e] = v;
-    atomicAdd(&G[t], v);
+    dz[(size_t)t * E + e] = dS[r] * row_score[r];
   }
 }
 
-// One warp per token: dz[t, j] -= s_tj G_t over the token's normaliser set, then the row is written in fp32
-// (the caller's dlogits) and bf16 (the operand of the two backward GEMMs).  Token choice and token rounding
-// take s_tj from topk_score (the token-choice gates); expert choice recomputes the softmax over all E logits.
+// One warp per token: the row dz[t, :] holds exactly the token's dS_r s_r at their experts, so G_t is its sum,
+// taken in a fixed order (each lane its own columns, then a butterfly), which keeps dz reproducible.  Then
+// dz[t, j] -= s_tj G_t over the token's normaliser set, and the row is written in fp32 (the caller's dlogits) and
+// bf16 (the operand of the two backward GEMMs).  Token choice and token rounding take s_tj from topk_score (the
+// token-choice gates); expert choice recomputes the softmax over all E logits.
 template <int NV>
 __global__ void __launch_bounds__(256) router_dz_tokens_kernel(const float *__restrict__ logits,
                                                                const int32_t *__restrict__ topk_idx,
-                                                               const float *__restrict__ topk_score,
-                                                               const float *__restrict__ G, int T, int E, int K,
-                                                               int ec, float *__restrict__ dz,
+                                                               const float *__restrict__ topk_score, int T, int E,
+                                                               int K, int ec, float *__restrict__ dz,
                                                                uint16_t *__restrict__ dz16) {
   griddep_wait();
   griddep_launch_dependents();
@@ -357,7 +357,11 @@ __global__ void __launch_bounds__(256) router_dz_tokens_kernel(const float *__re
     const int e = lane + 32 * j;
     v[j] = e < E ? dz[(size_t)t * E + e] : 0.f;
   }
-  const float g = G[t];
+  float g = 0.f;
+#pragma unroll
+  for (int j = 0; j < NV; ++j) g += v[j];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) g += __shfl_xor_sync(0xffffffffu, g, off);
   if (ec) {
     float z[NV], m = -INFINITY;
 #pragma unroll
@@ -431,7 +435,7 @@ int check_router_shape(int T, int d, int E) {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-size_t router_bwd_ws_bytes(int T, int E) { return align256((size_t)T * E * 2) + align256((size_t)T * 4); }
+size_t router_bwd_ws_bytes(int T, int E) { return align256((size_t)T * E * 2); }
 
 }  // namespace
 }  // namespace moe
@@ -483,16 +487,14 @@ int moe_router_backward(const float *dS, const moe_routing *r, const float *logi
   if (!ws || ws_bytes < router_bwd_ws_bytes(T, E)) return MOE_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint16_t *dz16 = static_cast<uint16_t *>(ws);
-  float *G = reinterpret_cast<float *>(static_cast<char *>(ws) + align256((size_t)T * E * 2));
 
   cudaError_t err = cudaMemsetAsync(dlogits, 0, (size_t)T * E * 4, s);
-  if (err == cudaSuccess) err = cudaMemsetAsync(G, 0, (size_t)T * 4, s);
   if (err == cudaSuccess) err = cudaMemsetAsync(dWr, 0, (size_t)d * E * 4, s);
   if (err != cudaSuccess) return record_cuda_error(err);
 
   prof_begin("router_dz_rows", s);
   err = launch_pdl(router_dz_rows_kernel, dim3(E), dim3(256), 0, s, dS, r->offsets, r->row_token, r->row_score, T, E,
-                   static_cast<int>(p_cap), dlogits, G, r->status);
+                   static_cast<int>(p_cap), dlogits, r->status);
   prof_end(s);
   count_launch();
   if (err != cudaSuccess) return record_cuda_error(err);
@@ -502,8 +504,8 @@ int moe_router_backward(const float *dS, const moe_routing *r, const float *logi
   const dim3 tgrid((T + 7) / 8);
   prof_begin("router_dz_tokens", s);
 #define MOE_DZ_LAUNCH(NV)                                                                                           \
-  err = launch_pdl(router_dz_tokens_kernel<NV>, tgrid, dim3(256), 0, s, logits, r->topk_idx, r->topk_score, G, T, E, \
-                   K, ec, dlogits, dz16)
+  err = launch_pdl(router_dz_tokens_kernel<NV>, tgrid, dim3(256), 0, s, logits, r->topk_idx, r->topk_score, T, E, K, \
+                   ec, dlogits, dz16)
   if (nv <= 1) MOE_DZ_LAUNCH(1);
   else if (nv <= 2) MOE_DZ_LAUNCH(2);
   else if (nv <= 4) MOE_DZ_LAUNCH(4);

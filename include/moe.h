@@ -221,7 +221,7 @@ int moe_backward_ex(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, c
 int moe_router_forward(const moe_bf16 *X, const moe_bf16 *Wr, int T, int d, int E, float *logits, int32_t *status,
                        void *stream);
 
-/* Router backward scratch: dz in bf16 [T, E] and the per-token sums G [T]. */
+/* Router backward scratch: dz in bf16 [T, E]. */
 int moe_router_backward_workspace_size(int T, int E, size_t *bytes);
 
 /*
@@ -237,6 +237,8 @@ int moe_router_backward_workspace_size(int T, int E, size_t *bytes);
  *   dWr      fp32 [d, E] output: X^T dz
  *   ws       scratch of moe_router_backward_workspace_size() bytes
  * Row metadata out of range is skipped and reported as MOE_ERR_BAD_METADATA in the routing status block.
+ * dlogits and the dX update are reproducible bit for bit (G_t is summed in a fixed order); dWr is summed over token
+ * splits with fp32 reduce-adds, whose order may vary in the last bits.
  */
 int moe_router_backward(const float *dS, const moe_routing *r, const float *logits, const moe_bf16 *X,
                         const moe_bf16 *Wr, int T, int d, int E, int K, int mode, size_t p_cap, float *dlogits,

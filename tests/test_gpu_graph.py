@@ -60,3 +60,63 @@ def test_route_forward_backward_replay_in_a_cuda_graph(name, mode):
     for k, t in dict(O=O, H=H[:P], dX=dX, dW1=dW1, dW2=dW2, dS=dS[:P]).items():
         ref = eager[k][:P] if k in ("H", "dS") else eager[k]
         assert_close(k, f64(t), f64(ref))
+
+
+@pytest.mark.parametrize("mode", ["tr", "ec"])
+def test_router_and_deterministic_layer_replay_bitwise(mode):
+    """Router forward, routing, the deterministic forward and backward, and the router backward in one CUDA graph:
+    with fixed-point aggregation every output is reproducible, so each replay must equal the eager run bit for
+    bit (the router's dW_r, summed with fp32 atomics over token splits, within the parity tolerance)."""
+    w = synth.WORKLOADS["tiny"]
+    g = to_dev(synth.make_inputs(w, 4))
+    Wr = synth.make_router_weights(w.d, w.E, 4).cuda()
+    rt = moe.Routing(w.T, w.E, w.K, mode, "cuda")
+    p = rt.p_cap
+    bf = torch.bfloat16
+    flags = moe.MOE_FLAG_DETERMINISTIC
+    z = torch.empty((w.T, w.E), dtype=torch.float32, device="cuda")
+    O = torch.empty((w.T, w.d), dtype=bf, device="cuda")
+    H = torch.empty((p, 2 * w.n), dtype=bf, device="cuda")
+    dX = torch.empty((w.T, w.d), dtype=bf, device="cuda")
+    dW1 = torch.empty((w.E, w.d, 2 * w.n), dtype=bf, device="cuda")
+    dW2 = torch.empty((w.E, w.n, w.d), dtype=bf, device="cuda")
+    dS = torch.empty(p, dtype=torch.float32, device="cuda")
+    dz = torch.empty((w.T, w.E), dtype=torch.float32, device="cuda")
+    dWr = torch.empty((w.d, w.E), dtype=torch.float32, device="cuda")
+    wsf = torch.empty(moe.moe_forward_workspace_size(w.T, w.d, w.n, w.E, w.K, p, flags), dtype=torch.uint8,
+                      device="cuda")
+    wsb = torch.empty(moe.moe_backward_workspace_size(w.T, w.d, w.n, w.E, w.K, p, flags), dtype=torch.uint8,
+                      device="cuda")
+
+    def step():
+        moe.moe_router_forward(g["X"], Wr, logits=z)
+        moe.moe_route(z, w.K, mode, routing=rt)
+        moe.moe_forward(g["X"], g["W1"], g["W2"], rt, O=O, H=H, ws=wsf, deterministic=True)
+        moe.moe_backward(g["dO"], g["X"], g["W1"], g["W2"], H, rt, dX=dX, dW1=dW1, dW2=dW2, dS=dS, ws=wsb,
+                         deterministic=True)
+        moe.moe_router_backward(dS, rt, z, g["X"], Wr, dX, dlogits=dz, dWr=dWr)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # eager: first-use set-up happens outside the capture
+    torch.cuda.synchronize()
+    code, P = rt.device_status()
+    assert code == 0
+    outs = dict(z=z, O=O, dX=dX, dW1=dW1, dW2=dW2, dz=dz)
+    eager = {k: t.clone() for k, t in outs.items()}
+    eager.update(H=H[:P].clone(), dS=dS[:P].clone(), dWr=dWr.clone())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        step()
+    for _ in range(2):
+        for t in list(outs.values()) + [H, dS, dWr]:
+            t.zero_()
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert rt.device_status() == (0, P)
+        for k, t in outs.items():
+            assert torch.equal(t, eager[k]), k
+        assert torch.equal(H[:P], eager["H"]) and torch.equal(dS[:P], eager["dS"])
+        assert_close("dWr", f64(dWr), f64(eager["dWr"]))
