@@ -16,7 +16,8 @@
 //   router_dz_tokens_kernel       one warp per token: G_t as the sum of its dz row (fixed order), the normaliser
 //                                 term, dz in fp32 (output) and bf16
 //   router_gemm_kernel<kRDX>      dX (bf16, read-modify-write) += dz W_r^T   M = T, N = d (256), K = E
-//   router_gemm_kernel<kRDW>      dW_r += X^T dz  (fp32 reduce-add)           M = d, N = E (128), K = T split
+//   router_gemm_kernel<kRDW>      one partial of X^T dz per token split       M = d, N = E (128), K = T split
+//   router_dw_sum_kernel          dW_r = the partials added in split order (reproducible bit for bit)
 // The GEMMs are dense contractions on tcgen05: operands arrive by TMA (128-byte swizzle, K-major or MN-major),
 // one thread issues the MMAs into TMEM, four warps drain it.  One output tile per CTA; two CTAs share an SM, so
 // one CTA's epilogue overlaps the other's main loop.  Epilogue staging reuses the drained pipeline stages.
@@ -34,7 +35,7 @@ struct RouterArgs {
   int n_tiles;       // output column tiles
   int kb_total;      // 64-wide k-blocks of the whole reduction
   int kb_per_split;  // k-blocks per CTA (the dW_r reduction over tokens is split across CTAs)
-  float *out;        // logits [T, E] or dW_r [d, E]
+  float *out;        // logits [T, E], or the dW_r partials [splits][d][E] (split s at out + s * d * E)
   int32_t *status;   // device error word (may be null)
 };
 
@@ -270,7 +271,7 @@ __global__ void __launch_bounds__(kRThreads) router_gemm_kernel(const __grid_con
         const uint32_t stg = base + (q * 32 + lane) * kRStgRow;
         const int grow = m0 + row;
         const bool live = MODE == kRLogits ? grow < a.T : grow < a.d;
-        float *out_row = a.out + (size_t)(live ? grow : 0) * a.E;
+        float *out_row = a.out + (MODE == kRDW ? (size_t)split * a.d * a.E : 0) + (size_t)(live ? grow : 0) * a.E;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           const int col = n0 + c * 32;
@@ -285,10 +286,7 @@ __global__ void __launch_bounds__(kRThreads) router_gemm_kernel(const __grid_con
                          __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
           fence_proxy_async_smem();
           const uint32_t bytes = static_cast<uint32_t>(min(32, a.E - col)) * 4u;
-          if (live) {
-            if (MODE == kRLogits) bulk_store(out_row + col, stg, bytes);
-            else bulk_reduce_add_f32(out_row + col, stg, bytes, policy_evict_last());
-          }
+          if (live) bulk_store(out_row + col, stg, bytes);
           bulk_commit();
         }
       }
@@ -402,6 +400,24 @@ __global__ void __launch_bounds__(256) router_dz_tokens_kernel(const float *__re
   }
 }
 
+// dW_r[i] = sum over the token splits, in split order, of the partials [splits][d][E]; four elements a step.
+__global__ void __launch_bounds__(256) router_dw_sum_kernel(const float4 *__restrict__ part, int splits, size_t n4,
+                                                            float4 *__restrict__ dWr) {
+  griddep_wait();
+  griddep_launch_dependents();
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+    float4 acc = __ldcs(part + i);
+    for (int sp = 1; sp < splits; ++sp) {
+      const float4 v = __ldcs(part + (size_t)sp * n4 + i);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    dWr[i] = acc;
+  }
+}
+
 // ------------------------------------------------------------------------------------------------ host
 
 namespace {
@@ -435,7 +451,14 @@ int check_router_shape(int T, int d, int E) {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-size_t router_bwd_ws_bytes(int T, int E) { return align256((size_t)T * E * 2); }
+// The token splits of dW_r (each a [d, E] fp32 partial); the count follows the SM count but never exceeds this,
+// so the workspace size does not depend on the device.
+constexpr int kRMaxSplits = 32;
+
+// dz in bf16 [T, E], then the dW_r partials [kRMaxSplits][d][E].
+size_t router_bwd_ws_bytes(int T, int d, int E) {
+  return align256((size_t)T * E * 2) + align256((size_t)kRMaxSplits * d * E * 4);
+}
 
 }  // namespace
 }  // namespace moe
@@ -467,10 +490,11 @@ int moe_router_forward(const moe_bf16 *X, const moe_bf16 *Wr, int T, int d, int 
   return launch_router_gemm<kRLogits>(tm, a, grid, s, "router_logits");
 }
 
-int moe_router_backward_workspace_size(int T, int E, size_t *bytes) {
+int moe_router_backward_workspace_size(int T, int d, int E, size_t *bytes) {
   if (!bytes) return MOE_ERR_INVALID_ARG;
-  if (T <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
-  *bytes = router_bwd_ws_bytes(T, E);
+  const int rc = check_router_shape(T, d, E);
+  if (rc != MOE_OK) return rc;
+  *bytes = router_bwd_ws_bytes(T, d, E);
   return MOE_OK;
 }
 
@@ -484,12 +508,12 @@ int moe_router_backward(const float *dS, const moe_routing *r, const float *logi
       !logits || !X || !Wr || !dlogits || !dX || !dWr)
     return MOE_ERR_INVALID_ARG;
   if (p_cap < (size_t)T * K || p_cap >= ((size_t)1 << 31)) return MOE_ERR_INVALID_ARG;
-  if (!ws || ws_bytes < router_bwd_ws_bytes(T, E)) return MOE_ERR_WORKSPACE;
+  if (!ws || ws_bytes < router_bwd_ws_bytes(T, d, E)) return MOE_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint16_t *dz16 = static_cast<uint16_t *>(ws);
+  float *part = reinterpret_cast<float *>(static_cast<char *>(ws) + align256((size_t)T * E * 2));
 
   cudaError_t err = cudaMemsetAsync(dlogits, 0, (size_t)T * E * 4, s);
-  if (err == cudaSuccess) err = cudaMemsetAsync(dWr, 0, (size_t)d * E * 4, s);
   if (err != cudaSuccess) return record_cuda_error(err);
 
   prof_begin("router_dz_rows", s);
@@ -532,18 +556,26 @@ int moe_router_backward(const float *dS, const moe_routing *r, const float *logi
   a.status = r->status;
   if ((rc = launch_router_gemm<kRDX>(tm, a, ((T + 127) / 128) * a.n_tiles, s, "router_dx")) != MOE_OK) return rc;
 
-  // dW_r += X^T dz  (M = d, N = E, K = T split into chunks across CTAs, fp32 reduce-add)
+  // dW_r = X^T dz  (M = d, N = E, K = T split into chunks across CTAs, one fp32 partial per split)
   if ((rc = make_tmap_bf16(&tm.a, X, d, T, 64)) != MOE_OK) return rc;       // X^T: MN-major A
   if ((rc = make_tmap_bf16(&tm.b, dz16, E, T, 64)) != MOE_OK) return rc;    // dz: MN-major B
   tm.c = tm.b;
   a.n_tiles = (E + 127) / 128;
   a.kb_total = (T + 63) / 64;
   const int tiles = (d / 128) * a.n_tiles;
-  const int want_splits = std::max(1, (2 * num_sms() + tiles - 1) / tiles);  // about two CTAs per SM
+  const int want_splits = std::min(kRMaxSplits, std::max(1, (2 * num_sms() + tiles - 1) / tiles));  // ~2 CTAs/SM
   a.kb_per_split = std::max(4, (a.kb_total + want_splits - 1) / want_splits);
-  const int splits = (a.kb_total + a.kb_per_split - 1) / a.kb_per_split;
-  a.out = dWr;
-  return launch_router_gemm<kRDW>(tm, a, tiles * splits, s, "router_dw");
+  const int splits = (a.kb_total + a.kb_per_split - 1) / a.kb_per_split;  // <= want_splits <= kRMaxSplits
+  a.out = part;
+  if ((rc = launch_router_gemm<kRDW>(tm, a, tiles * splits, s, "router_dw")) != MOE_OK) return rc;
+  const size_t n4 = (size_t)d * E / 4;  // d % 256 == 0
+  prof_begin("router_dw_sum", s);
+  err = launch_pdl(router_dw_sum_kernel, dim3(num_sms() * 4), dim3(256), 0, s, reinterpret_cast<const float4 *>(part),
+                   splits, n4, reinterpret_cast<float4 *>(dWr));
+  prof_end(s);
+  count_launch();
+  if (err == cudaSuccess) err = cudaGetLastError();
+  return err == cudaSuccess ? MOE_OK : record_cuda_error(err);
 }
 
 }  // extern "C"

@@ -80,7 +80,7 @@ def library() -> ctypes.CDLL:
     lib.moe_backward.argtypes = [_vp] * 5 + [ctypes.POINTER(moe_routing)] + [_c_int] * 5 + [_c_size] + [_vp] * 5 + [
         _c_size, _vp]
     lib.moe_router_forward.argtypes = [_vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp]
-    lib.moe_router_backward_workspace_size.argtypes = [_c_int, _c_int, sz]
+    lib.moe_router_backward_workspace_size.argtypes = [_c_int, _c_int, _c_int, sz]
     lib.moe_router_backward.argtypes = [_vp, ctypes.POINTER(moe_routing), _vp, _vp, _vp] + [_c_int] * 5 + [
         _c_size, _vp, _vp, _vp, _vp, _c_size, _vp]
     lib.moe_get_status.argtypes = [ctypes.POINTER(moe_routing), ctypes.POINTER(ctypes.c_int32),
@@ -292,7 +292,7 @@ def moe_router_backward(dS, routing: Routing, logits, X, Wr, dX, dlogits=None, d
     dlogits = torch.empty((T, E), dtype=torch.float32, device=dev) if dlogits is None else dlogits
     dWr = torch.empty((d, E), dtype=torch.float32, device=dev) if dWr is None else dWr
     out = _c_size(0)
-    _check(library().moe_router_backward_workspace_size(T, E, ctypes.byref(out)), "moe_router_backward_workspace_size")
+    _check(library().moe_router_backward_workspace_size(T, d, E, ctypes.byref(out)), "moe_router_backward_workspace_size")
     ws = torch.empty(out.value, dtype=torch.uint8, device=dev) if ws is None else ws
     _check(library().moe_router_backward(_ptr(dS), ctypes.byref(routing.struct), _ptr(logits), _ptr(X), _ptr(Wr), T, d,
                                          E, routing.K, routing.mode, routing.p_cap, _ptr(dlogits), _ptr(dX), _ptr(dWr),

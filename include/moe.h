@@ -221,8 +221,8 @@ int moe_backward_ex(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, c
 int moe_router_forward(const moe_bf16 *X, const moe_bf16 *Wr, int T, int d, int E, float *logits, int32_t *status,
                        void *stream);
 
-/* Router backward scratch: dz in bf16 [T, E]. */
-int moe_router_backward_workspace_size(int T, int E, size_t *bytes);
+/* Router backward scratch: dz in bf16 [T, E] and up to 32 token-split partials of dW_r [d, E] (fp32). */
+int moe_router_backward_workspace_size(int T, int d, int E, size_t *bytes);
 
 /*
  * moe_router_backward - gradients through the gates, the routing held fixed (selection is piecewise constant).
@@ -237,8 +237,8 @@ int moe_router_backward_workspace_size(int T, int E, size_t *bytes);
  *   dWr      fp32 [d, E] output: X^T dz
  *   ws       scratch of moe_router_backward_workspace_size() bytes
  * Row metadata out of range is skipped and reported as MOE_ERR_BAD_METADATA in the routing status block.
- * dlogits and the dX update are reproducible bit for bit (G_t is summed in a fixed order); dWr is summed over token
- * splits with fp32 reduce-adds, whose order may vary in the last bits.
+ * Every output is reproducible bit for bit: G_t is summed in a fixed order, and dWr adds its token splits'
+ * partials in split order.
  */
 int moe_router_backward(const float *dS, const moe_routing *r, const float *logits, const moe_bf16 *X,
                         const moe_bf16 *Wr, int T, int d, int E, int K, int mode, size_t p_cap, float *dlogits,
