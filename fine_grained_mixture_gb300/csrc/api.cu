@@ -405,7 +405,26 @@ int moe_forward_ex(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, co
   a.out_f32 = det ? nullptr : static_cast<float *>(Oacc);
   a.out_i64 = det ? static_cast<long long *>(Oacc) : nullptr;
   if ((rc = side.join()) != MOE_OK) return rc;
-  if ((rc = (fill_unused(tm), launch_down(a, tm, s, det))) != MOE_OK) return rc;
+  fill_unused(tm);
+  if (!det && d % 512 == 0 && (int64_t)T * d >= ((int64_t)48 << 20)) {
+    // Two launches over the column halves: the first half of O is final once the first launch ends, so its cast
+    // runs on the side stream beside the second launch and only the second half's cast stays on this stream.
+    // The second launch costs a prologue and a tail of its own, so this pays only where the cast is large
+    // (measured: T*d = 67 M gains about 1.5-2.5% of the step; T*d = 38 M loses 0.4%).
+    const int half = d / 2;
+    float *O32 = static_cast<float *>(Oacc);
+    a.Ndim = half;
+    a.nt_group = scatter_nt_group(T, half);
+    a.n_off = 0;
+    if ((rc = launch_down(a, tm, s, false)) != MOE_OK) return rc;
+    if ((rc = side.open(s)) != MOE_OK) return rc;
+    if ((rc = launch_f32_to_bf16_cols(O32, O, T, d, 0, half, side.side())) != MOE_OK) return rc;
+    a.n_off = half;
+    if ((rc = launch_down(a, tm, s, false)) != MOE_OK) return rc;
+    if ((rc = launch_f32_to_bf16_cols(O32, O, T, d, half, half, s)) != MOE_OK) return rc;
+    return side.join();
+  }
+  if ((rc = launch_down(a, tm, s, det)) != MOE_OK) return rc;
   if (det) return launch_fixed_to_bf16(static_cast<long long *>(Oacc), O, (size_t)T * d, s);
   return launch_f32_to_bf16(static_cast<float *>(Oacc), O, (size_t)T * d, s);
 }

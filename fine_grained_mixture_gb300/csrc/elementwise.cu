@@ -31,6 +31,34 @@ int launch_f32_to_bf16(const float *src, void *dst, size_t count, cudaStream_t s
   return err == cudaSuccess ? MOE_OK : record_cuda_error(err);
 }
 
+// Columns [c0, c0 + w) of every row: element group i (four columns) of the range sits at row i / (w / 4).
+__global__ void __launch_bounds__(256) f32_to_bf16_cols_kernel(const float *__restrict__ src, uint2 *__restrict__ dst,
+                                                               int rows, int ld, int c0, int w) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const size_t per_row = static_cast<size_t>(w) / 4;
+  const size_t n4 = per_row * rows;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = i / per_row, c = c0 + 4 * (i - r * per_row);
+    const float4 v = __ldcs(reinterpret_cast<const float4 *>(src + r * ld + c));
+    uint2 o;
+    o.x = pack_bf16x2(v.x, v.y);
+    o.y = pack_bf16x2(v.z, v.w);
+    __stcs(dst + (r * ld + c) / 4, o);
+  }
+}
+
+int launch_f32_to_bf16_cols(const float *src, void *dst, int rows, int ld, int c0, int w, cudaStream_t s) {
+  const int blocks = num_sms() * 8;
+  prof_begin("cast_f32_bf16", s);
+  cudaError_t err = launch_pdl(f32_to_bf16_cols_kernel, dim3(blocks), dim3(256), 0, s, src, static_cast<uint2 *>(dst),
+                               rows, ld, c0, w);
+  prof_end(s);
+  count_launch();
+  if (err == cudaSuccess) err = cudaGetLastError();
+  return err == cudaSuccess ? MOE_OK : record_cuda_error(err);
+}
+
 // Fixed-point accumulator (32 fractional bits) of the deterministic aggregation -> bf16, four elements per step.
 __global__ void __launch_bounds__(256) fixed_to_bf16_kernel(const longlong2 *__restrict__ src, uint2 *__restrict__ dst,
                                                             size_t n4) {

@@ -227,7 +227,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &a, int pair, int ran
     const int partner = 2 * mp + (rank ^ 1);
     t.shared = Traits<MODE>::paired && (2 * mp + 1 < total_m) && find_expert(a.tile_offsets, a.E, partner) == t.e;
     t.m0 = 0;
-    t.n0 = nt * BN;
+    t.n0 = a.n_off + nt * BN;  // n_off: first output column of this launch
     // a missing last tile (odd tile count) runs on rows past the last expert: zero operands, no output
     t.row0 = __ldg(&a.offsets[t.e]) + (mt - __ldg(&a.tile_offsets[t.e])) * kBM;
     t.row_end = __ldg(&a.offsets[t.e + 1]);

@@ -68,6 +68,7 @@ struct GemmArgs {
   int Ndim;  // output columns
   int Kdim;  // varlen-M: reduction length
   int nt_group;  // scatter-add GEMMs: column tiles per pass over all m-tiles (the fp32 slab kept in L2)
+  int n_off;     // varlen-M GEMMs: first output column of this launch (a launch may cover a column range)
   int wide_m;    // weight-gradient GEMMs: 256-row blocks (experts average >= 1024 rows) instead of 128
   void *out0;        // up: H;  dH: dH;  dW1/dW2: the weight gradient (both in one launch: dW1)
   void *out1;        // up: A;  dH: s*A;  both weight gradients in one launch: dW2
@@ -106,6 +107,8 @@ int launch_dw12(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s);
 
 // elementwise (elementwise.cu)
 int launch_f32_to_bf16(const float *src, void *dst, size_t count, cudaStream_t s);
+// Same for columns [c0, c0 + w) of a [rows, ld] matrix (w and c0 multiples of 4).
+int launch_f32_to_bf16_cols(const float *src, void *dst, int rows, int ld, int c0, int w, cudaStream_t s);
 // The fixed-point accumulator of the deterministic aggregation (32 fractional bits) to bf16.
 int launch_fixed_to_bf16(const long long *src, void *dst, size_t count, cudaStream_t s);
 // dS[r] = sum over the column tiles, in tile order, of the deterministic dH epilogue's partials [p_cap][tiles].
