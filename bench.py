@@ -51,6 +51,8 @@ def parse():
     p.add_argument("--mode", default="tc", choices=["tc", "tr", "tr_up", "tr_down", "tr_stoch", "ec"])
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle baseline sample")
     p.add_argument("--no-extras", action="store_true", help="skip the TR-vs-TC and e2e side measurements")
+    p.add_argument("--router", action="store_true",
+                   help="time only the router either side of the layer (logits, gate backward) and print its JSON")
     p.add_argument("--ingest-ncu", metavar="CSV", help="record per-launch DRAM bytes from an ncu --csv log "
                    "(dram__bytes_read.sum, dram__bytes_write.sum) in profiles/dram_traffic.json and exit")
     return p.parse_args()
@@ -435,6 +437,10 @@ def main():
     _b.build()
     import fine_grained_mixture_gb300 as moe
 
+    if args.router:
+        if rank == 0:
+            print(json.dumps({"router": router_timing(args, dev)}), flush=True)
+        return 0
     w = synth.WORKLOADS[args.workload]
     pk = peaks()
     inp = synth.make_inputs(w, seed=rank)
