@@ -12,7 +12,7 @@
 //
 // Kernels:
 //   router_gemm_kernel<kRLogits>  z = X W_r            M = T, N = E (128-column tiles), K = d
-//   router_dz_rows_kernel         one CTA per expert: dS_r s_r into dz[t, e] (each pair is unique)
+//   router_dz_rows_kernel         one thread per routed row: dS_r s_r into dz[t, e] (each pair is unique)
 //   router_dz_tokens_kernel       one warp per token: G_t as the sum of its dz row (fixed order), the normaliser
 //                                 term, dz in fp32 (output) and bf16
 //   router_gemm_kernel<kRDX>      dX (bf16, read-modify-write) += dz W_r^T   M = T, N = d (256), K = E
@@ -307,30 +307,39 @@ __global__ void __launch_bounds__(kRThreads) router_gemm_kernel(const __grid_con
   }
 }
 
-// One CTA per expert: row r = (t, e) of the expert puts dS_r s_r at dz[t, e] (the pair is unique, so a plain
-// store into the zeroed dz).
-__global__ void __launch_bounds__(256) router_dz_rows_kernel(const float *__restrict__ dS,
-                                                             const int32_t *__restrict__ offsets,
-                                                             const int32_t *__restrict__ row_token,
-                                                             const float *__restrict__ row_score, int T, int E,
-                                                             int p_cap, float *__restrict__ dz,
-                                                             int32_t *__restrict__ status) {
+// One thread per routed row r = (t, e): dS_r s_r goes to dz[t, e] (the pair is unique, so a plain store into the
+// zeroed dz).  The row's expert is found by a binary search over the offsets, which each CTA keeps in shared memory.
+constexpr int kDzRowsThreads = 256;
+__global__ void __launch_bounds__(kDzRowsThreads) router_dz_rows_kernel(const float *__restrict__ dS,
+                                                                        const int32_t *__restrict__ offsets,
+                                                                        const int32_t *__restrict__ row_token,
+                                                                        const float *__restrict__ row_score, int T,
+                                                                        int E, int p_cap, float *__restrict__ dz,
+                                                                        int32_t *__restrict__ status) {
+  __shared__ int s_off[kMaxExperts + 1];
   griddep_wait();
   griddep_launch_dependents();
-  const int e = blockIdx.x;
-  const int r0 = offsets[e], r1 = offsets[e + 1];
-  if (r0 < 0 || r1 < r0 || r1 > p_cap) {
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) s_off[e] = offsets[e];
+  __syncthreads();
+  const int P = s_off[E];
+  if (P < 0 || P > p_cap) {
     if (threadIdx.x == 0) set_status(status, MOE_ERR_BAD_METADATA);
     return;
   }
-  for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
-    const int t = row_token[r];
-    if (t < 0 || t >= T) {
-      set_status(status, MOE_ERR_BAD_METADATA);
-      continue;
-    }
-    dz[(size_t)t * E + e] = dS[r] * row_score[r];
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= P) return;
+  int lo = 0, hi = E;  // largest e with s_off[e] <= r
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_off[mid] <= r) lo = mid;
+    else hi = mid;
   }
+  const int t = row_token[r];
+  if (t < 0 || t >= T) {
+    set_status(status, MOE_ERR_BAD_METADATA);
+    return;
+  }
+  dz[(size_t)t * E + lo] = dS[r] * row_score[r];
 }
 
 // One warp per token: the row dz[t, :] holds exactly the token's dS_r s_r at their experts, so G_t is its sum,
@@ -517,7 +526,9 @@ int moe_router_backward(const float *dS, const moe_routing *r, const float *logi
   if (err != cudaSuccess) return record_cuda_error(err);
 
   prof_begin("router_dz_rows", s);
-  err = launch_pdl(router_dz_rows_kernel, dim3(E), dim3(256), 0, s, dS, r->offsets, r->row_token, r->row_score, T, E,
+  // one thread per row of the capacity (rows at and past P return at once)
+  err = launch_pdl(router_dz_rows_kernel, dim3(static_cast<unsigned>((p_cap + kDzRowsThreads - 1) / kDzRowsThreads)),
+                   dim3(kDzRowsThreads), 0, s, dS, r->offsets, r->row_token, r->row_score, T, E,
                    static_cast<int>(p_cap), dlogits, r->status);
   prof_end(s);
   count_launch();
