@@ -97,3 +97,30 @@ def test_null_arguments_rejected_before_any_device_work(lib):
     assert lib.moe_forward(None, None, None, ctypes.byref(r), 512, 256, 128, 8, 2, 1024, None, None, None, 0,
                            None) == 1
     assert lib.moe_strerror(6) == b"device pipeline wait timed out"
+
+
+def test_router_validation(lib):
+    out = ctypes.c_size_t(0)
+    assert lib.moe_router_backward_workspace_size(24576, 1536, 128, ctypes.byref(out)) == 0
+    # bf16 dz [T, E] plus up to 32 fp32 partials of dW_r [d, E]
+    assert out.value >= 24576 * 128 * 2 + 32 * 1536 * 128 * 4
+    assert lib.moe_router_backward_workspace_size(64, 256, 12, ctypes.byref(out)) == 2   # E % 8 != 0
+    assert lib.moe_router_backward_workspace_size(64, 200, 16, ctypes.byref(out)) == 2   # d % 256 != 0
+    assert lib.moe_router_backward_workspace_size(0, 256, 16, ctypes.byref(out)) == 1
+    assert lib.moe_router_backward_workspace_size(64, 256, 16, None) == 1
+    # null tensors are rejected before any device work
+    assert lib.moe_router_forward(None, None, 64, 256, 16, None, None, None) == 1
+    assert lib.moe_router_forward(ctypes.c_void_p(16), ctypes.c_void_p(16), 64, 256, 12, ctypes.c_void_p(16), None,
+                                  None) == 2
+    r = moe.moe.moe_routing()
+    assert lib.moe_router_backward(None, ctypes.byref(r), None, None, None, 64, 256, 16, 2, 0, 128, None, None, None,
+                                   None, 0, None) == 1
+
+
+def test_deterministic_entry_points_reject_unknown_flags(lib):
+    dummy = moe.moe.moe_routing(*([16] * 10))
+    p = ctypes.c_void_p(16)
+    assert lib.moe_forward_ex(p, p, p, ctypes.byref(dummy), 512, 256, 128, 8, 2, 1024, p, p, p, 1 << 30, 4,
+                              None) == 1
+    assert lib.moe_backward_ex(p, p, p, p, p, ctypes.byref(dummy), 512, 256, 128, 8, 2, 1024, p, p, p, p, p, 1 << 30,
+                               8, None) == 1
