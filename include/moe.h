@@ -11,6 +11,14 @@
  * "Key design 2: IO-aware fused kernels" and the X/H-only activation cache of "Key design 3:
  * minimal-activation-cache backward".
  *
+ * Entry points
+ *   routing      moe_route, moe_route_ex (stochastic rounding's uniforms), moe_route_noalloc; capacity and
+ *                workspace queries
+ *   layer        moe_forward, moe_backward, and their _ex forms with flags (MOE_FLAG_DETERMINISTIC)
+ *   router       moe_router_forward (logits = X W_r), moe_router_backward (dlogits, dX += dz W_r^T, dW_r)
+ *   diagnostics  moe_get_status, moe_strerror, moe_last_cuda_error, moe_kernel_launch_count, moe_profile_*,
+ *                moe_selftest_bounded_wait
+ *
  * Conventions shared by every call
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library allocates no device memory.
  *     Tensors are contiguous and row-major.  "bf16" arguments hold IEEE bfloat16 bit patterns (moe_bf16).
