@@ -46,6 +46,28 @@ def test_bad_token_ids_are_flagged_not_followed(mode):
     _routing_still_exact()
 
 
+def test_router_backward_flags_bad_token_ids():
+    """The router's row scatter skips rows whose token id is out of range and reports them; the rest of its
+    outputs stay finite and the next routing call is exact."""
+    w = synth.WORKLOADS["tiny"]
+    g = to_dev(synth.make_inputs(w, 1))
+    Wr = synth.make_router_weights(w.d, w.E, 1).cuda()
+    z = moe.moe_router_forward(g["X"], Wr)
+    rt = moe.moe_route(z, w.K, "tc")
+    torch.cuda.synchronize()
+    assert rt.device_status()[0] == 0
+    rt.row_token[0] = -1
+    rt.row_token[5] = w.T
+    dS = synth.make_row_grads(rt.p_cap, 1).cuda()
+    dX = torch.zeros((w.T, w.d), dtype=torch.bfloat16, device="cuda")
+    dlogits, dWr = moe.moe_router_backward(dS, rt, z, g["X"], Wr, dX)
+    torch.cuda.synchronize()
+    assert rt.device_status()[0] == MOE_ERR_BAD_METADATA
+    for t in (dlogits, dWr, dX):
+        assert bool(torch.isfinite(t.float()).all())
+    _routing_still_exact()
+
+
 def test_stuck_wait_times_out_and_the_context_survives():
     assert moe.selftest_bounded_wait() == MOE_ERR_DEVICE_TIMEOUT
     _routing_still_exact()
