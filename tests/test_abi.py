@@ -55,6 +55,8 @@ def test_capacity_and_workspace_queries(lib):
 @pytest.mark.parametrize("args,code", [
     ((0, 8, 2, 0), 1), ((16, 8, 9, 0), 1), ((16, 8, 2, 7), 1), ((16, 8, 2, 6), 1), ((16, 8, 2, -1), 1),
     ((16, 2000, 2, 0), 2), ((16, 64, 40, 0), 2), ((60000, 8, 2, 1), 2), ((60000, 8, 2, 5), 2),
+    # the selection modes hold one expert's keys for every token on chip: T = 49152 is their largest count
+    ((49152, 1024, 32, 1), 0), ((49153, 8, 2, 1), 2), ((49153, 8, 2, 4), 2), ((49153, 1024, 32, 0), 0),
 ])
 def test_route_validation(lib, args, code):
     out = ctypes.c_size_t(0)

@@ -52,6 +52,16 @@ def test_routing_edge_shapes(T, E, K, ties, mode):
     check_routing(rt, ref, P)
 
 
+@pytest.mark.parametrize("T,E,K,modes", [(49152, 128, 8, MODES), (49152, 1024, 32, ["tr", "ec"])])
+def test_routing_at_the_largest_token_count(T, E, K, modes):
+    """The selection modes keep one expert's keys for all T tokens in shared memory, so T = 49152 is the largest
+    count they accept; at that size (and with E and K at their maxima) the metadata is still bit-exact."""
+    z = torch.randn((T, E), generator=torch.Generator().manual_seed(T + E))
+    for mode in modes:
+        rt, P, ref = _route_both(z, K, mode, seed=T)
+        check_routing(rt, ref, P)
+
+
 def test_stochastic_rounding_without_uniforms_is_rejected():
     import fine_grained_mixture_gb300 as moe
     with pytest.raises(moe.MoeError) as ei:
