@@ -125,20 +125,53 @@ def _ptr(t: torch.Tensor | None):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream=None):
-    s = stream if stream is not None else torch.cuda.current_stream()
+def _stream(stream=None, device: torch.device | None = None):
+    """The cudaStream_t of `stream`, else of the current stream of `device` (the current device by default)."""
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    if device is not None and s.device != device:
+        raise ValueError(f"stream is on {s.device}, the tensors on {device}")
     return ctypes.c_void_p(s.cuda_stream)
 
 
 def _need(t: torch.Tensor, name: str, dtype: torch.dtype, numel: int | None = None):
-    if not (t.is_cuda and t.is_contiguous() and t.dtype == dtype):
-        raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor, got {t.dtype} {tuple(t.shape)}")
+    """A contiguous tensor of `dtype` with at least `numel` elements (the library reads and writes that many)."""
+    if t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous {dtype} tensor, got {t.dtype} {tuple(t.shape)}")
     if numel is not None and t.numel() < numel:
         raise ValueError(f"{name}: needs {numel} elements, has {t.numel()}")
 
 
+def _dims(t: torch.Tensor, name: str, ndim: int):
+    if t.dim() != ndim:
+        raise ValueError(f"{name}: expected {ndim} dimensions, got shape {tuple(t.shape)}")
+    return tuple(t.shape)
+
+
+def _device(**tensors) -> torch.device:
+    """The one CUDA device that every given tensor (None entries skipped) lives on; calls run with it current."""
+    devs: dict = {}
+    for name, t in tensors.items():
+        if t is not None:
+            devs.setdefault(t.device, name)
+    if len(devs) != 1:
+        raise ValueError("tensors on different devices: " + ", ".join(f"{n} on {d}" for d, n in devs.items()))
+    dev = next(iter(devs))
+    if dev.type != "cuda":
+        raise ValueError(f"expected CUDA tensors, got tensors on {dev}")
+    return dev
+
+
 def _mode(mode) -> int:
-    return MODES[mode] if isinstance(mode, str) else int(mode)
+    if isinstance(mode, str):
+        if mode not in MODES:
+            raise ValueError(f"unknown routing mode {mode!r}; one of {sorted(MODES)}")
+        return MODES[mode]
+    return int(mode)
+
+
+def _same_routing(routing: "Routing", T: int, E: int):
+    if (routing.T, routing.E) != (T, E):
+        raise ValueError(f"routing buffers were made for T={routing.T}, E={routing.E}; the tensors have T={T}, E={E}")
 
 
 def moe_route_capacity(T: int, E: int, K: int, mode="tc") -> int:
@@ -193,8 +226,10 @@ class Routing:
     def device_status(self, stream=None):
         """(device error code, P) after synchronising the stream."""
         code, P = ctypes.c_int32(0), ctypes.c_int32(0)
-        _check(library().moe_get_status(ctypes.byref(self.struct), ctypes.byref(code), ctypes.byref(P),
-                                        _stream(stream)), "moe_get_status")
+        dev = _device(status=self.status)
+        with torch.cuda.device(dev):
+            _check(library().moe_get_status(ctypes.byref(self.struct), ctypes.byref(code), ctypes.byref(P),
+                                            _stream(stream, dev)), "moe_get_status")
         return code.value, P.value
 
 
@@ -202,32 +237,51 @@ def moe_route(logits: torch.Tensor, K: int, mode="tc", routing: Routing | None =
               uniforms: torch.Tensor | None = None):
     """Routing metadata for fp32 logits [T, E]; returns the Routing (and P when want_P).
 
-    uniforms: fp32 [E] draws in [0, 1) for stochastic rounding ("tr_stoch"); other modes ignore them."""
-    T, E = logits.shape
+    uniforms: fp32 [E] draws in [0, 1) for stochastic rounding ("tr_stoch"); other modes ignore them.
+    routing: buffers from an earlier call (or Routing(...)) to fill again; they must match T, E, K and mode."""
+    T, E = _dims(logits, "logits", 2)
     _need(logits, "logits", torch.float32)
+    m = _mode(mode)
     if routing is None:
-        routing = Routing(T, E, K, mode, logits.device)
+        routing = Routing(T, E, K, m, logits.device)
+    elif (routing.T, routing.E, routing.K, routing.mode) != (T, E, K, m):
+        raise ValueError(f"routing buffers were made for T={routing.T}, E={routing.E}, K={routing.K}, mode "
+                         f"{routing.mode}; this call has T={T}, E={E}, K={K}, mode {m}")
     if uniforms is not None:
         _need(uniforms, "uniforms", torch.float32, E)
+    dev = _device(logits=logits, routing=routing.status, uniforms=uniforms)
     P = ctypes.c_int32(0)
-    _check(library().moe_route_ex(_ptr(logits), _ptr(uniforms), T, E, K, routing.mode, ctypes.byref(routing.struct),
-                                  _ptr(routing.ws), routing.ws.numel(), ctypes.byref(P) if want_P else None,
-                                  _stream(stream)), "moe_route_ex")
+    with torch.cuda.device(dev):
+        _check(library().moe_route_ex(_ptr(logits), _ptr(uniforms), T, E, K, routing.mode,
+                                      ctypes.byref(routing.struct), _ptr(routing.ws), routing.ws.numel(),
+                                      ctypes.byref(P) if want_P else None, _stream(stream, dev)), "moe_route_ex")
     return (routing, P.value) if want_P else routing
+
+
+def _layer_dims(X, W1, W2, routing: Routing):
+    """(T, d, E, n) from X [T, d], W1 [E, d, 2n], W2 [E, n, d], checked against each other and the routing."""
+    T, d = _dims(X, "X", 2)
+    E, d1, n2 = _dims(W1, "W1", 3)
+    if d1 != d or n2 % 2:
+        raise ValueError(f"W1: expected [E, {d}, 2n], got {(E, d1, n2)}")
+    n = n2 // 2
+    if _dims(W2, "W2", 3) != (E, n, d):
+        raise ValueError(f"W2: expected {(E, n, d)}, got {tuple(W2.shape)}")
+    _same_routing(routing, T, E)
+    return T, d, E, n
 
 
 def moe_forward(X, W1, W2, routing: Routing, O=None, H=None, ws=None, stream=None, deterministic=False):
     """O = sum_k s_k SwiGLU(X W1_e) W2_e; returns (O [T, d] bf16, H [P_cap, 2n] bf16).
 
     deterministic: fixed-point aggregation, bitwise identical results on every run."""
-    T, d = X.shape
-    E, _, n2 = W1.shape
-    n = n2 // 2
+    T, d, E, n = _layer_dims(X, W1, W2, routing)
+    n2 = 2 * n
     K, p_cap = routing.K, routing.p_cap
     bf = torch.bfloat16
-    _need(X, "X", bf, T * d)
-    _need(W1, "W1", bf, E * d * n2)
-    _need(W2, "W2", bf, E * n * d)
+    _need(X, "X", bf)
+    _need(W1, "W1", bf)
+    _need(W2, "W2", bf)
     O = torch.empty((T, d), dtype=bf, device=X.device) if O is None else O
     H = torch.empty((p_cap, n2), dtype=bf, device=X.device) if H is None else H
     flags = MOE_FLAG_DETERMINISTIC if deterministic else 0
@@ -235,8 +289,12 @@ def moe_forward(X, W1, W2, routing: Routing, O=None, H=None, ws=None, stream=Non
     ws = torch.empty(need, dtype=torch.uint8, device=X.device) if ws is None else ws
     _need(O, "O", bf, T * d)
     _need(H, "H", bf, p_cap * n2)
-    _check(library().moe_forward_ex(_ptr(X), _ptr(W1), _ptr(W2), ctypes.byref(routing.struct), T, d, n, E, K, p_cap,
-                                    _ptr(O), _ptr(H), _ptr(ws), ws.numel(), flags, _stream(stream)), "moe_forward_ex")
+    _need(ws, "ws", torch.uint8, need)
+    dev = _device(X=X, W1=W1, W2=W2, routing=routing.status, O=O, H=H, ws=ws)
+    with torch.cuda.device(dev):
+        _check(library().moe_forward_ex(_ptr(X), _ptr(W1), _ptr(W2), ctypes.byref(routing.struct), T, d, n, E, K,
+                                        p_cap, _ptr(O), _ptr(H), _ptr(ws), ws.numel(), flags, _stream(stream, dev)),
+               "moe_forward_ex")
     return O, H
 
 
@@ -245,13 +303,13 @@ def moe_backward(dO, X, W1, W2, H, routing: Routing, dX=None, dW1=None, dW2=None
     """Gradients for upstream dO; returns (dX [T, d], dW1 [E, d, 2n], dW2 [E, n, d], dS [P_cap] fp32).
 
     deterministic: fixed-point aggregation of dX and ordered dS sums, bitwise identical results on every run."""
-    T, d = X.shape
-    E, _, n2 = W1.shape
-    n = n2 // 2
+    T, d, E, n = _layer_dims(X, W1, W2, routing)
+    n2 = 2 * n
     K, p_cap = routing.K, routing.p_cap
     bf = torch.bfloat16
-    for t, name in ((dO, "dO"), (X, "X"), (W1, "W1"), (W2, "W2"), (H, "H")):
-        _need(t, name, bf)
+    for t, name, numel in ((dO, "dO", T * d), (X, "X", None), (W1, "W1", None), (W2, "W2", None),
+                           (H, "H", p_cap * n2)):
+        _need(t, name, bf, numel)
     dev = X.device
     dX = torch.empty((T, d), dtype=bf, device=dev) if dX is None else dX
     dW1 = torch.empty((E, d, n2), dtype=bf, device=dev) if dW1 is None else dW1
@@ -260,22 +318,42 @@ def moe_backward(dO, X, W1, W2, H, routing: Routing, dX=None, dW1=None, dW2=None
     flags = MOE_FLAG_DETERMINISTIC if deterministic else 0
     need = moe_backward_workspace_size(T, d, n, E, K, p_cap, flags)
     ws = torch.empty(need, dtype=torch.uint8, device=dev) if ws is None else ws
-    _check(library().moe_backward_ex(_ptr(dO), _ptr(X), _ptr(W1), _ptr(W2), _ptr(H), ctypes.byref(routing.struct),
-                                     T, d, n, E, K, p_cap, _ptr(dX), _ptr(dW1), _ptr(dW2), _ptr(dS), _ptr(ws),
-                                     ws.numel(), flags, _stream(stream)), "moe_backward_ex")
+    for t, name, dt, numel in ((dX, "dX", bf, T * d), (dW1, "dW1", bf, E * d * n2), (dW2, "dW2", bf, E * n * d),
+                               (dS, "dS", torch.float32, p_cap), (ws, "ws", torch.uint8, need)):
+        _need(t, name, dt, numel)
+    dev = _device(dO=dO, X=X, W1=W1, W2=W2, H=H, routing=routing.status, dX=dX, dW1=dW1, dW2=dW2, dS=dS, ws=ws)
+    with torch.cuda.device(dev):
+        _check(library().moe_backward_ex(_ptr(dO), _ptr(X), _ptr(W1), _ptr(W2), _ptr(H),
+                                         ctypes.byref(routing.struct), T, d, n, E, K, p_cap, _ptr(dX), _ptr(dW1),
+                                         _ptr(dW2), _ptr(dS), _ptr(ws), ws.numel(), flags, _stream(stream, dev)),
+               "moe_backward_ex")
     return dX, dW1, dW2, dS
 
 
+def _router_dims(X, Wr):
+    """(T, d, E) from X [T, d] and W_r [d, E]."""
+    T, d = _dims(X, "X", 2)
+    d1, E = _dims(Wr, "Wr", 2)
+    if d1 != d:
+        raise ValueError(f"Wr: expected [{d}, E], got {(d1, E)}")
+    return T, d, E
+
+
 def moe_router_forward(X, Wr, logits=None, status=None, stream=None):
-    """Router logits = X W_r (X bf16 [T, d], W_r bf16 [d, E]); returns fp32 logits [T, E]."""
-    T, d = X.shape
-    E = Wr.shape[1]
-    _need(X, "X", torch.bfloat16, T * d)
-    _need(Wr, "Wr", torch.bfloat16, d * E)
+    """Router logits = X W_r (X bf16 [T, d], W_r bf16 [d, E]); returns fp32 logits [T, E].
+
+    status: optional int32 device tensor that receives MOE_ERR_DEVICE_TIMEOUT if a bounded wait runs out."""
+    T, d, E = _router_dims(X, Wr)
+    _need(X, "X", torch.bfloat16)
+    _need(Wr, "Wr", torch.bfloat16)
     logits = torch.empty((T, E), dtype=torch.float32, device=X.device) if logits is None else logits
     _need(logits, "logits", torch.float32, T * E)
-    _check(library().moe_router_forward(_ptr(X), _ptr(Wr), T, d, E, _ptr(logits), _ptr(status), _stream(stream)),
-           "moe_router_forward")
+    if status is not None:
+        _need(status, "status", torch.int32, 1)
+    dev = _device(X=X, Wr=Wr, logits=logits, status=status)
+    with torch.cuda.device(dev):
+        _check(library().moe_router_forward(_ptr(X), _ptr(Wr), T, d, E, _ptr(logits), _ptr(status),
+                                            _stream(stream, dev)), "moe_router_forward")
     return logits
 
 
@@ -283,20 +361,27 @@ def moe_router_backward(dS, routing: Routing, logits, X, Wr, dX, dlogits=None, d
     """Router gradients through the gates (routing held fixed): returns (dlogits [T, E] fp32, dWr [d, E] fp32).
 
     dX (bf16 [T, d], the layer's input gradient from moe_backward) is updated in place with dz W_r^T."""
-    T, d = X.shape
-    E = Wr.shape[1]
-    for t, name, dt in ((dS, "dS", torch.float32), (logits, "logits", torch.float32), (X, "X", torch.bfloat16),
-                        (Wr, "Wr", torch.bfloat16), (dX, "dX", torch.bfloat16)):
-        _need(t, name, dt)
+    T, d, E = _router_dims(X, Wr)
+    _same_routing(routing, T, E)
+    f32, bf = torch.float32, torch.bfloat16
+    for t, name, dt, numel in ((dS, "dS", f32, routing.p_cap), (logits, "logits", f32, T * E), (X, "X", bf, None),
+                               (Wr, "Wr", bf, None), (dX, "dX", bf, T * d)):
+        _need(t, name, dt, numel)
     dev = X.device
-    dlogits = torch.empty((T, E), dtype=torch.float32, device=dev) if dlogits is None else dlogits
-    dWr = torch.empty((d, E), dtype=torch.float32, device=dev) if dWr is None else dWr
+    dlogits = torch.empty((T, E), dtype=f32, device=dev) if dlogits is None else dlogits
+    dWr = torch.empty((d, E), dtype=f32, device=dev) if dWr is None else dWr
     out = _c_size(0)
     _check(library().moe_router_backward_workspace_size(T, d, E, ctypes.byref(out)), "moe_router_backward_workspace_size")
     ws = torch.empty(out.value, dtype=torch.uint8, device=dev) if ws is None else ws
-    _check(library().moe_router_backward(_ptr(dS), ctypes.byref(routing.struct), _ptr(logits), _ptr(X), _ptr(Wr), T, d,
-                                         E, routing.K, routing.mode, routing.p_cap, _ptr(dlogits), _ptr(dX), _ptr(dWr),
-                                         _ptr(ws), ws.numel(), _stream(stream)), "moe_router_backward")
+    for t, name, dt, numel in ((dlogits, "dlogits", f32, T * E), (dWr, "dWr", f32, d * E),
+                               (ws, "ws", torch.uint8, out.value)):
+        _need(t, name, dt, numel)
+    dev = _device(dS=dS, routing=routing.status, logits=logits, X=X, Wr=Wr, dX=dX, dlogits=dlogits, dWr=dWr, ws=ws)
+    with torch.cuda.device(dev):
+        _check(library().moe_router_backward(_ptr(dS), ctypes.byref(routing.struct), _ptr(logits), _ptr(X), _ptr(Wr),
+                                             T, d, E, routing.K, routing.mode, routing.p_cap, _ptr(dlogits), _ptr(dX),
+                                             _ptr(dWr), _ptr(ws), ws.numel(), _stream(stream, dev)),
+               "moe_router_backward")
     return dlogits, dWr
 
 
