@@ -11,6 +11,25 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: long-running (full-size workloads)")
+    _plant_oracle_mistake()
+
+
+def _plant_oracle_mistake():
+    """For tests/test_oracle_mutants.py only: MOE_ORACLE_MUTANT = JSON [old, new] re-executes the oracle's
+    source with that one snippet replaced, in this (child) pytest process, so that its pins run against a
+    deliberately wrong oracle."""
+    spec = os.environ.get("MOE_ORACLE_MUTANT")
+    if not spec:
+        return
+    import json
+
+    from oracle import moe_oracle
+    old, new = json.loads(spec)
+    with open(moe_oracle.__file__) as f:
+        src = f.read()
+    if src.count(old) != 1:
+        raise RuntimeError(f"planted mistake: {old!r} occurs {src.count(old)} times in the oracle")
+    exec(compile(src.replace(old, new), moe_oracle.__file__, "exec"), moe_oracle.__dict__)
 
 
 def load_golden(name):

@@ -226,6 +226,27 @@ def test_tr_expected_total_unchanged():
     assert abs(diffs.mean()) / (T * K) < 0.01
 
 
+@pytest.mark.parametrize("mode", orc.ROUTE_MODES)
+def test_offsets_and_tile_offsets_by_walking_the_rows(mode):
+    """offsets and tile_offsets counted by walking each expert's rows: the expert's rows are the next counts[e]
+    rows, and cutting them into M_tile blocks from the first row gives full blocks and at most one partial one."""
+    rng = np.random.default_rng(7)
+    for T, E, K, M in ((300, 8, 2, 128), (50, 6, 3, 4), (9, 5, 1, 4)):
+        z = rng.standard_normal((T, E)).astype(np.float32)
+        rt = orc.route(z, K, mode, M, u=rng.random(E).astype(np.float32))
+        row, tile = 0, 0
+        for e in range(E):
+            assert rt["offsets"][e] == row and rt["tile_offsets"][e] == tile
+            start = row
+            while row < start + rt["counts"][e]:
+                block = min(M, start + rt["counts"][e] - row)   # one block: M rows, or the partial last one
+                assert 0 < block <= M
+                assert all(rt["row_expert"][row:row + block] == e)
+                row += block
+                tile += 1
+        assert rt["offsets"][E] == row == rt["P"] and rt["tile_offsets"][E] == tile
+
+
 @pytest.mark.parametrize("fixture", ["tr_pad_and_drop.txt", "tr_tie_rounds_down.txt", "tr_rules_and_ec.txt"])
 def test_routing_golden(fixture):
     g = load_golden(fixture)
