@@ -35,6 +35,44 @@ def test_every_declared_symbol_is_exported(lib):
     assert not missing, missing
 
 
+def declared_prototypes():
+    """{name: (return type, [parameter declarations])} of every function include/moe.h declares."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for ret, name, params in re.findall(r"^\s*((?:const\s+)?[A-Za-z_][\w\s\*]*?)\b(moe_\w+)\s*\(([^)]*)\)\s*;",
+                                        text, flags=re.M):
+        plist = [p.strip() for p in params.split(",") if p.strip() and p.strip() != "void"]
+        out[name] = (" ".join(ret.split()), plist)
+    return out
+
+
+_C_TO_CTYPES = {"int": ctypes.c_int, "unsigned": ctypes.c_uint, "size_t": ctypes.c_size_t,
+                "int32_t": ctypes.c_int32, "uint64_t": ctypes.c_uint64, "double": ctypes.c_double}
+
+
+def test_binding_signatures_match_the_header(lib):
+    """Every function the binding declares to ctypes takes the header's number of arguments, passes pointers
+    where the header has pointers and the header's scalar type elsewhere, and returns the header's type."""
+    protos = declared_prototypes()
+    checked = 0
+    for name, (ret, params) in protos.items():
+        fn = getattr(lib, name)
+        if fn.argtypes is None:
+            continue
+        checked += 1
+        assert len(fn.argtypes) == len(params), (name, params, fn.argtypes)
+        for decl, ct in zip(params, fn.argtypes):
+            if "*" in decl:
+                assert ct is ctypes.c_void_p or ct is ctypes.c_char_p or hasattr(ct, "_type_") and \
+                    issubclass(ct, ctypes._Pointer), (name, decl, ct)
+            else:
+                base = decl.replace("const", "").split()[0]
+                assert ct is _C_TO_CTYPES[base], (name, decl, ct)
+        want = {"int": ctypes.c_int, "uint64_t": ctypes.c_uint64, "const char *": ctypes.c_char_p}[ret]
+        assert fn.restype is want, (name, ret, fn.restype)
+    assert checked >= 20, checked
+
+
 def test_capacity_and_workspace_queries(lib):
     assert moe.moe_route_capacity(24576, 128, 8, "tc") == 24576 * 8
     assert moe.moe_route_capacity(24576, 128, 8, "tr") == 24576 * 8 + 128 * 64
