@@ -1,0 +1,68 @@
+"""bench.py's roofline bookkeeping on the CPU.
+
+The algorithmic work of the GEMM launches adds up to the layer's FLOPs; an ncu --csv log of DRAM bytes is averaged
+per launch and kernel into the traffic table; the table's figures are used only while the CUDA sources are the ones
+they were captured on.
+"""
+import json
+
+import pytest
+
+import bench
+from fine_grained_mixture_gb300 import synth
+from oracle import moe_oracle as orc
+
+HEADER = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Block Size","Grid Size",'
+          '"Device","CC","Section Name","Metric Name","Metric Unit","Metric Value"\n')
+
+
+def _row(launch, kernel, metric, unit, value):
+    return (f'"{launch}","1","python3.12","127.0.0.1","{kernel}","1","7","(448, 1, 1)","(152, 1, 1)","0","10.3",'
+            f'"Command line profiler metrics","{metric}","{unit}","{value}"\n')
+
+
+@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+def test_gemm_work_adds_up_to_the_layer(name):
+    w = synth.WORKLOADS[name]
+    P = w.T * w.K
+    fwd, bwd = orc.layer_flops(P, w.n, w.d)
+    work = {k: bench.kernel_flops_bytes(k, w, P) for k in bench.GEMM_NAMES}
+    assert all(bound == "tensor" for bound, _ in work.values())
+    step = sum(work[k][1] for k in ("gemm_up", "gemm_down", "gemm_dh", "gemm_dx", "gemm_dw"))
+    assert step == fwd + bwd == 18 * w.T * w.n * w.K * w.d
+    assert work["gemm_dw1"][1] + work["gemm_dw2"][1] == work["gemm_dw"][1]
+
+
+def test_kernel_names_from_ncu():
+    assert bench.bench_kernel_name("void moe_gemm_kernel<6, 256, 3, 2, 0>(TensorMaps, GemmArgs)") == "gemm_dw"
+    assert bench.bench_kernel_name("moe_gemm_kernel<(int)0, 256, 4, 1, 0>") == "gemm_up"
+    assert bench.bench_kernel_name("void route_topk_kernel<4, 0>(const float *, int)") == "route_topk"
+    assert bench.bench_kernel_name("void some_library_kernel()") is None
+
+
+def test_ingest_averages_per_launch_and_goes_stale_with_the_source(tmp_path, monkeypatch):
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    dw = "void moe_gemm_kernel<6, 256, 3, 2, 0>(TensorMaps, GemmArgs)"
+    csv = tmp_path / "traffic.csv"
+    csv.write_text("==PROF== Connected to process 1\n" + HEADER
+                   + _row(0, dw, "dram__bytes_read.sum", "Gbyte", "1.5")
+                   + _row(0, dw, "dram__bytes_write.sum", "Mbyte", "500")
+                   + _row(0, dw, "gpu__time_duration.sum", "us", "350")
+                   + _row(1, dw, "dram__bytes_read.sum", "byte", "500,000,000")
+                   + _row(1, dw, "dram__bytes_write.sum", "byte", "0")
+                   + _row(1, dw, "gpu__time_duration.sum", "ns", "250000")
+                   + _row(2, "void some_library_kernel()", "dram__bytes_read.sum", "byte", "7"))
+    monkeypatch.setattr(bench, "source_sha", lambda: "digest-a")
+    assert bench.ingest_ncu(str(csv), "fine7b") == 0
+    table = json.loads((tmp_path / "profiles" / "dram_traffic.json").read_text())
+    ent = table["gemm_dw"]["fine7b"]
+    assert ent["launches"] == 2 and ent["source_sha"] == "digest-a"
+    assert ent["read"] == pytest.approx(1.0e9) and ent["write"] == pytest.approx(2.5e8)
+    assert ent["bytes_per_launch"] == pytest.approx(1.25e9) and ent["ncu_time_us"] == pytest.approx(300.0)
+    assert set(table) == {"gemm_dw"}
+    assert bench.load_traffic("gemm_dw", "fine7b") == pytest.approx(1.25e9)
+    assert bench.load_traffic("gemm_dw", "sparse") is None
+    monkeypatch.setattr(bench, "source_sha", lambda: "digest-b")   # the kernels changed since the capture
+    assert bench.load_traffic("gemm_dw", "fine7b") is None
+
