@@ -66,3 +66,41 @@ def test_ingest_averages_per_launch_and_goes_stale_with_the_source(tmp_path, mon
     monkeypatch.setattr(bench, "source_sha", lambda: "digest-b")   # the kernels changed since the capture
     assert bench.load_traffic("gemm_dw", "fine7b") is None
 
+
+
+FAKE_SMI = r'''#!/usr/bin/env python3
+import sys, time
+# stand-in for the query loop: index, SM clock, max SM clock, power, active mask, then four throttle reasons
+for i in range(40):
+    now = time.time()
+    stamp = time.strftime("%Y/%m/%d %H:%M:%S", time.localtime(now)) + ".%03d" % int((now % 1) * 1000)
+    cap = "Active" if i == 3 else "Not Active"
+    print(f"{stamp}, 0, {2070 - 10 * (i % 2)}, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, {cap}",
+          flush=True)
+    time.sleep(0.05)
+'''
+
+
+def test_clock_sampler_reads_median_clock_and_throttle_reasons(tmp_path, monkeypatch):
+    smi = tmp_path / "nvidia-smi"
+    smi.write_text(FAKE_SMI)
+    smi.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{tmp_path}:{bench.os.environ['PATH']}")
+    sampler = bench.ClockSampler(0)
+    sampler.start()
+    t0 = bench.time.time()
+    bench.time.sleep(0.5)
+    t1 = bench.time.time()
+    out = sampler.stop(t0, t1)
+    assert out["samples"] >= 3 and out["samples_in_timed_region"] >= 3
+    assert out["sm_max_mhz"] == 2070.0
+    assert out["sm_mhz"] in (2060.0, 2065.0, 2070.0)
+    assert out["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_sampler_without_nvidia_smi(tmp_path, monkeypatch):
+    monkeypatch.setenv("PATH", str(tmp_path))
+    sampler = bench.ClockSampler(0)
+    sampler.start()
+    out = sampler.stop(0.0, 1.0)
+    assert out["sm_mhz"] is None and out["reasons"] == ["nvidia-smi unavailable"]
