@@ -435,9 +435,3 @@ def layer(X, W1, W2, dO, rt: dict):
     bwd = backward(dO, X, W1, W2, rt["row_token"], rt["row_expert"], rt["row_score"], fwd)
     return fwd, bwd
 
-
-def subset_rows(rt: dict, rows: np.ndarray) -> dict:
-    """The per-row routing data of a subset of rows (for sampled checks at full size)."""
-    rows = np.asarray(rows, dtype=np.int64)
-    return dict(row_token=rt["row_token"][rows], row_expert=rt["row_expert"][rows],
-                row_score=rt["row_score"][rows], rows=rows)

@@ -523,3 +523,32 @@ def test_router_backward_through_x_and_wr(mode):
             arr[i] = old
             g[i] = (lp - lm) / (2 * h)
         assert np.abs(g - out[name]).max() <= 1e-7 * max(np.abs(out[name]).max(), 1.0), name
+
+
+# -------------------------------------------------------------------- restriction used by sampled checks
+
+
+def test_oracle_on_rows_equals_the_full_layer_where_the_rows_decide():
+    """The full-size GPU checks run the oracle on a subset of rows: those of some tokens (their O and dX rows,
+    and the rows' H and dS) or of one expert (its dW1 and dW2).  On a small layer that subset computation must
+    equal the full oracle there, up to the last bits of fp64 (the library matmul may block a different number of
+    rows differently)."""
+    close = lambda a, b: np.allclose(a, b, rtol=1e-12, atol=1e-14)   # noqa: E731
+    from gpu_util import oracle_on_rows
+
+    w = synth.custom(300, 64, 32, 8, 2, skew=True)
+    inp = synth.make_inputs(w, 3)
+    ref = orc.route(inp["logits"].numpy(), w.K, "tr", 16)
+    f64 = lambda t: t.double().numpy()                      # noqa: E731
+    full_f, full_b = orc.layer(f64(inp["X"]), f64(inp["W1"]), f64(inp["W2"]), f64(inp["dO"]), ref)
+    toks = np.array([0, 7, 150, 299])
+    rows = np.nonzero(np.isin(ref["row_token"], toks))[0]
+    _, fwd, bwd = oracle_on_rows(inp, ref, rows)
+    assert close(fwd["O"][toks], full_f["O"][toks]) and close(bwd["dX"][toks], full_b["dX"][toks])
+    assert close(fwd["H"], full_f["H"][rows]) and close(bwd["dS"], full_b["dS"][rows])
+    assert not close(fwd["O"][toks] * 1.001, full_f["O"][toks])
+    for e in np.nonzero(ref["counts"])[0][:3]:
+        erows = np.arange(ref["offsets"][e], ref["offsets"][e + 1])
+        experts, _, be = oracle_on_rows(inp, ref, erows)
+        assert list(experts) == [e]
+        assert close(be["dW1"][0], full_b["dW1"][e]) and close(be["dW2"][0], full_b["dW2"][e])
