@@ -47,7 +47,7 @@ def test_routing_edge_shapes(T, E, K, ties, mode):
     gen = torch.Generator().manual_seed(T * 7 + E)
     z = torch.randn((T, E), generator=gen)
     if ties:
-        z = torch.round(z * 2) / 2          # many equal logits: exercises every tie-break rule
+        z = torch.round(z * 2) / 2          # many equal logits, -0.0 beside +0.0: every tie-break rule
     rt, P, ref = _route_both(z, K, mode, seed=T)
     check_routing(rt, ref, P)
 

@@ -29,7 +29,7 @@ def test_topk_bruteforce_with_ties():
     rng = np.random.default_rng(1)
     for _ in range(200):
         T, E, K = 3, 5, int(rng.integers(1, 5))
-        z = rng.choice([-1.0, 0.0, 0.5, 1.0], size=(T, E)).astype(np.float32)
+        z = rng.choice([-1.0, -0.0, 0.0, 0.5, 1.0], size=(T, E)).astype(np.float32)   # -0.0 ties +0.0
         got = orc.topk_token_choice(z, K)
         for t in range(T):
             # brute force: the K-subset whose (logit desc, expert asc) key list is smallest, listed in key order
