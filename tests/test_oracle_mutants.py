@@ -89,6 +89,19 @@ MUTANTS = [
      "dX = -_matmul(dz, np.asarray(Wr, np.float64).T)", "router_backward_through"),
     ("router: dW_r from the logits", "dWr = _matmul(np.asarray(X, np.float64).T, dz)",
      "dWr = _matmul(np.asarray(X, np.float64).T, z - z.mean())", "router_backward_through"),
+    # more lines of the same functions
+    ("gate exponent with the wrong sign", "return np.exp(zs - z0[:, None]) / den[:, None]",
+     "return np.exp(z0[:, None] - zs) / den[:, None]", "scores_are_softmax or routing_golden"),
+    ("token-rounding slot looked up in expert 0", "slots = slot_of[kept, e]", "slots = slot_of[kept, 0]",
+     "routing_golden or tr_bruteforce"),
+    ("expert-choice slot looked up in expert 0", "expert_rows.append((kept, slot_of[kept, e], prob[kept, e]))",
+     "expert_rows.append((kept, slot_of[kept, 0], prob[kept, e]))", "routing_golden or ec_per_expert"),
+    ("router: token rounding normalised over all experts",
+     'N = np.arange(E) if mode == "ec" else np.asarray(rt["topk_idx"][t])', "N = np.arange(E)", "router_dz"),
+    ("down-projection fed the gate instead of A", "Ye = _matmul(Ae, W2[e])", "Ye = _matmul(He[:, :n], W2[e])",
+     "dense_swiglu or ds_via_h or " + FD),
+    ("dX from the gate half of dH only", "dXt[sel] = _matmul(dHe, W1[e].T)",
+     "dXt[sel] = _matmul(np.concatenate([dg, 0 * du], axis=1), W1[e].T)", FD),
     # accounting
     ("backward FLOPs counted as the forward's", "return 6 * P * n * d, 12 * P * n * d",
      "return 6 * P * n * d, 6 * P * n * d", "flop_count"),
