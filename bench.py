@@ -102,20 +102,23 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.path = None
+        self.out = None
 
     def start(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
-        os.close(fd)
+        self.out = os.fdopen(fd, "w")
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
         time.sleep(0.3)
 
     def stop(self, t0, t1):
+        self.out.close()
         if self.proc is None:
+            os.unlink(self.path)
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         time.sleep(0.25)
         self.proc.terminate()
@@ -124,7 +127,9 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         rows = []
-        for line in open(self.path):
+        with open(self.path) as f:
+            lines = f.readlines()
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 10:
                 continue

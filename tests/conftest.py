@@ -8,7 +8,10 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+@pytest.hookimpl(tryfirst=True)
 def pytest_configure(config):
+    if config.option.basetemp is None:   # keep tmp_path directories inside the repository (git-ignored)
+        config.option.basetemp = os.path.join(ROOT, ".pytest_tmp")
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: long-running (full-size workloads)")
     _plant_oracle_mistake()
@@ -37,7 +40,8 @@ def load_golden(name):
     path = os.path.join(ROOT, "tests", "golden", name)
     out = {"expect": {}}
     cur = out
-    lines = [l.strip() for l in open(path) if l.strip() and not l.startswith("#")]
+    with open(path) as f:
+        lines = [l.strip() for l in f if l.strip() and not l.startswith("#")]
     i = 0
     while i < len(lines):
         parts = lines[i].split()

@@ -13,7 +13,8 @@ HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(moe_\w+)\s*\(", text, flags=re.M)))
 
@@ -37,7 +38,8 @@ def test_every_declared_symbol_is_exported(lib):
 
 def declared_prototypes():
     """{name: (return type, [parameter declarations])} of every function include/moe.h declares."""
-    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    with open(HEADER) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
     out = {}
     for ret, name, params in re.findall(r"^\s*((?:const\s+)?[A-Za-z_][\w\s\*]*?)\b(moe_\w+)\s*\(([^)]*)\)\s*;",
                                         text, flags=re.M):

@@ -86,6 +86,7 @@ def test_clock_sampler_reads_median_clock_and_throttle_reasons(tmp_path, monkeyp
     smi.write_text(FAKE_SMI)
     smi.chmod(0o755)
     monkeypatch.setenv("PATH", f"{tmp_path}:{bench.os.environ['PATH']}")
+    monkeypatch.setattr(bench.tempfile, "tempdir", str(tmp_path))   # the sample file stays in the test's folder
     sampler = bench.ClockSampler(0)
     sampler.start()
     t0 = bench.time.time()
@@ -96,11 +97,14 @@ def test_clock_sampler_reads_median_clock_and_throttle_reasons(tmp_path, monkeyp
     assert out["sm_max_mhz"] == 2070.0
     assert out["sm_mhz"] in (2060.0, 2065.0, 2070.0)
     assert out["reasons"] == ["sw_power_cap"]
+    assert not list(tmp_path.glob("*.csv"))
 
 
 def test_clock_sampler_without_nvidia_smi(tmp_path, monkeypatch):
     monkeypatch.setenv("PATH", str(tmp_path))
+    monkeypatch.setattr(bench.tempfile, "tempdir", str(tmp_path))
     sampler = bench.ClockSampler(0)
     sampler.start()
     out = sampler.stop(0.0, 1.0)
     assert out["sm_mhz"] is None and out["reasons"] == ["nvidia-smi unavailable"]
+    assert not list(tmp_path.glob("*.csv"))                          # the sample file is removed

@@ -110,7 +110,8 @@ MUTANTS = [
 
 
 def test_every_planted_line_is_in_the_oracle():
-    src = open(ORACLE).read()
+    with open(ORACLE) as f:
+        src = f.read()
     for name, old, new, _ in MUTANTS:
         assert src.count(old) == 1, name
         assert old != new, name
@@ -118,8 +119,10 @@ def test_every_planted_line_is_in_the_oracle():
 
 def _run_pins_against(old, new, pins):
     env = dict(os.environ, MOE_ORACLE_MUTANT=json.dumps([old, new]))
+    tag = f"{abs(hash((old, new))):x}"   # each child gets a temporary directory of its own
     cmd = [sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_oracle.py"), "-x", "-q",
-           "-p", "no:cacheprovider", "-m", "not gpu", "-k", pins]
+           "-p", "no:cacheprovider", "-m", "not gpu", "-k", pins,
+           "--basetemp", os.path.join(ROOT, ".pytest_tmp_children", tag)]
     return subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
 
 
