@@ -74,34 +74,31 @@ void prof_end(cudaStream_t s) {
   if (!p.recs.empty()) cudaEventRecord(p.recs.back().stop, s);
 }
 
-constexpr int kMaxDevices = 64;
-
 int num_sms() {
-  static int cache[kMaxDevices] = {0};
+  static DeviceCache cache;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
-  if (cache[dev] == 0) {
+  return cache.get(dev, [&]() {
     int n = 0;
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cache[dev] = n > 0 ? n : 1;
-  }
-  return cache[dev];
+    return n > 0 ? n : 1;
+  });
 }
 
-// 0 = not checked yet, 1 = supported, 2 = not supported
-static int check_device() {
-  static int cache[kMaxDevices] = {0};
+// MOE_OK on a compute capability 10.3 device, else MOE_ERR_DEVICE (or MOE_ERR_CUDA when no device is current).
+int check_device() {
+  static DeviceCache cache;  // 1 = supported, 2 = not supported
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return record_cuda_error(err);
   if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_DEVICE;
-  if (cache[dev] == 0) {
+  const int v = cache.get(dev, [&]() {
     int major = 0, minor = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-    cache[dev] = (major == 10 && minor == 3) ? 1 : 2;
-  }
-  return cache[dev] == 1 ? MOE_OK : MOE_ERR_DEVICE;
+    return (major == 10 && minor == 3) ? 1 : 2;
+  });
+  return v == 1 ? MOE_OK : MOE_ERR_DEVICE;
 }
 
 // Memory-bound steps that do not feed the next GEMM (zeroing an fp32 accumulator, the final cast of dX)
@@ -176,15 +173,17 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+static EncodeTiledFn lookup_encode_fn() {
+  void *p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<EncodeTiledFn>(p);
+  return nullptr;
+}
+
 static EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
+  static const EncodeTiledFn fn = lookup_encode_fn();  // initialised once, thread-safe
   return fn;
 }
 

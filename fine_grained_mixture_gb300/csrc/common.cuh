@@ -1,5 +1,6 @@
-// common.cuh - device helpers for sm_103a: mbarriers with bounded waits, TMA (tiled and gather4),
-// tcgen05 (TMEM alloc, UMMA issue/commit, TMEM loads) and shared-memory matrix descriptors.
+// common.cuh - device helpers for sm_103a: mbarriers with bounded waits, TMA tiled loads and stores, bulk
+// copies and reduce-adds, tcgen05 (TMEM alloc, UMMA issue/commit, TMEM loads) and shared-memory matrix
+// descriptors.  Every copy targets the issuing CTA's own shared memory.
 #pragma once
 
 #include <cuda.h>
@@ -92,17 +93,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm,
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
       "l"(tm), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
-      : "memory");
-}
-
-// Multicast variant: the box lands at the same shared-memory offset in every CTA of `cta_mask` and
-// completes `bytes` on the mbarrier at the same offset in each of them.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *tm, int c0, int c1, uint32_t bar,
-                                               uint16_t cta_mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
-      "l"(tm), "r"(c0), "r"(c1), "r"(bar), "h"(cta_mask), "l"(policy)
       : "memory");
 }
 
@@ -199,14 +189,6 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
                : "memory");
 }
 
-// Arrive on the mbarrier at offset `bar` of every CTA in `cta_mask` once this thread's MMAs complete.
-__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   bar),
-               "h"(cta_mask)
-               : "memory");
-}
-
 // Each thread of the warp reads 32 consecutive fp32 columns of its TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
@@ -245,31 +227,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
          | ((b_mn_major ? 1u : 0u) << 16)            // B major-ness
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
-}
-
-// ------------------------------------------------------------------------------------------ cluster
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_id_x() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t num_clusters_x() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-  return r;
-}
-
-// Every thread of every CTA in the cluster arrives (release) and waits (acquire).
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // ------------------------------------------------------------------------ programmatic dependent launch

@@ -24,9 +24,9 @@
 // the gather out of L1.
 // Tiles: 128 x BN x 64 (256-row blocks in the weight gradients), STAGES-deep shared-memory ring, two TMEM
 // accumulators of BN fp32 columns.  Each CTA decodes its tiles once into shared memory.
-// CTAs run in clusters of two on neighbouring tiles.  Where the two tiles need the same TMA-loaded operand
-// (down, dH, the weight gradients) each CTA loads half of it and multicasts it to both, and a stage is
-// released to both producers by a multicast commit; the up-projection and dX~ run unpaired.
+// CTAs 2i and 2i+1 take neighbouring tiles (consecutive m-tiles of one expert, or neighbouring tiles of one
+// weight gradient), so the operand they share is read from L2 by the second CTA; every CTA loads its whole
+// tiles itself and releases its own stages (no clusters, nothing is sent between CTAs).
 // Every wait is bounded; on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT, drains its own copies and
 // MMAs, frees TMEM and returns.
 #pragma once
@@ -55,11 +55,6 @@ struct Traits {
   static constexpr bool a_mn = varlen_k;  // A operand MN-major in shared memory
   static constexpr bool b_mn = (MODE == kUp || MODE == kDown || varlen_k);
   static constexpr bool nt_outer = (MODE == kDown || MODE == kDX);  // keep one fp32 column slab hot in L2
-  // Paired CTAs of a cluster split the shared operand and multicast it, so each stage is released only when
-  // both CTAs' MMAs are done with it.  That lockstep costs more than the saved L2 reads where the CTAs' load
-  // latencies differ most (the X gather of the up-projection, the dense dH stream of dX~): there each CTA
-  // loads its whole tile and releases its own stages.
-  static constexpr bool paired = !(MODE == kUp || MODE == kDX);
 };
 
 constexpr int kGatherThreads = 128;
@@ -121,8 +116,7 @@ __host__ __device__ constexpr int epi_bytes() {
 
 struct Tile {
   int e, m0, n0, row0, row_end, kblocks;
-  bool shared;  // both CTAs of the cluster need the same shared-operand tile (load halves + multicast)
-  bool w2;      // weight gradients: a dW2 tile (gathered B, TMA-loaded A) rather than a dW1 tile
+  bool w2;  // weight gradients: a dW2 tile (gathered B, TMA-loaded A) rather than a dW1 tile
 };
 
 // Pairs of one expert's weight-gradient tiles: dW1 pairs along M (they share the dH tile), dW2 pairs along N
@@ -144,7 +138,7 @@ __device__ __forceinline__ int find_expert(const int32_t *__restrict__ tile_offs
   return lo;
 }
 
-// Number of cluster work items (pairs of tiles).
+// Number of work items (pairs of tiles; CTA 2i + rank takes tile `rank` of pair i, i + grid/2, ...).
 template <int MODE, int BN, int MB>
 __device__ __forceinline__ int total_pairs(const GemmArgs &a, int total_m) {
   const int n_tiles = a.Ndim / BN;
@@ -159,7 +153,6 @@ template <int MODE, int BN, int MB>
 __device__ __forceinline__ Tile decode_tile(const GemmArgs &a, int pair, int rank, int total_m) {
   Tile t;
   const int n_tiles = a.Ndim / BN;
-  t.shared = true;
   t.w2 = false;
   if (Traits<MODE>::varlen_k) {
     bool w2 = MODE == kDW2;
@@ -223,9 +216,6 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &a, int pair, int ran
     }
     const int mt = 2 * mp + rank;
     t.e = find_expert(a.tile_offsets, a.E, mt);
-    // the partner tile shares this weight tile only if it exists and belongs to the same expert
-    const int partner = 2 * mp + (rank ^ 1);
-    t.shared = Traits<MODE>::paired && (2 * mp + 1 < total_m) && find_expert(a.tile_offsets, a.E, partner) == t.e;
     t.m0 = 0;
     t.n0 = a.n_off + nt * BN;  // n_off: first output column of this launch
     // a missing last tile (odd tile count) runs on rows past the last expert: zero operands, no output
@@ -237,7 +227,6 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &a, int pair, int ran
       t.row_end = t.row0;  // nothing is written
     }
   }
-  if (!Traits<MODE>::paired) t.shared = false;
   return t;
 }
 
@@ -246,7 +235,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &a, int pair, int ran
 constexpr int kTileCache = 128;  // tiles per CTA kept in shared memory; later tiles are decoded on the fly
 struct TileRec {
   int row0, row_end;
-  uint32_t e_nt;  // expert (bits 0-15) | n-tile (bits 16-30) | shared (bit 31)
+  uint32_t e_nt;  // expert (bits 0-15) | n-tile (bits 16-31)
 };
 template <int MODE>
 __host__ __device__ constexpr int tile_cache_bytes() {
@@ -261,8 +250,7 @@ __device__ __forceinline__ Tile tile_at(const GemmArgs &a, const TileRec *cache,
   const TileRec r = cache[i];
   Tile t;
   t.e = static_cast<int>(r.e_nt & 0xffffu);
-  t.n0 = static_cast<int>((r.e_nt >> 16) & 0x7fffu) * BN;
-  t.shared = (r.e_nt >> 31) != 0u;
+  t.n0 = static_cast<int>(r.e_nt >> 16) * BN;
   t.w2 = false;
   t.m0 = 0;
   t.row0 = r.row0;
@@ -327,7 +315,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), TR::gather ? 1 + kGatherThreads : 1);
-      mbar_init(empty_bar(s), TR::paired ? 2 : 1);  // released by the MMA issuers of both CTAs (paired)
+      mbar_init(empty_bar(s), 1);  // released by this CTA's MMA issuer
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -354,16 +342,16 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  cluster_sync();  // barriers of both CTAs initialised before any multicast lands in them
+  __syncthreads();  // barriers initialised and the TMEM address published before any role starts
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // everything above overlaps the previous kernel's tail; its outputs are read only after this wait
   griddep_wait();
   griddep_launch_dependents();
 
-  const int rank = static_cast<int>(cluster_ctarank());
-  const int first_pair = static_cast<int>(cluster_id_x());
-  const int pair_step = static_cast<int>(num_clusters_x());
+  const int rank = static_cast<int>(blockIdx.x & 1u);
+  const int first_pair = static_cast<int>(blockIdx.x >> 1);
+  const int pair_step = static_cast<int>(gridDim.x >> 1);  // the grid is even
   const int total_m = TR::varlen_k ? 0 : __ldg(&a.tile_offsets[a.E]);
   const int total = total_pairs<MODE, BN, MB>(a, total_m);
   TileRec *tile_cache = reinterpret_cast<TileRec *>(gbase + SM::kCacheOff);
@@ -372,9 +360,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
     for (int i = threadIdx.x; i < min(mine, kTileCache); i += blockDim.x) {
       const int pair = first_pair + i * pair_step;
       const Tile t = decode_tile<MODE, BN, MB>(a, pair, rank, total_m);
-      tile_cache[i] = TileRec{t.row0, t.row_end,
-                              static_cast<uint32_t>(t.e) | (static_cast<uint32_t>(t.n0 / BN) << 16) |
-                                  (t.shared ? 0x80000000u : 0u)};
+      tile_cache[i] = TileRec{t.row0, t.row_end, static_cast<uint32_t>(t.e) | (static_cast<uint32_t>(t.n0 / BN) << 16)};
     }
     __syncthreads();
   }
@@ -409,44 +395,38 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
           const uint32_t a_dst = sA + s * SM::kABytesMB;
           const uint32_t b_dst = sB + s * SM::kBBytes;
           const uint32_t fb = full_bar(s);
-          // the shared operand: this CTA's half (multicast to both) or, when the partner needs a
-          // different tile, the whole tile locally
-          auto shared_box = [&](uint32_t dst, const CUtensorMap *tmap, int c0, int c1, bool mine) {
-            if (!t.shared) tma_load_2d(dst, tmap, c0, c1, fb, pol_w);
-            else if (mine) tma_load_2d_mc(dst, tmap, c0, c1, fb, 0x3, pol_w);
-          };
           if (MODE == kUp) {
             // W1_e rows [kb*64, +64): gate columns [n0/2, +128) and up columns [n + n0/2, +128)
             const int hcol = t.n0 / 2;
             const int wrow = t.e * a.d + kb * kBK;
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-              shared_box(b_dst + c * 8192, &tmB, (c < 2 ? 0 : a.n) + hcol + (c & 1) * 64, wrow, (c >> 1) == rank);
+              tma_load_2d(b_dst + c * 8192, &tmB, (c < 2 ? 0 : a.n) + hcol + (c & 1) * 64, wrow, fb, pol_w);
           } else if (MODE == kDH) {
             // K-major W2_e: N index = rows n0..n0+BN of W2_e (two halves), K-elements [kb*64, +64)
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-              shared_box(b_dst + h * (BN / 2) * 128, &tmB, kb * kBK, t.e * a.n + t.n0 + h * (BN / 2), h == rank);
+              tma_load_2d(b_dst + h * (BN / 2) * 128, &tmB, kb * kBK, t.e * a.n + t.n0 + h * (BN / 2), fb, pol_w);
           } else if (MODE == kDown) {
             tma_load_2d(a_dst, &tmA, kb * kBK, t.row0, fb, pol_x);
 #pragma unroll
             for (int c = 0; c < BN / 64; ++c)
-              shared_box(b_dst + c * 8192, &tmB, t.n0 + c * 64, t.e * a.n + kb * kBK, (c * 2) / (BN / 64) == rank);
+              tma_load_2d(b_dst + c * 8192, &tmB, t.n0 + c * 64, t.e * a.n + kb * kBK, fb, pol_w);
           } else if (MODE == kDX) {
             tma_load_2d(a_dst, &tmA, kb * kBK, t.row0, fb, pol_x);
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-              shared_box(b_dst + h * (BN / 2) * 128, &tmB, kb * kBK, t.e * a.d + t.n0 + h * (BN / 2), h == rank);
+              tma_load_2d(b_dst + h * (BN / 2) * 128, &tmB, kb * kBK, t.e * a.d + t.n0 + h * (BN / 2), fb, pol_w);
           } else if (MODE == kDW1 || (MODE == kDW && !t.w2)) {
             // B = dH rows [rb, rb+64) (MN-major); rows past the expert meet zero A rows
 #pragma unroll
             for (int c = 0; c < BN / 64; ++c)
-              shared_box(b_dst + c * 8192, &tmB, t.n0 + c * 64, t.row0 + kb * kBK, (c * 2) / (BN / 64) == rank);
+              tma_load_2d(b_dst + c * 8192, &tmB, t.n0 + c * 64, t.row0 + kb * kBK, fb, pol_w);
           } else {
             // kDW2: A = (s*A) rows [rb, rb+64) (MN-major); rows past the expert meet zero B rows
 #pragma unroll
             for (int c = 0; c < MB * kBM / 64; ++c)
-              shared_box(a_dst + c * 8192, &tmA, t.m0 + c * 64, t.row0 + kb * kBK, c / MB == rank);
+              tma_load_2d(a_dst + c * 8192, &tmA, t.m0 + c * 64, t.row0 + kb * kBK, fb, pol_w);
           }
           ++issued;
           if (++s == STAGES) {
@@ -591,8 +571,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
               umma_bf16(d_tmem + mb * BN, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
             }
           }
-          if (TR::paired) umma_commit_mc(empty_bar(s), 0x3);  // the stage is free for the producers of both CTAs
-          else umma_commit(empty_bar(s));
+          umma_commit(empty_bar(s));  // the stage is free once these MMAs have read it
           if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
@@ -968,47 +947,41 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
-  cluster_sync();  // the partner's multicasts and stage releases into this CTA are all done
 }
 
-// Host launcher for one instantiation: clusters of two CTAs, one CTA per SM, as many clusters as fit.
+// Host launcher for one instantiation: one CTA per SM, an even number of CTAs (CTA 2i + rank takes tile
+// `rank` of each of its pairs).  The shared-memory attribute and the grid size are set up once per device.
 template <int MODE, int BN, int STAGES, int MB = 1, bool DET = false>
 int launch_gemm(const GemmArgs &a, const TensorMaps &tm, cudaStream_t stream) {
   using SM = Smem<BN, STAGES, epi_bytes<MODE, MB>(), MB, tile_cache_bytes<MODE>()>;
-  static int attr_dev = -1;
-  static int grid_cache = 0;
+  auto kernel = moe_gemm_kernel<MODE, BN, STAGES, MB, DET>;
+  static DeviceCache grid_cache;
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return record_cuda_error(err);
+  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_DEVICE;
+  const int grid = grid_cache.get(dev, [&]() -> int {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
+    if (e != cudaSuccess) return -static_cast<int>(e);
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, cta_threads<MODE, MB>(), SM::kBytes);
+    if (e != cudaSuccess || per_sm <= 0) per_sm = 1;
+    return 2 * ((num_sms() * per_sm) / 2);
+  });
+  if (grid <= 0) return record_cuda_error(static_cast<cudaError_t>(-grid));
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(cta_threads<MODE, MB>(), 1, 1);
   cfg.dynamicSmemBytes = SM::kBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;  // occupancy query with the cluster shape only
-  if (attr_dev != dev) {
-    err = cudaFuncSetAttribute(moe_gemm_kernel<MODE, BN, STAGES, MB, DET>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               SM::kBytes);
-    if (err != cudaSuccess) return record_cuda_error(err);
-    int clusters = 0;
-    cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
-    err = cudaOccupancyMaxActiveClusters(&clusters, moe_gemm_kernel<MODE, BN, STAGES, MB, DET>, &cfg);
-    if (err != cudaSuccess || clusters <= 0) clusters = num_sms() / 2;
-    grid_cache = 2 * clusters;
-    attr_dev = dev;
-  }
-  cfg.gridDim = dim3(grid_cache, 1, 1);
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   static const char *const kNames[] = {"gemm_up", "gemm_down", "gemm_dh", "gemm_dx", "gemm_dw1", "gemm_dw2", "gemm_dw"};
   prof_begin(kNames[MODE], stream);
-  err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<MODE, BN, STAGES, MB, DET>, tm, a);
+  err = cudaLaunchKernelEx(&cfg, kernel, tm, a);
   prof_end(stream);
   count_launch();
   if (err == cudaSuccess) err = cudaGetLastError();

@@ -6,6 +6,9 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "moe.h"
 
 namespace moe {
@@ -13,6 +16,26 @@ namespace moe {
 constexpr int kMaxTrTokens = 49152;  // token rounding keeps one expert's keys for all T tokens in shared memory
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
+constexpr int kMaxDevices = 64;
+
+// One positive int per device (a grid size, or 1 for "attributes set"), computed once by the first call on
+// that device and safe to read from several host threads at once.  `init` runs under the lock; a result <= 0
+// (a failure code) is returned but not kept, so the next call tries again.
+struct DeviceCache {
+  std::atomic<int> value[kMaxDevices];
+  std::mutex mu;
+  template <class F>
+  int get(int dev, F &&init) {
+    int v = value[dev].load(std::memory_order_acquire);
+    if (v > 0) return v;
+    std::lock_guard<std::mutex> lk(mu);
+    v = value[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    v = init();
+    if (v > 0) value[dev].store(v, std::memory_order_release);
+    return v;
+  }
+};
 
 // Remembers `err` as this thread's last CUDA error and returns MOE_ERR_CUDA.
 int record_cuda_error(cudaError_t err);
@@ -94,6 +117,9 @@ int make_tmap_bf16(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t r
 int make_tmap_bf16_epi(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t rows);
 
 int num_sms();
+// MOE_OK when the current device is compute capability 10.3 (the only target of this library), else
+// MOE_ERR_DEVICE, or MOE_ERR_CUDA when no device can be made current.
+int check_device();
 
 // det: deterministic aggregation (fixed-point accumulators, dS partials per column tile)
 int launch_up(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s);

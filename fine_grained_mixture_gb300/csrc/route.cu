@@ -756,26 +756,30 @@ int launch_route(const float *logits, const float *uniforms, int T, int E, int K
   const int den_all = mode == MOE_ROUTE_EC ? 1 : 0;
   const size_t topk_smem = route_topk_smem_bytes(E, mode);
   const int nv = (E + 31) / 32;
-  // the key tile of E = 1024 needs more than the default 48 KB of dynamic shared memory
-  static int attr_dev = -1;
+  // the key tile of E = 1024 needs more than the default 48 KB of dynamic shared memory (set once per device)
+  static DeviceCache attrs;
   int dev = 0;
-  cudaGetDevice(&dev);
+  err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return record_cuda_error(err);
+  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_DEVICE;
 #define MOE_TOPK_KERNEL(NV, TRB) route_topk_kernel<NV, TRB>
 #define MOE_TOPK_EACH(F)                                                                                          \
   F(1, false) F(2, false) F(4, false) F(8, false) F(16, false) F(32, false) F(1, true) F(2, true) F(4, true)      \
       F(8, true) F(16, true) F(32, true)
-  if (attr_dev != dev) {
+  const int attr_rc = attrs.get(dev, [&]() -> int {
+    cudaError_t e = cudaSuccess;
 #define MOE_TOPK_ATTR(NV, TRB)                                                                                    \
-  if (err == cudaSuccess)                                                                                         \
-    err = cudaFuncSetAttribute(MOE_TOPK_KERNEL(NV, TRB), cudaFuncAttributeMaxDynamicSharedMemorySize,             \
-                               static_cast<int>(route_topk_smem_bytes(1024, TRB ? MOE_ROUTE_TR : MOE_ROUTE_TC)));
+  if (e == cudaSuccess)                                                                                           \
+    e = cudaFuncSetAttribute(MOE_TOPK_KERNEL(NV, TRB), cudaFuncAttributeMaxDynamicSharedMemorySize,               \
+                             static_cast<int>(route_topk_smem_bytes(1024, TRB ? MOE_ROUTE_TR : MOE_ROUTE_TC)));
     MOE_TOPK_EACH(MOE_TOPK_ATTR)
 #undef MOE_TOPK_ATTR
-    if (err == cudaSuccess) err = cudaFuncSetAttribute(route_fill_tr_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                       static_cast<int>(kTrDynSmemMax));
-    if (err != cudaSuccess) return record_cuda_error(err);
-    attr_dev = dev;
-  }
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(route_fill_tr_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kTrDynSmemMax));
+    return e == cudaSuccess ? 1 : -static_cast<int>(e);
+  });
+  if (attr_rc <= 0) return record_cuda_error(static_cast<cudaError_t>(-attr_rc));
 #undef MOE_TOPK_EACH
 #define MOE_TOPK_LAUNCH(NV)                                                                                       \
   do {                                                                                                            \

@@ -32,7 +32,10 @@ int scratch_address(void **out) {
   if (!g_scratch_addr[dev]) {
     void *p = nullptr;
     err = cudaGetSymbolAddress(&p, g_route_scratch);
-    if (err != cudaSuccess) return record_cuda_error(err);
+    if (err != cudaSuccess) {
+      cudaGetLastError();  // do not leave the failure pending for a later, unrelated error check
+      return record_cuda_error(err);
+    }
     g_scratch_addr[dev] = p;
   }
   *out = g_scratch_addr[dev];
@@ -44,6 +47,8 @@ int scratch_address(void **out) {
 
 extern "C" int moe_route_noalloc(const float *logits, int T, int E, int K, int mode, const moe_routing *r,
                                  int32_t *P_host, void *stream) {
+  // stochastic rounding needs per-expert uniforms, which only moe_route_ex takes
+  if (mode == MOE_ROUTE_TR_STOCHASTIC) return MOE_ERR_INVALID_ARG;
   size_t need = 0;
   int rc = moe_route_workspace_size(T, E, K, mode, &need);
   if (rc != MOE_OK) return rc;
@@ -55,6 +60,10 @@ extern "C" int moe_route_noalloc(const float *logits, int T, int E, int K, int m
     need = moe::route_workspace_bytes(T, E, K, mode, false);
   }
   if (need > MOE_ROUTE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
+  // the device check comes first, so a wrong GPU reads MOE_ERR_DEVICE (as from moe_route) rather than a
+  // failed symbol lookup
+  rc = moe::check_device();
+  if (rc != MOE_OK) return rc;
   void *scratch = nullptr;
   rc = moe::scratch_address(&scratch);
   if (rc != MOE_OK) return rc;

@@ -433,16 +433,17 @@ namespace {
 
 template <int MODE>
 int launch_router_gemm(const RouterMaps &tm, const RouterArgs &a, int grid, cudaStream_t s, const char *name) {
-  static int attr_dev = -1;
+  static DeviceCache attrs;  // the shared-memory attribute, set once per device
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return record_cuda_error(err);
-  if (attr_dev != dev) {
-    err = cudaFuncSetAttribute(router_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               RTraits<MODE>::kSmem);
-    if (err != cudaSuccess) return record_cuda_error(err);
-    attr_dev = dev;
-  }
+  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_DEVICE;
+  const int attr_rc = attrs.get(dev, [&]() -> int {
+    const cudaError_t e = cudaFuncSetAttribute(router_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               RTraits<MODE>::kSmem);
+    return e == cudaSuccess ? 1 : -static_cast<int>(e);
+  });
+  if (attr_rc <= 0) return record_cuda_error(static_cast<cudaError_t>(-attr_rc));
   prof_begin(name, s);
   err = launch_pdl(router_gemm_kernel<MODE>, dim3(grid), dim3(kRThreads), RTraits<MODE>::kSmem, s, tm, a);
   prof_end(s);

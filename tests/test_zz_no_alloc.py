@@ -47,10 +47,10 @@ def _same(a, b, P):
     np.testing.assert_allclose(a.row_score[:P].cpu().numpy(), b.row_score[:P].cpu().numpy(), rtol=1e-6, atol=0)
 
 
-@pytest.mark.parametrize("mode", ["tc", "tr"])
+@pytest.mark.parametrize("mode", ["tc", "tr", "tr_up", "tr_down", "ec"])
 @pytest.mark.parametrize("T,E,K", [(6144, 128, 8), (49152, 128, 8)])
 def test_noalloc_matches_workspace_route_twice(mode, T, E, K):
-    # at T=49152, E=128 token rounding's full scratch (with the 25 MB expert-major key copy) exceeds the
+    # at T=49152, E=128 the selection modes' full scratch (with the 25 MB expert-major key copy) exceeds the
     # static array, so the call takes the compact layout and reads the logits in place
     fn = _noalloc_fn()
     gen = torch.Generator().manual_seed(123)
@@ -77,3 +77,21 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     out = moe_routing()
     rc = fn(ctypes.c_void_p(dummy.data_ptr()), T, E, K, 0, ctypes.byref(out), None, None)
     assert rc == 3                            # MOE_ERR_WORKSPACE, before any device work
+
+
+def test_noalloc_compact_layout_is_taken_by_every_selection_mode():
+    # the shapes above exercise both scratch layouts: the full one fits at T=6144, only the compact one at 49152
+    cap = 16 << 20
+    for mode in ("tr", "tr_up", "tr_down", "ec"):
+        assert moe.moe_route_workspace_size(6144, 128, 8, mode) <= cap
+        assert moe.moe_route_workspace_size(49152, 128, 8, mode) > cap
+
+
+def test_noalloc_rejects_stochastic_rounding():
+    # stochastic rounding draws one uniform per expert, which only moe_route_ex takes
+    fn = _noalloc_fn()
+    logits = torch.randn((256, 16), device="cuda")
+    out = moe.Routing(256, 16, 2, "tr", logits.device)
+    rc = fn(ctypes.c_void_p(logits.data_ptr()), 256, 16, 2, moe.moe.MOE_ROUTE_TR_STOCHASTIC, ctypes.byref(out.struct),
+            None, None)
+    assert rc == 1                            # MOE_ERR_INVALID_ARG, before any device work
