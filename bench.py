@@ -10,8 +10,9 @@ E=128, K=8.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload fine7b] [--mode tc|tr]
   python bench.py --impl reference ...      # the CPU oracle on the host cores, bounded sample per step
 
-Multi-GPU: the layer is run as independent replicas, one per rank (weak scaling, no collective on the
-data path); launch with torchrun, rank 0 prints the line.
+Multi-GPU: data parallelism, one rank per GPU (launch with torchrun; rank 0 prints the line).  Every rank holds
+a replica of W1/W2 (broadcast from rank 0) and its own T tokens, runs route + forward + backward on them, and the
+step ends with the all-reduce of dW1 and dW2 over NCCL (weak scaling: the global batch is N*T tokens).
 """
 from __future__ import annotations
 
@@ -199,23 +200,40 @@ def oracle_call_experts(i, E):
     return [(i * ORACLE_EXPERTS_PER_CALL + j) % E for j in range(ORACLE_EXPERTS_PER_CALL)]
 
 
-def cpu_baseline(w, inp, mode, budget_s):
+def oracle_timing(workload, mode, budget_s=None, steps=None, warmup=1):
+    """Times the fp64 oracle's forward+backward on the host cores, one call of ORACLE_EXPERTS_PER_CALL experts'
+    rows per step: `steps` timed steps after `warmup`, or as many as fit in `budget_s` seconds.  Returns the
+    timed rows, seconds and calls.  Runs in a process without a CUDA context (see cpu_baseline)."""
+    w = synth.WORKLOADS[workload]
+    inp = synth.make_inputs(w, seed=0)
     ref, ref_inp = prepare_oracle_inputs(w, inp, mode)
-    oracle_sample(w, ref_inp, ref, oracle_call_experts(0, w.E))  # warm the BLAS threads
-    t0 = time.perf_counter()
-    rows = 0
-    calls = 0
+    for i in range(warmup):  # warms the BLAS threads and the allocator
+        oracle_sample(w, ref_inp, ref, oracle_call_experts(i, w.E))
+    rows, t_timed, calls = 0, 0.0, 0
     while True:
-        rows += oracle_sample(w, ref_inp, ref, oracle_call_experts(calls, w.E))
+        t0 = time.perf_counter()
+        rows += oracle_sample(w, ref_inp, ref, oracle_call_experts(warmup + calls, w.E))
+        t_timed += time.perf_counter() - t0
         calls += 1
-        if time.perf_counter() - t0 > budget_s:
+        if (steps is not None and calls >= steps) or (budget_s is not None and t_timed > budget_s):
             break
-    dt = time.perf_counter() - t0
-    flops = 18.0 * rows * w.n * w.d
-    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-            "sample": f"fp64 NumPy oracle forward+backward, {calls} calls of {ORACLE_EXPERTS_PER_CALL} experts' rows "
-                      f"each (experts cycled from 0; {rows} routed rows, {dt:.1f} s) of the {w.name} layer; "
-                      f"routing untimed"}
+    return {"rows": rows, "seconds": t_timed, "calls": calls, "P": int(ref["P"]), "cores": cpu_threads()}
+
+
+def cpu_baseline(w, mode, budget_s):
+    """The oracle timed on the host cores beside the GPU arm.  It runs in a spawned child process: a process
+    that holds a CUDA context pays more for its large host allocations and unmaps (the oracle allocates the
+    T x d outputs on every call), which measured the same oracle 1.7x slower than the reference arm's
+    CUDA-free process."""
+    import multiprocessing as mp
+
+    with mp.get_context("spawn").Pool(1) as pool:
+        r = pool.apply(oracle_timing, (w.name, mode), {"budget_s": budget_s})
+    flops = 18.0 * r["rows"] * w.n * w.d
+    return {"value": flops / r["seconds"] / 1e12, "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+            "sample": f"fp64 NumPy oracle forward+backward, {r['calls']} calls of {ORACLE_EXPERTS_PER_CALL} experts' "
+                      f"rows each (experts cycled from 0; {r['rows']} of {r['P']} routed rows, {r['seconds']:.1f} s) "
+                      f"of the {w.name} layer, in a CUDA-free child process; routing untimed"}
 
 
 def run_reference(args):
@@ -223,20 +241,9 @@ def run_reference(args):
     if rank != 0:
         return 0
     w = synth.WORKLOADS[args.workload]
-    inp = synth.make_inputs(w, seed=0)
-    ref, ref_inp = prepare_oracle_inputs(w, inp, args.mode)
     per_step = ORACLE_EXPERTS_PER_CALL
-    nsteps = args.warmup + args.steps
-    rows_timed = 0
-    t_timed = 0.0
-    for i in range(nsteps):
-        experts = oracle_call_experts(i, w.E)
-        t0 = time.perf_counter()
-        r = oracle_sample(w, ref_inp, ref, experts)
-        dt = time.perf_counter() - t0
-        if i >= args.warmup:
-            rows_timed += r
-            t_timed += dt
+    r = oracle_timing(w.name, args.mode, steps=args.steps, warmup=args.warmup)
+    rows_timed, t_timed = r["rows"], r["seconds"]
     flops = 18.0 * rows_timed * w.n * w.d
     value = flops / t_timed / 1e12
     sample = (f"fp64 NumPy oracle forward+backward on the rows of {per_step} experts per step "
@@ -259,10 +266,11 @@ def run_reference(args):
 class Layer:
     """Resident device buffers for one workload and the step = route + forward + backward."""
 
-    def __init__(self, w, inp, mode, dev, det=False):
+    def __init__(self, w, inp, mode, dev, det=False, a_from_h=False, allreduce=False):
         import fine_grained_mixture_gb300 as moe
 
-        self.moe, self.w, self.mode, self.det = moe, w, mode, det
+        self.moe, self.w, self.mode, self.det, self.a_from_h = moe, w, mode, det, a_from_h
+        self.allreduce = allreduce  # data parallel: sum dW1/dW2 over the ranks at the end of each step
         flags = moe.MOE_FLAG_DETERMINISTIC if det else 0
         self.g = {k: v.to(dev) for k, v in inp.items()}
         self.u = synth.make_uniforms(w.E, 0).to(dev)  # per-expert draws of stochastic rounding
@@ -275,7 +283,8 @@ class Layer:
         self.dW1 = torch.empty((w.E, w.d, 2 * w.n), dtype=bf, device=dev)
         self.dW2 = torch.empty((w.E, w.n, w.d), dtype=bf, device=dev)
         self.dS = torch.empty(p, dtype=torch.float32, device=dev)
-        self.wsf = torch.empty(moe.moe_forward_workspace_size(w.T, w.d, w.n, w.E, w.K, p, flags), dtype=torch.uint8,
+        fflags = flags | (moe.MOE_FLAG_A_FROM_H if a_from_h else 0)
+        self.wsf = torch.empty(moe.moe_forward_workspace_size(w.T, w.d, w.n, w.E, w.K, p, fflags), dtype=torch.uint8,
                                device=dev)
         self.wsb = torch.empty(moe.moe_backward_workspace_size(w.T, w.d, w.n, w.E, w.K, p, flags), dtype=torch.uint8,
                                device=dev)
@@ -285,7 +294,7 @@ class Layer:
 
     def forward(self):
         self.moe.moe_forward(self.g["X"], self.g["W1"], self.g["W2"], self.rt, O=self.O, H=self.H, ws=self.wsf,
-                             deterministic=self.det)
+                             deterministic=self.det, a_from_h=self.a_from_h)
 
     def backward(self):
         self.moe.moe_backward(self.g["dO"], self.g["X"], self.g["W1"], self.g["W2"], self.H, self.rt, dX=self.dX,
@@ -295,6 +304,9 @@ class Layer:
         self.route()
         self.forward()
         self.backward()
+        if self.allreduce:
+            from fine_grained_mixture_gb300 import dp
+            dp.allreduce_weight_grads(self.dW1, self.dW2)
 
     def cached_bytes(self):
         """Bytes that live from forward to backward: X, H (P rows) and the routing metadata."""
@@ -445,6 +457,8 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
+        from fine_grained_mixture_gb300 import dp
+        dp.nccl_environment()
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local)
@@ -459,8 +473,11 @@ def main():
         return 0
     w = synth.WORKLOADS[args.workload]
     pk = peaks()
-    inp = synth.make_inputs(w, seed=rank)
-    layer = Layer(w, inp, args.mode, dev)
+    inp = synth.make_inputs(w, seed=rank)  # each rank's own tokens; the weights are made equal below
+    layer = Layer(w, inp, args.mode, dev, allreduce=world > 1)
+    if world > 1:
+        from fine_grained_mixture_gb300 import dp
+        dp.broadcast_weights(layer.g["W1"], layer.g["W2"])
     for _ in range(max(args.warmup, 3)):
         layer.step()
     torch.cuda.synchronize()
@@ -523,7 +540,9 @@ def main():
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": DATA,
         "config": {"workload": f"{w.name}: T={w.T}, d={w.d}, n={w.n}, E={w.E}, K={w.K}, routing={args.mode}, "
-                               f"M_tile=128", "parallelism": "replicas" if world > 1 else "single GPU",
+                               f"M_tile=128",
+                   "parallelism": (f"data parallel x{world}: T tokens per rank, W1/W2 replicas, dW1/dW2 all-reduce "
+                                   f"(NCCL, NVLS off) in every step") if world > 1 else "single GPU",
                    "l2": f"inputs larger than L2: one step touches ~{(2*w.T*w.d*3 + 6*w.E*w.d*w.n*2 + 12*P*w.n)/2**30:.1f} GiB"
                          f" vs {L2_BYTES/2**20:.0f} MiB L2; no flush"},
         "frac_of_peak": {"burst": value / world / pk["bf16"], "sustained": value / world / pk["bf16_sus"],
@@ -547,8 +566,9 @@ def main():
             line["tr_vs_tc"] = tr_vs_tc(args, dev)
             line["router"] = router_timing(args, dev)
             line["deterministic"] = deterministic_timing(args, w, inp, line["ms_per_step"], dev)
+            line["a_from_h"] = a_from_h_timing(args, dev)
     if rank == 0 and world == 1:
-        line["cpu_baseline"] = cpu_baseline(w, inp, args.mode, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(w, args.mode, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -672,6 +692,34 @@ def deterministic_timing(args, w, inp, ms_default, dev):
     del layer
     torch.cuda.empty_cache()
     return {"ms_per_step": ms, "tflops": (ff + fb) / (ms * 1e-3) / 1e12, "slowdown_vs_default": ms / ms_default}
+
+
+def a_from_h_timing(args, dev):
+    """Forward with A kept on chip (the down-projection recomputes A = SwiGLU(H) from the cached H, A is never
+    written) against the default forward that writes A and reads it back, on the metric's workload and on the
+    high-sparsity one; whole steps (route + forward + backward) and the forward alone."""
+    out = {}
+    for name in dict.fromkeys((args.workload, "sparse")):
+        w = synth.WORKLOADS[name]
+        inp = synth.make_inputs(w, seed=0)
+        res = {}
+        for key, flag in (("default", False), ("a_from_h", True)):
+            layer = Layer(w, inp, args.mode, dev, a_from_h=flag)
+            for _ in range(3):
+                layer.step()
+            torch.cuda.synchronize()
+            n = max(args.steps, 20)
+            total, parts = time_steps(layer, n, split=True)
+            ff, fb = layer_flops(w)
+            res[key] = {"ms_per_step": total / n, "forward_ms": parts[1] / n,
+                        "tflops": (ff + fb) / (total / n * 1e-3) / 1e12,
+                        "forward_workspace_bytes": layer.wsf.numel()}
+            del layer
+            torch.cuda.empty_cache()
+        res["step_speedup"] = res["default"]["ms_per_step"] / res["a_from_h"]["ms_per_step"]
+        res["forward_speedup"] = res["default"]["forward_ms"] / res["a_from_h"]["forward_ms"]
+        out[name] = res
+    return out
 
 
 def router_timing(args, dev):

@@ -241,13 +241,16 @@ static bool routing_ok(const moe_routing *r) {
 }
 
 static bool det_flag(unsigned flags) { return (flags & MOE_FLAG_DETERMINISTIC) != 0u; }
+static bool a_from_h_flag(unsigned flags) { return (flags & MOE_FLAG_A_FROM_H) != 0u; }
+constexpr unsigned kForwardFlags = MOE_FLAG_DETERMINISTIC | MOE_FLAG_A_FROM_H;
 
 // Column tile of the dH GEMM (n = 256 * k uses 256-wide tiles, else 128).
 static int dh_bn(int n) { return (n % 256 == 0) ? 256 : 128; }
 
-// A [P_cap, n] bf16, then the accumulator of O: fp32, or 64-bit fixed point when deterministic.
+// A [P_cap, n] bf16 (not with MOE_FLAG_A_FROM_H), then the accumulator of O: fp32, or 64-bit fixed point when
+// deterministic.
 static size_t fwd_ws_bytes(int T, int d, int n, size_t p_cap, unsigned flags) {
-  return align256(p_cap * n * 2) + align256((size_t)T * d * (det_flag(flags) ? 8 : 4));
+  return (a_from_h_flag(flags) ? 0 : align256(p_cap * n * 2)) + align256((size_t)T * d * (det_flag(flags) ? 8 : 4));
 }
 
 // dH [P_cap, 2n], s*A [P_cap, n], the accumulator of dX (fp32 or fixed point); deterministic mode adds the
@@ -345,7 +348,7 @@ int moe_route_ex(const float *logits, const float *uniforms, int T, int E, int K
 
 
 int moe_forward_workspace_size_ex(int T, int d, int n, int E, int K, size_t p_cap, unsigned flags, size_t *bytes) {
-  if (!bytes || (flags & ~MOE_FLAG_DETERMINISTIC)) return MOE_ERR_INVALID_ARG;
+  if (!bytes || (flags & ~kForwardFlags)) return MOE_ERR_INVALID_ARG;
   const int rc = check_layer_shape(T, d, n, E, K, p_cap);
   if (rc != MOE_OK) return rc;
   *bytes = fwd_ws_bytes(T, d, n, p_cap, flags);
@@ -361,15 +364,16 @@ int moe_forward_ex(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, co
                    unsigned flags, void *stream) {
   int rc = check_layer_shape(T, d, n, E, K, p_cap);
   if (rc != MOE_OK) return rc;
-  if (!X || !W1 || !W2 || !O || !H || !routing_ok(r) || (flags & ~MOE_FLAG_DETERMINISTIC)) return MOE_ERR_INVALID_ARG;
+  if (!X || !W1 || !W2 || !O || !H || !routing_ok(r) || (flags & ~kForwardFlags)) return MOE_ERR_INVALID_ARG;
   if (!ws || ws_bytes < fwd_ws_bytes(T, d, n, p_cap, flags)) return MOE_ERR_WORKSPACE;
   rc = check_device();
   if (rc != MOE_OK) return rc;
   const bool det = det_flag(flags);
+  const bool a_from_h = a_from_h_flag(flags);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char *p = static_cast<char *>(ws);
-  moe_bf16 *A = reinterpret_cast<moe_bf16 *>(p);
-  p += align256(p_cap * n * 2);
+  moe_bf16 *A = a_from_h ? nullptr : reinterpret_cast<moe_bf16 *>(p);
+  if (!a_from_h) p += align256(p_cap * n * 2);
   void *Oacc = p;  // fp32, or 64-bit fixed point when deterministic
 
   Fork side;
@@ -389,23 +393,28 @@ int moe_forward_ex(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, co
   a.out0 = H;
   a.out1 = A;
   fill_unused(tm);
-  // the epilogue stores H and A as 32 x 32 boxes from shared memory
+  // the epilogue stores H (and A) as 32 x 32 boxes from shared memory
   if ((rc = make_tmap_bf16_epi(&tm.dh, H, 2 * (uint64_t)n, p_cap)) != MOE_OK) return rc;
-  if ((rc = make_tmap_bf16_epi(&tm.sa, A, n, p_cap)) != MOE_OK) return rc;
+  if (!a_from_h && (rc = make_tmap_bf16_epi(&tm.sa, A, n, p_cap)) != MOE_OK) return rc;
   if ((rc = launch_up(a, tm, s)) != MOE_OK) return rc;
-  // down-projection + aggregation: O32[tok] += s * A W2_e (N = d, K = n)
-  if ((rc = make_tmap_bf16(&tm.a, A, n, p_cap, 128)) != MOE_OK) return rc;
+  // down-projection + aggregation: O32[tok] += s * A W2_e (N = d, K = n), A read from the workspace or
+  // recomputed from H inside the kernel
+  if (a_from_h) tm.a = tm.b;  // unused
+  else if ((rc = make_tmap_bf16(&tm.a, A, n, p_cap, 128)) != MOE_OK) return rc;
   if ((rc = make_tmap_bf16(&tm.b, W2, d, (uint64_t)E * n, 64)) != MOE_OK) return rc;
   a.Ndim = d;
   a.Kdim = n;
   a.out0 = nullptr;
   a.out1 = nullptr;
   a.gsrc = nullptr;
+  a.Hin = H;
   a.out_f32 = det ? nullptr : static_cast<float *>(Oacc);
   a.out_i64 = det ? static_cast<long long *>(Oacc) : nullptr;
   if ((rc = side.join()) != MOE_OK) return rc;
   fill_unused(tm);
-  if (!det && d % 512 == 0 && (int64_t)T * d >= ((int64_t)48 << 20)) {
+  if (a_from_h) {
+    if ((rc = launch_down_h(a, tm, s, det)) != MOE_OK) return rc;
+  } else if (!det && d % 512 == 0 && (int64_t)T * d >= ((int64_t)48 << 20)) {
     // Two launches over the column halves: the first half of O is final once the first launch ends, so its cast
     // runs on the side stream beside the second launch and only the second half's cast stays on this stream.
     // The second launch costs a prologue and a tail of its own, so this pays only where the cast is large
@@ -422,10 +431,11 @@ int moe_forward_ex(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, co
     if ((rc = launch_down(a, tm, s, false)) != MOE_OK) return rc;
     if ((rc = launch_f32_to_bf16_cols(O32, O, T, d, half, half, s)) != MOE_OK) return rc;
     return side.join();
+  } else if ((rc = launch_down(a, tm, s, det)) != MOE_OK) {
+    return rc;
   }
-  if ((rc = launch_down(a, tm, s, det)) != MOE_OK) return rc;
   if (det) return launch_fixed_to_bf16(static_cast<long long *>(Oacc), O, (size_t)T * d, s);
-  return launch_f32_to_bf16(static_cast<float *>(Oacc), O, (size_t)T * d, s);
+  return launch_f32_to_bf16(static_cast<float *>(Oacc), O, T, d, s);
 }
 
 int moe_forward(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const moe_routing *r, int T, int d, int n,
@@ -506,7 +516,7 @@ int moe_backward_ex(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, c
   // the cast of dX overlaps the weight-gradient GEMMs, which read neither the accumulator nor dX
   if ((rc = side.open(s)) != MOE_OK) return rc;
   rc = det ? launch_fixed_to_bf16(static_cast<long long *>(dXacc), dX, (size_t)T * d, side.side())
-           : launch_f32_to_bf16(static_cast<float *>(dXacc), dX, (size_t)T * d, side.side());
+           : launch_f32_to_bf16(static_cast<float *>(dXacc), dX, T, d, side.side());
   if (rc != MOE_OK) return rc;
   GemmArgs aw = base_args(r, T, d, n, E, p_cap);
   aw.wide_m = (int64_t)T * K >= (int64_t)1024 * E;  // experts average >= 1024 rows: >= 16 k-blocks per tile

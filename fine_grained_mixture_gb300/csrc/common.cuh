@@ -46,6 +46,11 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Drops the 128-byte L2 line at `p` (128-byte aligned) without writing it back; its contents become undefined.
+__device__ __forceinline__ void discard_l2_line(const void *p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
@@ -242,12 +247,67 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 
 // ---------------------------------------------------------------------------------------- numerics
 
+// SiLU(x) = x * sigmoid(x) with sigmoid(x) = (1 + tanh(x/2)) / 2, i.e. h + h * tanh(h) for h = x/2: one
+// hardware tanh (tanh.approx.f32, relative error about 2^-11, below a bf16 rounding) instead of an exponential and
+// a reciprocal.
+__device__ __forceinline__ float silu_tanh(float x) {
+  const float h = 0.5f * x;
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+  return fmaf(h, t, h);
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Rows [r0, r1) x columns [c0, c0 + w) of an fp32 accumulator with row length ld, rounded to bf16 into `out`
+// (same layout), by threads tid = 0 .. nthreads-1 of the caller's group (nthreads a multiple of 32, w a multiple
+// of 256 floats, c0 and ld multiples of 32).  A warp takes 1 KB spans of a row (256 floats, eight 128-byte
+// lines) with fully coalesced 16-byte loads, U spans at a time so that 2U loads per lane are in flight; once a
+// span has been read, lanes 0..7 discard its lines from L2: the accumulator is dead once cast, so its dirty
+// lines are never written back.
+template <int U>
+__device__ __forceinline__ void cast_rows_discard(const float *acc, uint16_t *out, int ld, int r0, int r1, int c0,
+                                                  int w, int tid, int nthreads) {
+  const int spans_row = w / 256;
+  const int total = (r1 - r0) * spans_row;
+  const int lane = tid & 31;
+  const int nwarps = nthreads >> 5;
+  for (int base = (tid >> 5) * U; base < total; base += nwarps * U) {  // uniform across the warp
+    size_t off[U];
+    float4 x[U], y[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int sp = base + u < total ? base + u : total - 1;  // a repeated span is re-read, not re-written
+      off[u] = static_cast<size_t>(r0 + sp / spans_row) * ld + c0 + (sp % spans_row) * 256;
+      x[u] = __ldcg(reinterpret_cast<const float4 *>(acc + off[u]) + lane);
+      y[u] = __ldcg(reinterpret_cast<const float4 *>(acc + off[u] + 128) + lane);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (base + u >= total) break;
+      uint2 a, b;
+      a.x = pack_bf16x2(x[u].x, x[u].y);
+      a.y = pack_bf16x2(x[u].z, x[u].w);
+      b.x = pack_bf16x2(y[u].x, y[u].y);
+      b.y = pack_bf16x2(y[u].z, y[u].w);
+      reinterpret_cast<uint2 *>(out + off[u])[lane] = a;
+      reinterpret_cast<uint2 *>(out + off[u] + 128)[lane] = b;
+    }
+    __syncwarp();  // every lane's loads of these spans have returned
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (base + u < total && lane < 8) discard_l2_line(acc + off[u] + 32 * lane);
+  }
 }
 
 // Bulk (TMA engine) element-wise fp32 add of `bytes` from shared memory into global memory.

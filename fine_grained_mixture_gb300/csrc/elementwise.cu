@@ -6,57 +6,31 @@
 
 namespace moe {
 
-__global__ void __launch_bounds__(256) f32_to_bf16_kernel(const float4 *__restrict__ src, uint2 *__restrict__ dst,
-                                                          size_t n4) {
+// Columns [c0, c0 + w) of rows [0, rows) of an fp32 accumulator (row length ld) to bf16; CTA b takes rows
+// [b*rows/grid, (b+1)*rows/grid).  The accumulator is dead once cast, so its lines are dropped from L2 rather
+// than written back.
+__global__ void __launch_bounds__(256) f32_to_bf16_kernel(const float *__restrict__ src, uint16_t *__restrict__ dst,
+                                                          int rows, int ld, int c0, int w) {
   griddep_wait();
   griddep_launch_dependents();
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
-    const float4 v = __ldcs(src + i);
-    uint2 o;
-    o.x = pack_bf16x2(v.x, v.y);
-    o.y = pack_bf16x2(v.z, v.w);
-    __stcs(dst + i, o);
-  }
-}
-
-int launch_f32_to_bf16(const float *src, void *dst, size_t count, cudaStream_t s) {
-  const size_t n4 = count / 4;  // count is a multiple of 256 (d % 256 == 0)
-  const int blocks = num_sms() * 8;
-  prof_begin("cast_f32_bf16", s);
-  cudaError_t err = launch_pdl(f32_to_bf16_kernel, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const float4 *>(src),
-                               reinterpret_cast<uint2 *>(dst), n4);
-  prof_end(s);
-  count_launch();
-  if (err == cudaSuccess) err = cudaGetLastError();
-  return err == cudaSuccess ? MOE_OK : record_cuda_error(err);
-}
-
-// Columns [c0, c0 + w) of every row: element group i (four columns) of the range sits at row i / (w / 4).
-__global__ void __launch_bounds__(256) f32_to_bf16_cols_kernel(const float *__restrict__ src, uint2 *__restrict__ dst,
-                                                               int rows, int ld, int c0, int w) {
-  griddep_wait();
-  griddep_launch_dependents();
-  const size_t per_row = static_cast<size_t>(w) / 4;
-  const size_t n4 = per_row * rows;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
-    const size_t r = i / per_row, c = c0 + 4 * (i - r * per_row);
-    const float4 v = __ldcs(reinterpret_cast<const float4 *>(src + r * ld + c));
-    uint2 o;
-    o.x = pack_bf16x2(v.x, v.y);
-    o.y = pack_bf16x2(v.z, v.w);
-    __stcs(dst + (r * ld + c) / 4, o);
-  }
+  const int r0 = static_cast<int>(static_cast<long long>(blockIdx.x) * rows / gridDim.x);
+  const int r1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * rows / gridDim.x);
+  cast_rows_discard<4>(src, dst, ld, r0, r1, c0, w, threadIdx.x, blockDim.x);
 }
 
 int launch_f32_to_bf16_cols(const float *src, void *dst, int rows, int ld, int c0, int w, cudaStream_t s) {
-  const int blocks = num_sms() * 8;
+  const int blocks = num_sms() * 4;
   prof_begin("cast_f32_bf16", s);
-  cudaError_t err = launch_pdl(f32_to_bf16_cols_kernel, dim3(blocks), dim3(256), 0, s, src, static_cast<uint2 *>(dst),
+  cudaError_t err = launch_pdl(f32_to_bf16_kernel, dim3(blocks), dim3(256), 0, s, src, static_cast<uint16_t *>(dst),
                                rows, ld, c0, w);
   prof_end(s);
   count_launch();
   if (err == cudaSuccess) err = cudaGetLastError();
   return err == cudaSuccess ? MOE_OK : record_cuda_error(err);
+}
+
+int launch_f32_to_bf16(const float *src, void *dst, int rows, int ld, cudaStream_t s) {
+  return launch_f32_to_bf16_cols(src, dst, rows, ld, 0, ld, s);
 }
 
 // Fixed-point accumulator (32 fractional bits) of the deterministic aggregation -> bf16, four elements per step.

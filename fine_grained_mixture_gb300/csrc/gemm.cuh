@@ -14,6 +14,8 @@
 //   kDW1  dW1_e = X[tok]^T dH   (reduction over the expert's rows)                  M=d     N=2n  K=rows
 //   kDW2  dW2_e = (sA)^T dO[tok]                                                    M=n     N=d   K=rows
 //   kDW   both weight gradients in one launch: the dW1 pairs of every expert, then the dW2 pairs (256-row blocks)
+//   kDownH  as kDown, with the A operand recomputed from the cached H (A = SiLU(H_gate) * H_up) by producer
+//           warps straight into shared memory, so A [P, n] is never written to or read from HBM
 //
 // CTA = 6 or 10 warps: warp 0 issues TMA tiled loads of the dense operands, warp 1 owns TMEM and one
 // elected lane issues tcgen05.mma, warps 2..5 (2..9 in the scatter-add GEMMs) drain TMEM in the epilogue,
@@ -36,7 +38,7 @@
 
 namespace moe {
 
-enum GemmMode : int { kUp = 0, kDown = 1, kDH = 2, kDX = 3, kDW1 = 4, kDW2 = 5, kDW = 6 };
+enum GemmMode : int { kUp = 0, kDown = 1, kDH = 2, kDX = 3, kDW1 = 4, kDW2 = 5, kDW = 6, kDownH = 7 };
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
@@ -49,12 +51,14 @@ struct Traits {
   static constexpr bool gather_a_mn = (MODE == kDW1);                // A: token rows along K, MN-major
   static constexpr bool gather_b_mn = (MODE == kDW2);                // B: token rows along K, MN-major
   static constexpr bool gather = gather_a_k || gather_a_mn || gather_b_mn || MODE == kDW;  // kDW: A or B per tile
-  static constexpr bool nt_outer_ = (MODE == kDown || MODE == kDX);
+  static constexpr bool transform_a = (MODE == kDownH);  // A computed from H by warps 6..9
+  static constexpr bool producers = gather || transform_a;  // warps 6..9 fill the A (or B) stages
+  static constexpr bool nt_outer_ = (MODE == kDown || MODE == kDX || MODE == kDownH);
   // the scatter-add GEMMs drain TMEM with eight warps (two per TMEM lane quarter, half the columns each)
   static constexpr int epi_warps = nt_outer_ ? 8 : 4;
   static constexpr bool a_mn = varlen_k;  // A operand MN-major in shared memory
-  static constexpr bool b_mn = (MODE == kUp || MODE == kDown || varlen_k);
-  static constexpr bool nt_outer = (MODE == kDown || MODE == kDX);  // keep one fp32 column slab hot in L2
+  static constexpr bool b_mn = (MODE == kUp || MODE == kDown || MODE == kDownH || varlen_k);
+  static constexpr bool nt_outer = nt_outer_;  // keep one fp32 column slab hot in L2
 };
 
 constexpr int kGatherThreads = 128;
@@ -89,9 +93,12 @@ struct Smem {
 // pieces per lane and chunk through L1, twice the requests of the cp.async gather they compete with.
 constexpr int kUpWarpBytes = 6144;
 
-// Weight-gradient epilogue, per warp: two 2 KB staging tiles (32 rows x 32 columns of dW, 64-byte swizzle)
-// drained by TMA stores, one box in flight while the next is written.
+// Weight-gradient epilogue, per warp: with 256-row blocks (one unoverlapped accumulator, shared memory full) two
+// 2 KB staging tiles (32 rows x 32 columns of dW, 64-byte swizzle) drained by TMA stores, one box in flight while
+// the next is written; with 128-row blocks (short k-loops, double-buffered accumulators) the warp's whole 32 x 256
+// block (eight boxes, 16 KB), so it drains TMEM in one go, frees the accumulator and issues all eight stores.
 constexpr int kDwWarpBytes = 2 * 2048;
+constexpr int kDwWarpBytesFull = 8 * 2048;
 
 // Epilogue warps: the weight-gradient GEMMs with 256-row blocks drain their single (unoverlapped) 256 x 256
 // accumulator with eight warps, one 128-row block per group of four (warps 2..5 and 10..13).
@@ -102,7 +109,7 @@ __host__ __device__ constexpr int epi_warps() {
 
 template <int MODE, int MB>
 __host__ __device__ constexpr int cta_threads() {
-  return Traits<MODE>::gather ? 192 + 32 * epi_warps<MODE, MB>() : 64 + 32 * epi_warps<MODE, MB>();
+  return Traits<MODE>::producers ? 192 + 32 * epi_warps<MODE, MB>() : 64 + 32 * epi_warps<MODE, MB>();
 }
 
 template <int MODE, int MB = 1>
@@ -110,7 +117,7 @@ __host__ __device__ constexpr int epi_bytes() {
   return Traits<MODE>::nt_outer ? kStgBytes
          : MODE == kDH          ? 4 * kDhWarpBytes
          : MODE == kUp          ? 4 * kUpWarpBytes
-         : Traits<MODE>::varlen_k ? epi_warps<MODE, MB>() * kDwWarpBytes
+         : Traits<MODE>::varlen_k ? epi_warps<MODE, MB>() * (MB == 1 ? kDwWarpBytesFull : kDwWarpBytes)  // BN = 256
                                   : 0;
 }
 
@@ -314,7 +321,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), TR::gather ? 1 + kGatherThreads : 1);
+      mbar_init(full_bar(s), TR::producers ? 1 + kGatherThreads : 1);
       mbar_init(empty_bar(s), 1);  // released by this CTA's MMA issuer
     }
     for (int b = 0; b < 2; ++b) {
@@ -376,6 +383,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
                                    : MODE == kDW1 ? SM::kBBytes
                                    : MODE == kDW2 ? SM::kABytesMB
                                    : MODE == kDW ? SM::kBBytes
+                                   : MODE == kDownH ? SM::kBBytes
                                                   : SM::kStageBytes;
     int s = 0;
     uint32_t ph = 0;
@@ -407,8 +415,8 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
 #pragma unroll
             for (int h = 0; h < 2; ++h)
               tma_load_2d(b_dst + h * (BN / 2) * 128, &tmB, kb * kBK, t.e * a.n + t.n0 + h * (BN / 2), fb, pol_w);
-          } else if (MODE == kDown) {
-            tma_load_2d(a_dst, &tmA, kb * kBK, t.row0, fb, pol_x);
+          } else if (MODE == kDown || MODE == kDownH) {
+            if (MODE == kDown) tma_load_2d(a_dst, &tmA, kb * kBK, t.row0, fb, pol_x);
 #pragma unroll
             for (int c = 0; c < BN / 64; ++c)
               tma_load_2d(b_dst + c * 8192, &tmB, t.n0 + c * 64, t.e * a.n + kb * kBK, fb, pol_w);
@@ -532,6 +540,80 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
       }
     }
     cp_async_wait<0>();
+  } else if (TR::transform_a && warp >= 6 && warp < 10) {
+    // ------------------------------------------------------- A = SwiGLU(H) producers (down-projection)
+    // Thread gt takes 16-byte piece j (eight columns) of rows rsub + 16q (q = 0..7) of the 128-row A tile at
+    // every k-block: it loads those columns of the cached gate and up halves of H, forms SiLU(g) * u in fp32,
+    // rounds to bf16 and writes the piece at its 128-byte-swizzled place in the stage, as a TMA load would.
+    const int gt = threadIdx.x - 192;
+    const int j = gt & 7;
+    const int rsub = gt >> 3;
+    const uint32_t swz = static_cast<uint32_t>((j ^ (rsub & 7)) << 4);
+    const uint8_t *hbase = static_cast<const uint8_t *>(a.Hin);
+    const size_t hld = static_cast<size_t>(2 * a.n) * 2;  // bytes per row of H
+    int s = 0;
+    uint32_t ph = 0;
+    bool aborted = false;
+    // the 128-byte gate and up segments of a row's next k-block go to L2 ahead of their loads (one thread per row)
+    auto prefetch_kblock = [&](const Tile &tt, int kb) {
+      if (j != 0) return;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int r = tt.row0 + rsub + 16 * q;
+        if (r < tt.row_end) {
+          const uint8_t *hp = hbase + static_cast<size_t>(r) * hld + static_cast<size_t>(kb * kBK) * 2;
+          prefetch_l2(hp);
+          prefetch_l2(hp + static_cast<size_t>(a.n) * 2);
+        }
+      }
+    };
+    for (int pair = first_pair, ti = 0; pair < total && !aborted; pair += pair_step, ++ti) {
+      const Tile t = tile_at<MODE, BN, MB>(a, tile_cache, ti, pair, rank, total_m);
+      if (t.kblocks == 0) continue;
+      for (int kb = 0; kb < t.kblocks; ++kb) {
+        uint4 g[8], u[8];
+        const size_t col = static_cast<size_t>(kb * kBK + j * 8) * 2;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int r = t.row0 + rsub + 16 * q;
+          if (r < t.row_end) {  // rows past the expert are never read (they may lie past the end of H)
+            const uint8_t *hp = hbase + static_cast<size_t>(r) * hld + col;
+            g[q] = __ldcg(reinterpret_cast<const uint4 *>(hp));
+            u[q] = __ldcg(reinterpret_cast<const uint4 *>(hp + static_cast<size_t>(a.n) * 2));
+          } else {
+            g[q] = make_uint4(0u, 0u, 0u, 0u);
+            u[q] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        if (kb + 1 < t.kblocks) prefetch_kblock(t, kb + 1);
+        if (!mbar_wait(empty_bar(s), ph ^ 1u) || *abort_flag) {
+          set_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
+          *abort_flag = 1;
+          aborted = true;
+          break;
+        }
+        const uint32_t dst = sA + s * SM::kABytesMB + rsub * 128 + swz;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t gw[4] = {g[q].x, g[q].y, g[q].z, g[q].w};
+          const uint32_t uw[4] = {u[q].x, u[q].y, u[q].z, u[q].w};
+          float o[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            o[2 * i] = silu_tanh(bf16_lo(gw[i])) * bf16_lo(uw[i]);
+            o[2 * i + 1] = silu_tanh(bf16_hi(gw[i])) * bf16_hi(uw[i]);
+          }
+          st_shared_v4(dst + q * 2048, __uint_as_float(pack_bf16x2(o[0], o[1])), __uint_as_float(pack_bf16x2(o[2], o[3])),
+                       __uint_as_float(pack_bf16x2(o[4], o[5])), __uint_as_float(pack_bf16x2(o[6], o[7])));
+        }
+        fence_proxy_async_smem();  // these generic-proxy writes are read by the tensor cores (async proxy)
+        mbar_arrive(full_bar(s));
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
   } else if (warp == 1) {
     // -------------------------------------------------------------------------------- MMA issuer
     if (lane == 0) {
@@ -555,7 +637,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
             aborted = true;
             break;
           }
-          if (TR::gather) fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tensor-core reads
+          if (TR::producers) fence_proxy_async_smem();  // generic-proxy writes (cp.async, st.shared) -> tensor-core reads
           tc_fence_after();
           const uint32_t a_st = sA + s * SM::kABytesMB;
           const uint32_t b_st = sB + s * SM::kBBytes;
@@ -589,7 +671,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
         *abort_flag = 1;
       }
     }
-  } else if (TR::gather ? ((warp >= 2 && warp < 6) || (kEpiWarps == 8 && warp >= 10 && warp < 14))
+  } else if (TR::producers ? ((warp >= 2 && warp < 6) || (kEpiWarps == 8 && warp >= 10 && warp < 14))
                         : (warp >= 2 && warp < 2 + kEpiWarps)) {
     // ---------------------------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -629,6 +711,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
       }
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
+      bool released = false;  // this warp has already handed the accumulator back
 
       if (MODE == kUp) {
         const int r = t.row0 + row;
@@ -640,6 +723,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
         const int sw = (lane >> 1) & 3;  // 64-byte swizzle: piece p of row `lane` at piece p ^ ((lane >> 1) & 3)
         uint8_t *hrow = static_cast<uint8_t *>(a.out0) + (size_t)r * (2 * a.n) * 2;
         uint8_t *arow = static_cast<uint8_t *>(a.out1) + (size_t)r * a.n * 2;
+        const bool store_a = a.out1 != nullptr;  // A is not kept when the down-projection recomputes it from H
 #pragma unroll 1
         for (int c = 0; c < BN / 64; ++c) {
           uint32_t g[32], u[32];
@@ -676,7 +760,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
             if (lane == 0) {
               tma_store_2d(&tm.dh, out_st, j, wrow, pol_stream);
               tma_store_2d(&tm.dh, out_st + 2048, a.n + j, wrow, pol_stream);
-              tma_store_2d(&tm.sa, out_st + 4096, j, wrow, pol_stream);
+              if (store_a) tma_store_2d(&tm.sa, out_st + 4096, j, wrow, pol_stream);
               bulk_commit();
             }
           } else if (valid) {
@@ -687,13 +771,14 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
                          pol_stream);
               st_v4_hint(hrow + (size_t)(a.n + j) * 2 + v * 16, hu[4 * v], hu[4 * v + 1], hu[4 * v + 2], hu[4 * v + 3],
                          pol_stream);
-              st_v4_hint(arow + (size_t)j * 2 + v * 16, av[4 * v], av[4 * v + 1], av[4 * v + 2], av[4 * v + 3],
-                         pol_stream);
+              if (store_a)
+                st_v4_hint(arow + (size_t)j * 2 + v * 16, av[4 * v], av[4 * v + 1], av[4 * v + 2], av[4 * v + 3],
+                           pol_stream);
             }
           }
           __syncwarp();
         }
-      } else if (MODE == kDown || MODE == kDX) {
+      } else if (MODE == kDown || MODE == kDX || MODE == kDownH) {
         const int r = t.row0 + row;
         int tok = -1;
         float sc = 1.f;
@@ -703,10 +788,12 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
             set_status(a.status, MOE_ERR_BAD_METADATA);
             tok = -1;
           }
-          if (MODE == kDown) sc = __ldg(&a.row_score[r]);
+          if (MODE != kDX) sc = __ldg(&a.row_score[r]);
         }
-        const int half = (warp - 2) >> 2;  // which half of the BN columns this warp drains
-        const uint32_t stg = base + SM::kStgOff + ((warp - 2) * 32 + lane) * kStgRowBytes;
+        // epilogue warp index 0..7: warps 2..9, or 2..5 and 10..13 beside the producer warps
+        const int ew = (TR::producers && warp >= 10) ? warp - 6 : warp - 2;
+        const int half = ew >> 2;  // which half of the BN columns this warp drains
+        const uint32_t stg = base + SM::kStgOff + (ew * 32 + lane) * kStgRowBytes;
         if (DET) {
           // 32 columns per bulk add: 32 64-bit integers fill the 256-byte staging row
           long long *grow = a.out_i64 + (size_t)(tok >= 0 ? tok : 0) * a.d + t.n0 + half * (BN / 2);
@@ -889,10 +976,49 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
         // Two 32-column chunks per TMEM wait, stored as two boxes from the warp's two staging tiles.
         const CUtensorMap *omap = (MODE == kDW && t.w2) ? &tm.sa : &tm.dh;
         const int ew = (warp >= 10) ? 4 + q : q;  // this warp's staging slot
-        const uint32_t stg = base + SM::kStgOff + ew * kDwWarpBytes;
+        const uint32_t stg = base + SM::kStgOff + ew * (MB == 1 && BN == 256 ? kDwWarpBytesFull : kDwWarpBytes);
         const int sw = (lane >> 1) & 3;  // 64-byte swizzle
+        constexpr bool kFullStage = MB == 1 && BN == 256;  // the weight-gradient launches with 128-row blocks
+        if (kFullStage) {
+          if (lane == 0) bulk_wait_read<0>();  // the previous tile's eight boxes have left the staging tile
+          __syncwarp();
 #pragma unroll 1
-        for (int mb = mb_lo; mb < mb_hi; ++mb) {
+          for (int c = 0; c < BN / 32; c += 2) {
+            uint32_t v0[32], v1[32];
+            tmem_ld32(tacc + c * 32, v0);
+            tmem_ld32(tacc + (c + 1) * 32, v1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const uint32_t o = lane * 64 + ((w ^ sw) << 4);
+              st_shared_v4(stg + c * 2048 + o,
+                           __uint_as_float(pack_bf16x2(__uint_as_float(v0[8 * w]), __uint_as_float(v0[8 * w + 1]))),
+                           __uint_as_float(pack_bf16x2(__uint_as_float(v0[8 * w + 2]), __uint_as_float(v0[8 * w + 3]))),
+                           __uint_as_float(pack_bf16x2(__uint_as_float(v0[8 * w + 4]), __uint_as_float(v0[8 * w + 5]))),
+                           __uint_as_float(pack_bf16x2(__uint_as_float(v0[8 * w + 6]), __uint_as_float(v0[8 * w + 7]))));
+              st_shared_v4(stg + (c + 1) * 2048 + o,
+                           __uint_as_float(pack_bf16x2(__uint_as_float(v1[8 * w]), __uint_as_float(v1[8 * w + 1]))),
+                           __uint_as_float(pack_bf16x2(__uint_as_float(v1[8 * w + 2]), __uint_as_float(v1[8 * w + 3]))),
+                           __uint_as_float(pack_bf16x2(__uint_as_float(v1[8 * w + 4]), __uint_as_float(v1[8 * w + 5]))),
+                           __uint_as_float(pack_bf16x2(__uint_as_float(v1[8 * w + 6]), __uint_as_float(v1[8 * w + 7]))));
+            }
+          }
+          // the accumulator is drained: the next tile's MMAs may overwrite it while the stores go out
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(buf));
+          released = true;
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int orow = t.e * dw_m + t.m0 + q * 32;
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) tma_store_2d(omap, stg + c * 2048, t.n0 + c * 32, orow, policy_evict_first());
+            bulk_commit();
+          }
+        }
+#pragma unroll 1
+        for (int mb = mb_lo; mb < (kFullStage ? mb_lo : mb_hi); ++mb) {
 #pragma unroll 1
           for (int c = 0; c < BN / 32; c += 2) {
             uint32_t v0[32], v1[32];
@@ -926,9 +1052,11 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(buf));
+      if (!released) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(buf));
+      }
       if (++buf == kBufs) {
         buf = 0;
         bph ^= 1u;
@@ -979,7 +1107,8 @@ int launch_gemm(const GemmArgs &a, const TensorMaps &tm, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  static const char *const kNames[] = {"gemm_up", "gemm_down", "gemm_dh", "gemm_dx", "gemm_dw1", "gemm_dw2", "gemm_dw"};
+  static const char *const kNames[] = {"gemm_up",  "gemm_down", "gemm_dh", "gemm_dx",
+                                       "gemm_dw1", "gemm_dw2",  "gemm_dw", "gemm_down_h"};
   prof_begin(kNames[MODE], stream);
   err = cudaLaunchKernelEx(&cfg, kernel, tm, a);
   prof_end(stream);

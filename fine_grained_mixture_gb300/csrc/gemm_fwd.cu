@@ -1,5 +1,6 @@
 // gemm_fwd.cu - forward instantiations of the grouped-GEMM kernel: up-projection with the token gather and
-// SwiGLU epilogue, down-projection with the score-weighted aggregation epilogue.
+// SwiGLU epilogue, down-projection with the score-weighted aggregation epilogue (reading A, or recomputing it
+// from the cached H).
 #include "gemm.cuh"
 
 namespace moe {
@@ -9,6 +10,11 @@ int launch_up(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) { return 
 int launch_down(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, bool det) {
   if (det) return launch_gemm<kDown, 256, 3, 1, true>(a, tm, s);
   return launch_gemm<kDown, 256, 3>(a, tm, s);
+}
+
+int launch_down_h(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, bool det) {
+  if (det) return launch_gemm<kDownH, 256, 3, 1, true>(a, tm, s);
+  return launch_gemm<kDownH, 256, 3>(a, tm, s);
 }
 
 }  // namespace moe

@@ -124,6 +124,8 @@ int check_device();
 // det: deterministic aggregation (fixed-point accumulators, dS partials per column tile)
 int launch_up(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s);
 int launch_down(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, bool det);
+// The down-projection with A = SwiGLU(H) recomputed from the cached H (a.Hin) inside the kernel.
+int launch_down_h(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, bool det);
 int launch_dh(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, int bn, bool det);
 int launch_dx(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, bool det);
 int launch_dw1(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s);
@@ -132,8 +134,9 @@ int launch_dw2(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s);
 int launch_dw12(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s);
 
 // elementwise (elementwise.cu)
-int launch_f32_to_bf16(const float *src, void *dst, size_t count, cudaStream_t s);
-// Same for columns [c0, c0 + w) of a [rows, ld] matrix (w and c0 multiples of 4).
+// fp32 [rows, ld] -> bf16 (ld a multiple of 256); the fp32 lines are discarded from L2, not written back.
+int launch_f32_to_bf16(const float *src, void *dst, int rows, int ld, cudaStream_t s);
+// Same for columns [c0, c0 + w) (c0 and w multiples of 256).
 int launch_f32_to_bf16_cols(const float *src, void *dst, int rows, int ld, int c0, int w, cudaStream_t s);
 // The fixed-point accumulator of the deterministic aggregation (32 fractional bits) to bf16.
 int launch_fixed_to_bf16(const long long *src, void *dst, size_t count, cudaStream_t s);

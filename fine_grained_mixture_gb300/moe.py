@@ -22,6 +22,7 @@ MOE_ROUTE_EC = 5
 M_TILE = 128
 STATUS_WORDS = 4
 MOE_FLAG_DETERMINISTIC = 1  # bitwise-reproducible aggregation (fixed-point accumulators)
+MOE_FLAG_A_FROM_H = 2  # the down-projection recomputes A = SwiGLU(H) on chip; A is never written
 # token choice; token rounding to the nearest tile, always up, always down, stochastically; expert choice
 MODES = {"tc": MOE_ROUTE_TC, "tr": MOE_ROUTE_TR, "tr_up": MOE_ROUTE_TR_UP, "tr_down": MOE_ROUTE_TR_DOWN,
          "tr_stoch": MOE_ROUTE_TR_STOCHASTIC, "ec": MOE_ROUTE_EC}
@@ -271,10 +272,12 @@ def _layer_dims(X, W1, W2, routing: Routing):
     return T, d, E, n
 
 
-def moe_forward(X, W1, W2, routing: Routing, O=None, H=None, ws=None, stream=None, deterministic=False):
+def moe_forward(X, W1, W2, routing: Routing, O=None, H=None, ws=None, stream=None, deterministic=False,
+                a_from_h=False):
     """O = sum_k s_k SwiGLU(X W1_e) W2_e; returns (O [T, d] bf16, H [P_cap, 2n] bf16).
 
-    deterministic: fixed-point aggregation, bitwise identical results on every run."""
+    deterministic: fixed-point aggregation, bitwise identical results on every run.
+    a_from_h: the down-projection recomputes A = SwiGLU(H) from the cached H on chip (A is never written)."""
     T, d, E, n = _layer_dims(X, W1, W2, routing)
     n2 = 2 * n
     K, p_cap = routing.K, routing.p_cap
@@ -284,7 +287,7 @@ def moe_forward(X, W1, W2, routing: Routing, O=None, H=None, ws=None, stream=Non
     _need(W2, "W2", bf)
     O = torch.empty((T, d), dtype=bf, device=X.device) if O is None else O
     H = torch.empty((p_cap, n2), dtype=bf, device=X.device) if H is None else H
-    flags = MOE_FLAG_DETERMINISTIC if deterministic else 0
+    flags = (MOE_FLAG_DETERMINISTIC if deterministic else 0) | (MOE_FLAG_A_FROM_H if a_from_h else 0)
     need = moe_forward_workspace_size(T, d, n, E, K, p_cap, flags)
     ws = torch.empty(need, dtype=torch.uint8, device=X.device) if ws is None else ws
     _need(O, "O", bf, T * d)

@@ -163,7 +163,8 @@ int moe_route_noalloc(const float *logits, int T, int E, int K, int mode, const 
 
 /* Forward scratch: A [P_cap, n] bf16 and the fp32 accumulation buffer of O [T, d]. */
 int moe_forward_workspace_size(int T, int d, int n, int E, int K, size_t p_cap, size_t *bytes);
-/* Same for the given flags (MOE_FLAG_DETERMINISTIC: the accumulation buffer of O holds 64-bit integers). */
+/* Same for the given flags (MOE_FLAG_DETERMINISTIC: the accumulation buffer of O holds 64-bit integers;
+ * MOE_FLAG_A_FROM_H: no A buffer). */
 int moe_forward_workspace_size_ex(int T, int d, int n, int E, int K, size_t p_cap, unsigned flags, size_t *bytes);
 
 /*
@@ -179,7 +180,8 @@ int moe_forward_workspace_size_ex(int T, int d, int n, int E, int K, size_t p_ca
 int moe_forward(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const moe_routing *r, int T,
                 int d, int n, int E, int K, size_t p_cap, moe_bf16 *O, moe_bf16 *H, void *ws,
                 size_t ws_bytes, void *stream);
-/* moe_forward with flags (0 or MOE_FLAG_DETERMINISTIC); ws sized by moe_forward_workspace_size_ex. */
+/* moe_forward with flags (0, MOE_FLAG_DETERMINISTIC, MOE_FLAG_A_FROM_H or both); ws sized by
+ * moe_forward_workspace_size_ex with the same flags.  moe_backward_ex does not take MOE_FLAG_A_FROM_H. */
 int moe_forward_ex(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, const moe_routing *r, int T, int d,
                    int n, int E, int K, size_t p_cap, moe_bf16 *O, moe_bf16 *H, void *ws, size_t ws_bytes,
                    unsigned flags, void *stream);
@@ -195,6 +197,18 @@ int moe_forward_ex(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, co
  * dH W1^T) must stay below 2^21 in magnitude, else MOE_ERR_RANGE in the status block.
  */
 #define MOE_FLAG_DETERMINISTIC 1u
+
+/*
+ * A kept on chip (flag of moe_forward_ex; "Key design 3: minimal-activation-cache backward" keeps only X, H and
+ * the routing metadata, and "Key design 2" fuses elementwise work into the GEMMs).  By default the
+ * up-projection's epilogue also writes A = SiLU(H_gate) * H_up [P, n] bf16 to the workspace, and the
+ * down-projection reads it back (once per column slab).  With this flag A is never written: producer warps of the
+ * down-projection load the cached H rows and compute A in fp32 straight into the tensor cores' shared-memory
+ * operand, once per 256-column tile of O.  The forward then moves no A bytes (P*n*2 written, read twice at d =
+ * 1536) but reads H (twice A's bytes) in its place and recomputes SwiGLU per column tile; A is formed from the
+ * bf16 H rather than from the fp32 accumulators (as the backward also does), so O differs in the last bits.
+ */
+#define MOE_FLAG_A_FROM_H 2u
 
 /* Backward scratch: dH [P_cap, 2n] bf16, s*A [P_cap, n] bf16 and the fp32 accumulation buffer of dX. */
 int moe_backward_workspace_size(int T, int d, int n, int E, int K, size_t p_cap, size_t *bytes);

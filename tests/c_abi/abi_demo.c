@@ -66,7 +66,7 @@ static int host_checks(void) {
   CHECK(moe_forward_workspace_size_ex(T, D, N, E, K, (size_t)T * K, MOE_FLAG_DETERMINISTIC, &ws));
   if (moe_route_capacity(T, E, E + 1, MOE_ROUTE_TC, &cap) != MOE_ERR_INVALID_ARG) return 1;
   if (moe_forward_workspace_size(T, 200, N, E, K, (size_t)T * K, &ws) != MOE_ERR_UNSUPPORTED_SHAPE) return 1;
-  if (moe_forward_workspace_size_ex(T, D, N, E, K, (size_t)T * K, 2u, &ws) != MOE_ERR_INVALID_ARG) return 1;
+  if (moe_forward_workspace_size_ex(T, D, N, E, K, (size_t)T * K, 4u, &ws) != MOE_ERR_INVALID_ARG) return 1;
   if (strcmp(moe_strerror(MOE_ERR_WORKSPACE), "workspace missing or too small") != 0) return 1;
   printf("host checks ok\n");
   return 0;

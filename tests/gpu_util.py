@@ -40,10 +40,10 @@ def to_dev(inp: dict, dev="cuda") -> dict:
     return {k: v.to(dev) for k, v in inp.items()}
 
 
-def run_gpu(g: dict, K: int, mode: str, backward=True, uniforms=None):
+def run_gpu(g: dict, K: int, mode: str, backward=True, uniforms=None, a_from_h=False):
     u = None if uniforms is None else uniforms.to(g["logits"].device)
     rt = moe.moe_route(g["logits"], K, mode, uniforms=u)
-    O, H = moe.moe_forward(g["X"], g["W1"], g["W2"], rt)
+    O, H = moe.moe_forward(g["X"], g["W1"], g["W2"], rt, a_from_h=a_from_h)
     out = dict(rt=rt, O=O, H=H)
     if backward:
         dX, dW1, dW2, dS = moe.moe_backward(g["dO"], g["X"], g["W1"], g["W2"], H, rt)

@@ -124,8 +124,11 @@ def test_deterministic_flag_queries(lib):
     assert moe.moe_backward_workspace_size(512, 256, 512, 8, 2, p, moe.MOE_FLAG_DETERMINISTIC) >= \
         base_b + 512 * 256 * 4 + p * 2 * 4
     out = ctypes.c_size_t(0)
-    assert lib.moe_forward_workspace_size_ex(512, 256, 128, 8, 2, p, 2, ctypes.byref(out)) == 1   # unknown flag
+    assert lib.moe_forward_workspace_size_ex(512, 256, 128, 8, 2, p, 4, ctypes.byref(out)) == 1   # unknown flag
     assert lib.moe_backward_workspace_size_ex(512, 256, 128, 8, 2, p, 6, ctypes.byref(out)) == 1
+    # A kept on chip: the forward workspace holds no A [P_cap, n] bf16; the backward does not take the flag
+    assert moe.moe_forward_workspace_size(512, 256, 128, 8, 2, p, moe.MOE_FLAG_A_FROM_H) == base_f - p * 128 * 2
+    assert lib.moe_backward_workspace_size_ex(512, 256, 128, 8, 2, p, moe.MOE_FLAG_A_FROM_H, ctypes.byref(out)) == 1
     assert lib.moe_strerror(9) == b"value beyond the deterministic accumulator's range"
 
 

@@ -7,7 +7,7 @@ import torch
 
 import fine_grained_mixture_gb300 as moe
 from fine_grained_mixture_gb300 import synth
-from gpu_util import assert_close, check_routing, f64, to_dev
+from gpu_util import assert_close, check_routing, f64, oracle_on_rows, to_dev
 from oracle import moe_oracle as orc
 
 pytestmark = pytest.mark.gpu
@@ -62,3 +62,30 @@ def test_deterministic_range_overflow_is_reported():
     assert out["code"] == 9  # MOE_ERR_RANGE
     ok = _run(g, w.K, "tc")  # the next call on normal data is clean again
     assert ok["code"] == 0
+
+
+def test_deterministic_full_size_matches_oracle_on_samples():
+    """At the fine7b size the deterministic path is checked against the oracle itself, not only against the default
+    path: O, dX and dS of sampled tokens (which need exactly those tokens' rows), H of those rows, and dW1/dW2 of
+    the largest and a median expert."""
+    w = synth.WORKLOADS["fine7b"]
+    inp = synth.make_inputs(w, 0)
+    out = _run(to_dev(inp), w.K, "tc")
+    assert out["code"] == 0
+    ref = orc.route(inp["logits"].numpy(), w.K, "tc")
+    check_routing(out["rt"], ref, out["P"])
+    rng = np.random.default_rng(1)
+    toks = rng.choice(w.T, size=48, replace=False)
+    rows = np.nonzero(np.isin(ref["row_token"], toks))[0]
+    _, fwd, bwd = oracle_on_rows(inp, ref, rows)
+    tsel, rsel = torch.from_numpy(toks), torch.from_numpy(rows)
+    assert_close("O[sampled tokens]", f64(out["O"].cpu()[tsel]), fwd["O"][toks])
+    assert_close("dX[sampled tokens]", f64(out["dX"].cpu()[tsel]), bwd["dX"][toks])
+    assert_close("H[rows of sampled tokens]", f64(out["H"].cpu()[rsel]), fwd["H"])
+    assert_close("dS[rows of sampled tokens]", f64(out["dS"].cpu()[rsel]), bwd["dS"])
+    counts = ref["counts"]
+    live = np.nonzero(counts > 0)[0]
+    for e in (int(np.argmax(counts)), int(live[np.argsort(counts[live])[len(live) // 2]])):
+        _, _, be = oracle_on_rows(inp, ref, np.arange(ref["offsets"][e], ref["offsets"][e + 1]))
+        assert_close(f"dW1[{e}]", f64(out["dW1"][e]), be["dW1"][0])
+        assert_close(f"dW2[{e}]", f64(out["dW2"][e]), be["dW2"][0])

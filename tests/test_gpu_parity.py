@@ -78,10 +78,10 @@ def test_routing_nonfinite_logits_flagged():
     assert code == 5  # MOE_ERR_NONFINITE_LOGITS
 
 
-def _full_compare(inp, K, mode):
+def _full_compare(inp, K, mode, a_from_h=False):
     g = to_dev(inp)
     u = synth.make_uniforms(inp["logits"].shape[1], 0)
-    out = run_gpu(g, K, mode, uniforms=u)
+    out = run_gpu(g, K, mode, uniforms=u, a_from_h=a_from_h)
     assert out["code"] == 0
     ref = orc.route(inp["logits"].numpy(), K, mode, u=u.numpy())
     check_routing(out["rt"], ref, out["P"])
@@ -124,15 +124,36 @@ def test_layer_small_shapes(T, d, n, E, K, skew, mode):
     _full_compare(synth.make_inputs(w, 1), K, mode)
 
 
-@pytest.mark.parametrize("name,mode", [("fine7b", "tc"), ("fine7b", "tr"), ("coarse", "tc"), ("sparse", "tc"),
-                                       ("sparse", "tr"), ("skew", "tc"), ("skew", "tr"), ("sparse", "tr_stoch"),
-                                       ("skew", "ec")])
-def test_layer_full_size_sampled(name, mode):
+# The forward that recomputes A = SwiGLU(H) inside the down-projection (A never written): every element at the
+# tiny size and on the ragged and skewed shapes, sampled outputs at the four full-size workloads below.
+@pytest.mark.parametrize("mode", ["tc", "tr", "ec"])
+def test_layer_tiny_full_a_from_h(mode):
+    w = synth.WORKLOADS["tiny"]
+    _full_compare(synth.make_inputs(w, 0), w.K, mode, a_from_h=True)
+
+
+@pytest.mark.parametrize("T,d,n,E,K,skew,mode", [
+    (300, 256, 128, 5, 2, False, "tc"),      # ragged tail tiles: the producers stop at the expert's last row
+    (1000, 512, 256, 16, 4, True, "tr"),     # skewed, empty experts
+    (260, 256, 384, 1, 1, False, "tc"),      # n = 3 x 128: the k-blocks of A span the gate and up halves of H
+    (1, 256, 128, 4, 2, False, "tc"),        # a single token
+])
+def test_layer_small_shapes_a_from_h(T, d, n, E, K, skew, mode):
+    w = synth.custom(T, d, n, E, K, skew=skew)
+    _full_compare(synth.make_inputs(w, 1), K, mode, a_from_h=True)
+
+
+@pytest.mark.parametrize("name,mode,a_from_h", [
+    ("fine7b", "tc", False), ("fine7b", "tr", False), ("coarse", "tc", False), ("sparse", "tc", False),
+    ("sparse", "tr", False), ("skew", "tc", False), ("skew", "tr", False), ("sparse", "tr_stoch", False),
+    ("skew", "ec", False),
+    ("fine7b", "tc", True), ("coarse", "tc", True), ("sparse", "tr", True), ("skew", "tc", True)])
+def test_layer_full_size_sampled(name, mode, a_from_h):
     w = synth.WORKLOADS[name]
     inp = synth.make_inputs(w, 0)
     g = to_dev(inp)
     u = synth.make_uniforms(w.E, 0)
-    out = run_gpu(g, w.K, mode, uniforms=u)
+    out = run_gpu(g, w.K, mode, uniforms=u, a_from_h=a_from_h)
     assert out["code"] == 0
     ref = orc.route(inp["logits"].numpy(), w.K, mode, u=u.numpy())
     check_routing(out["rt"], ref, out["P"])

@@ -54,7 +54,9 @@ def _threads(name):
     m = re.search(r"moe_gemm_kernelILi(\d+)ELi\d+ELi\d+ELi(\d+)E", name)
     if m:
         mode, mb = int(m.group(1)), int(m.group(2))
-        return (448 if mode in (4, 5, 6) and mb == 2 else 320), 1
+        # 448 threads: the weight gradients on 256-row blocks (eight epilogue warps beside the gatherers) and the
+        # down-projection that recomputes A from H (eight epilogue warps beside the A producers)
+        return (448 if (mode in (4, 5, 6) and mb == 2) or mode == 7 else 320), 1
     if "router_gemm_kernel" in name:
         return 192, 2
     return None
@@ -67,7 +69,7 @@ def report():
 
 def test_every_tensor_core_kernel_is_reported(report):
     gemms = [k for k in report if _threads(k)]
-    assert sum("moe_gemm_kernel" in k for k in gemms) >= 7 and sum("router_gemm_kernel" in k for k in gemms) == 3
+    assert sum("moe_gemm_kernel" in k for k in gemms) >= 8 and sum("router_gemm_kernel" in k for k in gemms) == 3
 
 
 def test_tensor_core_kernels_do_not_spill(report):
