@@ -93,12 +93,9 @@ struct Smem {
 // pieces per lane and chunk through L1, twice the requests of the cp.async gather they compete with.
 constexpr int kUpWarpBytes = 6144;
 
-// Weight-gradient epilogue, per warp: with 256-row blocks (one unoverlapped accumulator, shared memory full) two
-// 2 KB staging tiles (32 rows x 32 columns of dW, 64-byte swizzle) drained by TMA stores, one box in flight while
-// the next is written; with 128-row blocks (short k-loops, double-buffered accumulators) the warp's whole 32 x 256
-// block (eight boxes, 16 KB), so it drains TMEM in one go, frees the accumulator and issues all eight stores.
+// Weight-gradient epilogue, per warp: two 2 KB staging tiles (32 rows x 32 columns of dW, 64-byte swizzle)
+// drained by TMA stores, one box in flight while the next is written.
 constexpr int kDwWarpBytes = 2 * 2048;
-constexpr int kDwWarpBytesFull = 8 * 2048;
 
 // Epilogue warps: the weight-gradient GEMMs with 256-row blocks drain their single (unoverlapped) 256 x 256
 // accumulator with eight warps, one 128-row block per group of four (warps 2..5 and 10..13).
@@ -117,7 +114,7 @@ __host__ __device__ constexpr int epi_bytes() {
   return Traits<MODE>::nt_outer ? kStgBytes
          : MODE == kDH          ? 4 * kDhWarpBytes
          : MODE == kUp          ? 4 * kUpWarpBytes
-         : Traits<MODE>::varlen_k ? epi_warps<MODE, MB>() * (MB == 1 ? kDwWarpBytesFull : kDwWarpBytes)  // BN = 256
+         : Traits<MODE>::varlen_k ? epi_warps<MODE, MB>() * kDwWarpBytes
                                   : 0;
 }
 
@@ -237,32 +234,47 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &a, int pair, int ran
   return t;
 }
 
-// Varlen-M tiles of one CTA, decoded once after the grid-dependency wait (the expert search over the tile
-// offsets is a chain of dependent loads: done per tile and per role it costs more than a k-block of MMA).
+// The tiles of one CTA, decoded once after the grid-dependency wait: finding a tile's expert and rows is a chain
+// of dependent loads (a search over the tile offsets, or the expert's row offsets), and done per tile in every
+// role it stalls the MMA issuer at each tile start (about 0.5 us, more than a k-block of MMA).
 constexpr int kTileCache = 128;  // tiles per CTA kept in shared memory; later tiles are decoded on the fly
 struct TileRec {
   int row0, row_end;
-  uint32_t e_nt;  // expert (bits 0-15) | n-tile (bits 16-31)
+  uint32_t code;  // expert (bits 0-10) | n-tile (bits 11-18) | m-tile (bits 19-30) | dW2 tile (bit 31)
 };
 template <int MODE>
 __host__ __device__ constexpr int tile_cache_bytes() {
-  return Traits<MODE>::varlen_k ? 0 : kTileCache * static_cast<int>(sizeof(TileRec));
+  return kTileCache * static_cast<int>(sizeof(TileRec));
+}
+
+// The packing above holds every tile of a launch when its column tiles number at most 256 (and hence its
+// m-tiles at most 4096); E <= 1024 always fits.
+template <int BN>
+__device__ __forceinline__ bool tiles_cacheable(const GemmArgs &a) {
+  return max(a.d, 2 * a.n) / BN < 256;
+}
+
+template <int BN, int MB>
+__device__ __forceinline__ TileRec pack_tile(const Tile &t) {
+  return TileRec{t.row0, t.row_end,
+                 static_cast<uint32_t>(t.e) | (static_cast<uint32_t>(t.n0 / BN) << 11) |
+                     (static_cast<uint32_t>(t.m0 / (kBM * MB)) << 19) | (t.w2 ? 0x80000000u : 0u)};
 }
 
 // Tile i of this CTA (pair = first_pair + i * pair_step): from the cache when it holds it.
 template <int MODE, int BN, int MB>
-__device__ __forceinline__ Tile tile_at(const GemmArgs &a, const TileRec *cache, int i, int pair, int rank,
-                                        int total_m) {
-  if (Traits<MODE>::varlen_k || i >= kTileCache) return decode_tile<MODE, BN, MB>(a, pair, rank, total_m);
+__device__ __forceinline__ Tile tile_at(const GemmArgs &a, const TileRec *cache, bool cached, int i, int pair,
+                                        int rank, int total_m) {
+  if (!cached || i >= kTileCache) return decode_tile<MODE, BN, MB>(a, pair, rank, total_m);
   const TileRec r = cache[i];
   Tile t;
-  t.e = static_cast<int>(r.e_nt & 0xffffu);
-  t.n0 = static_cast<int>(r.e_nt >> 16) * BN;
-  t.w2 = false;
-  t.m0 = 0;
+  t.e = static_cast<int>(r.code & 0x7ffu);
+  t.n0 = static_cast<int>((r.code >> 11) & 0xffu) * BN;
+  t.m0 = static_cast<int>((r.code >> 19) & 0xfffu) * (kBM * MB);
+  t.w2 = (r.code >> 31) != 0u;
   t.row0 = r.row0;
   t.row_end = r.row_end;
-  t.kblocks = a.Kdim / kBK;
+  t.kblocks = Traits<MODE>::varlen_k ? (t.row_end - t.row0 + kBK - 1) / kBK : a.Kdim / kBK;
   return t;
 }
 
@@ -362,15 +374,13 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
   const int total_m = TR::varlen_k ? 0 : __ldg(&a.tile_offsets[a.E]);
   const int total = total_pairs<MODE, BN, MB>(a, total_m);
   TileRec *tile_cache = reinterpret_cast<TileRec *>(gbase + SM::kCacheOff);
-  if (!TR::varlen_k) {
+  const bool cached = tiles_cacheable<BN>(a);
+  if (cached) {
     const int mine = first_pair < total ? (total - first_pair + pair_step - 1) / pair_step : 0;
-    for (int i = threadIdx.x; i < min(mine, kTileCache); i += blockDim.x) {
-      const int pair = first_pair + i * pair_step;
-      const Tile t = decode_tile<MODE, BN, MB>(a, pair, rank, total_m);
-      tile_cache[i] = TileRec{t.row0, t.row_end, static_cast<uint32_t>(t.e) | (static_cast<uint32_t>(t.n0 / BN) << 16)};
-    }
-    __syncthreads();
+    for (int i = threadIdx.x; i < min(mine, kTileCache); i += blockDim.x)
+      tile_cache[i] = pack_tile<BN, MB>(decode_tile<MODE, BN, MB>(a, first_pair + i * pair_step, rank, total_m));
   }
+  __syncthreads();
 
   if (warp == 0) {
     // ------------------------------------------------------------------------------ TMA producer
@@ -391,7 +401,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
     bool aborted = false;
     if (lane == 0) {
       for (int pair = first_pair, ti = 0; pair < total && !aborted; pair += pair_step, ++ti) {
-        const Tile t = tile_at<MODE, BN, MB>(a, tile_cache, ti, pair, rank, total_m);
+        const Tile t = tile_at<MODE, BN, MB>(a, tile_cache, cached, ti, pair, rank, total_m);
         for (int kb = 0; kb < t.kblocks; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u) || *abort_flag) {
             set_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
@@ -473,11 +483,11 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
     };
     Tile t_next;
     if (TR::gather_a_k && first_pair < total) {
-      t_next = tile_at<MODE, BN, MB>(a, tile_cache, 0, first_pair, rank, total_m);
+      t_next = tile_at<MODE, BN, MB>(a, tile_cache, cached, 0, first_pair, rank, total_m);
       fetch_tokens(t_next);
     }
     for (int pair = first_pair, ti = 0; pair < total && !aborted; pair += pair_step, ++ti) {
-      const Tile t = TR::gather_a_k ? t_next : tile_at<MODE, BN, MB>(a, tile_cache, ti, pair, rank, total_m);
+      const Tile t = TR::gather_a_k ? t_next : tile_at<MODE, BN, MB>(a, tile_cache, cached, ti, pair, rank, total_m);
       if (t.kblocks == 0) continue;
       const uint8_t *rowp[8];
       uint32_t rown[8];
@@ -490,7 +500,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
           rowp[q] = src_a + (tok < a.T ? tok : 0) * ld_bytes + j * 16;
         }
         if (pair + pair_step < total) {
-          t_next = tile_at<MODE, BN, MB>(a, tile_cache, ti + 1, pair + pair_step, rank, total_m);
+          t_next = tile_at<MODE, BN, MB>(a, tile_cache, cached, ti + 1, pair + pair_step, rank, total_m);
           fetch_tokens(t_next);
         }
       }
@@ -500,6 +510,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
       for (int kb = 0; kb < t.kblocks; ++kb) {
         if (!TR::gather_a_k) {
           // varlen-K: rows rb + rsub + 16q (q = 0..3) of this k-block, by token id
+          // (loading these ids one k-block ahead, before the stage wait, measured slower: fine7b dW 373 -> 595 us)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int tok = token_or_oob(a, t.row0 + kb * kBK + rsub + 16 * q, t.row_end);
@@ -568,7 +579,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
       }
     };
     for (int pair = first_pair, ti = 0; pair < total && !aborted; pair += pair_step, ++ti) {
-      const Tile t = tile_at<MODE, BN, MB>(a, tile_cache, ti, pair, rank, total_m);
+      const Tile t = tile_at<MODE, BN, MB>(a, tile_cache, cached, ti, pair, rank, total_m);
       if (t.kblocks == 0) continue;
       for (int kb = 0; kb < t.kblocks; ++kb) {
         uint4 g[8], u[8];
@@ -624,7 +635,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
       uint32_t bph = 0;
       bool aborted = false;
       for (int pair = first_pair, ti = 0; pair < total && !aborted; pair += pair_step, ++ti) {
-        const Tile t = tile_at<MODE, BN, MB>(a, tile_cache, ti, pair, rank, total_m);
+        const Tile t = tile_at<MODE, BN, MB>(a, tile_cache, cached, ti, pair, rank, total_m);
         if (t.kblocks == 0) continue;
         if (!mbar_wait(tempty_bar(buf), bph ^ 1u) || *abort_flag) {
           aborted = true;
@@ -685,7 +696,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
     const uint64_t pol_acc = policy_evict_last();  // keep the fp32 accumulator slab in L2
     const uint64_t pol_stream = policy_evict_first();  // streamed epilogue traffic (H, A, dH, s*A) is touched once here
     for (int pair = first_pair, ti = 0; pair < total; pair += pair_step, ++ti) {
-      const Tile t = tile_at<MODE, BN, MB>(a, tile_cache, ti, pair, rank, total_m);
+      const Tile t = tile_at<MODE, BN, MB>(a, tile_cache, cached, ti, pair, rank, total_m);
       // weight gradients: the output of this tile and its row length
       const int dw_m = MODE == kDW ? (t.w2 ? a.n : a.d) : a.Mdim;
       const int dw_n = MODE == kDW ? (t.w2 ? a.d : 2 * a.n) : a.Ndim;
@@ -711,7 +722,6 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
       }
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
-      bool released = false;  // this warp has already handed the accumulator back
 
       if (MODE == kUp) {
         const int r = t.row0 + row;
@@ -976,49 +986,10 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
         // Two 32-column chunks per TMEM wait, stored as two boxes from the warp's two staging tiles.
         const CUtensorMap *omap = (MODE == kDW && t.w2) ? &tm.sa : &tm.dh;
         const int ew = (warp >= 10) ? 4 + q : q;  // this warp's staging slot
-        const uint32_t stg = base + SM::kStgOff + ew * (MB == 1 && BN == 256 ? kDwWarpBytesFull : kDwWarpBytes);
+        const uint32_t stg = base + SM::kStgOff + ew * kDwWarpBytes;
         const int sw = (lane >> 1) & 3;  // 64-byte swizzle
-        constexpr bool kFullStage = MB == 1 && BN == 256;  // the weight-gradient launches with 128-row blocks
-        if (kFullStage) {
-          if (lane == 0) bulk_wait_read<0>();  // the previous tile's eight boxes have left the staging tile
-          __syncwarp();
 #pragma unroll 1
-          for (int c = 0; c < BN / 32; c += 2) {
-            uint32_t v0[32], v1[32];
-            tmem_ld32(tacc + c * 32, v0);
-            tmem_ld32(tacc + (c + 1) * 32, v1);
-            tmem_ld_wait();
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              const uint32_t o = lane * 64 + ((w ^ sw) << 4);
-              st_shared_v4(stg + c * 2048 + o,
-                           __uint_as_float(pack_bf16x2(__uint_as_float(v0[8 * w]), __uint_as_float(v0[8 * w + 1]))),
-                           __uint_as_float(pack_bf16x2(__uint_as_float(v0[8 * w + 2]), __uint_as_float(v0[8 * w + 3]))),
-                           __uint_as_float(pack_bf16x2(__uint_as_float(v0[8 * w + 4]), __uint_as_float(v0[8 * w + 5]))),
-                           __uint_as_float(pack_bf16x2(__uint_as_float(v0[8 * w + 6]), __uint_as_float(v0[8 * w + 7]))));
-              st_shared_v4(stg + (c + 1) * 2048 + o,
-                           __uint_as_float(pack_bf16x2(__uint_as_float(v1[8 * w]), __uint_as_float(v1[8 * w + 1]))),
-                           __uint_as_float(pack_bf16x2(__uint_as_float(v1[8 * w + 2]), __uint_as_float(v1[8 * w + 3]))),
-                           __uint_as_float(pack_bf16x2(__uint_as_float(v1[8 * w + 4]), __uint_as_float(v1[8 * w + 5]))),
-                           __uint_as_float(pack_bf16x2(__uint_as_float(v1[8 * w + 6]), __uint_as_float(v1[8 * w + 7]))));
-            }
-          }
-          // the accumulator is drained: the next tile's MMAs may overwrite it while the stores go out
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(tempty_bar(buf));
-          released = true;
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            const int orow = t.e * dw_m + t.m0 + q * 32;
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) tma_store_2d(omap, stg + c * 2048, t.n0 + c * 32, orow, policy_evict_first());
-            bulk_commit();
-          }
-        }
-#pragma unroll 1
-        for (int mb = mb_lo; mb < (kFullStage ? mb_lo : mb_hi); ++mb) {
+        for (int mb = mb_lo; mb < mb_hi; ++mb) {
 #pragma unroll 1
           for (int c = 0; c < BN / 32; c += 2) {
             uint32_t v0[32], v1[32];
@@ -1052,11 +1023,9 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
           }
         }
       }
-      if (!released) {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tempty_bar(buf));
-      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(buf));
       if (++buf == kBufs) {
         buf = 0;
         bph ^= 1u;

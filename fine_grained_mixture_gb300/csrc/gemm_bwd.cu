@@ -19,16 +19,15 @@ int launch_dx(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, bool det)
 }
 
 // 256-row M blocks (see Smem) when the weight's row count allows it and the experts' K loops are long
-// enough to hide the unoverlapped epilogue; else 128-row blocks with double-buffered TMEM and three stages (the
-// fourth stage's shared memory holds the epilogue's full 32 x 256 staging tile per warp instead).
+// enough to hide the unoverlapped epilogue; else 128-row blocks with double-buffered TMEM.
 int launch_dw1(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) {
   if (a.wide_m && a.Mdim % 256 == 0) return launch_gemm<kDW1, 256, 3, 2>(a, tm, s);
-  return launch_gemm<kDW1, 256, 3, 1>(a, tm, s);
+  return launch_gemm<kDW1, 256, 4, 1>(a, tm, s);
 }
 
 int launch_dw2(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) {
   if (a.wide_m && a.Mdim % 256 == 0) return launch_gemm<kDW2, 256, 3, 2>(a, tm, s);
-  return launch_gemm<kDW2, 256, 3, 1>(a, tm, s);
+  return launch_gemm<kDW2, 256, 4, 1>(a, tm, s);
 }
 
 int launch_dw12(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) {
