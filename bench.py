@@ -369,7 +369,7 @@ def load_traffic(kernel, workload):
     ent = table.get(kernel, {}).get(workload)
     if not ent:
         return None
-    if ent.get("source_sha") != source_sha():
+    if ent.get("source_sha") != source_sha(kernel):
         return None
     return ent.get("bytes_per_launch")
 
@@ -422,12 +422,11 @@ def ingest_ncu(csv_path, workload):
             table = json.load(f)
     except Exception:
         table = {}
-    sha = source_sha()
     for name, a in sorted(agg.items()):
         n = a["n"]
         table.setdefault(name, {})[workload] = {
             "bytes_per_launch": (a["read"] + a["write"]) / n, "read": a["read"] / n, "write": a["write"] / n,
-            "launches": n, "ncu_time_us": a["us"] / n, "source_sha": sha}
+            "launches": n, "ncu_time_us": a["us"] / n, "source_sha": source_sha(name)}
     with open(path, "w") as f:
         json.dump(table, f, indent=1, sort_keys=True)
         f.write("\n")
@@ -435,10 +434,31 @@ def ingest_ncu(csv_path, workload):
     return 0
 
 
-def source_sha():
+# The sources that define each kernel family: a captured traffic figure stays valid while these are unchanged.
+KERNEL_SOURCES = {
+    "gemm": ("gemm.cuh", "gemm_fwd.cu", "gemm_bwd.cu", "common.cuh", "internal.h"),
+    "route": ("route.cu", "common.cuh", "internal.h"),
+    "router": ("router.cu", "common.cuh", "internal.h"),
+    "cast": ("elementwise.cu", "common.cuh", "internal.h"),
+}
+
+
+def kernel_family(kernel):
+    if kernel and kernel.startswith("gemm_"):
+        return "gemm"
+    if kernel and kernel.startswith("router_"):
+        return "router"
+    if kernel and kernel.startswith("route_"):
+        return "route"
+    return "cast"
+
+
+def source_sha(kernel=None):
+    """Digest of the sources of `kernel`'s family (all of csrc/ when kernel is None)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fine_grained_mixture_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    files = sorted(os.listdir(csrc)) if kernel is None else KERNEL_SOURCES[kernel_family(kernel)]
+    for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode())
             h.update(fh.read())

@@ -74,6 +74,10 @@ void prof_end(cudaStream_t s) {
   if (!p.recs.empty()) cudaEventRecord(p.recs.back().stop, s);
 }
 
+// While per-kernel timing is on, side-stream work stays on the caller's stream, so that each kernel's events
+// bracket that kernel alone rather than the time it spends beside another one.
+static bool prof_serial() { return prof().enabled; }
+
 int num_sms() {
   static DeviceCache cache;
   int dev = 0;
@@ -126,6 +130,11 @@ class Fork {
   }
   // side waits for the work enqueued on s so far
   int open(cudaStream_t s) {
+    if (prof_serial()) {
+      serial_ = true;
+      s_ = s;
+      return MOE_OK;
+    }
     if (!sd_) {
       int dev = 0;
       cudaError_t err = cudaGetDevice(&dev);
@@ -155,13 +164,15 @@ class Fork {
   // s waits for the work enqueued on the side stream so far
   int join() {
     open_ = false;
+    if (serial_ || !sd_) return MOE_OK;
     cudaError_t err = cudaEventRecord(sd_->join, sd_->stream);
     if (err == cudaSuccess) err = cudaStreamWaitEvent(s_, sd_->join, 0);
     return err == cudaSuccess ? MOE_OK : record_cuda_error(err);
   }
-  cudaStream_t side() const { return sd_->stream; }
+  cudaStream_t side() const { return serial_ ? s_ : sd_->stream; }
 
  private:
+  bool serial_ = false;  // per-kernel timing: the "side" stream is the caller's
   SideStream *sd_ = nullptr;
   std::unique_lock<std::mutex> lk_;
   cudaStream_t s_ = nullptr;

@@ -306,12 +306,15 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
   const CUtensorMap &tmB = tm.b;
   using TR = Traits<MODE>;
   using SM = Smem<BN, STAGES, epi_bytes<MODE, MB>(), MB, tile_cache_bytes<MODE>()>;
-  static_assert(MODE != kDW || (MB == 2 && BN == 256), "merged weight gradients: A and B stages of equal size");
+  static_assert(MODE != kDW || MB == 2, "merged weight gradients: 256-row blocks");
   constexpr int kEpiWarps = epi_warps<MODE, MB>();
   static_assert(cta_threads<MODE, MB>() <= 448, "one CTA per SM at up to 146 registers a thread");
-  constexpr int kBufs = MB == 1 ? 2 : 1;           // TMEM accumulator buffers (double-buffered when MB = 1)
-  constexpr uint32_t kTmemCols = 2 * BN;            // MB * BN * kBufs == 2 * BN in both layouts
-  static_assert(MB * kBufs == 2, "TMEM holds two BN-column accumulators");
+  // TMEM accumulator buffers: two (one tile's epilogue overlaps the next tile's MMAs) whenever two fit in the
+  // 512 columns; 256-row blocks of 256 columns fill TMEM with one
+  constexpr int kBufs = MB * BN * 2 <= 512 ? 2 : 1;
+  constexpr uint32_t kBufCols = MB * BN;  // columns of one accumulator (M block mb at columns mb * BN)
+  constexpr uint32_t kTmemCols = kBufCols * kBufs < 32 ? 32 : kBufCols * kBufs;
+  static_assert(kBufCols * kBufs <= 512, "the accumulators fit TMEM");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -409,7 +412,8 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
             aborted = true;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(s), kTmaBytes);
+          // merged weight gradients: a dW2 tile loads its A (s*A, 256 rows) by TMA, a dW1 tile its B (dH)
+          mbar_arrive_expect_tx(full_bar(s), (MODE == kDW && t.w2) ? static_cast<uint32_t>(SM::kABytesMB) : kTmaBytes);
           const uint32_t a_dst = sA + s * SM::kABytesMB;
           const uint32_t b_dst = sB + s * SM::kBBytes;
           const uint32_t fb = full_bar(s);
@@ -510,13 +514,17 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
       for (int kb = 0; kb < t.kblocks; ++kb) {
         if (!TR::gather_a_k) {
           // varlen-K: rows rb + rsub + 16q (q = 0..3) of this k-block, by token id
-          // (loading these ids one k-block ahead, before the stage wait, measured slower: fine7b dW 373 -> 595 us)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int tok = token_or_oob(a, t.row0 + kb * kBK + rsub + 16 * q, t.row_end);
             rown[q] = tok < a.T ? 16u : 0u;
             rowp[q] = src_base + (tok < a.T ? tok : 0) * ld_bytes + j * 16;
           }
+          // the next k-block's ids (256 bytes: at most three lines) into L1 while this one's copies are issued;
+          // loading them into registers one k-block ahead measured slower (fine7b dW 373 -> 595 us before the
+          // stage wait, 362 -> 381 us after the copies), this prefetch faster (362 -> 357 us)
+          if (gt < 3 && kb + 1 < t.kblocks)
+            prefetch_l1(a.row_token + min(t.row0 + (kb + 1) * kBK + gt * 31, t.row_end - 1));
         }
         if (!mbar_wait(empty_bar(s), ph ^ 1u) || *abort_flag) {
           set_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
@@ -531,15 +539,19 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
           for (int q = 0; q < 8; ++q) cp_async_16_hint(dst + q * 2048, rowp[q] + koff, rown[q], pol_rows);
         } else {
           // MN-major: K-row k = rsub + 16q at byte k*128 of each 64-column chunk c (8 KB apart)
-          constexpr int kChunks = TR::gather_a_mn ? MB * kBM / 64 : BN / 64;  // equal for kDW
+          constexpr int kChunksA = MB * kBM / 64, kChunksB = BN / 64;
+          constexpr int kChunks = TR::gather_a_mn ? kChunksA : TR::gather_b_mn ? kChunksB
+                                                                : (kChunksA > kChunksB ? kChunksA : kChunksB);
+          const int nchunks = into_a ? kChunksA : kChunksB;  // kDW: the gathered operand of this tile
           const uint32_t base_dst = (into_a ? sA + s * SM::kABytesMB : sB + s * SM::kBBytes) + rsub * 128 + swz;
           const int mn0 = into_a ? t.m0 : t.n0;
 #pragma unroll
           for (int q = 0; q < 4; ++q)
 #pragma unroll
             for (int c = 0; c < kChunks; ++c)
-              cp_async_16_hint(base_dst + q * 2048 + c * 8192, rowp[q] + static_cast<size_t>(mn0 + c * 64) * 2, rown[q],
-                               pol_rows);
+              if (c < nchunks)
+                cp_async_16_hint(base_dst + q * 2048 + c * 8192, rowp[q] + static_cast<size_t>(mn0 + c * 64) * 2,
+                                 rown[q], pol_rows);
         }
         // the stage's barrier counts this thread's arrival when its copies have landed; the MMA issuer
         // fences the async proxy after the barrier before the tensor cores read the stage
@@ -642,7 +654,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf) * kBufCols;
         for (int kb = 0; kb < t.kblocks; ++kb) {
           if (!mbar_wait(full_bar(s), ph) || *abort_flag) {
             aborted = true;
@@ -721,7 +733,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
         break;
       }
       tc_fence_after();
-      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf) * kBufCols;
 
       if (MODE == kUp) {
         const int r = t.row0 + row;

@@ -53,7 +53,7 @@ def test_ingest_averages_per_launch_and_goes_stale_with_the_source(tmp_path, mon
                    + _row(1, dw, "dram__bytes_write.sum", "byte", "0")
                    + _row(1, dw, "gpu__time_duration.sum", "ns", "250000")
                    + _row(2, "void some_library_kernel()", "dram__bytes_read.sum", "byte", "7"))
-    monkeypatch.setattr(bench, "source_sha", lambda: "digest-a")
+    monkeypatch.setattr(bench, "source_sha", lambda kernel=None: "digest-a")
     assert bench.ingest_ncu(str(csv), "fine7b") == 0
     table = json.loads((tmp_path / "profiles" / "dram_traffic.json").read_text())
     ent = table["gemm_dw"]["fine7b"]
@@ -63,8 +63,16 @@ def test_ingest_averages_per_launch_and_goes_stale_with_the_source(tmp_path, mon
     assert set(table) == {"gemm_dw"}
     assert bench.load_traffic("gemm_dw", "fine7b") == pytest.approx(1.25e9)
     assert bench.load_traffic("gemm_dw", "sparse") is None
-    monkeypatch.setattr(bench, "source_sha", lambda: "digest-b")   # the kernels changed since the capture
+    monkeypatch.setattr(bench, "source_sha", lambda kernel=None: "digest-b")   # the kernels changed since the capture
     assert bench.load_traffic("gemm_dw", "fine7b") is None
+
+
+def test_traffic_digest_follows_the_kernel_family_sources():
+    # a GEMM's captured traffic depends on the GEMM sources, not on the host-side api.cu or the routing kernels
+    assert "api.cu" not in bench.KERNEL_SOURCES["gemm"] and "route.cu" not in bench.KERNEL_SOURCES["gemm"]
+    assert bench.kernel_family("gemm_dw") == "gemm" and bench.kernel_family("route_topk") == "route"
+    assert bench.kernel_family("router_dz_rows") == "router" and bench.kernel_family("cast_f32_bf16") == "cast"
+    assert bench.source_sha("gemm_dw") == bench.source_sha("gemm_up") != bench.source_sha("route_topk")
 
 
 
