@@ -234,6 +234,36 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// ------------------------------------------------------------------------------------------ cluster
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster arrives (release) and waits (acquire): shared-memory writes before it
+// are visible to the other CTAs' distributed-shared-memory loads after it.  (A CTA launched without a cluster is
+// a cluster of one.)
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// 32-bit load from the shared memory of CTA `rank` of this cluster, at the offset of the local address `p`
+// (distributed shared memory: a plain load, nothing is sent to other CTAs).
+__device__ __forceinline__ uint32_t ld_dsmem_u32(const void *p, uint32_t rank) {
+  uint32_t remote, v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+  return v;
+}
+
 // ------------------------------------------------------------------------ programmatic dependent launch
 
 // Wait until the kernels this launch depends on have completed and their writes are visible (no-op when

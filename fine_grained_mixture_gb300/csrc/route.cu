@@ -391,17 +391,22 @@ __global__ void __launch_bounds__(kChunk) route_fill_tc_kernel(int T, int E, int
   }
 }
 
-// One CTA (1024 threads) per expert.  Keys of all T tokens for this expert live in shared memory.
-//   selection: a 4-pass radix select (8 bits per pass, most significant first) over the candidates finds the
-//              key of the R-th best candidate; each group of four warps fills its own 256-bin histogram (lanes
-//              in one bin add once) and one warp scans the bins; after the first pass (or from the start when dropping) the
-//              candidates are listed so the later passes skip the rest of the tokens; candidates equal to the
-//              boundary key are kept lowest token first
-//   output:    each warp owns a contiguous token range; ballots give in-order ranks, so the whole pass needs
-//              two block-wide scans (tie ranks, row positions)
-constexpr int kTrThreads = 1024;
+// Token rounding and expert choice: the kept rows of each expert.  A cluster of C CTAs (C = 1 .. 8) takes one
+// expert; CTA c takes the token words [c * Wc, (c + 1) * Wc) (Wc = ceil(ceil(T / 32) / C)) and keeps that slice's
+// keys in shared memory.  The CTAs of a cluster combine their results through distributed shared memory (plain
+// loads of each other's shared memory; nothing is multicast):
+//   selection: a 4-pass radix select (8 bits per pass, most significant first) over the candidates finds the key
+//              of the R-th best.  Each CTA fills a 256-bin histogram of its slice (lanes in one bin add once) and
+//              every CTA sums the cluster's histograms in the same order, so all of them take the same boundary.
+//              After the first pass (or from the start when dropping) each CTA lists its candidates, so the later
+//              passes skip the rest of its tokens.
+//   ties:      candidates equal to the boundary key are kept lowest token first: a CTA's ties rank after the ties
+//              of the CTAs before it.
+//   output:    a CTA's kept rows follow those of the CTAs before it, in ascending token order.
+constexpr int kTrThreads = 512;
 constexpr int kTrWarps = kTrThreads / 32;
-constexpr int kTrHists = 8;  // histogram copies, one per four warps
+constexpr int kTrHists = 4;  // histogram copies, one per four warps
+constexpr int kTrMaxCluster = 8;
 
 __device__ __forceinline__ int warp_scan_exclusive(int v, int *total) {
   const int lane = threadIdx.x & 31;
@@ -415,41 +420,47 @@ __device__ __forceinline__ int warp_scan_exclusive(int v, int *total) {
   return x - v;
 }
 
-__global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
+__global__ void __launch_bounds__(kTrThreads, 4) route_fill_tr_kernel(
     const uint32_t *__restrict__ keys_em, const float *__restrict__ logits, int T, int E, int K,
     const int32_t *__restrict__ topk_idx,
     const float *__restrict__ topk_score, const float *__restrict__ tok_max, const float *__restrict__ tok_den,
     const uint32_t *__restrict__ member, int member_words, int m_tile, const int32_t *__restrict__ tc_counts,
     const int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ tile_offsets,
     int32_t *__restrict__ status, int32_t *__restrict__ row_token, int32_t *__restrict__ row_slot,
-    float *__restrict__ row_score, int list_cap, int ec) {
+    float *__restrict__ row_score, int slice_words, int list_cap, int ec) {
   // ec (expert choice): every token is a candidate (as if all had chosen the expert) and a row's gate is the
   // token's softmax over all E logits (tok_den holds that denominator)
   extern __shared__ uint32_t sm[];
-  uint32_t *key = sm;                                       // [T]
-  uint32_t *mem = sm + T;                                   // [member_words]
-  int *hist = reinterpret_cast<int *>(mem + member_words);  // [kTrHists][256]
-  uint32_t *keep_bits = reinterpret_cast<uint32_t *>(hist + kTrHists * 256);  // [member_words]
-  int *list = reinterpret_cast<int *>(keep_bits + member_words);              // [list_cap] candidate tokens
+  uint32_t *key = sm;                                          // [32 * slice_words]: key of token t0 + i at i
+  uint32_t *mem = key + 32 * slice_words;                      // [slice_words] token-choice membership
+  uint32_t *keep_bits = mem + slice_words;                     // [slice_words]
+  uint32_t *tie = keep_bits + slice_words;                     // [slice_words] ties, then kept rows before a word
+  int *hist = reinterpret_cast<int *>(tie + slice_words);      // [2][kTrHists][256], alternate passes
+  int *list = hist + 2 * kTrHists * 256;                       // [list_cap] candidate (local) token indices
   __shared__ int list_n;
-  __shared__ int warp_tot[kTrWarps];
-  __shared__ int warp_base[kTrWarps];
   __shared__ int sel_state[2];
+  __shared__ int xch[2];     // shown to the cluster: this CTA's boundary ties, its kept rows
+  __shared__ int before[2];  // the same, summed over the CTAs before this one
   __shared__ int s_off[kMaxExperts + 1], s_toff[kMaxExperts + 1], scratch[32];
   griddep_wait();
   griddep_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int e = blockIdx.x;
+  const int C = static_cast<int>(cluster_nctarank()), c = static_cast<int>(cluster_ctarank());
+  const int e = static_cast<int>(blockIdx.x) / C;
   expert_offsets(counts, E, m_tile, s_off, s_toff, scratch);
   publish_offsets(E, s_off, s_toff, offsets, tile_offsets, status);
   const int f = ec ? T : tc_counts[e], r = counts[e], base = s_off[e];
-  if (r == 0) return;
-  for (int w = threadIdx.x; w < member_words; w += blockDim.x) mem[w] = member[(size_t)e * member_words + w];
+  if (r == 0) return;  // the same in every CTA of the cluster: none of them touches another's shared memory
+  const int w0 = c * slice_words, w1 = min(member_words, w0 + slice_words);
+  const int nw = max(0, w1 - w0);                  // words of this CTA's slice
+  const int t0 = 32 * w0;
+  const int nloc = max(0, min(T, 32 * w1) - t0);   // tokens of this CTA's slice
+  for (int w = threadIdx.x; w < nw; w += blockDim.x) mem[w] = member[(size_t)e * member_words + w0 + w];
   if (keys_em && (T & 3) == 0) {
-    // the expert's row of keys, 16 bytes a load and four loads in flight per thread before any store
-    const uint4 *src = reinterpret_cast<const uint4 *>(keys_em + (size_t)e * T);
+    // the slice of the expert's row of keys, 16 bytes a load and four loads in flight per thread before any store
+    const uint4 *src = reinterpret_cast<const uint4 *>(keys_em + (size_t)e * T + t0);
     uint4 *dst = reinterpret_cast<uint4 *>(key);
-    const int n4 = T >> 2;
+    const int n4 = nloc >> 2;
     for (int i0 = threadIdx.x; i0 < n4; i0 += 4 * kTrThreads) {
       uint4 v[4];
 #pragma unroll
@@ -460,49 +471,50 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
         if (i0 + u * kTrThreads < n4) dst[i0 + u * kTrThreads] = v[u];
     }
   } else if (keys_em) {
-    for (int t = threadIdx.x; t < T; t += blockDim.x) key[t] = __ldcs(&keys_em[(size_t)e * T + t]);
+    for (int i = threadIdx.x; i < nloc; i += blockDim.x) key[i] = __ldcs(&keys_em[(size_t)e * T + t0 + i]);
   } else {  // compact scratch: the expert's column of the logits, one strided word per token
-    for (int t = threadIdx.x; t < T; t += blockDim.x) key[t] = order_key(logits[(size_t)t * E + e]);
+    for (int i = threadIdx.x; i < nloc; i += blockDim.x) key[i] = order_key(logits[(size_t)(t0 + i) * E + e]);
   }
   __syncthreads();
   // candidates: token-choice tokens when dropping, the other tokens when padding
   const bool drop = r < f;
-  const int R = drop ? r : r - f;  // how many candidates to keep
+  const int R = drop ? r : r - f;  // how many candidates the cluster keeps
   uint32_t prefix = 0u, mask = 0u;
   int remaining = R;
   const uint32_t lt = (1u << lane) - 1u;
-  // Tokens satisfying `pred`, in no particular order, into list[]; -1 when there are more than list_cap.
+  // This slice's tokens satisfying `pred`, in no particular order, into list[]; -1 when more than list_cap.
   auto build_list = [&](auto pred) -> int {
     if (threadIdx.x == 0) list_n = 0;
     __syncthreads();
-    for (int t0 = 0; t0 < T; t0 += blockDim.x) {
-      const int t = t0 + threadIdx.x;
-      const bool p = t < T && pred(t);
+    for (int i0 = 0; i0 < nloc; i0 += blockDim.x) {
+      const int i = i0 + threadIdx.x;
+      const bool p = i < nloc && pred(i);
       const uint32_t b = __ballot_sync(0xffffffffu, p);
       int at = 0;
       if (lane == 0 && b) at = atomicAdd(&list_n, __popc(b));
       at = __shfl_sync(0xffffffffu, at, 0) + __popc(b & lt);
-      if (p && at < list_cap) list[at] = t;
+      if (p && at < list_cap) list[at] = i;
     }
     __syncthreads();
     return list_n <= list_cap ? list_n : -1;
   };
-  auto is_tc = [&](int t) { return ((mem[t >> 5] >> (t & 31)) & 1u) != 0u; };
-  auto first = [&](int t) { return ec || is_tc(t); };  // ranked ahead of the other tokens
-  int nlist = -1;  // candidates listed in list[] (-1: not listed)
+  auto is_tc = [&](int i) { return ((mem[i >> 5] >> (i & 31)) & 1u) != 0u; };
+  auto first = [&](int i) { return ec || is_tc(i); };  // ranked ahead of the other tokens
+  int nlist = -1;  // this slice's candidates listed in list[] (-1: not listed)
   if (r != f) {
-    // Candidates are few next to T: the expert's token-choice tokens when dropping, and when padding the
-    // other tokens in the top-byte bin of the boundary.  Once they are listed, the remaining radix passes
-    // walk the list instead of all T tokens (all T when the list would overflow its space, or under expert
+    // Candidates are few next to T: the expert's token-choice tokens when dropping, and when padding the other
+    // tokens in the top-byte bin of the boundary.  Once they are listed, the remaining radix passes walk the list
+    // instead of all the slice's tokens (all of them when the list would overflow its space, or under expert
     // choice, where every token is a candidate).
     nlist = (drop && !ec) ? build_list(is_tc) : -1;
-    int *my_hist = hist + (warp >> 2) * 256;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = threadIdx.x; i < kTrHists * 256; i += blockDim.x) hist[i] = 0;
+    for (int pass = 0, shift = 24; shift >= 0; ++pass, shift -= 8) {
+      // the two buffers alternate: a CTA zeroes this pass's buffer only after the whole cluster has passed the
+      // barrier of the previous pass, by which time every CTA has read the buffer's previous contents
+      int *hb = hist + (pass & 1) * kTrHists * 256;
+      for (int i = threadIdx.x; i < kTrHists * 256; i += blockDim.x) hb[i] = 0;
       __syncthreads();
-      // lanes that fall in the same bin add once (many keys share their leading bits); grouping the lanes
-      // with __match_any_sync measured faster than ballot rounds on the leading lane's bin
-      const int n_iter = nlist >= 0 ? nlist : T;
+      int *my_hist = hb + (warp >> 2) * 256;
+      const int n_iter = nlist >= 0 ? nlist : nloc;
       for (int i0 = 0; i0 < n_iter; i0 += blockDim.x) {
         const int i = i0 + threadIdx.x;
         uint32_t bin = 256u;
@@ -511,34 +523,41 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
           const uint32_t k = key[t];
           if ((nlist >= 0 || first(t) == drop) && (k & mask) == prefix) bin = (k >> shift) & 255u;
         }
+        // lanes that fall in the same bin add once (many keys share their leading bits)
         const uint32_t same = __match_any_sync(0xffffffffu, bin);
         if (bin < 256u && lane == __ffs(same) - 1) atomicAdd(&my_hist[bin], __popc(same));
       }
       __syncthreads();
+      for (int b = threadIdx.x; b < 256; b += blockDim.x) {
+        int v = 0;
+#pragma unroll
+        for (int g = 1; g < kTrHists; ++g) v += hb[g * 256 + b];
+        hb[b] += v;
+      }
+      cluster_sync();  // every CTA's histogram of this pass is complete in its copy 0
       if (warp == 0) {
-        // lane l owns bins 255 - 8l - i (i = 0..7), i.e. lane 0 the highest bins
-        int c[8], lane_sum = 0;
+        // lane l owns bins 255 - 8l - i (i = 0..7), i.e. lane 0 the highest bins, summed over the cluster
+        int cnt[8], lane_sum = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int b = 255 - (lane * 8 + i);
           int v = 0;
-#pragma unroll
-          for (int g = 0; g < kTrHists; ++g) v += hist[g * 256 + b];
-          c[i] = v;
+          for (int q = 0; q < C; ++q) v += static_cast<int>(ld_dsmem_u32(hb + b, static_cast<uint32_t>(q)));
+          cnt[i] = v;
           lane_sum += v;
         }
         int tot;
-        const int before = warp_scan_exclusive(lane_sum, &tot);
-        if (before < remaining && remaining <= before + lane_sum) {
-          int acc = before;
+        const int bef = warp_scan_exclusive(lane_sum, &tot);
+        if (bef < remaining && remaining <= bef + lane_sum) {
+          int acc = bef;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            if (acc + c[i] >= remaining) {
+            if (acc + cnt[i] >= remaining) {
               sel_state[0] = 255 - (lane * 8 + i);
               sel_state[1] = remaining - acc;
               break;
             }
-            acc += c[i];
+            acc += cnt[i];
           }
         }
       }
@@ -547,144 +566,114 @@ __global__ void __launch_bounds__(kTrThreads) route_fill_tr_kernel(
       mask |= 255u << shift;
       remaining = sel_state[1];
       if (shift == 24 && (!drop || nlist < 0)) {
-        // the candidates whose top byte is at or above the boundary's: every candidate that can still be kept
-        // (when padding, or when the first list would not fit or was not built, as under expert choice)
+        // the slice's candidates whose top byte is at or above the boundary's: every candidate that can still be
+        // kept (when padding, or when the first list would not fit or was not built, as under expert choice)
         const uint32_t top = prefix;
-        nlist = build_list([&](int t) { return first(t) == drop && (key[t] & 0xff000000u) >= top; });
+        nlist = build_list([&](int i) { return first(i) == drop && (key[i] & 0xff000000u) >= top; });
       }
     }
   }
-  // prefix = key of the R-th best candidate; `remaining` candidates equal to it are kept, lowest token first.
-  // the row of kept token t at position pos: its token-choice slot (if any) and its gate
-  auto write_row = [&](int pos, int t) {
+  // prefix = key of the R-th best candidate of the expert; `remaining` candidates equal to it are kept, lowest
+  // token first.  Keep masks word by word; each thread owns a contiguous run of the slice's words.
+  const int per = (nw + kTrThreads - 1) / kTrThreads;
+  const int wa = min(nw, static_cast<int>(threadIdx.x) * per), wb = min(nw, wa + per);
+  for (int w = wa; w < wb; ++w) {
+    uint32_t m = 0u;
+    if (r == f || !drop) {
+      const int gw = w0 + w;  // the word's index over all T tokens
+      if (ec) m = (32 * gw + 32 <= T) ? 0xffffffffu : ((1u << (T - 32 * gw)) - 1u);
+      else m = mem[w];
+    }
+    keep_bits[w] = m;
+    tie[w] = 0u;
+  }
+  __syncthreads();
+  if (r != f) {
+    const int n_iter = nlist >= 0 ? nlist : nloc;
+    for (int i = threadIdx.x; i < n_iter; i += blockDim.x) {
+      const int t = nlist >= 0 ? list[i] : i;
+      if (nlist < 0 && first(t) != drop) continue;
+      const uint32_t k = key[t];
+      if (k > prefix) atomicOr(&keep_bits[t >> 5], 1u << (t & 31));
+      else if (k == prefix) atomicOr(&tie[t >> 5], 1u << (t & 31));
+    }
+    __syncthreads();
+    int ties = 0, total;
+    for (int w = wa; w < wb; ++w) ties += __popc(tie[w]);
+    int rank = block_exclusive_scan(ties, scratch, &total);
+    if (threadIdx.x == 0) xch[0] = total;
+    cluster_sync();  // the ties of every slice are counted
+    if (threadIdx.x == 0) {
+      int sum = 0;
+      for (int q = 0; q < c; ++q) sum += static_cast<int>(ld_dsmem_u32(&xch[0], static_cast<uint32_t>(q)));
+      before[0] = sum;
+    }
+    __syncthreads();
+    rank += before[0];
+    for (int w = wa; w < wb; ++w) {
+      uint32_t m = tie[w];
+      while (m) {
+        const uint32_t bit = m & (0u - m);
+        if (rank < remaining) keep_bits[w] |= bit;
+        ++rank;
+        m ^= bit;
+      }
+    }
+    __syncthreads();
+  }
+  // rows: this thread's words start after the kept rows of the earlier threads and of the earlier slices
+  int kept = 0, ktotal;
+  for (int w = wa; w < wb; ++w) kept += __popc(keep_bits[w]);
+  int kbase = block_exclusive_scan(kept, scratch, &ktotal);
+  if (threadIdx.x == 0) xch[1] = ktotal;
+  cluster_sync();  // the kept rows of every slice are counted
+  if (threadIdx.x == 0) {
+    int sum = 0;
+    for (int q = 0; q < c; ++q) sum += static_cast<int>(ld_dsmem_u32(&xch[1], static_cast<uint32_t>(q)));
+    before[1] = sum;
+  }
+  for (int w = wa; w < wb; ++w) {  // kept rows of the slice before each word
+    tie[w] = static_cast<uint32_t>(kbase);
+    kbase += __popc(keep_bits[w]);
+  }
+  __syncthreads();
+  const int row0 = base + before[1];
+  // the row of kept token t0 + i at position pos: its token-choice slot (if any) and its gate
+  auto write_row = [&](int pos, int i) {
+    const int t = t0 + i;
     int slot = -1;
-    if ((mem[t >> 5] >> (t & 31)) & 1u) {
+    if (is_tc(i)) {
       for (int k = 0; k < K; ++k)
         if (topk_idx[(size_t)t * K + k] == e) slot = k;
     }
     const float sc = (slot >= 0 && !ec) ? topk_score[(size_t)t * K + slot]
-                                        : expf(key_to_float(key[t]) - tok_max[t]) / tok_den[t];
+                                        : expf(key_to_float(key[i]) - tok_max[t]) / tok_den[t];
     row_token[pos] = t;
     row_slot[pos] = slot;
     row_score[pos] = sc;
   };
-  const int span = ((T + kTrThreads - 1) / kTrThreads) * 32;  // tokens per warp, a multiple of 32
-  const int t_lo = warp * span;
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  int keep_count = 0;  // kept tokens in this warp's token range
-  if (r == f || nlist >= 0) {
-    // Keep masks word by word (32 tokens a word): tokens ranked first are kept whole unless dropping; listed
-    // candidates above the boundary key are kept; of those equal to it, the first `remaining` in token order.
-    // Each thread owns a contiguous run of words, so one block scan of popcounts ranks the ties.
-    uint32_t *tie = reinterpret_cast<uint32_t *>(hist);  // the radix histograms are free (8 x 256 >= T / 32 words)
-    const int per = (member_words + kTrThreads - 1) / kTrThreads;
-    const int w0 = threadIdx.x * per, w1 = min(member_words, w0 + per);
-    for (int w = w0; w < w1; ++w) {
-      uint32_t m = 0u;
-      if (r == f || !drop) {
-        if (ec) m = (32 * w + 32 <= T) ? 0xffffffffu : ((1u << (T - 32 * w)) - 1u);
-        else m = mem[w];
-      }
-      keep_bits[w] = m;
-      tie[w] = 0u;
-    }
-    __syncthreads();
-    if (r != f) {
-      for (int i = threadIdx.x; i < nlist; i += blockDim.x) {
-        const int t = list[i];
-        const uint32_t k = key[t];
-        if (k > prefix) atomicOr(&keep_bits[t >> 5], 1u << (t & 31));
-        else if (k == prefix) atomicOr(&tie[t >> 5], 1u << (t & 31));
-      }
-      __syncthreads();
-      int ties = 0, total;
-      for (int w = w0; w < w1; ++w) ties += __popc(tie[w]);
-      int rank = block_exclusive_scan(ties, scratch, &total);
-      for (int w = w0; w < w1; ++w) {
-        uint32_t m = tie[w];
-        while (m) {
-          const uint32_t bit = m & (0u - m);
-          if (rank < remaining) keep_bits[w] |= bit;
-          ++rank;
-          m ^= bit;
-        }
+  if (ktotal <= list_cap) {
+    // the kept tokens compacted in token order into the (free again) candidate list, then one thread per row, so
+    // the rows' global loads (slot, gate) are all in flight at once
+    for (int w = wa; w < wb; ++w) {
+      uint32_t m = keep_bits[w];
+      int at = static_cast<int>(tie[w]);
+      while (m) {
+        const int b = __ffs(m) - 1;
+        list[at++] = 32 * w + b;
+        m &= m - 1u;
       }
     }
     __syncthreads();
-    // this warp's kept tokens: its words' popcounts (lane i takes words i, i + 32, ...)
-    for (int t0 = t_lo + 32 * lane; t0 < t_lo + span && t0 < T; t0 += 32 * 32) keep_count += __popc(keep_bits[t0 >> 5]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) keep_count += __shfl_xor_sync(0xffffffffu, keep_count, off);
+    for (int i = threadIdx.x; i < ktotal; i += blockDim.x) write_row(row0 + i, list[i]);
   } else {
-    // Token-order passes, for candidate sets too large for the list.
-    // pass 1: ties (candidates whose key equals the boundary key) per warp
-    int eq_count = 0;
-    for (int t0 = t_lo; t0 < t_lo + span && t0 < T; t0 += 32) {
-      const int t = t0 + lane;
-      bool eq = false;
-      if (t < T) eq = (first(t) == drop) && key[t] == prefix;
-      eq_count += __popc(__ballot_sync(0xffffffffu, eq));
-    }
-    if (lane == 0) warp_tot[warp] = eq_count;
-    __syncthreads();
-    if (warp == 0) {
-      int tot;
-      const int b = warp_scan_exclusive(warp_tot[lane], &tot);
-      warp_base[lane] = b;
-    }
-    __syncthreads();
-    // pass 2: keep decisions in token order; the kept bits of each 32-token group go to shared memory
-    int eq_run = warp_base[warp];
-    for (int t0 = t_lo; t0 < t_lo + span && t0 < T; t0 += 32) {
-      const int t = t0 + lane;
-      bool tc = false, gt = false, eq = false;
-      if (t < T) {
-        tc = first(t);
-        if (tc == drop) {
-          const uint32_t k = key[t];
-          gt = k > prefix;
-          eq = k == prefix;
-        }
-      }
-      const uint32_t eq_bal = __ballot_sync(0xffffffffu, eq);
-      const int eq_rank = eq_run + __popc(eq_bal & lt_mask);
-      eq_run += __popc(eq_bal);
-      const bool take = gt || (eq && eq_rank < remaining);
-      const bool keep = drop ? take : (tc || take);
-      const uint32_t kb = __ballot_sync(0xffffffffu, keep);
-      if (lane == 0) keep_bits[t0 >> 5] = kb;
-      keep_count += __popc(kb);
+    // more rows than the list holds: one word per warp at a time, one lane per token
+    for (int w = warp; w < nw; w += kTrWarps) {
+      const uint32_t m = keep_bits[w];
+      if ((m >> lane) & 1u) write_row(row0 + static_cast<int>(tie[w]) + __popc(m & lt), 32 * w + lane);
     }
   }
-  __syncthreads();
-  if (lane == 0) warp_tot[warp] = keep_count;
-  __syncthreads();
-  if (warp == 0) {
-    int tot;
-    const int b = warp_scan_exclusive(warp_tot[lane], &tot);
-    warp_base[lane] = b;
-  }
-  __syncthreads();
-  if (r <= list_cap) {
-    // pass 3: the kept tokens, compacted in token order into the candidate list (free again), then one thread per
-    // row, so the rows' global loads (slot, gate) are all in flight at once rather than chunk after chunk
-    int at = warp_base[warp];
-    for (int t0 = t_lo; t0 < t_lo + span && t0 < T; t0 += 32) {
-      const uint32_t kb = keep_bits[t0 >> 5];
-      if ((kb >> lane) & 1u) list[at + __popc(kb & lt_mask)] = t0 + lane;
-      at += __popc(kb);
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < r; i += blockDim.x) write_row(base + i, list[i]);
-  } else {
-    // pass 3 for an expert with more rows than the list holds: rows in ascending token order, warp by warp
-    int row = base + warp_base[warp];
-    for (int t0 = t_lo; t0 < t_lo + span && t0 < T; t0 += 32) {
-      const uint32_t kb = keep_bits[t0 >> 5];
-      if ((kb >> lane) & 1u) write_row(row + __popc(kb & lt_mask), t0 + lane);
-      row += __popc(kb);
-    }
-  }
+  cluster_sync();  // no CTA leaves while another may still read its shared memory
 }
 
 // ------------------------------------------------------------------------------------------- host
@@ -734,17 +723,34 @@ static RouteWs carve(void *ws, int T, int E, int mode, bool em_keys) {
   return w;
 }
 
-size_t route_tr_smem_bytes(int T) {
-  return (size_t)T * 4 + (size_t)((T + 31) / 32) * 4 * 2 + kTrHists * 256 * 4;
+// The token-rounding fill's launch: C CTAs per expert, each with slice_words words of tokens.  C doubles (up to 8)
+// while E*C CTAs stay within about four per SM (so one cluster per expert still runs in a single wave), and no
+// slice is empty.
+struct TrLaunch {
+  int C, slice_words, list_cap;
+  size_t smem;
+};
+
+// Dynamic shared memory of one CTA: the slice's keys, three word arrays, two sets of histograms.
+static size_t route_tr_fixed_bytes(int slice_words) {
+  return (size_t)slice_words * 32 * 4 + (size_t)slice_words * 4 * 3 + 2 * kTrHists * 256 * 4;
 }
 
-// Candidate-list entries the token-rounding fill gets beside its fixed shared memory: up to 4096 (16 KB keeps
-// two CTAs per SM at T = 16384), less where T leaves less room.
-constexpr size_t kTrDynSmemMax = 218 * 1024;  // + about 8.4 KB of static shared memory stays under 227 KB
-static int route_tr_list_cap(int T) {
-  const size_t fixed = route_tr_smem_bytes(T);
-  const size_t room = fixed < kTrDynSmemMax ? (kTrDynSmemMax - fixed) / 4 : 0;
-  return static_cast<int>(room < 4096 ? room : 4096);
+constexpr size_t kTrDynSmemMax = 218 * 1024;  // + about 8.3 KB of static shared memory stays under 227 KB
+static TrLaunch route_tr_launch(int T, int E) {
+  TrLaunch l;
+  const int words = (T + 31) / 32;
+  l.C = 1;
+  while (l.C < kTrMaxCluster && (int64_t)E * l.C * 2 <= 4 * (int64_t)num_sms() && l.C * 2 <= words) l.C *= 2;
+  l.slice_words = (words + l.C - 1) / l.C;
+  // candidate-list entries beside the fixed part: up to 4096, and with several CTAs per expert no more than keeps
+  // a CTA (with its 8.4 KB of static shared memory) to a quarter of the SM's 228 KB: four CTAs of 512 threads
+  const size_t fixed = route_tr_fixed_bytes(l.slice_words);
+  const size_t cap_bytes = l.C > 1 ? std::max<size_t>(fixed + 4096, 46 * 1024) : kTrDynSmemMax;
+  const size_t room = fixed < cap_bytes ? (cap_bytes - fixed) / 4 : 0;
+  l.list_cap = static_cast<int>(room < 4096 ? room : 4096);
+  l.smem = fixed + (size_t)l.list_cap * 4;
+  return l;
 }
 
 int launch_route(const float *logits, const float *uniforms, int T, int E, int K, int mode, const moe_routing *r,
@@ -813,14 +819,29 @@ int launch_route(const float *logits, const float *uniforms, int T, int E, int K
                      r->status, r->row_token, r->row_slot, r->row_score);
     if (err != cudaSuccess) return record_cuda_error(err);
   } else {
-    const int list_cap = route_tr_list_cap(T);
-    const size_t smem = route_tr_smem_bytes(T) + (size_t)list_cap * 4;
+    const TrLaunch tl = route_tr_launch(T, E);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;  // one cluster of C CTAs per expert
+    attr[0].val.clusterDim.x = tl.C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(E * tl.C);
+    cfg.blockDim = dim3(kTrThreads);
+    cfg.dynamicSmemBytes = tl.smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
     prof_begin("route_fill_tr", stream);
-    err = launch_pdl(route_fill_tr_kernel, dim3(E), dim3(kTrThreads), smem, stream, w.keys_em, logits, T, E, K,
-                     r->topk_idx,
-                     r->topk_score, w.tok_max, w.tok_den, w.member, w.member_words, MOE_M_TILE, r->tc_counts, r->counts,
-                     r->offsets, r->tile_offsets, r->status, r->row_token, r->row_slot, r->row_score, list_cap,
-                     den_all);
+    err = cudaLaunchKernelEx(&cfg, route_fill_tr_kernel, static_cast<const uint32_t *>(w.keys_em), logits, T, E, K,
+                             static_cast<const int32_t *>(r->topk_idx), static_cast<const float *>(r->topk_score),
+                             static_cast<const float *>(w.tok_max), static_cast<const float *>(w.tok_den),
+                             static_cast<const uint32_t *>(w.member), w.member_words, static_cast<int>(MOE_M_TILE),
+                             static_cast<const int32_t *>(r->tc_counts), static_cast<const int32_t *>(r->counts),
+                             r->offsets, r->tile_offsets, r->status, r->row_token, r->row_slot, r->row_score,
+                             tl.slice_words, tl.list_cap, den_all);
     if (err != cudaSuccess) return record_cuda_error(err);
   }
   prof_end(stream);
