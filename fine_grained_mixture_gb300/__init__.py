@@ -13,3 +13,5 @@ __all__ = ["M_TILE", "MODES", "MOE_FLAG_A_FROM_H", "MOE_FLAG_DETERMINISTIC", "MO
            "moe_backward", "moe_backward_workspace_size", "moe_forward", "moe_forward_workspace_size", "moe_route",
            "moe_route_capacity", "moe_route_workspace_size", "moe_router_backward", "moe_router_forward",
            "profile_enable", "profile_summary", "selftest_bounded_wait"]
+
+from . import dp  # noqa: E402  (data parallelism: token shards and the weight-gradient all-reduce)
