@@ -530,7 +530,10 @@ int moe_backward_ex(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, c
            : launch_f32_to_bf16(static_cast<float *>(dXacc), dX, T, d, side.side());
   if (rc != MOE_OK) return rc;
   GemmArgs aw = base_args(r, T, d, n, E, p_cap);
-  aw.wide_m = (int64_t)T * K >= (int64_t)1024 * E;  // experts average >= 1024 rows: >= 16 k-blocks per tile
+  // 256-row blocks (one accumulator, B shared by two M blocks) once experts average >= 256 rows (>= 4 k-blocks per
+  // tile): measured faster than double-buffered 128-row blocks there (high-sparsity layer, 256 rows on average:
+  // dW1 + dW2 239 -> 198 us)
+  aw.wide_m = (int64_t)T * K >= (int64_t)256 * E;
   if (aw.wide_m && d % 256 == 0 && n % 256 == 0) {
     // both weight gradients in one launch: dW1 tiles gather X into A and load dH as B, dW2 tiles load s*A
     // as A and gather dO into B (one wave quantisation instead of two)

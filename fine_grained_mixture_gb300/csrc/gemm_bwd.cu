@@ -19,7 +19,7 @@ int launch_dx(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, bool det)
 }
 
 // 256-row M blocks (see Smem) when the weight's row count allows it and the experts' K loops are long
-// enough to hide the unoverlapped epilogue; else 128-row blocks with double-buffered TMEM.
+// enough (experts averaging >= 256 rows); else 128-row blocks with double-buffered TMEM.
 int launch_dw1(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) {
   if (a.wide_m && a.Mdim % 256 == 0) return launch_gemm<kDW1, 256, 3, 2>(a, tm, s);
   return launch_gemm<kDW1, 256, 4, 1>(a, tm, s);

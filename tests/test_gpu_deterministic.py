@@ -89,3 +89,25 @@ def test_deterministic_full_size_matches_oracle_on_samples():
         _, _, be = oracle_on_rows(inp, ref, np.arange(ref["offsets"][e], ref["offsets"][e + 1]))
         assert_close(f"dW1[{e}]", f64(out["dW1"][e]), be["dW1"][0])
         assert_close(f"dW2[{e}]", f64(out["dW2"][e]), be["dW2"][0])
+
+
+@pytest.mark.parametrize("mode", ["tc", "tr"])
+def test_deterministic_with_a_kept_off_hbm(mode):
+    """Both forward flags at once: the down-projection that recomputes A from H, with the fixed-point aggregation.
+    Against the oracle, and bitwise identical on a second run."""
+    w = synth.custom(300, 256, 384, 5, 2)   # ragged tail tiles; n = 3 x 128
+    inp = synth.make_inputs(w, 3)
+    g = to_dev(inp)
+    outs = []
+    for _ in range(2):
+        rt = moe.moe_route(g["logits"], w.K, mode)
+        O, H = moe.moe_forward(g["X"], g["W1"], g["W2"], rt, deterministic=True, a_from_h=True)
+        torch.cuda.synchronize()
+        code, P = rt.device_status()
+        assert code == 0
+        outs.append((O.clone(), H[:P].clone(), P))
+    ref = orc.route(inp["logits"].numpy(), w.K, mode)
+    fwd, _ = orc.layer(f64(inp["X"]), f64(inp["W1"]), f64(inp["W2"]), f64(inp["dO"]), ref)
+    assert_close("O", f64(outs[0][0]), fwd["O"])
+    assert_close("H", f64(outs[0][1]), fwd["H"])
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
