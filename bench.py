@@ -300,13 +300,17 @@ class Layer:
         self.moe.moe_backward(self.g["dO"], self.g["X"], self.g["W1"], self.g["W2"], self.H, self.rt, dX=self.dX,
                               dW1=self.dW1, dW2=self.dW2, dS=self.dS, ws=self.wsb, deterministic=self.det)
 
+    def exchange(self):
+        """Data parallel: the weight gradients summed over the ranks (nothing with a single rank)."""
+        if self.allreduce:
+            from fine_grained_mixture_gb300 import dp
+            dp.allreduce_weight_grads(self.dW1, self.dW2)
+
     def step(self):
         self.route()
         self.forward()
         self.backward()
-        if self.allreduce:
-            from fine_grained_mixture_gb300 import dp
-            dp.allreduce_weight_grads(self.dW1, self.dW2)
+        self.exchange()
 
     def cached_bytes(self):
         """Bytes that live from forward to backward: X, H (P rows) and the routing metadata."""
@@ -318,7 +322,8 @@ class Layer:
 
 
 def time_steps(layer, steps, split=False):
-    """Times `steps` back-to-back steps with CUDA events on the current stream."""
+    """Times `steps` back-to-back steps with CUDA events on the current stream (split: also route, forward and
+    backward apart; the data-parallel all-reduce is part of every step and of the total, not of the three parts)."""
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     marks = []
     ev[0].record()
@@ -332,6 +337,7 @@ def time_steps(layer, steps, split=False):
             e[2].record()
             layer.backward()
             e[3].record()
+            layer.exchange()
             marks.append(e)
         else:
             layer.step()

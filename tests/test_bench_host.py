@@ -116,3 +116,48 @@ def test_clock_sampler_without_nvidia_smi(tmp_path, monkeypatch):
     out = sampler.stop(0.0, 1.0)
     assert out["sm_mhz"] is None and out["reasons"] == ["nvidia-smi unavailable"]
     assert not list(tmp_path.glob("*.csv"))                          # the sample file is removed
+
+
+def test_every_timed_step_includes_the_data_parallel_exchange(monkeypatch):
+    """The split timing pass calls route, forward and backward apart; the all-reduce of the weight gradients must
+    still run in every timed step (and the plain step must run it too)."""
+    calls = []
+
+    class FakeEvent:
+        def __init__(self, **kw):
+            pass
+
+        def record(self, *a):
+            calls.append("ev")
+
+        def elapsed_time(self, other):
+            return 1.0
+
+    class FakeLayer:
+        allreduce = True
+
+        def route(self):
+            calls.append("route")
+
+        def forward(self):
+            calls.append("forward")
+
+        def backward(self):
+            calls.append("backward")
+
+        def exchange(self):
+            calls.append("exchange")
+
+        def step(self):
+            for f in (self.route, self.forward, self.backward, self.exchange):
+                f()
+
+    monkeypatch.setattr(bench.torch.cuda, "Event", FakeEvent)
+    monkeypatch.setattr(bench.torch.cuda, "synchronize", lambda *a: None)
+    for split in (True, False):
+        calls.clear()
+        bench.time_steps(FakeLayer(), 3, split=split)
+        assert calls.count("exchange") == 3 and calls.count("backward") == 3
+        # each step's exchange follows its backward
+        seq = [c for c in calls if c != "ev"]
+        assert seq == ["route", "forward", "backward", "exchange"] * 3
