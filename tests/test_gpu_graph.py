@@ -15,8 +15,11 @@ from gpu_util import assert_close, f64, to_dev
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("name,mode", [("tiny", "tc"), ("tiny", "tr"), ("fine7b", "tc")])
-def test_route_forward_backward_replay_in_a_cuda_graph(name, mode):
+# token rounding runs its fill as clusters of 8 (tiny), 4 (fine7b) and 2 (sparse) CTAs per expert; the sparse
+# layer's weight gradients take the merged 256-row launch; a_from_h: the down-projection recomputes A from H
+@pytest.mark.parametrize("name,mode,a_from_h", [("tiny", "tc", False), ("tiny", "tr", False), ("fine7b", "tc", False),
+                                               ("fine7b", "tr", True), ("sparse", "tr", False)])
+def test_route_forward_backward_replay_in_a_cuda_graph(name, mode, a_from_h):
     w = synth.WORKLOADS[name]
     g = to_dev(synth.make_inputs(w, 3))
     rt = moe.Routing(w.T, w.E, w.K, mode, "cuda")
@@ -28,12 +31,14 @@ def test_route_forward_backward_replay_in_a_cuda_graph(name, mode):
     dW1 = torch.empty((w.E, w.d, 2 * w.n), dtype=bf, device="cuda")
     dW2 = torch.empty((w.E, w.n, w.d), dtype=bf, device="cuda")
     dS = torch.empty(p, dtype=torch.float32, device="cuda")
-    wsf = torch.empty(moe.moe_forward_workspace_size(w.T, w.d, w.n, w.E, w.K, p), dtype=torch.uint8, device="cuda")
+    fflags = moe.MOE_FLAG_A_FROM_H if a_from_h else 0
+    wsf = torch.empty(moe.moe_forward_workspace_size(w.T, w.d, w.n, w.E, w.K, p, fflags), dtype=torch.uint8,
+                      device="cuda")
     wsb = torch.empty(moe.moe_backward_workspace_size(w.T, w.d, w.n, w.E, w.K, p), dtype=torch.uint8, device="cuda")
 
     def step():
         moe.moe_route(g["logits"], w.K, mode, routing=rt)
-        moe.moe_forward(g["X"], g["W1"], g["W2"], rt, O=O, H=H, ws=wsf)
+        moe.moe_forward(g["X"], g["W1"], g["W2"], rt, O=O, H=H, ws=wsf, a_from_h=a_from_h)
         moe.moe_backward(g["dO"], g["X"], g["W1"], g["W2"], H, rt, dX=dX, dW1=dW1, dW2=dW2, dS=dS, ws=wsb)
 
     s = torch.cuda.Stream()
