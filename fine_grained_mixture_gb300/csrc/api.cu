@@ -224,6 +224,34 @@ int make_tmap_bf16_epi(CUtensorMap *tm, const void *base, uint64_t inner, uint64
   return r == CUDA_SUCCESS ? MOE_OK : record_cu_error(r);
 }
 
+static int encode_bf16(CUtensorMap *tm, const void *base, cuuint32_t rank, const cuuint64_t *dims,
+                       const cuuint64_t *strides, const cuuint32_t *box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return record_cuda_error(cudaErrorNotSupported);
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : record_cu_error(r);
+}
+
+int make_tmap_bf16_chunks(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t rows, uint32_t box_rows,
+                          uint32_t chunks) {
+  if (inner % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const cuuint64_t dims[3] = {64, rows, inner / 64};
+  const cuuint64_t strides[2] = {inner * 2, 128};  // row pitch; the next 64-column chunk is 128 bytes on
+  const cuuint32_t box[3] = {64, box_rows, chunks};
+  return encode_bf16(tm, base, 3, dims, strides, box);
+}
+
+int make_tmap_bf16_halves(CUtensorMap *tm, const void *base, uint64_t n, uint64_t rows) {
+  if (n % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const cuuint64_t dims[4] = {64, rows, n / 64, 2};
+  const cuuint64_t strides[3] = {4 * n, 128, 2 * n};  // row pitch (2n bf16), next chunk, the up half n columns on
+  const cuuint32_t box[4] = {64, 64, 2, 2};
+  return encode_bf16(tm, base, 4, dims, strides, box);
+}
+
 static void fill_unused(TensorMaps &tm) { tm.h = tm.dh = tm.sa = tm.b; }
 
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -395,7 +423,7 @@ int moe_forward_ex(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, co
   GemmArgs a = base_args(r, T, d, n, E, p_cap);
   TensorMaps tm;
   // up-projection: H = X[tok] W1_e (N = 2n, K = d); X rows are gathered with cp.async
-  if ((rc = make_tmap_bf16(&tm.b, W1, 2 * (uint64_t)n, (uint64_t)E * d, 64)) != MOE_OK) return rc;
+  if ((rc = make_tmap_bf16_halves(&tm.b, W1, n, (uint64_t)E * d)) != MOE_OK) return rc;
   tm.a = tm.b;  // unused by this GEMM
   a.gsrc = X;
   a.gld = d;
@@ -412,7 +440,7 @@ int moe_forward_ex(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, co
   // recomputed from H inside the kernel
   if (a_from_h) tm.a = tm.b;  // unused
   else if ((rc = make_tmap_bf16(&tm.a, A, n, p_cap, 128)) != MOE_OK) return rc;
-  if ((rc = make_tmap_bf16(&tm.b, W2, d, (uint64_t)E * n, 64)) != MOE_OK) return rc;
+  if ((rc = make_tmap_bf16_chunks(&tm.b, W2, d, (uint64_t)E * n, 64, 4)) != MOE_OK) return rc;  // 256 columns
   a.Ndim = d;
   a.Kdim = n;
   a.out0 = nullptr;
@@ -498,7 +526,7 @@ int moe_backward_ex(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, c
   GemmArgs a = base_args(r, T, d, n, E, p_cap);
   TensorMaps tm;
   // dH: dA' = dO[tok] W2_e^T (N = n, K = d); epilogue dSwiGLU, dS, s*A
-  if ((rc = make_tmap_bf16(&tm.b, W2, d, (uint64_t)E * n, bn / 2)) != MOE_OK) return rc;  // two N halves
+  if ((rc = make_tmap_bf16(&tm.b, W2, d, (uint64_t)E * n, bn)) != MOE_OK) return rc;  // all BN rows of W2_e
   tm.a = tm.b;  // unused: dO rows are gathered with cp.async
   a.gsrc = dO;
   a.gld = d;
@@ -516,7 +544,7 @@ int moe_backward_ex(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, c
   if (det && (rc = launch_ds_sum(dS_part, n / bn, r->offsets, E, dS, s)) != MOE_OK) return rc;
   // dX~: dX32[tok] += dH W1_e^T (N = d, K = 2n)
   if ((rc = make_tmap_bf16(&tm.a, dH, 2 * (uint64_t)n, p_cap, 128)) != MOE_OK) return rc;
-  if ((rc = make_tmap_bf16(&tm.b, W1, 2 * (uint64_t)n, (uint64_t)E * d, 128)) != MOE_OK) return rc;  // two N halves
+  if ((rc = make_tmap_bf16(&tm.b, W1, 2 * (uint64_t)n, (uint64_t)E * d, 256)) != MOE_OK) return rc;  // 256 rows of W1_e
   GemmArgs ax = base_args(r, T, d, n, E, p_cap);
   ax.Ndim = d;
   ax.Kdim = 2 * n;
@@ -537,8 +565,8 @@ int moe_backward_ex(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, c
   if (aw.wide_m && d % 256 == 0 && n % 256 == 0) {
     // both weight gradients in one launch: dW1 tiles gather X into A and load dH as B, dW2 tiles load s*A
     // as A and gather dO into B (one wave quantisation instead of two)
-    if ((rc = make_tmap_bf16(&tm.b, dH, 2 * (uint64_t)n, p_cap, 64)) != MOE_OK) return rc;
-    if ((rc = make_tmap_bf16(&tm.a, sA, n, p_cap, 64)) != MOE_OK) return rc;
+    if ((rc = make_tmap_bf16_chunks(&tm.b, dH, 2 * (uint64_t)n, p_cap, 64, 4)) != MOE_OK) return rc;
+    if ((rc = make_tmap_bf16_chunks(&tm.a, sA, n, p_cap, 64, 4)) != MOE_OK) return rc;
     aw.out0 = dW1;
     aw.out1 = dW2;
     aw.gsrc = X;
@@ -551,7 +579,7 @@ int moe_backward_ex(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, c
     return side.join();
   }
   // dW1_e = X[tok]^T dH_e (M = d, N = 2n, K = rows of e); X rows gathered with cp.async
-  if ((rc = make_tmap_bf16(&tm.b, dH, 2 * (uint64_t)n, p_cap, 64)) != MOE_OK) return rc;
+  if ((rc = make_tmap_bf16_chunks(&tm.b, dH, 2 * (uint64_t)n, p_cap, 64, 4)) != MOE_OK) return rc;  // BN = 256
   tm.a = tm.b;
   aw.Mdim = d;
   aw.Ndim = 2 * n;
@@ -562,7 +590,9 @@ int moe_backward_ex(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, c
   if ((rc = make_tmap_bf16_epi(&tm.dh, dW1, 2 * (uint64_t)n, (uint64_t)E * d)) != MOE_OK) return rc;
   if ((rc = launch_dw1(aw, tm, s)) != MOE_OK) return rc;
   // dW2_e = (s*A)_e^T dO[tok] (M = n, N = d, K = rows of e); dO rows gathered with cp.async
-  if ((rc = make_tmap_bf16(&tm.a, sA, n, p_cap, 64)) != MOE_OK) return rc;
+  // the s*A tile spans the M block: 256 columns (four chunks) in 256-row blocks, else 128 (two)
+  const uint32_t sa_chunks = (aw.wide_m && n % 256 == 0) ? 4 : 2;
+  if ((rc = make_tmap_bf16_chunks(&tm.a, sA, n, p_cap, 64, sa_chunks)) != MOE_OK) return rc;
   tm.b = tm.a;
   aw.Mdim = n;
   aw.Ndim = d;

@@ -417,38 +417,29 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
           const uint32_t a_dst = sA + s * SM::kABytesMB;
           const uint32_t b_dst = sB + s * SM::kBBytes;
           const uint32_t fb = full_bar(s);
+          // one request per operand: the tensor maps' boxes span the whole stage tile
           if (MODE == kUp) {
-            // W1_e rows [kb*64, +64): gate columns [n0/2, +128) and up columns [n + n0/2, +128)
-            const int hcol = t.n0 / 2;
+            // W1_e rows [kb*64, +64): gate columns [n0/2, +128) and up columns [n + n0/2, +128), as the
+            // chunks (gate 0, gate 1, up 0, up 1) of a {64, 64, 2, 2} box
             const int wrow = t.e * a.d + kb * kBK;
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              tma_load_2d(b_dst + c * 8192, &tmB, (c < 2 ? 0 : a.n) + hcol + (c & 1) * 64, wrow, fb, pol_w);
+            tma_load_4d(b_dst, &tmB, 0, wrow, t.n0 / 128, 0, fb, pol_w);
           } else if (MODE == kDH) {
-            // K-major W2_e: N index = rows n0..n0+BN of W2_e (two halves), K-elements [kb*64, +64)
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-              tma_load_2d(b_dst + h * (BN / 2) * 128, &tmB, kb * kBK, t.e * a.n + t.n0 + h * (BN / 2), fb, pol_w);
+            // K-major W2_e: N index = rows n0..n0+BN of W2_e (a {64, BN} box), K-elements [kb*64, +64)
+            tma_load_2d(b_dst, &tmB, kb * kBK, t.e * a.n + t.n0, fb, pol_w);
           } else if (MODE == kDown || MODE == kDownH) {
             if (MODE == kDown) tma_load_2d(a_dst, &tmA, kb * kBK, t.row0, fb, pol_x);
-#pragma unroll
-            for (int c = 0; c < BN / 64; ++c)
-              tma_load_2d(b_dst + c * 8192, &tmB, t.n0 + c * 64, t.e * a.n + kb * kBK, fb, pol_w);
+            // W2_e rows [kb*64, +64), columns [n0, +BN) as BN/64 chunks of a {64, 64, BN/64} box
+            tma_load_3d(b_dst, &tmB, 0, t.e * a.n + kb * kBK, t.n0 / 64, fb, pol_w);
           } else if (MODE == kDX) {
             tma_load_2d(a_dst, &tmA, kb * kBK, t.row0, fb, pol_x);
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-              tma_load_2d(b_dst + h * (BN / 2) * 128, &tmB, kb * kBK, t.e * a.d + t.n0 + h * (BN / 2), fb, pol_w);
+            tma_load_2d(b_dst, &tmB, kb * kBK, t.e * a.d + t.n0, fb, pol_w);  // a {64, 256} box of W1_e rows
           } else if (MODE == kDW1 || (MODE == kDW && !t.w2)) {
-            // B = dH rows [rb, rb+64) (MN-major); rows past the expert meet zero A rows
-#pragma unroll
-            for (int c = 0; c < BN / 64; ++c)
-              tma_load_2d(b_dst + c * 8192, &tmB, t.n0 + c * 64, t.row0 + kb * kBK, fb, pol_w);
+            // B = dH rows [rb, rb+64) (MN-major), columns [n0, +BN); rows past the expert meet zero A rows
+            tma_load_3d(b_dst, &tmB, 0, t.row0 + kb * kBK, t.n0 / 64, fb, pol_w);
           } else {
-            // kDW2: A = (s*A) rows [rb, rb+64) (MN-major); rows past the expert meet zero B rows
-#pragma unroll
-            for (int c = 0; c < MB * kBM / 64; ++c)
-              tma_load_2d(a_dst + c * 8192, &tmA, t.m0 + c * 64, t.row0 + kb * kBK, fb, pol_w);
+            // kDW2: A = (s*A) rows [rb, rb+64) (MN-major), columns [m0, +MB*128); rows past the expert meet
+            // zero B rows
+            tma_load_3d(a_dst, &tmA, 0, t.row0 + kb * kBK, t.m0 / 64, fb, pol_w);
           }
           ++issued;
           if (++s == STAGES) {

@@ -115,6 +115,14 @@ struct TensorMaps {
 int make_tmap_bf16(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t rows, uint32_t box_rows);
 // Same with a {32, 32} box and 64-byte swizzle (the dH epilogue's per-warp tiles).
 int make_tmap_bf16_epi(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t rows);
+// 3D view (64 columns, rows, inner / 64 column chunks) of a row-major bf16 [rows, inner] matrix (inner a multiple of
+// 64) with a {64, box_rows, chunks} box: one load lands `chunks` consecutive 128-byte-swizzled [box_rows x 64]
+// tiles, column chunk c at c * box_rows * 128 bytes.
+int make_tmap_bf16_chunks(CUtensorMap *tm, const void *base, uint64_t inner, uint64_t rows, uint32_t box_rows,
+                          uint32_t chunks);
+// 4D view of W1 [rows, 2n] as (64 columns, rows, n / 64 chunks of one half, the gate and up halves) with a
+// {64, 64, 2, 2} box: the two 64-column chunks of the gate half and the same two of the up half in one load.
+int make_tmap_bf16_halves(CUtensorMap *tm, const void *base, uint64_t n, uint64_t rows);
 
 int num_sms();
 // MOE_OK when the current device is compute capability 10.3 (the only target of this library), else
