@@ -440,7 +440,9 @@ int moe_forward_ex(const moe_bf16 *X, const moe_bf16 *W1, const moe_bf16 *W2, co
   // recomputed from H inside the kernel
   if (a_from_h) tm.a = tm.b;  // unused
   else if ((rc = make_tmap_bf16(&tm.a, A, n, p_cap, 128)) != MOE_OK) return rc;
-  if ((rc = make_tmap_bf16_chunks(&tm.b, W2, d, (uint64_t)E * n, 64, 4)) != MOE_OK) return rc;  // 256 columns
+  // W2_e tiles: a CTA of a pair loads half of the 256 columns, a lone CTA all of them
+  const bool down_pairs = !a_from_h && use_cta_pairs(n);
+  if ((rc = make_tmap_bf16_chunks(&tm.b, W2, d, (uint64_t)E * n, 64, down_pairs ? 2 : 4)) != MOE_OK) return rc;
   a.Ndim = d;
   a.Kdim = n;
   a.out0 = nullptr;
@@ -544,7 +546,9 @@ int moe_backward_ex(const moe_bf16 *dO, const moe_bf16 *X, const moe_bf16 *W1, c
   if (det && (rc = launch_ds_sum(dS_part, n / bn, r->offsets, E, dS, s)) != MOE_OK) return rc;
   // dX~: dX32[tok] += dH W1_e^T (N = d, K = 2n)
   if ((rc = make_tmap_bf16(&tm.a, dH, 2 * (uint64_t)n, p_cap, 128)) != MOE_OK) return rc;
-  if ((rc = make_tmap_bf16(&tm.b, W1, 2 * (uint64_t)n, (uint64_t)E * d, 256)) != MOE_OK) return rc;  // 256 rows of W1_e
+  // W1_e rows: half of the 256-row tile per CTA of a pair, all of it for a lone CTA
+  const uint32_t dx_rows = use_cta_pairs(2 * n) ? 128 : 256;
+  if ((rc = make_tmap_bf16(&tm.b, W1, 2 * (uint64_t)n, (uint64_t)E * d, dx_rows)) != MOE_OK) return rc;
   GemmArgs ax = base_args(r, T, d, n, E, p_cap);
   ax.Ndim = d;
   ax.Kdim = 2 * n;

@@ -59,6 +59,9 @@ struct Traits {
   static constexpr bool a_mn = varlen_k;  // A operand MN-major in shared memory
   static constexpr bool b_mn = (MODE == kUp || MODE == kDown || MODE == kDownH || varlen_k);
   static constexpr bool nt_outer = nt_outer_;  // keep one fp32 column slab hot in L2
+  // the scatter-add GEMMs with TMA-loaded operands may run on CTA pairs (M = 256 across two SMs, each holding its
+  // 128 rows of A and half of B's columns): a third fewer operand bytes per FLOP on each SM
+  static constexpr bool pairable = (MODE == kDown || MODE == kDX);
 };
 
 constexpr int kGatherThreads = 128;
@@ -77,15 +80,16 @@ constexpr int kDhWarpBytes = 4096 + 4096;
 // MB = 128-row M blocks per CTA.  The weight-gradient GEMMs (long K loop, light epilogue) use MB = 2: two
 // M=128 MMAs per k-step share the B tile, halving shared-memory bytes per FLOP so the same shared memory
 // covers twice the load latency; both accumulators fill TMEM (512 columns), so there is one buffer.
-template <int BN, int STAGES, int EPI_BYTES, int MB = 1, int CACHE_BYTES = 0>
+template <int BN, int STAGES, int EPI_BYTES, int MB = 1, int CACHE_BYTES = 0, int CG = 1>
 struct Smem {
   static constexpr int kABytesMB = MB * kABytes;
-  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kBBytes = (BN / CG) * kBK * 2;  // a CTA pair holds half of B in each CTA
   static constexpr int kStageBytes = kABytesMB + kBBytes;
   static constexpr int kStgOff = STAGES * kStageBytes;
   static constexpr int kBarOff = kStgOff + EPI_BYTES;
-  static constexpr int kCacheOff = kBarOff + 256;                // barriers/flags, then the tile cache
-  static constexpr int kBytes = kCacheOff + CACHE_BYTES + 1024;  // + alignment slack
+  static constexpr int kCacheOff = kBarOff + 256;  // barriers/flags, then the tile cache
+  static constexpr int kPairOff = kCacheOff + CACHE_BYTES;  // CTA pairs: per-expert prefix of 256-row pair tiles
+  static constexpr int kBytes = kPairOff + (CG == 2 ? 4 * (kMaxExperts + 1 + 32) : 0) + 1024;  // + alignment slack
 };
 
 // Up-projection epilogue, per warp: one 6 KB staging tile (H gate | H up | A, 32 rows x 32 columns each,
@@ -153,8 +157,10 @@ __device__ __forceinline__ int total_pairs(const GemmArgs &a, int total_m) {
   return ((total_m + 1) / 2) * n_tiles;                           // pairs of consecutive m-tiles
 }
 
+// poff: CTA pairs only, the per-expert prefix of 256-row pair tiles (shared memory), else null.
 template <int MODE, int BN, int MB>
-__device__ __forceinline__ Tile decode_tile(const GemmArgs &a, int pair, int rank, int total_m) {
+__device__ __forceinline__ Tile decode_tile(const GemmArgs &a, int pair, int rank, int total_m,
+                                            const int32_t *poff = nullptr) {
   Tile t;
   const int n_tiles = a.Ndim / BN;
   t.w2 = false;
@@ -204,6 +210,35 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &a, int pair, int ran
       t.row_end = t.row0 = 0;
     }
     t.kblocks = (t.row_end - t.row0 + kBK - 1) / kBK;
+  } else if (Traits<MODE>::pairable && poff != nullptr) {
+    // CTA pairs: a work item is (256-row pair tile of one expert, column tile), passes of nt_group column tiles
+    // as below.  CTA `rank` takes m-tile 2*lp + rank of the expert's pair tile lp; when the expert has an odd
+    // number of m-tiles the last pair's second m-tile lies past its rows: that CTA loads whatever is there (zeros
+    // past P_cap) for the pair's MMA and writes nothing.
+    const int total_pt = poff[a.E];
+    const int per_pass = total_pt * a.nt_group;
+    const int g = pair / per_pass;
+    const int rem = pair - g * per_pass;
+    const int mp = rem / a.nt_group;
+    const int nt = g * a.nt_group + (rem - mp * a.nt_group);
+    int lo = 0, hi = a.E;  // largest e with poff[e] <= mp
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (poff[mid] <= mp) lo = mid;
+      else hi = mid;
+    }
+    t.e = lo;
+    const int mt_local = 2 * (mp - poff[lo]) + rank;
+    const int mt_e = __ldg(&a.tile_offsets[lo + 1]) - __ldg(&a.tile_offsets[lo]);
+    t.m0 = 0;
+    t.n0 = a.n_off + nt * BN;
+    t.row0 = __ldg(&a.offsets[lo]) + mt_local * kBM;
+    t.row_end = __ldg(&a.offsets[lo + 1]);
+    t.kblocks = a.Kdim / kBK;
+    if (mt_local < mt_e && (t.row0 < 0 || t.row_end > a.p_cap || t.row0 >= t.row_end)) {
+      set_status(a.status, MOE_ERR_BAD_METADATA);
+      t.row_end = t.row0;  // nothing is written
+    }
   } else {
     const int n_pairs_m = (total_m + 1) / 2;
     int mp, nt;
@@ -264,8 +299,8 @@ __device__ __forceinline__ TileRec pack_tile(const Tile &t) {
 // Tile i of this CTA (pair = first_pair + i * pair_step): from the cache when it holds it.
 template <int MODE, int BN, int MB>
 __device__ __forceinline__ Tile tile_at(const GemmArgs &a, const TileRec *cache, bool cached, int i, int pair,
-                                        int rank, int total_m) {
-  if (!cached || i >= kTileCache) return decode_tile<MODE, BN, MB>(a, pair, rank, total_m);
+                                        int rank, int total_m, const int32_t *poff) {
+  if (!cached || i >= kTileCache) return decode_tile<MODE, BN, MB>(a, pair, rank, total_m, poff);
   const TileRec r = cache[i];
   Tile t;
   t.e = static_cast<int>(r.code & 0x7ffu);
@@ -299,14 +334,16 @@ __device__ __forceinline__ long long to_fixed(float x, bool &range_ok) {
   return __float2ll_rn(x * kFixScale);
 }
 
-template <int MODE, int BN, int STAGES, int MB, bool DET>
+// CG: CTAs per MMA (2: this CTA and its cluster peer; see the CTA-pair helpers in common.cuh).
+template <int MODE, int BN, int STAGES, int MB, bool DET, int CG>
 __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
     moe_gemm_kernel(const __grid_constant__ TensorMaps tm, const GemmArgs a) {
   const CUtensorMap &tmA = tm.a;
   const CUtensorMap &tmB = tm.b;
   using TR = Traits<MODE>;
-  using SM = Smem<BN, STAGES, epi_bytes<MODE, MB>(), MB, tile_cache_bytes<MODE>()>;
+  using SM = Smem<BN, STAGES, epi_bytes<MODE, MB>(), MB, tile_cache_bytes<MODE>(), CG>;
   static_assert(MODE != kDW || MB == 2, "merged weight gradients: 256-row blocks");
+  static_assert(CG == 1 || (CG == 2 && Traits<MODE>::pairable && MB == 1), "CTA pairs: the TMA-fed scatter-add GEMMs");
   constexpr int kEpiWarps = epi_warps<MODE, MB>();
   static_assert(cta_threads<MODE, MB>() <= 448, "one CTA per SM at up to 146 registers a thread");
   // TMEM accumulator buffers: two (one tile's epilogue overlaps the next tile's MMAs) whenever two fit in the
@@ -341,7 +378,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), kEpiWarps);
+      mbar_init(tempty_bar(b), CG * kEpiWarps);  // a pair's leader counts both CTAs' epilogue warps
     }
     mbar_init(drain_bar, 1);
     if (MODE == kDH)
@@ -360,11 +397,17 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
-    tmem_relinquish();
+    if (CG == 2) {  // collective over the pair: the same columns in both CTAs
+      tmem_alloc_pair(smem_u32(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();  // barriers initialised and the TMEM address published before any role starts
+  if (CG == 2) cluster_sync();  // the peer's barriers too: its loads and arrivals may target the leader's
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // everything above overlaps the previous kernel's tail; its outputs are read only after this wait
@@ -375,13 +418,53 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
   const int first_pair = static_cast<int>(blockIdx.x >> 1);
   const int pair_step = static_cast<int>(gridDim.x >> 1);  // the grid is even
   const int total_m = TR::varlen_k ? 0 : __ldg(&a.tile_offsets[a.E]);
-  const int total = total_pairs<MODE, BN, MB>(a, total_m);
+  const int32_t *poff = nullptr;
+  if (CG == 2) {
+    // per-expert prefix of 256-row pair tiles, ceil(m-tiles / 2) per expert: each thread scans a run of experts,
+    // then the runs are offset by a block-wide exclusive scan of their sums
+    int32_t *ps = reinterpret_cast<int32_t *>(gbase + SM::kPairOff);
+    int32_t *wsum = ps + kMaxExperts + 1;  // one total per warp
+    const int per = (a.E + static_cast<int>(blockDim.x) - 1) / static_cast<int>(blockDim.x);
+    const int e0 = min(a.E, static_cast<int>(threadIdx.x) * per), e1 = min(a.E, e0 + per);
+    auto pairs_of = [&](int e) { return (__ldg(&a.tile_offsets[e + 1]) - __ldg(&a.tile_offsets[e]) + 1) >> 1; };
+    int sum = 0;
+    for (int e = e0; e < e1; ++e) sum += pairs_of(e);
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int nw = static_cast<int>(blockDim.x) >> 5;
+      const int v = lane < nw ? wsum[lane] : 0;
+      int inc2 = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, inc2, o);
+        if (lane >= o) inc2 += u;
+      }
+      if (lane < nw) wsum[lane] = inc2 - v;
+    }
+    __syncthreads();
+    int run = wsum[warp] + incl - sum;
+    for (int e = e0; e < e1; ++e) {
+      ps[e] = run;
+      run += pairs_of(e);
+    }
+    if (e0 < e1 && e1 == a.E) ps[a.E] = run;
+    __syncthreads();
+    poff = ps;
+  }
+  const int total = CG == 2 ? poff[a.E] * (a.Ndim / BN) : total_pairs<MODE, BN, MB>(a, total_m);
   TileRec *tile_cache = reinterpret_cast<TileRec *>(gbase + SM::kCacheOff);
   const bool cached = tiles_cacheable<BN>(a);
   if (cached) {
     const int mine = first_pair < total ? (total - first_pair + pair_step - 1) / pair_step : 0;
     for (int i = threadIdx.x; i < min(mine, kTileCache); i += blockDim.x)
-      tile_cache[i] = pack_tile<BN, MB>(decode_tile<MODE, BN, MB>(a, first_pair + i * pair_step, rank, total_m));
+      tile_cache[i] = pack_tile<BN, MB>(decode_tile<MODE, BN, MB>(a, first_pair + i * pair_step, rank, total_m, poff));
   }
   __syncthreads();
 
@@ -404,7 +487,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
     bool aborted = false;
     if (lane == 0) {
       for (int pair = first_pair, ti = 0; pair < total && !aborted; pair += pair_step, ++ti) {
-        const Tile t = tile_at<MODE, BN, MB>(a, tile_cache, cached, ti, pair, rank, total_m);
+        const Tile t = tile_at<MODE, BN, MB>(a, tile_cache, cached, ti, pair, rank, total_m, poff);
         for (int kb = 0; kb < t.kblocks; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u) || *abort_flag) {
             set_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
@@ -412,8 +495,11 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
             aborted = true;
             break;
           }
-          // merged weight gradients: a dW2 tile loads its A (s*A, 256 rows) by TMA, a dW1 tile its B (dH)
-          mbar_arrive_expect_tx(full_bar(s), (MODE == kDW && t.w2) ? static_cast<uint32_t>(SM::kABytesMB) : kTmaBytes);
+          // merged weight gradients: a dW2 tile loads its A (s*A, 256 rows) by TMA, a dW1 tile its B (dH).
+          // CTA pairs: both CTAs' loads complete on the leader's barrier, which expects both
+          if (CG == 1 || rank == 0)
+            mbar_arrive_expect_tx(full_bar(s),
+                                  (MODE == kDW && t.w2) ? static_cast<uint32_t>(SM::kABytesMB) : CG * kTmaBytes);
           const uint32_t a_dst = sA + s * SM::kABytesMB;
           const uint32_t b_dst = sB + s * SM::kBBytes;
           const uint32_t fb = full_bar(s);
@@ -426,6 +512,14 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
           } else if (MODE == kDH) {
             // K-major W2_e: N index = rows n0..n0+BN of W2_e (a {64, BN} box), K-elements [kb*64, +64)
             tma_load_2d(b_dst, &tmB, kb * kBK, t.e * a.n + t.n0, fb, pol_w);
+          } else if (CG == 2) {
+            // this CTA's 128 rows of A and its half of the BN columns of B
+            const uint32_t lead = mapa_shared(fb, 0);
+            tma_load_2d_pair(a_dst, &tmA, kb * kBK, t.row0, lead, pol_x);
+            if (MODE == kDown)  // W2_e rows [kb*64, +64), columns [n0 + rank*BN/2, +BN/2): BN/128 chunks
+              tma_load_3d_pair(b_dst, &tmB, 0, t.e * a.n + kb * kBK, t.n0 / 64 + rank * (BN / 128), lead, pol_w);
+            else  // a {64, BN/2} box of W1_e rows
+              tma_load_2d_pair(b_dst, &tmB, kb * kBK, t.e * a.d + t.n0 + rank * (BN / 2), lead, pol_w);
           } else if (MODE == kDown || MODE == kDownH) {
             if (MODE == kDown) tma_load_2d(a_dst, &tmA, kb * kBK, t.row0, fb, pol_x);
             // W2_e rows [kb*64, +64), columns [n0, +BN) as BN/64 chunks of a {64, 64, BN/64} box
@@ -448,8 +542,17 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
           }
         }
       }
-      if (aborted) {
-        // let every copy this CTA issued land before the CTA's shared memory is released
+      if (CG == 2 && !aborted) {
+        // the leader's last releases of this CTA's stages are arrivals from another SM: they land before the
+        // CTA may exit
+        for (int st = 0; st < STAGES && st < issued; ++st) {
+          const int last = st + ((issued - 1 - st) / STAGES) * STAGES;
+          mbar_wait(empty_bar(st), static_cast<uint32_t>((last / STAGES) & 1));
+        }
+      }
+      if (aborted && (CG == 1 || rank == 0)) {
+        // let every copy this CTA issued land before the CTA's shared memory is released (a pair's copies land
+        // on the leader's barriers: the leader drains both, and the pair's closing cluster barrier holds the peer)
         for (int st = 0; st < STAGES && st < issued; ++st) {
           const int last = st + ((issued - 1 - st) / STAGES) * STAGES;
           mbar_wait(full_bar(st), static_cast<uint32_t>((last / STAGES) & 1));
@@ -478,11 +581,11 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
     };
     Tile t_next;
     if (TR::gather_a_k && first_pair < total) {
-      t_next = tile_at<MODE, BN, MB>(a, tile_cache, cached, 0, first_pair, rank, total_m);
+      t_next = tile_at<MODE, BN, MB>(a, tile_cache, cached, 0, first_pair, rank, total_m, poff);
       fetch_tokens(t_next);
     }
     for (int pair = first_pair, ti = 0; pair < total && !aborted; pair += pair_step, ++ti) {
-      const Tile t = TR::gather_a_k ? t_next : tile_at<MODE, BN, MB>(a, tile_cache, cached, ti, pair, rank, total_m);
+      const Tile t = TR::gather_a_k ? t_next : tile_at<MODE, BN, MB>(a, tile_cache, cached, ti, pair, rank, total_m, poff);
       if (t.kblocks == 0) continue;
       const uint8_t *rowp[8];
       uint32_t rown[8];
@@ -495,7 +598,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
           rowp[q] = src_a + (tok < a.T ? tok : 0) * ld_bytes + j * 16;
         }
         if (pair + pair_step < total) {
-          t_next = tile_at<MODE, BN, MB>(a, tile_cache, cached, ti + 1, pair + pair_step, rank, total_m);
+          t_next = tile_at<MODE, BN, MB>(a, tile_cache, cached, ti + 1, pair + pair_step, rank, total_m, poff);
           fetch_tokens(t_next);
         }
       }
@@ -582,7 +685,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
       }
     };
     for (int pair = first_pair, ti = 0; pair < total && !aborted; pair += pair_step, ++ti) {
-      const Tile t = tile_at<MODE, BN, MB>(a, tile_cache, cached, ti, pair, rank, total_m);
+      const Tile t = tile_at<MODE, BN, MB>(a, tile_cache, cached, ti, pair, rank, total_m, poff);
       if (t.kblocks == 0) continue;
       for (int kb = 0; kb < t.kblocks; ++kb) {
         uint4 g[8], u[8];
@@ -630,15 +733,16 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, TR::a_mn, TR::b_mn);
+    // (CTA pairs: the leader issues the pair's M = 256 MMAs and commits to both CTAs' barriers)
+    if (lane == 0 && (CG == 1 || rank == 0)) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM * CG, BN, TR::a_mn, TR::b_mn);
       int s = 0;
       uint32_t ph = 0;
       int buf = 0;
       uint32_t bph = 0;
       bool aborted = false;
       for (int pair = first_pair, ti = 0; pair < total && !aborted; pair += pair_step, ++ti) {
-        const Tile t = tile_at<MODE, BN, MB>(a, tile_cache, cached, ti, pair, rank, total_m);
+        const Tile t = tile_at<MODE, BN, MB>(a, tile_cache, cached, ti, pair, rank, total_m, poff);
         if (t.kblocks == 0) continue;
         if (!mbar_wait(tempty_bar(buf), bph ^ 1u) || *abort_flag) {
           aborted = true;
@@ -664,17 +768,29 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
               const uint32_t a_blk = a_st + mb * kABytes;
               const uint64_t ad = TR::a_mn ? smem_desc_sw128(a_blk + k * 2048, 8192, 1024)
                                            : smem_desc_sw128(a_blk + k * 32, 16, 1024);
-              umma_bf16(d_tmem + mb * BN, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+              if (CG == 2) umma_bf16_pair(d_tmem + mb * BN, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+              else umma_bf16(d_tmem + mb * BN, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
             }
           }
-          umma_commit(empty_bar(s));  // the stage is free once these MMAs have read it
+          // the stage is free once these MMAs have read it
+          if (CG == 2) {
+            umma_commit_pair(empty_bar(s));
+            umma_commit_pair(mapa_shared(empty_bar(s), 1));
+          } else {
+            umma_commit(empty_bar(s));
+          }
           if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
           }
         }
         if (aborted) break;
-        umma_commit(tfull_bar(buf));
+        if (CG == 2) {
+          umma_commit_pair(tfull_bar(buf));
+          umma_commit_pair(mapa_shared(tfull_bar(buf), 1));
+        } else {
+          umma_commit(tfull_bar(buf));
+        }
         if (++buf == kBufs) {
           buf = 0;
           bph ^= 1u;
@@ -699,7 +815,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
     const uint64_t pol_acc = policy_evict_last();  // keep the fp32 accumulator slab in L2
     const uint64_t pol_stream = policy_evict_first();  // streamed epilogue traffic (H, A, dH, s*A) is touched once here
     for (int pair = first_pair, ti = 0; pair < total; pair += pair_step, ++ti) {
-      const Tile t = tile_at<MODE, BN, MB>(a, tile_cache, cached, ti, pair, rank, total_m);
+      const Tile t = tile_at<MODE, BN, MB>(a, tile_cache, cached, ti, pair, rank, total_m, poff);
       // weight gradients: the output of this tile and its row length
       const int dw_m = MODE == kDW ? (t.w2 ? a.n : a.d) : a.Mdim;
       const int dw_n = MODE == kDW ? (t.w2 ? a.d : 2 * a.n) : a.Ndim;
@@ -827,7 +943,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
             if (tok >= 0) bulk_reduce_add_u64(grow + c * 32, stg, 256, pol_acc);
             bulk_commit();
           }
-          if (!range_ok) set_status(a.status, MOE_ERR_RANGE);
+          if (!range_ok && tok >= 0) set_status(a.status, MOE_ERR_RANGE);  // rows that are written
         } else {
           float *grow = a.out_f32 + (size_t)(tok >= 0 ? tok : 0) * a.d + t.n0 + half * (BN / 2);
 #pragma unroll 1
@@ -1028,7 +1144,10 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(buf));
+      if (lane == 0) {
+        if (CG == 2 && rank != 0) mbar_arrive_remote(mapa_shared(tempty_bar(buf), 0));  // the leader's MMAs wait
+        else mbar_arrive(tempty_bar(buf));
+      }
       if (++buf == kBufs) {
         buf = 0;
         bph ^= 1u;
@@ -1038,47 +1157,67 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
   }
 
   __syncthreads();
+  if (warp == 1 && *abort_flag && lane == 0 && (CG == 1 || rank == 0)) {
+    if (CG == 2) umma_commit_pair(drain_bar);
+    else umma_commit(drain_bar);  // all MMAs this CTA issued are complete once this arrives
+    mbar_wait(drain_bar, 0);
+  }
+  if (CG == 2) {  // neither CTA frees its TMEM (or exits) while the leader's MMAs may still write the peer's
+    tc_fence_before();
+    cluster_sync();
+  }
   if (warp == 1) {
-    if (*abort_flag && lane == 0) {
-      umma_commit(drain_bar);  // all MMAs this CTA issued are complete once this arrives
-      mbar_wait(drain_bar, 0);
-    }
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if (CG == 2) tmem_dealloc_pair(tmem_base, kTmemCols);
+    else tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
 // Host launcher for one instantiation: one CTA per SM, an even number of CTAs (CTA 2i + rank takes tile
 // `rank` of each of its pairs).  The shared-memory attribute and the grid size are set up once per device.
-template <int MODE, int BN, int STAGES, int MB = 1, bool DET = false>
+template <int MODE, int BN, int STAGES, int MB = 1, bool DET = false, int CG = 1>
 int launch_gemm(const GemmArgs &a, const TensorMaps &tm, cudaStream_t stream) {
-  using SM = Smem<BN, STAGES, epi_bytes<MODE, MB>(), MB, tile_cache_bytes<MODE>()>;
-  auto kernel = moe_gemm_kernel<MODE, BN, STAGES, MB, DET>;
+  using SM = Smem<BN, STAGES, epi_bytes<MODE, MB>(), MB, tile_cache_bytes<MODE>(), CG>;
+  auto kernel = moe_gemm_kernel<MODE, BN, STAGES, MB, DET, CG>;
   static DeviceCache grid_cache;
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return record_cuda_error(err);
   if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_DEVICE;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;  // CTA pairs: clusters of two
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(cta_threads<MODE, MB>(), 1, 1);
+  cfg.dynamicSmemBytes = SM::kBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = CG == 2 ? 2 : 1;
   const int grid = grid_cache.get(dev, [&]() -> int {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
     if (e != cudaSuccess) return -static_cast<int>(e);
+    if (CG == 2) {
+      // persistent: exactly the pairs that can be resident at once (an SM left over in a GPC takes no pair)
+      int clusters = 0;
+      cudaLaunchConfig_t q = cfg;
+      q.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+      e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &q);
+      if (e != cudaSuccess) return -static_cast<int>(e);
+      if (clusters <= 0) return -static_cast<int>(cudaErrorInvalidConfiguration);
+      return 2 * clusters;
+    }
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, cta_threads<MODE, MB>(), SM::kBytes);
     if (e != cudaSuccess || per_sm <= 0) per_sm = 1;
     return 2 * ((num_sms() * per_sm) / 2);
   });
   if (grid <= 0) return record_cuda_error(static_cast<cudaError_t>(-grid));
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(cta_threads<MODE, MB>(), 1, 1);
-  cfg.dynamicSmemBytes = SM::kBytes;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   static const char *const kNames[] = {"gemm_up",  "gemm_down", "gemm_dh", "gemm_dx",
                                        "gemm_dw1", "gemm_dw2",  "gemm_dw", "gemm_down_h"};
   prof_begin(kNames[MODE], stream);

@@ -14,6 +14,10 @@ int launch_dh(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, int bn, b
 }
 
 int launch_dx(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, bool det) {
+  if (use_cta_pairs(a.Kdim)) {
+    if (det) return launch_gemm<kDX, 256, 4, 1, true, 2>(a, tm, s);
+    return launch_gemm<kDX, 256, 4, 1, false, 2>(a, tm, s);
+  }
   if (det) return launch_gemm<kDX, 256, 3, 1, true>(a, tm, s);
   return launch_gemm<kDX, 256, 3>(a, tm, s);
 }

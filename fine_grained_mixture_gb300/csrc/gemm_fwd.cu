@@ -8,6 +8,10 @@ namespace moe {
 int launch_up(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s) { return launch_gemm<kUp, 256, 4>(a, tm, s); }
 
 int launch_down(const GemmArgs &a, const TensorMaps &tm, cudaStream_t s, bool det) {
+  if (use_cta_pairs(a.Kdim)) {
+    if (det) return launch_gemm<kDown, 256, 4, 1, true, 2>(a, tm, s);
+    return launch_gemm<kDown, 256, 4, 1, false, 2>(a, tm, s);
+  }
   if (det) return launch_gemm<kDown, 256, 3, 1, true>(a, tm, s);
   return launch_gemm<kDown, 256, 3>(a, tm, s);
 }

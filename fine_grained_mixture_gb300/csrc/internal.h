@@ -124,6 +124,12 @@ int make_tmap_bf16_chunks(CUtensorMap *tm, const void *base, uint64_t inner, uin
 // {64, 64, 2, 2} box: the two 64-column chunks of the gate half and the same two of the up half in one load.
 int make_tmap_bf16_halves(CUtensorMap *tm, const void *base, uint64_t n, uint64_t rows);
 
+// The scatter-add GEMMs (down-projection, dX~) run on CTA pairs when their K loop is at least this long: measured
+// at K = 768 and above (coarse, skew layers: the step 4-7% faster); at K = 256 and 512 (fine7b, sparse) the pair's
+// coupled epilogues and its half-empty last tiles cost more than the operand traffic saved (step 2% slower).
+constexpr int kPairMinK = 768;
+inline bool use_cta_pairs(int Kdim) { return Kdim >= kPairMinK; }
+
 int num_sms();
 // MOE_OK when the current device is compute capability 10.3 (the only target of this library), else
 // MOE_ERR_DEVICE, or MOE_ERR_CUDA when no device can be made current.

@@ -24,7 +24,8 @@ def _run(g, K, mode, det=True, W2=None):
 
 
 @pytest.mark.parametrize("T,d,n,E,K,mode", [(512, 256, 128, 8, 2, "tc"), (512, 256, 128, 8, 2, "tr"),
-                                            (1000, 512, 512, 16, 4, "tc"), (300, 256, 384, 5, 2, "ec")])
+                                            (1000, 512, 512, 16, 4, "tc"), (300, 256, 384, 5, 2, "ec"),
+                                            (400, 256, 768, 5, 2, "tc")])   # CTA-pair down-projection and dX~
 def test_deterministic_matches_oracle(T, d, n, E, K, mode):
     w = synth.custom(T, d, n, E, K)
     inp = synth.make_inputs(w, 2)

@@ -118,6 +118,11 @@ def test_layer_tiny_full(mode):
     (1000, 512, 256, 16, 4, True, "ec"),     # expert choice: equal counts whatever the skew
     (300, 256, 128, 5, 2, False, "tr_stoch"),
     (100, 256, 128, 64, 1, False, "ec"),     # T K < E: C = 1 row per expert
+    # K loops of 768 and more run the scatter-add GEMMs on CTA pairs: experts with odd m-tile counts (a pair's
+    # second m-tile past the expert), empty experts, ragged tails
+    (700, 256, 768, 6, 2, True, "tc"),
+    (300, 512, 1024, 3, 2, False, "tr"),
+    (513, 256, 768, 4, 3, False, "ec"),
 ])
 def test_layer_small_shapes(T, d, n, E, K, skew, mode):
     w = synth.custom(T, d, n, E, K, skew=skew)
