@@ -60,7 +60,8 @@ struct Traits {
   static constexpr bool b_mn = (MODE == kUp || MODE == kDown || MODE == kDownH || varlen_k);
   static constexpr bool nt_outer = nt_outer_;  // keep one fp32 column slab hot in L2
   // the scatter-add GEMMs with TMA-loaded operands may run on CTA pairs (M = 256 across two SMs, each holding its
-  // 128 rows of A and half of B's columns): a third fewer operand bytes per FLOP on each SM
+  // 128 rows of A and half of B's columns): a third fewer operand bytes per FLOP on each SM.  (The gather GEMMs
+  // would need the peer's gathered rows forwarded to the leader's barrier: measured 2x slower, not built.)
   static constexpr bool pairable = (MODE == kDown || MODE == kDX);
 };
 
@@ -215,8 +216,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs &a, int pair, int ran
     // as below.  CTA `rank` takes m-tile 2*lp + rank of the expert's pair tile lp; when the expert has an odd
     // number of m-tiles the last pair's second m-tile lies past its rows: that CTA loads whatever is there (zeros
     // past P_cap) for the pair's MMA and writes nothing.
-    const int total_pt = poff[a.E];
-    const int per_pass = total_pt * a.nt_group;
+    const int per_pass = poff[a.E] * a.nt_group;
     const int g = pair / per_pass;
     const int rem = pair - g * per_pass;
     const int mp = rem / a.nt_group;
@@ -504,15 +504,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
           const uint32_t b_dst = sB + s * SM::kBBytes;
           const uint32_t fb = full_bar(s);
           // one request per operand: the tensor maps' boxes span the whole stage tile
-          if (MODE == kUp) {
-            // W1_e rows [kb*64, +64): gate columns [n0/2, +128) and up columns [n + n0/2, +128), as the
-            // chunks (gate 0, gate 1, up 0, up 1) of a {64, 64, 2, 2} box
-            const int wrow = t.e * a.d + kb * kBK;
-            tma_load_4d(b_dst, &tmB, 0, wrow, t.n0 / 128, 0, fb, pol_w);
-          } else if (MODE == kDH) {
-            // K-major W2_e: N index = rows n0..n0+BN of W2_e (a {64, BN} box), K-elements [kb*64, +64)
-            tma_load_2d(b_dst, &tmB, kb * kBK, t.e * a.n + t.n0, fb, pol_w);
-          } else if (CG == 2) {
+          if (CG == 2) {
             // this CTA's 128 rows of A and its half of the BN columns of B
             const uint32_t lead = mapa_shared(fb, 0);
             tma_load_2d_pair(a_dst, &tmA, kb * kBK, t.row0, lead, pol_x);
@@ -520,6 +512,14 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
               tma_load_3d_pair(b_dst, &tmB, 0, t.e * a.n + kb * kBK, t.n0 / 64 + rank * (BN / 128), lead, pol_w);
             else  // a {64, BN/2} box of W1_e rows
               tma_load_2d_pair(b_dst, &tmB, kb * kBK, t.e * a.d + t.n0 + rank * (BN / 2), lead, pol_w);
+          } else if (MODE == kUp) {
+            // W1_e rows [kb*64, +64): gate columns [n0/2, +128) and up columns [n + n0/2, +128), as the
+            // chunks (gate 0, gate 1, up 0, up 1) of a {64, 64, 2, 2} box
+            const int wrow = t.e * a.d + kb * kBK;
+            tma_load_4d(b_dst, &tmB, 0, wrow, t.n0 / 128, 0, fb, pol_w);
+          } else if (MODE == kDH) {
+            // K-major W2_e: N index = rows n0..n0+BN of W2_e (a {64, BN} box), K-elements [kb*64, +64)
+            tma_load_2d(b_dst, &tmB, kb * kBK, t.e * a.n + t.n0, fb, pol_w);
           } else if (MODE == kDown || MODE == kDownH) {
             if (MODE == kDown) tma_load_2d(a_dst, &tmA, kb * kBK, t.row0, fb, pol_x);
             // W2_e rows [kb*64, +64), columns [n0, +BN) as BN/64 chunks of a {64, 64, BN/64} box
@@ -744,14 +744,16 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
       for (int pair = first_pair, ti = 0; pair < total && !aborted; pair += pair_step, ++ti) {
         const Tile t = tile_at<MODE, BN, MB>(a, tile_cache, cached, ti, pair, rank, total_m, poff);
         if (t.kblocks == 0) continue;
-        if (!mbar_wait(tempty_bar(buf), bph ^ 1u) || *abort_flag) {
+        // CTA pairs: both barriers also receive the peer's arrivals (cluster-scope acquire)
+        if (!(CG == 2 ? mbar_wait_cluster(tempty_bar(buf), bph ^ 1u) : mbar_wait(tempty_bar(buf), bph ^ 1u)) ||
+            *abort_flag) {
           aborted = true;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf) * kBufCols;
         for (int kb = 0; kb < t.kblocks; ++kb) {
-          if (!mbar_wait(full_bar(s), ph) || *abort_flag) {
+          if (!(CG == 2 ? mbar_wait_cluster(full_bar(s), ph) : mbar_wait(full_bar(s), ph)) || *abort_flag) {
             aborted = true;
             break;
           }
