@@ -831,6 +831,16 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
         }
         continue;
       }
+      // scatter-add GEMMs: the row's token and score are read before the accumulator wait (their latency
+      // overlaps it)
+      constexpr bool kScatter = (MODE == kDown || MODE == kDX || MODE == kDownH);
+      int tok = -1;
+      float sc = 1.f;
+      if (kScatter && t.row0 + row < t.row_end) {
+        tok = __ldg(&a.row_token[t.row0 + row]);
+        if (MODE != kDX) sc = __ldg(&a.row_score[t.row0 + row]);
+      }
+      bool released = false;  // TMEM handed back to the MMA issuer before the end of the tile
       int ok = 1;
       if (lane == 0) ok = mbar_wait(tfull_bar(buf), bph) && !*abort_flag;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -909,17 +919,10 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
           }
           __syncwarp();
         }
-      } else if (MODE == kDown || MODE == kDX || MODE == kDownH) {
-        const int r = t.row0 + row;
-        int tok = -1;
-        float sc = 1.f;
-        if (r < t.row_end) {
-          tok = __ldg(&a.row_token[r]);
-          if (tok < 0 || tok >= a.T) {
-            set_status(a.status, MOE_ERR_BAD_METADATA);
-            tok = -1;
-          }
-          if (MODE != kDX) sc = __ldg(&a.row_score[r]);
+      } else if (kScatter) {
+        if (t.row0 + row < t.row_end && (tok < 0 || tok >= a.T)) {
+          set_status(a.status, MOE_ERR_BAD_METADATA);
+          tok = -1;
         }
         // epilogue warp index 0..7: warps 2..9, or 2..5 and 10..13 beside the producer warps
         const int ew = (TR::producers && warp >= 10) ? warp - 6 : warp - 2;
@@ -948,25 +951,57 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
           if (!range_ok && tok >= 0) set_status(a.status, MOE_ERR_RANGE);  // rows that are written
         } else {
           float *grow = a.out_f32 + (size_t)(tok >= 0 ? tok : 0) * a.d + t.n0 + half * (BN / 2);
+          static_assert(!kScatter || BN == 256, "the scatter epilogue drains 128 columns per warp");
+          if (MODE == kDownH) {
+            // 448 threads leave no room for all 128 columns in registers: 64 columns per TMEM wait
 #pragma unroll 1
-          for (int c = 0; c < BN / 128; ++c) {
-            uint32_t v0[32], v1[32];
-            const uint32_t col = half * (BN / 2) + c * 64;
-            tmem_ld32(tacc + col, v0);
-            tmem_ld32(tacc + col + 32, v1);
+            for (int c = 0; c < 2; ++c) {
+              uint32_t v0[32], v1[32];
+              const uint32_t col = half * (BN / 2) + c * 64;
+              tmem_ld32(tacc + col, v0);
+              tmem_ld32(tacc + col + 32, v1);
+              tmem_ld_wait();
+              bulk_wait_read<0>();  // the previous bulk add has read the staging row
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                st_shared_v4(stg + i * 16, sc * __uint_as_float(v0[4 * i]), sc * __uint_as_float(v0[4 * i + 1]),
+                             sc * __uint_as_float(v0[4 * i + 2]), sc * __uint_as_float(v0[4 * i + 3]));
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                st_shared_v4(stg + 128 + i * 16, sc * __uint_as_float(v1[4 * i]), sc * __uint_as_float(v1[4 * i + 1]),
+                             sc * __uint_as_float(v1[4 * i + 2]), sc * __uint_as_float(v1[4 * i + 3]));
+              fence_proxy_async_smem();
+              if (tok >= 0) bulk_reduce_add_f32(grow + c * 64, stg, 256, pol_acc);
+              bulk_commit();
+            }
+          } else {
+            // all 128 columns of this warp's half in one wait, then TMEM goes back to the MMA issuer while the two
+            // 64-column reduce-adds go out through the staging row
+            uint32_t v[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tacc + half * (BN / 2) + c * 32, v[c]);
             tmem_ld_wait();
-            bulk_wait_read<0>();  // the previous bulk add has read the staging row
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if (CG == 2 && rank != 0) mbar_arrive_remote(mapa_shared(tempty_bar(buf), 0));
+              else mbar_arrive(tempty_bar(buf));
+            }
+            released = true;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              st_shared_v4(stg + i * 16, sc * __uint_as_float(v0[4 * i]), sc * __uint_as_float(v0[4 * i + 1]),
-                           sc * __uint_as_float(v0[4 * i + 2]), sc * __uint_as_float(v0[4 * i + 3]));
+            for (int c = 0; c < 2; ++c) {
+              bulk_wait_read<0>();  // the previous bulk add has read the staging row
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              st_shared_v4(stg + 128 + i * 16, sc * __uint_as_float(v1[4 * i]), sc * __uint_as_float(v1[4 * i + 1]),
-                           sc * __uint_as_float(v1[4 * i + 2]), sc * __uint_as_float(v1[4 * i + 3]));
-            fence_proxy_async_smem();
-            if (tok >= 0) bulk_reduce_add_f32(grow + c * 64, stg, 256, pol_acc);
-            bulk_commit();
+              for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  st_shared_v4(stg + h * 128 + i * 16, sc * __uint_as_float(v[2 * c + h][4 * i]),
+                               sc * __uint_as_float(v[2 * c + h][4 * i + 1]), sc * __uint_as_float(v[2 * c + h][4 * i + 2]),
+                               sc * __uint_as_float(v[2 * c + h][4 * i + 3]));
+              fence_proxy_async_smem();
+              if (tok >= 0) bulk_reduce_add_f32(grow + c * 64, stg, 256, pol_acc);
+              bulk_commit();
+            }
           }
         }
       } else if (MODE == kDH) {
@@ -1146,7 +1181,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
+      if (lane == 0 && !released) {
         if (CG == 2 && rank != 0) mbar_arrive_remote(mapa_shared(tempty_bar(buf), 0));  // the leader's MMAs wait
         else mbar_arrive(tempty_bar(buf));
       }
