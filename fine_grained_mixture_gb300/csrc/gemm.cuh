@@ -814,6 +814,8 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
     int buf = 0;
     uint32_t bph = 0;
     uint32_t hin_par = 0u;                       // dH epilogue: bit b = parity of H buffer b's next fill
+    bool h_pre = false;  // dH epilogue: the tile's first chunk of H was requested at the end of the previous tile
+    const int p_rows = MODE == kDH ? __ldg(&a.offsets[a.E]) : 0;  // dH: rows routed in total
     const uint64_t pol_acc = policy_evict_last();  // keep the fp32 accumulator slab in L2
     const uint64_t pol_stream = policy_evict_first();  // streamed epilogue traffic (H, A, dH, s*A) is touched once here
     for (int pair = first_pair, ti = 0; pair < total; pair += pair_step, ++ti) {
@@ -840,6 +842,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
         tok = __ldg(&a.row_token[t.row0 + row]);
         if (MODE != kDX) sc = __ldg(&a.row_score[t.row0 + row]);
       }
+      const float dh_sc = (MODE == kDH && t.row0 + row < t.row_end) ? __ldg(&a.row_score[t.row0 + row]) : 0.f;
       bool released = false;  // TMEM handed back to the MMA issuer before the end of the tile
       int ok = 1;
       if (lane == 0) ok = mbar_wait(tfull_bar(buf), bph) && !*abort_flag;
@@ -848,6 +851,7 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
         if (lane == 0) {
           set_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
           *abort_flag = 1;
+          if (MODE == kDH && h_pre) mbar_wait(hin_bar(q, 0), hin_par & 1u);  // the requested H chunk lands first
         }
         break;
       }
@@ -1008,25 +1012,28 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
         const int r = t.row0 + row;
         const bool valid = r < t.row_end;
         const bool full_warp = t.row0 + q * 32 + 31 < t.row_end;  // all 32 rows belong to this expert
-        const float sc = valid ? __ldg(&a.row_score[r]) : 0.f;
+        const float sc = dh_sc;
         // rows past the last expert (up to the end of its last tile) get zeros: the weight-gradient GEMMs read
         // them as the zero tail of that expert's last 64-row block
-        const bool zero_row = !valid && t.row_end == __ldg(&a.offsets[a.E]) && r < a.p_cap;
+        const bool zero_row = !valid && t.row_end == p_rows && r < a.p_cap;
         const int wrow = t.row0 + q * 32;                          // first row of this warp's 32
         const uint32_t wbase = base + SM::kStgOff + q * kDhWarpBytes;
         const uint32_t out_st = wbase + 4096;                      // dH gate | dH up staging
         // 64-byte swizzle: 16-byte piece p of row `lane` sits at piece p ^ ((lane >> 1) & 3)
         const int sw = (lane >> 1) & 3;
-        auto issue_h = [&](int c, int b) {
+        // chunk c (32 columns of the gate half and the same of the up half) of the H rows [wr, wr + 32) of a tile
+        auto issue_h_at = [&](int n0, int wr, int c, int b) {
           const uint32_t hb = hin_bar(q, b);
           mbar_arrive_expect_tx(hb, 4096);
-          tma_load_2d(wbase + b * 4096, &tm.h, t.n0 + c * 32, wrow, hb, pol_stream);
-          tma_load_2d(wbase + b * 4096 + 2048, &tm.h, a.n + t.n0 + c * 32, wrow, hb, pol_stream);
+          tma_load_2d(wbase + b * 4096, &tm.h, n0 + c * 32, wr, hb, pol_stream);
+          tma_load_2d(wbase + b * 4096 + 2048, &tm.h, a.n + n0 + c * 32, wr, hb, pol_stream);
         };
-        if (lane == 0) {
+        auto issue_h = [&](int c, int b) { issue_h_at(t.n0, wrow, c, b); };
+        if (lane == 0 && !h_pre) {
           fence_proxy_async_smem();  // the previous tile's reads of the buffer come before this refill
           issue_h(0, 0);
         }
+        h_pre = false;
         uint8_t *dhrow = static_cast<uint8_t *>(a.out0) + (size_t)r * (2 * a.n) * 2;
         uint8_t *sarow = static_cast<uint8_t *>(a.out1) + (size_t)r * a.n * 2;
         float ds = 0.f;
@@ -1057,9 +1064,19 @@ __global__ void __launch_bounds__(cta_threads<MODE, MB>(), 1)
             hu[4 * p + 3] = __float_as_uint(u4.w);
           }
           __syncwarp();  // every lane has read this chunk of H: the buffer can be refilled
-          if (c + 1 < BN / 32 && lane == 0) {
-            fence_proxy_async_smem();  // the warp's generic-proxy reads are ordered before the TMA refill
-            issue_h(c + 1, 0);
+          if (c + 1 < BN / 32) {
+            if (lane == 0) {
+              fence_proxy_async_smem();  // the warp's generic-proxy reads are ordered before the TMA refill
+              issue_h(c + 1, 0);
+            }
+          } else if (pair + pair_step < total) {
+            // the next tile's first chunk, while this tile's last chunk is computed and stored
+            if (lane == 0) {
+              const Tile tn = tile_at<MODE, BN, MB>(a, tile_cache, cached, ti + 1, pair + pair_step, rank, total_m, poff);
+              fence_proxy_async_smem();
+              issue_h_at(tn.n0, tn.row0 + q * 32, 0, 0);
+            }
+            h_pre = true;
           }
           uint32_t dg[16], du[16], sa[16];
 #pragma unroll
