@@ -26,9 +26,10 @@ def _routing_still_exact():
     check_routing(rt, orc.route(z.numpy(), 4, "tc"), P)
 
 
-@pytest.mark.parametrize("mode", ["tc", "tr"])
-def test_bad_token_ids_are_flagged_not_followed(mode):
-    w = synth.WORKLOADS["tiny"]
+# "pairs" (n = 768): the down-projection and dX~ run on CTA pairs, whose epilogues check the ids the same way
+@pytest.mark.parametrize("name,mode", [("tiny", "tc"), ("tiny", "tr"), ("pairs", "tc")])
+def test_bad_token_ids_are_flagged_not_followed(name, mode):
+    w = synth.custom(700, 256, 768, 6, 2) if name == "pairs" else synth.WORKLOADS["tiny"]
     g = to_dev(synth.make_inputs(w, 0))
     rt = moe.moe_route(g["logits"], w.K, mode)
     torch.cuda.synchronize()

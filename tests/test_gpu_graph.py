@@ -16,11 +16,16 @@ pytestmark = pytest.mark.gpu
 
 
 # token rounding runs its fill as clusters of 8 (tiny), 4 (fine7b) and 2 (sparse) CTAs per expert; the sparse
-# layer's weight gradients take the merged 256-row launch; a_from_h: the down-projection recomputes A from H
+# layer's weight gradients take the merged 256-row launch; a_from_h: the down-projection recomputes A from H;
+# "pairs" (n = 768): the down-projection and dX~ run on CTA pairs (two-CTA clusters)
+PAIRS = synth.custom(700, 256, 768, 6, 2, skew=True)
+
+
 @pytest.mark.parametrize("name,mode,a_from_h", [("tiny", "tc", False), ("tiny", "tr", False), ("fine7b", "tc", False),
-                                               ("fine7b", "tr", True), ("sparse", "tr", False)])
+                                               ("fine7b", "tr", True), ("sparse", "tr", False), ("pairs", "tc", False),
+                                               ("pairs", "tr", False)])
 def test_route_forward_backward_replay_in_a_cuda_graph(name, mode, a_from_h):
-    w = synth.WORKLOADS[name]
+    w = PAIRS if name == "pairs" else synth.WORKLOADS[name]
     g = to_dev(synth.make_inputs(w, 3))
     rt = moe.Routing(w.T, w.E, w.K, mode, "cuda")
     p = rt.p_cap
