@@ -1,6 +1,7 @@
 // common.cuh - device helpers for sm_103a: mbarriers with bounded waits, TMA tiled loads and stores, bulk
 // copies and reduce-adds, tcgen05 (TMEM alloc, UMMA issue/commit, TMEM loads) and shared-memory matrix
-// descriptors.  Every copy targets the issuing CTA's own shared memory.
+// descriptors.  Every copy targets the issuing CTA's own shared memory (a CTA pair's loads may complete on the
+// other CTA's barrier, which is shared memory of the cluster, not a copy destination).
 #pragma once
 
 #include <cuda.h>

@@ -28,7 +28,12 @@
 // accumulators of BN fp32 columns.  Each CTA decodes its tiles once into shared memory.
 // CTAs 2i and 2i+1 take neighbouring tiles (consecutive m-tiles of one expert, or neighbouring tiles of one
 // weight gradient), so the operand they share is read from L2 by the second CTA; every CTA loads its whole
-// tiles itself and releases its own stages (no clusters, nothing is sent between CTAs).
+// tiles itself and releases its own stages.
+// CTA pairs (CG = 2; the scatter-add GEMMs with K loops of 768 and more): CTAs 2i and 2i+1 form a two-CTA
+// cluster and share one M = 256 tcgen05.mma.cta_group::2 issued by the even CTA.  Each loads its own 128 rows
+// of A and half of B's columns; both CTAs' TMA loads complete on the leader's barrier, and the leader commits
+// each stage and accumulator to both CTAs' barriers (no multicast form).  Work items are 256-row pair tiles of
+// one expert.
 // Every wait is bounded; on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT, drains its own copies and
 // MMAs, frees TMEM and returns.
 #pragma once
