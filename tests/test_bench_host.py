@@ -36,6 +36,9 @@ def test_gemm_work_adds_up_to_the_layer(name):
 def test_kernel_names_from_ncu():
     assert bench.bench_kernel_name("void moe_gemm_kernel<6, 256, 3, 2, 0>(TensorMaps, GemmArgs)") == "gemm_dw"
     assert bench.bench_kernel_name("moe_gemm_kernel<(int)0, 256, 4, 1, 0>") == "gemm_up"
+    # the last template argument is the number of CTAs per MMA (2: the CTA-pair scatter-add GEMMs)
+    assert bench.bench_kernel_name("void moe_gemm_kernel<3, 256, 4, 1, 0, 2>(TensorMaps, GemmArgs)") == "gemm_dx"
+    assert bench.bench_kernel_name("void moe_gemm_kernel<1, 256, 4, 1, 1, 2>(TensorMaps, GemmArgs)") == "gemm_down"
     assert bench.bench_kernel_name("void route_topk_kernel<4, 0>(const float *, int)") == "route_topk"
     assert bench.bench_kernel_name("void some_library_kernel()") is None
 
